@@ -1,0 +1,172 @@
+/*
+ * q4k.h -- C ABI of the GB300 (sm_103a) Q4_K decode library.
+ *
+ * The library computes the memory-bound decode products of a GGUF Q4_K_M
+ * engine directly on 4-bit block-quantized weights:
+ *   - q4k_gemv         y = W x for one token or a small batch of tokens
+ *                      ("custom quantized GEMV for decode (Q8_0, Q4_K, Q6_K)"
+ *                      with "on-the-fly weight dequantization", dotLLM README,
+ *                      News 2026-03 "CUDA GPU backend"; the batch form is the
+ *                      VerifyBatch pass of the Glacier.Inference article,
+ *                      section 4 "Beating Hardware Bandwidth Ceilings with
+ *                      Speculative Decoding": one weight read for K+1 tokens)
+ *   - q4k_gemv_argmax  the LM-head product fused with a greedy argmax that
+ *                      writes one int32 token id per batch row (Glacier.Inference
+ *                      article, section 2 "Eliminating PCIe Starvation: In-VRAM
+ *                      Warp-Shuffle Argmax")
+ *   - q4k_gemm_prefill the prefill product with bf16 activations ("cuBLAS HGEMM
+ *                      for prefill", dotLLM README, News 2026-03), here on the
+ *                      tcgen05 tensor cores after a dequantize-to-bf16 step.
+ *
+ * ---------------------------------------------------------------------------
+ * Q4_K super-block (144 bytes, 256 weights, 4.5 bits per weight)
+ * ---------------------------------------------------------------------------
+ * The pages name the format (Q4_K, Q4_K_M) but print no byte layout; this
+ * library fixes the GGUF Q4_K packing:
+ *   bytes   0..1   d     IEEE binary16, little-endian (super-block scale)
+ *   bytes   2..3   dmin  IEEE binary16, little-endian (super-block min scale)
+ *   bytes   4..15  s[12] eight 6-bit scales sc_j and eight 6-bit mins m_j:
+ *                    j < 4 : sc_j = s[j] & 63,  m_j = s[j+4] & 63
+ *                    j >= 4: sc_j = (s[j+4] & 15) | ((s[j-4] >> 6) << 4)
+ *                            m_j  = (s[j+4] >> 4) | ((s[j]   >> 6) << 4)
+ *   bytes  16..143 qs[128] 4-bit quants; for p = 0..3 and i = 0..31:
+ *                    q[64p + i]      = qs[32p + i] & 15   (sub-block 2p)
+ *                    q[64p + 32 + i] = qs[32p + i] >> 4   (sub-block 2p+1)
+ *   weight 32j + i of the block:   w = d * sc_j * q[32j+i] - dmin * m_j
+ *
+ * A matrix W of N rows and K columns (K a positive multiple of 256) is stored
+ * row-major as N rows of K/256 consecutive super-blocks: row n starts at byte
+ * n * (K/256) * 144.  Every row therefore starts on a 16-byte boundary when W
+ * does.
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions for every entry point
+ * ---------------------------------------------------------------------------
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     never frees or retains them.  Calls are asynchronous on `stream` (a
+ *     cudaStream_t passed as void*; NULL is the legacy default stream) and
+ *     never synchronize the host.
+ *   - Outputs are overwritten, never accumulated.  Inputs and outputs must not
+ *     overlap.
+ *   - Argument errors are detected on the host before anything is launched and
+ *     returned as a status; Q4K_ERR_CUDA reports a launch failure (the CUDA
+ *     error is left for cudaGetLastError to clear).
+ *   - x and X are read only inside the kernels; they may be produced by the
+ *     kernel that ran just before on the same stream.
+ */
+#ifndef Q4K_H
+#define Q4K_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define Q4K_BLOCK_WEIGHTS 256
+#define Q4K_BLOCK_BYTES 144
+#define Q4K_MAX_BATCH 16
+#define Q4K_ABI_VERSION 1
+
+typedef enum {
+    Q4K_OK = 0,
+    Q4K_ERR_INVALID_ARG = 1,        /* null pointer, bad size or batch */
+    Q4K_ERR_MISALIGNED = 2,         /* a pointer is not 16-byte aligned */
+    Q4K_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+    Q4K_ERR_CUDA = 4                /* a CUDA call or a launch failed */
+} q4k_status;
+
+/* Human-readable text of a status (static storage, never NULL). */
+const char *q4k_status_string(q4k_status s);
+
+/* Q4K_ABI_VERSION of the loaded library. */
+int q4k_abi_version(void);
+
+/*
+ * y[b][n] = sum_k w[n][k] * x[b][k]   for b < batch, n < N.
+ *   W     uint8  [N][K/256*144]  Q4_K rows (layout above), 16-byte aligned
+ *   x     fp32   [batch][K]      row-major, 16-byte aligned
+ *   y     fp32   [batch][N]      row-major
+ *   N >= 0 (N == 0 is a no-op), K a positive multiple of 256, K/256 < 2^24,
+ *   1 <= batch <= 16.
+ * Accumulation is fp32.  Each weight super-block is read from memory once for
+ * all batch rows.  x may hold any finite fp32 values.
+ * Errors: INVALID_ARG (null pointer, N < 0, K <= 0 or K % 256 != 0, batch out
+ * of range), MISALIGNED (W or x), UNSUPPORTED_DEVICE, CUDA.
+ */
+q4k_status q4k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch,
+                    void *stream);
+
+/*
+ * idx[b] = the smallest n with y[b][n] == max_n' y[b][n'], where y = W x is the
+ * product q4k_gemv computes (the very same fp32 values).  NaN never wins; a row
+ * whose values are all NaN gives 0; -0.0 and +0.0 compare equal.  No logits
+ * leave the device: the only output is batch int32 values.
+ *   idx   int32 [batch]
+ *   1 <= N <= 2^31 - 1; other arguments as for q4k_gemv.
+ * Scratch: 8*batch + 4 bytes taken from the stream-ordered allocator
+ * (cudaMallocAsync / cudaFreeAsync on `stream`), so concurrent calls on
+ * different streams are independent.
+ */
+q4k_status q4k_gemv_argmax(const void *W, const float *x, int32_t *idx, int64_t N, int64_t K,
+                           int batch, void *stream);
+
+/*
+ * Same as q4k_gemv_argmax, and also writes the logits it reduced to
+ * `logits` (fp32 [batch][N]); meant for tests that check the argmax bit for bit
+ * against a scan of the very values the kernel compared.
+ */
+q4k_status q4k_gemv_argmax_debug(const void *W, const float *x, int32_t *idx, float *logits,
+                                 int64_t N, int64_t K, int batch, void *stream);
+
+/*
+ * Y[t][n] = sum_k w[n][k] * X[t][k]   for t < T, n < N (prefill).
+ *   W  Q4_K rows as above (16-byte aligned)
+ *   X  bf16 [T][K] row-major (16-byte aligned)
+ *   Y  fp32 [T][N] row-major
+ * The weights are dequantized to bf16 (round to nearest even) in shared memory
+ * and multiplied on the tcgen05 tensor cores with fp32 accumulation in tensor
+ * memory.  Any T >= 0 is accepted (T == 0 or N == 0 is a no-op); the tensor
+ * path is built for T >= 32.
+ * Errors: INVALID_ARG, MISALIGNED (W or X), UNSUPPORTED_DEVICE, CUDA.
+ */
+q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t N, int64_t K,
+                            int64_t T, void *stream);
+
+/*
+ * Extended launch control (tests and benchmarks).  Zero-initialised options
+ * reproduce the plain entry points exactly.
+ *   split_k  0 = automatic; 1 <= s <= 8 forces the K range of every row tile to
+ *            be split over s cooperating CTAs of a thread-block cluster
+ *            (clamped to K/256).
+ *   flags    Q4K_FLAG_PDL: launch with programmatic dependent launch, so the
+ *            kernel may start streaming W while the previous kernel on the
+ *            stream is still running.  W must then not be written by that
+ *            previous kernel (weights are constant during decode); x is still
+ *            read only after the previous kernel has completed.
+ */
+#define Q4K_FLAG_PDL 1u
+typedef struct {
+    int split_k;
+    unsigned flags;
+    int reserved[6];
+} q4k_launch_opts;
+
+q4k_status q4k_gemv_ex(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch,
+                       void *stream, const q4k_launch_opts *opts);
+
+/* Launch plan the automatic heuristics pick for a shape (for tests and
+ * reports): out[0] = split_k, out[1] = number of CTAs, out[2] = rows per CTA
+ * tile, out[3] = K blocks per x chunk held in shared memory. */
+q4k_status q4k_gemv_plan(int64_t N, int64_t K, int batch, int out[4]);
+
+/* Sticky device-side error bits of the library's kernels, read synchronously
+ * from the current device: bit 0 = a bounded wait inside a kernel timed out and
+ * the kernel wound down early (its outputs are then invalid).  0 = no error. */
+unsigned int q4k_device_error_flags(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4K_H */

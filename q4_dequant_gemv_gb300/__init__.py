@@ -1,0 +1,183 @@
+"""Python binding of the GB300 Q4_K decode library (libq4k.so, C ABI in include/q4k.h).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels.  torch supplies device memory and the current CUDA stream.  There
+is no CPU fallback: if the library is not built or cannot load, every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libq4k.so")
+
+Q4K_OK = 0
+Q4K_FLAG_PDL = 1
+QK = 256
+QBYTES = 144
+MAX_BATCH = 16
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Q4KError(RuntimeError):
+    def __init__(self, fn: str, status: int, text: str):
+        super().__init__(f"{fn} failed: status {status} ({text})")
+        self.status = status
+
+
+class LaunchOpts(ctypes.Structure):
+    _fields_ = [("split_k", ctypes.c_int), ("flags", ctypes.c_uint), ("reserved", ctypes.c_int * 6)]
+
+
+# Every symbol the header declares (checked by the CPU tests).
+EXPORTS = ("q4k_status_string", "q4k_abi_version", "q4k_gemv", "q4k_gemv_argmax", "q4k_gemv_argmax_debug",
+           "q4k_gemm_prefill", "q4k_gemv_ex", "q4k_gemv_plan", "q4k_device_error_flags")
+
+
+def lib():
+    """Load libq4k.so (raises if missing -- there is no fallback path)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libq4k.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.q4k_status_string.argtypes = [I]
+        L.q4k_status_string.restype = ctypes.c_char_p
+        L.q4k_abi_version.restype = I
+        L.q4k_gemv.argtypes = [P, P, P, I64, I64, I, P]
+        L.q4k_gemv.restype = I
+        L.q4k_gemv_ex.argtypes = [P, P, P, I64, I64, I, P, ctypes.POINTER(LaunchOpts)]
+        L.q4k_gemv_ex.restype = I
+        L.q4k_gemv_argmax.argtypes = [P, P, P, I64, I64, I, P]
+        L.q4k_gemv_argmax.restype = I
+        L.q4k_gemv_argmax_debug.argtypes = [P, P, P, P, I64, I64, I, P]
+        L.q4k_gemv_argmax_debug.restype = I
+        L.q4k_gemm_prefill.argtypes = [P, P, P, I64, I64, I64, P]
+        L.q4k_gemm_prefill.restype = I
+        L.q4k_gemv_plan.argtypes = [I64, I64, I, ctypes.POINTER(ctypes.c_int * 4)]
+        L.q4k_gemv_plan.restype = I
+        L.q4k_device_error_flags.restype = ctypes.c_uint
+        _lib = L
+        return L
+
+
+def status_string(s: int) -> str:
+    return lib().q4k_status_string(int(s)).decode()
+
+
+def _check(fn: str, st: int):
+    if st != Q4K_OK:
+        raise Q4KError(fn, st, status_string(st))
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(t, name, dtype, cuda=True):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _shape_wk(W, K):
+    N = W.shape[0]
+    if W.dim() != 2 or W.shape[1] != (K // QK) * QBYTES:
+        raise ValueError(f"W must be uint8 [N, K/256*144] for K={K}, got {tuple(W.shape)}")
+    return N
+
+
+def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False):
+    """y [B, N] (fp32) = W_q4k [N, K] . x [B, K] (fp32); x may also be [K]."""
+    import torch
+    _dev(W, "W", torch.uint8)
+    _dev(x, "x", torch.float32)
+    squeeze = x.dim() == 1
+    x2 = x.view(1, -1) if squeeze else x
+    B, K = x2.shape
+    N = _shape_wk(W, K)
+    if y is None:
+        y = torch.empty((B, N), dtype=torch.float32, device=x.device)
+    _dev(y, "y", torch.float32)
+    if y.numel() != B * N:
+        raise ValueError("y has the wrong size")
+    L = lib()
+    if split_k or pdl:
+        o = LaunchOpts(split_k, Q4K_FLAG_PDL if pdl else 0)
+        st = L.q4k_gemv_ex(W.data_ptr(), x2.data_ptr(), y.data_ptr(), N, K, B, _stream_ptr(stream), ctypes.byref(o))
+        _check("q4k_gemv_ex", st)
+    else:
+        st = L.q4k_gemv(W.data_ptr(), x2.data_ptr(), y.data_ptr(), N, K, B, _stream_ptr(stream))
+        _check("q4k_gemv", st)
+    return y.view(N) if squeeze and y.dim() == 2 else y
+
+
+def gemv_argmax(W, x, idx=None, *, logits=None, stream=None):
+    """int32 idx [B] = argmax_n (W . x[b])[n] (lowest index on ties)."""
+    import torch
+    _dev(W, "W", torch.uint8)
+    _dev(x, "x", torch.float32)
+    x2 = x.view(1, -1) if x.dim() == 1 else x
+    B, K = x2.shape
+    N = _shape_wk(W, K)
+    if idx is None:
+        idx = torch.empty(B, dtype=torch.int32, device=x.device)
+    _dev(idx, "idx", torch.int32)
+    L = lib()
+    if logits is not None:
+        _dev(logits, "logits", torch.float32)
+        st = L.q4k_gemv_argmax_debug(W.data_ptr(), x2.data_ptr(), idx.data_ptr(), logits.data_ptr(), N, K, B,
+                                     _stream_ptr(stream))
+        _check("q4k_gemv_argmax_debug", st)
+    else:
+        st = L.q4k_gemv_argmax(W.data_ptr(), x2.data_ptr(), idx.data_ptr(), N, K, B, _stream_ptr(stream))
+        _check("q4k_gemv_argmax", st)
+    return idx
+
+
+def gemm_prefill(W, X, Y=None, *, stream=None):
+    """Y [T, N] (fp32) = X [T, K] (bf16) . W_q4k^T."""
+    import torch
+    _dev(W, "W", torch.uint8)
+    _dev(X, "X", torch.bfloat16)
+    T, K = X.shape
+    N = _shape_wk(W, K)
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.float32, device=X.device)
+    _dev(Y, "Y", torch.float32)
+    st = lib().q4k_gemm_prefill(W.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, _stream_ptr(stream))
+    _check("q4k_gemm_prefill", st)
+    return Y
+
+
+def gemv_plan(N: int, K: int, batch: int):
+    out = (ctypes.c_int * 4)()
+    _check("q4k_gemv_plan", lib().q4k_gemv_plan(N, K, batch, ctypes.byref(out)))
+    return {"split_k": out[0], "ctas": out[1], "rows_per_tile": out[2], "x_chunk_blocks": out[3]}
+
+
+def device_error_flags() -> int:
+    return int(lib().q4k_device_error_flags())
+
+
+def raw_call(name: str, *args):
+    """Call an exported entry point with raw integer/pointer arguments (tests)."""
+    return getattr(lib(), name)(*args)

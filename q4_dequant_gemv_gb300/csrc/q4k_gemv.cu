@@ -1,0 +1,777 @@
+// q4k_gemv.cu -- Q4_K decode GEMV / VerifyBatch GEMV / fused LM-head argmax
+// for GB300 (sm_103a).
+//
+// What is computed: y[b][n] = sum_k w[n][k] x[b][k] with w the Q4_K weight
+// w = d*sc_j*q - dmin*m_j, directly on the quantized blocks ("fused scale x
+// int dot-product kernels operating directly on quantized blocks", dotLLM
+// README, Key Features / Performance), reading every super-block once for all
+// batch rows (Glacier.Inference article, section 4: VerifyBatch pulls the
+// weights through the memory bus once for K+1 tokens), optionally followed by
+// the greedy argmax of each batch row (same article, section 2: one int32 per
+// row, logits stay on the device).
+//
+// Design (GB300-first; the pages' own kernels were HLSL Wave32 shaders and
+// sm_75..sm_90 cubins):
+//   * Weights are streamed HBM -> shared memory with 1-D TMA bulk copies
+//     (cp.async.bulk) by one producer warp per CTA into a ring of stages
+//     guarded by mbarriers; the consumers never issue global loads for W.
+//   * The inner product runs on the tensor cores with mma.sync m16n8k16:
+//     A = the weights' q*sc_j as exact fp16 integers (<= 945), built in
+//     registers from the nibbles with one LOP3 (magic-exponent trick) and one
+//     HFMA2 per two weights; B = the activations split into fp16 hi + lo parts
+//     (x = hi + lo to ~2^-22 relative), one column each, so the fp32
+//     accumulation sees x at nearly full fp32 precision.  Column pairs hold
+//     batch rows (up to 4 per n8 tile).  The dmin*m_j term is one extra k16
+//     step per super-block whose A holds m_j and whose B holds the per
+//     sub-block sums of x (again hi + lo).  Per super-block the two fp32 tiles
+//     are combined as d*C - dmin*Cmin.
+//   * x is rescaled by a power of two per chunk and batch row before the fp16
+//     split (so any finite fp32 x works); the scale is undone in the fp32
+//     epilogue.
+//   * Row tiles of 64 rows (4 consumer warps x 16 rows).  When there are too
+//     few row tiles to fill the GPU the K range of a tile is split over the
+//     CTAs of a thread-block cluster, and the partial sums are added in rank
+//     order through distributed shared memory (deterministic, no atomics, no
+//     global scratch).  With a single K slice the grid is persistent and CTAs
+//     loop over row tiles, so the weight stream never drains between tiles.
+//   * The argmax variant keeps per-CTA (max, lowest index) keys in shared
+//     memory and combines CTAs with one 64-bit atomicMax per batch row plus a
+//     last-CTA ticket (no spin-waits).
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/q4k.h"
+#include "ptx.cuh"
+#include "q4k_internal.h"
+
+namespace q4k {
+
+constexpr int kBlockBytes = 144;
+constexpr int kWarps = 4;                 // consumer warps per CTA
+constexpr int kRows = 16 * kWarps;        // rows per tile
+constexpr int kThreads = 32 * (kWarps + 1);
+constexpr int kKsteps = 17;               // 16 k16 steps + 1 min-term step per super-block
+constexpr int kStages = 3;                // W ring depth
+constexpr int kStageBlocks = 2;           // super-blocks per row per stage
+constexpr int kRowStride = kStageBlocks * kBlockBytes + 16;   // padded (bank spread)
+constexpr int kStageBytes = kRows * kRowStride;
+constexpr size_t kSmemPerCta = 112 * 1024;   // two CTAs per SM
+constexpr uint64_t kWaitLimitNs = 2000000000ull;               // 2 s
+
+__device__ unsigned int g_device_error = 0;   // bit 0: an mbarrier wait timed out
+
+struct GemvArgs {
+    const uint8_t *W;
+    const float *x;
+    float *y;            // may be null in the argmax variant (logits not wanted)
+    int N;
+    int nb;              // super-blocks per row
+    int B;               // batch
+    int tiles;           // ceil(N / kRows)
+    int kc;              // super-blocks per x chunk in shared memory
+    unsigned long long *keys;  // argmax: [B] 64-bit keys (zeroed), null otherwise
+    unsigned int *ticket;      // argmax: CTA ticket (zeroed)
+    int32_t *idx;              // argmax: output [B]
+};
+
+__host__ __device__ inline int frag_lanes(int NT, int B) { return NT == 1 ? 8 * B : 32; }
+
+__host__ __device__ inline size_t xfrag_bytes_per_block(int NT, int B)
+{
+    return static_cast<size_t>(kKsteps) * NT * frag_lanes(NT, B) * 8;
+}
+
+__host__ inline size_t gemv_smem_bytes(int NT, int B, int kc)
+{
+    size_t s = 0;
+    s += static_cast<size_t>(kStages) * kStageBytes;             // W ring
+    s += xfrag_bytes_per_block(NT, B) * kc;                      // x fragments
+    s += 2 * kStages * 8;                                        // mbarriers
+    s += 16 * 4 * 3;                                             // scale / unscale / amax per batch row
+    s += 16 * 8;                                                 // argmax keys
+    s += static_cast<size_t>(kRows) * 16 * 4;                    // split-K partials
+    return s + 256;                                              // alignment slack
+}
+
+// ---------------------------------------------------------------------------
+// x chunk -> fp16 hi/lo B fragments in shared memory.
+// Entry (bl, s, nt, L) is a uint2 {b01, b23} for lane L = 4*col8 + t of n-tile
+// nt at k-step s of local super-block bl.  Thread t of an A fragment handles
+// sub-block pair t of each super-block (sub-blocks 2t and 2t+1), so for k-step
+// s < 16 (word u = s/2, sub-block 2t + (s&1)) the four B values are the x
+// entries 4u..4u+3 of that sub-block ordered {4u, 4u+2 | 4u+1, 4u+3}.  Step 16
+// holds the sub-block sums of x for sub-blocks 2t, 2t+1 (the dmin*m term).
+// ---------------------------------------------------------------------------
+template <int NT>
+__device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int kb0, int nblk, uint2 *xf,
+                                float *s_scale, float *s_unscale, uint32_t *s_amax, int tid, int nthr)
+{
+    const int LW = frag_lanes(NT, B);
+    // 1) per-batch-row max |x| over the chunk -> power-of-two scale
+    for (int b = tid; b < B; b += nthr) s_amax[b] = 0u;
+    named_bar_sync(1, nthr);
+    const int n4 = nblk * 64;  // float4 per batch row in the chunk
+    for (int b = 0; b < B; ++b) {
+        const float4 *xb = reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K + static_cast<size_t>(kb0) * 256);
+        uint32_t m = 0u;
+        for (int e = tid; e < n4; e += nthr) {
+            float4 v = __ldg(xb + e);
+            m = max(m, __float_as_uint(fabsf(v.x)));
+            m = max(m, __float_as_uint(fabsf(v.y)));
+            m = max(m, __float_as_uint(fabsf(v.z)));
+            m = max(m, __float_as_uint(fabsf(v.w)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((tid & 31) == 0 && m) atomicMax(&s_amax[b], m);
+    }
+    named_bar_sync(1, nthr);
+    for (int b = tid; b < B; b += nthr) {
+        uint32_t bits = s_amax[b];
+        int E = static_cast<int>((bits >> 23) & 255u);
+        int s = 0;
+        if (bits != 0u && E != 255) s = 136 - E;             // max|x| * 2^s in [2^9, 2^10)
+        s = max(-126, min(126, s));
+        s_scale[b] = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
+        s_unscale[b] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+    }
+    named_bar_sync(1, nthr);
+    // 2) main entries: items (bl, s<16, b, t)
+    const int items = nblk * 16 * B * 4;
+    for (int it = tid; it < items; it += nthr) {
+        int t = it & 3;
+        int r = it >> 2;
+        int b = r % B;
+        r /= B;
+        int s = r & 15;
+        int bl = r >> 4;
+        int pos = (kb0 + bl) * 256 + 32 * (2 * t + (s & 1)) + 4 * (s >> 1);
+        float4 v = __ldg(reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K + pos));
+        const float sc = s_scale[b];
+        v.x *= sc; v.y *= sc; v.z *= sc; v.w *= sc;
+        uint32_t h01 = pack_half2(v.x, v.z);
+        uint32_t h23 = pack_half2(v.y, v.w);
+        uint32_t l01 = pack_half2(v.x - half_lo_f32(h01), v.z - half_hi_f32(h01));
+        uint32_t l23 = pack_half2(v.y - half_lo_f32(h23), v.w - half_hi_f32(h23));
+        const int chi = 2 * b, clo = 2 * b + 1;
+        const size_t base = static_cast<size_t>(bl * kKsteps + s) * NT;
+        xf[(base + chi / 8) * LW + 4 * (chi % 8) + t] = make_uint2(h01, h23);
+        xf[(base + clo / 8) * LW + 4 * (clo % 8) + t] = make_uint2(l01, l23);
+    }
+    // 3) min-term entries: items (bl, b, t): sums of sub-blocks 2t and 2t+1
+    const int mitems = nblk * B * 4;
+    for (int it = tid; it < mitems; it += nthr) {
+        int t = it & 3;
+        int r = it >> 2;
+        int b = r % B;
+        int bl = r / B;
+        const float sc = s_scale[b];
+        const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K +
+                                                           static_cast<size_t>(kb0 + bl) * 256 + 64 * t);
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float4 v = __ldg(p + e);
+            s0 += (v.x * sc + v.y * sc) + (v.z * sc + v.w * sc);
+        }
+#pragma unroll
+        for (int e = 8; e < 16; ++e) {
+            float4 v = __ldg(p + e);
+            s1 += (v.x * sc + v.y * sc) + (v.z * sc + v.w * sc);
+        }
+        uint32_t h = pack_half2(s0, s1);
+        uint32_t l = pack_half2(s0 - half_lo_f32(h), s1 - half_hi_f32(h));
+        const int chi = 2 * b, clo = 2 * b + 1;
+        const size_t base = static_cast<size_t>(bl * kKsteps + 16) * NT;
+        xf[(base + chi / 8) * LW + 4 * (chi % 8) + t] = make_uint2(h, 0u);
+        xf[(base + clo / 8) * LW + 4 * (clo % 8) + t] = make_uint2(l, 0u);
+    }
+    named_bar_sync(1, nthr);
+}
+
+// Scale/min constants of one row of a super-block for thread t (pair t).
+struct RowConsts {
+    uint32_t mulE, addE, mulO, addO;  // f16x2 (sc_2t), (-1024 sc_2t), (sc_2t+1 / 16), (-64 sc_2t+1)
+    uint32_t mpair;                   // f16x2 {m_2t, m_2t+1}
+    float d, dmin;
+};
+
+__device__ __forceinline__ RowConsts decode_header(uint4 h, int t)
+{
+    RowConsts rc;
+    rc.d = half_lo_f32(h.x);
+    rc.dmin = half_hi_f32(h.x);
+    const uint32_t sh = (t & 1) ? 16u : 0u;
+    const uint32_t a0 = (h.y >> sh) & 0xFFFFu;   // s[2(t&1)], s[2(t&1)+1]
+    const uint32_t a1 = (h.z >> sh) & 0xFFFFu;   // s[4+...]
+    const uint32_t a2 = (h.w >> sh) & 0xFFFFu;   // s[8+...]
+    uint32_t scp, mp;
+    if (t < 2) {
+        scp = a0 & 0x3F3Fu;
+        mp = a1 & 0x3F3Fu;
+    } else {
+        scp = (a2 & 0x0F0Fu) | ((a0 >> 2) & 0x3030u);
+        mp = ((a2 >> 4) & 0x0F0Fu) | ((a1 >> 2) & 0x3030u);
+    }
+    const uint32_t k1024 = 0x64006400u;          // f16x2 {1024, 1024}
+    uint32_t sch = hsub2_u32(__byte_perm(scp, 0u, 0x4140u) | k1024, k1024);   // {sc_2t, sc_2t+1}
+    rc.mpair = hsub2_u32(__byte_perm(mp, 0u, 0x4140u) | k1024, k1024);       // {m_2t, m_2t+1}
+    const uint32_t lo2 = __byte_perm(sch, 0u, 0x1010u);   // {sc_2t, sc_2t}
+    const uint32_t hi2 = __byte_perm(sch, 0u, 0x3232u);   // {sc_2t+1, sc_2t+1}
+    rc.mulE = lo2;
+    rc.addE = hmul2_u32(lo2, 0xE400E400u);        // * -1024
+    rc.mulO = hmul2_u32(hi2, 0x2C002C00u);        // * 1/16
+    rc.addO = hmul2_u32(hi2, 0xD400D400u);        // * -64
+    return rc;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.  Warps 0..3 consume (16 rows each), warp 4 produces.
+// grid = (row-tile CTAs, split) with cluster dims (1, split, 1) when split > 1.
+// ---------------------------------------------------------------------------
+template <int NT, bool ARGMAX>
+__global__ void __launch_bounds__(kThreads, 2) q4k_gemv_kernel(const GemvArgs args)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint8_t *ring = smem;
+    const int B = args.B;
+    const int LW = frag_lanes(NT, B);
+    uint2 *xf = reinterpret_cast<uint2 *>(ring + kStages * kStageBytes);
+    uint8_t *after_xf = reinterpret_cast<uint8_t *>(xf) + xfrag_bytes_per_block(NT, B) * args.kc;
+    uint64_t *bars = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(after_xf) + 7) & ~uintptr_t(7));
+    uint64_t *full = bars;
+    uint64_t *empty = bars + kStages;
+    float *s_scale = reinterpret_cast<float *>(bars + 2 * kStages);
+    float *s_unscale = s_scale + 16;
+    uint32_t *s_amax = reinterpret_cast<uint32_t *>(s_unscale + 16);
+    unsigned long long *s_best = reinterpret_cast<unsigned long long *>(
+        (reinterpret_cast<uintptr_t>(s_amax + 16) + 7) & ~uintptr_t(7));
+    float *s_red = reinterpret_cast<float *>(s_best + 16);
+    __shared__ int s_abort;
+    __shared__ int s_issued;
+    __shared__ int s_cons[kWarps];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int split = gridDim.y;
+    const int rank = blockIdx.y;
+    const int nb = args.nb;
+    const int kb_begin = static_cast<int>((static_cast<long long>(rank) * nb) / split);
+    const int kb_end = static_cast<int>((static_cast<long long>(rank + 1) * nb) / split);
+    const int ks = kb_end - kb_begin;
+    const int nstage_per_tile = (ks + kStageBlocks - 1) / kStageBlocks;
+    const size_t row_bytes = static_cast<size_t>(nb) * kBlockBytes;
+
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), kWarps);
+        }
+        s_abort = 0;
+        s_issued = 0;
+        for (int w = 0; w < kWarps; ++w) s_cons[w] = 0;
+        fence_barrier_init();
+    }
+    if (ARGMAX && tid < 16) s_best[tid] = 0ull;
+    __syncthreads();
+
+    pdl_launch_dependents();
+
+    if (warp == kWarps) {
+        // ------------------------------------------------------------ producer
+        const uint64_t policy = l2_policy_evict_first();
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
+            const int row0 = tile * kRows;
+            const int rows = min(kRows, args.N - row0);
+            for (int st = 0; st < nstage_per_tile; ++st) {
+                const int kb = kb_begin + st * kStageBlocks;
+                const int nblk = min(kStageBlocks, kb_end - kb);
+                // After an abort the producer keeps walking the schedule without
+                // waiting or copying, so nothing ever blocks on it.
+                if (!*(volatile int *)&s_abort &&
+                    !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
+                    atomicOr(&g_device_error, 1u);
+                    s_abort = 1;
+                }
+                if (*(volatile int *)&s_abort) {
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                    continue;
+                }
+                const uint32_t bytes = static_cast<uint32_t>(rows * nblk * kBlockBytes);
+                if (lane == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), bytes);
+                __syncwarp();
+                for (int r = lane; r < rows; r += 32) {
+                    const uint8_t *src = args.W + static_cast<size_t>(row0 + r) * row_bytes +
+                                         static_cast<size_t>(kb) * kBlockBytes;
+                    bulk_g2s(smem_u32(ring + stage * kStageBytes + r * kRowStride), src,
+                             static_cast<uint32_t>(nblk * kBlockBytes), smem_u32(&full[stage]), policy);
+                }
+                ++issued;
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (lane == 0) s_issued = issued;
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int g = lane >> 2;
+        const int t = lane & 3;
+        const int ctid = tid;                   // 0..127
+        pdl_wait();                             // x may come from the previous kernel
+        const int nchunks = (ks + args.kc - 1) / args.kc;
+        const bool single_chunk = (nchunks == 1);
+        if (single_chunk) {
+            convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_scale, s_unscale, s_amax, ctid,
+                                kWarps * 32);
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        int consumed = 0;
+        for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
+            const int row0 = tile * kRows;
+            float acc[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
+            float unscale[NT];
+            int chunk_end = -1;
+            bool reload_scale = false;
+            int blk_in_stage = 0;
+            const uint8_t *stage_base = nullptr;
+            for (int kbl = 0; kbl < ks; ++kbl) {
+                if (!single_chunk && kbl > chunk_end) {
+                    const int c0 = kbl;
+                    const int cn = min(args.kc, ks - c0);
+                    named_bar_sync(1, kWarps * 32);     // everyone done with the previous chunk
+                    convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + c0, cn, xf, s_scale, s_unscale, s_amax,
+                                        ctid, kWarps * 32);
+                    chunk_end = c0 + cn - 1;
+                    reload_scale = true;
+                }
+                if (kbl == 0 || reload_scale) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int b = t + 4 * nt;
+                        unscale[nt] = (b < B) ? s_unscale[b] : 0.f;
+                    }
+                    reload_scale = false;
+                }
+                if (blk_in_stage == 0) {
+                    // After an abort the consumers keep walking the same schedule
+                    // (all named barriers are still reached) but stop waiting.
+                    if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs)) {
+                        atomicOr(&g_device_error, 1u);
+                        s_abort = 1;
+                    }
+                    stage_base = ring + stage * kStageBytes;
+                }
+                const int xbl = single_chunk ? kbl : (kbl % args.kc);
+                {
+                    const uint8_t *rg = stage_base + (warp * 16 + g) * kRowStride + blk_in_stage * kBlockBytes;
+                    const uint8_t *rg8 = rg + 8 * kRowStride;
+                    const uint4 h0 = *reinterpret_cast<const uint4 *>(rg);
+                    const uint4 h1 = *reinterpret_cast<const uint4 *>(rg8);
+                    const uint4 qa0 = *reinterpret_cast<const uint4 *>(rg + 16 + 32 * t);
+                    const uint4 qb0 = *reinterpret_cast<const uint4 *>(rg + 32 + 32 * t);
+                    const uint4 qa1 = *reinterpret_cast<const uint4 *>(rg8 + 16 + 32 * t);
+                    const uint4 qb1 = *reinterpret_cast<const uint4 *>(rg8 + 32 + 32 * t);
+                    const RowConsts r0 = decode_header(h0, t);
+                    const RowConsts r1 = decode_header(h1, t);
+                    const uint32_t w0[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qb0.x, qb0.y, qb0.z, qb0.w};
+                    const uint32_t w1[8] = {qa1.x, qa1.y, qa1.z, qa1.w, qb1.x, qb1.y, qb1.z, qb1.w};
+                    float cE[NT][4], cO[NT][4], cM[NT][4];
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) cE[nt][i] = cO[nt][i] = cM[nt][i] = 0.f;
+                    const uint2 *xrow = xf + static_cast<size_t>(xbl) * kKsteps * NT * LW;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const uint32_t a = w0[u], a8 = a >> 8;
+                        const uint32_t c = w1[u], c8 = c >> 8;
+                        const uint32_t mask_lo = 0x000F000Fu, mask_hi = 0x00F000F0u, magic = 0x64006400u;
+                        const uint32_t e0 = hfma2_u32(and_or(a, mask_lo, magic), r0.mulE, r0.addE);
+                        const uint32_t e1 = hfma2_u32(and_or(a8, mask_lo, magic), r0.mulE, r0.addE);
+                        const uint32_t o0 = hfma2_u32(and_or(a, mask_hi, magic), r0.mulO, r0.addO);
+                        const uint32_t o1 = hfma2_u32(and_or(a8, mask_hi, magic), r0.mulO, r0.addO);
+                        const uint32_t f0 = hfma2_u32(and_or(c, mask_lo, magic), r1.mulE, r1.addE);
+                        const uint32_t f1 = hfma2_u32(and_or(c8, mask_lo, magic), r1.mulE, r1.addE);
+                        const uint32_t p0 = hfma2_u32(and_or(c, mask_hi, magic), r1.mulO, r1.addO);
+                        const uint32_t p1 = hfma2_u32(and_or(c8, mask_hi, magic), r1.mulO, r1.addO);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const bool live = (g + 8 * nt) < 2 * B;   // lane's column holds a batch row
+                            uint2 be = make_uint2(0u, 0u), bo = make_uint2(0u, 0u);
+                            if (live) {
+                                be = xrow[(static_cast<size_t>(2 * u) * NT + nt) * LW + lane];
+                                bo = xrow[(static_cast<size_t>(2 * u + 1) * NT + nt) * LW + lane];
+                            }
+                            mma_16816(cE[nt], e0, f0, e1, f1, be.x, be.y);
+                            mma_16816(cO[nt], o0, p0, o1, p1, bo.x, bo.y);
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const bool live = (g + 8 * nt) < 2 * B;
+                        uint2 bm = make_uint2(0u, 0u);
+                        if (live) bm = xrow[(static_cast<size_t>(16) * NT + nt) * LW + lane];
+                        mma_16816(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
+                        const float s0 = (cE[nt][0] + cO[nt][0]) + (cE[nt][1] + cO[nt][1]);
+                        const float s1 = (cE[nt][2] + cO[nt][2]) + (cE[nt][3] + cO[nt][3]);
+                        const float m0 = cM[nt][0] + cM[nt][1];
+                        const float m1 = cM[nt][2] + cM[nt][3];
+                        acc[nt][0] = fmaf(r0.d * unscale[nt], s0, acc[nt][0]);
+                        acc[nt][0] = fmaf(-r0.dmin * unscale[nt], m0, acc[nt][0]);
+                        acc[nt][1] = fmaf(r1.d * unscale[nt], s1, acc[nt][1]);
+                        acc[nt][1] = fmaf(-r1.dmin * unscale[nt], m1, acc[nt][1]);
+                    }
+                }
+                if (++blk_in_stage == kStageBlocks || kbl == ks - 1) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+                    ++consumed;
+                    blk_in_stage = 0;
+                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            // ---------------- tile epilogue
+            if (split == 1 && !*(volatile int *)&s_abort) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int b = t + 4 * nt;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int row = row0 + warp * 16 + g + 8 * h;
+                        if (b < B && row < args.N) {
+                            const float v = acc[nt][h];
+                            if (args.y) args.y[static_cast<size_t>(b) * args.N + row] = v;
+                            if (ARGMAX && !isnan(v)) atomicMax(&s_best[b], argmax_key(v, static_cast<uint32_t>(row)));
+                        }
+                    }
+                }
+            } else if (split > 1) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int b = t + 4 * nt;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        if (b < B) s_red[(warp * 16 + g + 8 * h) * B + b] = acc[nt][h];
+                }
+            }
+        }
+        if (lane == 0) s_cons[warp] = consumed;
+    }
+
+    // After a timed-out wait, wait (bounded) for the bulk copies this CTA issued
+    // but did not consume, so that none of them lands after the CTA has exited.
+    __syncthreads();
+    if (*(volatile int *)&s_abort && tid == kWarps * 32) {
+        int lo = s_cons[0];
+        for (int w = 1; w < kWarps; ++w) lo = min(lo, s_cons[w]);
+        for (int i = lo; i < s_issued; ++i)
+            if (!mbar_wait_bounded(smem_u32(&full[i % kStages]), static_cast<uint32_t>((i / kStages) & 1), kWaitLimitNs))
+                break;
+    }
+
+    if (split > 1) {
+        // Deterministic cross-CTA reduction of the single row tile through
+        // distributed shared memory: rank r sums rows [r*64/split, (r+1)*64/split)
+        // over ranks 0..split-1 in order.
+        cluster_sync_all();
+        if (!*(volatile int *)&s_abort) {
+            const int row0 = blockIdx.x * kRows;
+            const int lr0 = (rank * kRows) / split;
+            const int lr1 = ((rank + 1) * kRows) / split;
+            const int items = (lr1 - lr0) * B;
+            const uint32_t red_local = smem_u32(s_red);
+            for (int it = tid; it < items; it += kThreads) {
+                const int lr = lr0 + it / B;
+                const int b = it % B;
+                const uint32_t off = static_cast<uint32_t>((lr * B + b) * 4);
+                float s = 0.f;
+                for (int q = 0; q < split; ++q) s += ld_shared_cluster_f32(map_shared_rank(red_local + off, q));
+                const int row = row0 + lr;
+                if (row < args.N) {
+                    if (args.y) args.y[static_cast<size_t>(b) * args.N + row] = s;
+                    if (ARGMAX && !isnan(s)) atomicMax(&s_best[b], argmax_key(s, static_cast<uint32_t>(row)));
+                }
+            }
+        }
+        cluster_sync_all();
+    }
+
+    if (ARGMAX) {
+        __syncthreads();
+        if (tid == 0 && !*(volatile int *)&s_abort) {
+            for (int b = 0; b < B; ++b)
+                if (s_best[b]) atomicMax(&args.keys[b], s_best[b]);
+            __threadfence();
+            const unsigned total = gridDim.x * gridDim.y;
+            const unsigned prev = atomicAdd(args.ticket, 1u);
+            if (prev == total - 1) {
+                __threadfence();
+                for (int b = 0; b < B; ++b) {
+                    const unsigned long long k = atomicAdd(&args.keys[b], 0ull);
+                    args.idx[b] = k ? static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull)) : 0;
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+struct DeviceInfo {
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    size_t smem_optin = 0;
+    bool ok = false;
+};
+
+static DeviceInfo g_dev[64];
+static std::once_flag g_dev_once[64];
+
+static const DeviceInfo &device_info(int dev)
+{
+    std::call_once(g_dev_once[dev & 63], [dev]() {
+        DeviceInfo &d = g_dev[dev & 63];
+        cudaDeviceProp p;
+        if (cudaGetDeviceProperties(&p, dev) != cudaSuccess) return;
+        d.sms = p.multiProcessorCount;
+        d.cc_major = p.major;
+        d.cc_minor = p.minor;
+        d.smem_optin = p.sharedMemPerBlockOptin;
+        d.ok = true;
+    });
+    return g_dev[dev & 63];
+}
+
+q4k_status check_device(int *sms_out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4K_ERR_CUDA;
+    const DeviceInfo &d = device_info(dev);
+    if (!d.ok) return Q4K_ERR_CUDA;
+    if (d.cc_major != 10 || d.cc_minor != 3) return Q4K_ERR_UNSUPPORTED_DEVICE;
+    if (sms_out) *sms_out = d.sms;
+    return Q4K_OK;
+}
+
+struct GemvPlan {
+    int NT;
+    int split;
+    int grid_x;
+    int tiles;
+    int kc;
+    size_t smem;
+};
+
+static int batch_ntiles(int B) { return (2 * B + 7) / 8; }
+
+// Pick the K split: minimise (max row-tile units per SM) x (blocks per unit
+// + per-CTA overhead), preferring fewer CTAs on ties.
+static GemvPlan make_plan(int64_t N, int64_t K, int B, int sms, int forced_split)
+{
+    GemvPlan p{};
+    const int nb = static_cast<int>(K / 256);
+    p.NT = batch_ntiles(B);
+    p.tiles = static_cast<int>((N + kRows - 1) / kRows);
+    int best_s = 1;
+    if (forced_split > 0) {
+        best_s = std::min(std::min(forced_split, nb), 8);
+    } else {
+        double best = 1e30;
+        const int smax = std::min(nb, 8);
+        for (int s = 1; s <= smax; ++s) {
+            const long long units = static_cast<long long>(p.tiles) * s;
+            const long long per_sm = (units + sms - 1) / sms;
+            const int per_unit = (nb + s - 1) / s;
+            const double cost = static_cast<double>(per_sm) * (per_unit + 0.5);
+            if (cost < best - 1e-9) { best = cost; best_s = s; }
+        }
+    }
+    p.split = best_s;
+    const int ks_max = (nb + p.split - 1) / p.split;
+    const size_t per_blk = xfrag_bytes_per_block(p.NT, B);
+    const size_t fixed = gemv_smem_bytes(p.NT, B, 0);
+    int kc = static_cast<int>(std::max<size_t>(1, (kSmemPerCta - fixed) / per_blk));
+    p.kc = std::min(kc, ks_max);
+    p.smem = gemv_smem_bytes(p.NT, B, p.kc);
+    if (p.split == 1) {
+        const int ctas_per_sm = 2;
+        p.grid_x = std::min(p.tiles, sms * ctas_per_sm);
+    } else {
+        p.grid_x = p.tiles;
+    }
+    return p;
+}
+
+template <int NT, bool ARGMAX>
+static cudaError_t launch_one(const GemvPlan &p, const GemvArgs &a, cudaStream_t stream, bool pdl)
+{
+    auto kern = q4k_gemv_kernel<NT, ARGMAX>;
+    static std::mutex mu;
+    static int smem_set[64] = {0};   // per device: largest dynamic smem size already allowed
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        if (smem_set[dev & 63] < static_cast<int>(p.smem)) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem));
+            if (e != cudaSuccess) return e;
+            smem_set[dev & 63] = static_cast<int>(p.smem);
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.grid_x, p.split, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (p.split > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = p.split;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <bool ARGMAX>
+static cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_t s, bool pdl)
+{
+    switch (p.NT) {
+        case 1: return launch_one<1, ARGMAX>(p, a, s, pdl);
+        case 2: return launch_one<2, ARGMAX>(p, a, s, pdl);
+        case 3: return launch_one<3, ARGMAX>(p, a, s, pdl);
+        default: return launch_one<4, ARGMAX>(p, a, s, pdl);
+    }
+}
+
+static q4k_status validate(const void *W, const void *x, const void *out, int64_t N, int64_t K, int batch,
+                           bool argmax)
+{
+    if (!W || !x || !out) return Q4K_ERR_INVALID_ARG;
+    if (N < 0 || K <= 0 || (K % 256) != 0 || K / 256 >= (1ll << 24)) return Q4K_ERR_INVALID_ARG;
+    if (batch < 1 || batch > Q4K_MAX_BATCH) return Q4K_ERR_INVALID_ARG;
+    if (argmax && (N < 1 || N > 0x7FFFFFFFll)) return Q4K_ERR_INVALID_ARG;
+    if (N > 0x7FFFFFFFll) return Q4K_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W) & 15u) || (reinterpret_cast<uintptr_t>(x) & 15u)) return Q4K_ERR_MISALIGNED;
+    return Q4K_OK;
+}
+
+q4k_status gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream,
+                     const q4k_launch_opts *opts)
+{
+    q4k_status st = validate(W, x, y, N, K, batch, false);
+    if (st != Q4K_OK) return st;
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != Q4K_OK) return st;
+    if (N == 0) return Q4K_OK;
+    const int forced = opts ? opts->split_k : 0;
+    if (forced < 0 || forced > 8) return Q4K_ERR_INVALID_ARG;
+    GemvPlan p = make_plan(N, K, batch, sms, forced);
+    GemvArgs a{};
+    a.W = static_cast<const uint8_t *>(W);
+    a.x = x;
+    a.y = y;
+    a.N = static_cast<int>(N);
+    a.nb = static_cast<int>(K / 256);
+    a.B = batch;
+    a.tiles = p.tiles;
+    a.kc = p.kc;
+    const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
+    cudaError_t e = launch_gemv<false>(p, a, static_cast<cudaStream_t>(stream), pdl);
+    return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
+}
+
+q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *logits, int64_t N, int64_t K,
+                            int batch, void *stream, unsigned long long *scratch_keys, unsigned int *scratch_ticket,
+                            const q4k_launch_opts *opts)
+{
+    q4k_status st = validate(W, x, idx, N, K, batch, true);
+    if (st != Q4K_OK) return st;
+    int sms = 0;
+    st = check_device(&sms);
+    if (st != Q4K_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int forced = opts ? opts->split_k : 0;
+    if (forced < 0 || forced > 8) return Q4K_ERR_INVALID_ARG;
+    GemvPlan p = make_plan(N, K, batch, sms, forced);
+    GemvArgs a{};
+    a.W = static_cast<const uint8_t *>(W);
+    a.x = x;
+    a.y = logits;
+    a.N = static_cast<int>(N);
+    a.nb = static_cast<int>(K / 256);
+    a.B = batch;
+    a.tiles = p.tiles;
+    a.kc = p.kc;
+    a.idx = idx;
+    const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
+    void *buf = nullptr;
+    const size_t bytes = 8 * 16 + 16;
+    if (scratch_keys == nullptr) {
+        if (cudaMallocAsync(&buf, bytes, s) != cudaSuccess) return Q4K_ERR_CUDA;
+        if (cudaMemsetAsync(buf, 0, bytes, s) != cudaSuccess) {
+            cudaFreeAsync(buf, s);
+            return Q4K_ERR_CUDA;
+        }
+        a.keys = static_cast<unsigned long long *>(buf);
+        a.ticket = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(buf) + 8 * 16);
+    } else {
+        a.keys = scratch_keys;
+        a.ticket = scratch_ticket;
+    }
+    cudaError_t e = launch_gemv<true>(p, a, s, pdl && scratch_keys != nullptr);
+    if (buf) {
+        cudaError_t e2 = cudaFreeAsync(buf, s);
+        if (e == cudaSuccess) e = e2;
+    }
+    return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
+}
+
+q4k_status gemv_plan_impl(int64_t N, int64_t K, int batch, int out[4])
+{
+    if (!out || N < 0 || K <= 0 || K % 256 || batch < 1 || batch > Q4K_MAX_BATCH) return Q4K_ERR_INVALID_ARG;
+    int sms = 0;
+    q4k_status st = check_device(&sms);
+    if (st != Q4K_OK) return st;
+    GemvPlan p = make_plan(N, K, batch, sms, 0);
+    out[0] = p.split;
+    out[1] = p.grid_x * p.split;
+    out[2] = kRows;
+    out[3] = p.kc;
+    return Q4K_OK;
+}
+
+unsigned int read_device_error()
+{
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+    return v;
+}
+
+}  // namespace q4k

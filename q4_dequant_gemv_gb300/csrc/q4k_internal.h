@@ -1,0 +1,20 @@
+// q4k_internal.h -- declarations shared by the translation units of the library.
+#pragma once
+#include <cstdint>
+
+#include "../../include/q4k.h"
+
+namespace q4k {
+
+q4k_status check_device(int *sms_out);
+q4k_status gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream,
+                     const q4k_launch_opts *opts);
+// scratch_keys == nullptr: take 8*16 + 16 bytes from the stream-ordered allocator.
+q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *logits, int64_t N, int64_t K,
+                            int batch, void *stream, unsigned long long *scratch_keys, unsigned int *scratch_ticket,
+                            const q4k_launch_opts *opts);
+q4k_status gemv_plan_impl(int64_t N, int64_t K, int batch, int out[4]);
+q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream);
+unsigned int read_device_error();
+
+}  // namespace q4k

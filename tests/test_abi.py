@@ -1,0 +1,110 @@
+"""CPU-side checks of the C ABI: the library builds, loads, exports every
+declared symbol, and rejects bad arguments on the host without launching."""
+import ctypes
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def q4k():
+    from q4_dequant_gemv_gb300 import _build
+    _build.build()
+    import q4_dequant_gemv_gb300 as m
+    m.lib()
+    return m
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "q4k.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(q4k_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_symbols_exported(q4k):
+    names = _declared()
+    assert "q4k_gemv" in names and "q4k_gemv_argmax" in names and "q4k_gemm_prefill" in names
+    L = q4k.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(q4k.EXPORTS)
+
+
+def test_abi_version_and_strings(q4k):
+    assert q4k.lib().q4k_abi_version() == 1
+    for s in range(5):
+        assert len(q4k.status_string(s)) > 0
+    assert q4k.status_string(99) == "unknown status"
+
+
+P = ctypes.c_void_p
+
+
+def _gemv(q4k, W, x, y, N, K, B):
+    return q4k.raw_call("q4k_gemv", P(W), P(x), P(y), N, K, B, P(0))
+
+
+def test_host_validation(q4k):
+    """Argument errors come back before any device call (no GPU needed)."""
+    ok = 0x10000  # aligned fake addresses; never dereferenced on these paths
+    assert _gemv(q4k, 0, ok, ok, 64, 256, 1) == 1
+    assert _gemv(q4k, ok, 0, ok, 64, 256, 1) == 1
+    assert _gemv(q4k, ok, ok, 0, 64, 256, 1) == 1
+    assert _gemv(q4k, ok, ok, ok, 64, 255, 1) == 1
+    assert _gemv(q4k, ok, ok, ok, 64, 0, 1) == 1
+    assert _gemv(q4k, ok, ok, ok, 64, 384, 1) == 1
+    assert _gemv(q4k, ok, ok, ok, -1, 256, 1) == 1
+    assert _gemv(q4k, ok, ok, ok, 64, 256, 0) == 1
+    assert _gemv(q4k, ok, ok, ok, 64, 256, 17) == 1
+    assert _gemv(q4k, ok, ok, ok, 2 ** 31, 256, 1) == 1
+    assert _gemv(q4k, ok + 8, ok, ok, 64, 256, 1) == 2
+    assert _gemv(q4k, ok, ok + 4, ok, 64, 256, 1) == 2
+    am = lambda W, x, i, N, K, B: q4k.raw_call("q4k_gemv_argmax", P(W), P(x), P(i), N, K, B, P(0))
+    assert am(ok, ok, ok, 0, 256, 1) == 1           # argmax of nothing is undefined
+    assert am(ok, ok, 0, 8, 256, 1) == 1
+    assert am(ok, ok, ok, 8, 256, 17) == 1
+    dbg = q4k.raw_call("q4k_gemv_argmax_debug", P(ok), P(ok), P(ok), P(0), 8, 256, 1, P(0))
+    assert dbg == 1
+    pf = lambda W, X, Y, N, K, T: q4k.raw_call("q4k_gemm_prefill", P(W), P(X), P(Y), N, K, T, P(0))
+    assert pf(0, ok, ok, 64, 256, 32) == 1
+    assert pf(ok, ok, ok, 64, 100, 32) == 1
+    assert pf(ok, ok, ok, 64, 256, -1) == 1
+    assert pf(ok, ok + 2, ok, 64, 256, 32) == 2
+
+
+def test_no_device_reports_status(q4k):
+    """A well-formed call on a machine without a usable GPU returns a status, not a crash."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("has a GPU")
+    st = _gemv(q4k, 0x10000, 0x10000, 0x10000, 64, 256, 1)
+    assert st in (3, 4)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without libq4k.so the binding raises; there is no CPU fallback."""
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "import q4_dequant_gemv_gb300 as q\n"
+        "q.LIB_PATH = %r\n"
+        "try:\n    q.lib()\nexcept RuntimeError as e:\n    print('raised', e)\n"
+    ) % (ROOT, str(tmp_path / "nope.so"))
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
+    assert "raised" in out.stdout
+
+
+def test_product_does_not_touch_oracle():
+    """The product package never imports or names the oracle."""
+    pkg = os.path.join(ROOT, "q4_dequant_gemv_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f
+    text = open(os.path.join(ROOT, "include", "q4k.h")).read()
+    assert "oracle" not in text.lower()

@@ -1,0 +1,218 @@
+"""GPU parity of the decode GEMV (batch 1 .. 16) against the fp64 CPU oracle.
+
+Every case draws its inputs from `synth` (seeded), runs the CUDA kernels
+through the C ABI (via the thin binding) and compares element by element with
+the oracle within the stated tolerances."""
+import numpy as np
+import pytest
+
+import synth
+from parity import assert_close
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle
+    import q4_dequant_gemv_gb300 as q4k
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+    return q4k, oracle
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _run(q4k, W, x, **kw):
+    y = q4k.gemv(_dev(W), _dev(x), **kw)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+SMALL = [
+    (1, 256, 1), (7, 256, 1), (33, 512, 1), (64, 768, 2), (100, 1280, 5), (200, 2048, 4),
+    (129, 3584, 1), (65, 3584, 3), (250, 512, 8), (90, 1024, 9), (17, 2560, 16), (300, 4096, 5),
+]
+
+
+@pytest.mark.parametrize("N,K,B", SMALL)
+def test_small_shapes(env, N, K, B):
+    q4k, oracle = env
+    W = synth.q4k_weights(N, K, (N, K, B))
+    x = synth.normal_f32((B, K), (N, K, B, 1))
+    y = _run(q4k, W, x)
+    assert_close(y, oracle.gemv(W, x, N, K), x, K, f"N={N} K={K} B={B}")
+
+
+@pytest.mark.parametrize("split", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("B", [1, 5])
+def test_forced_split(env, split, B):
+    q4k, oracle = env
+    N, K = 150, 2304
+    W = synth.q4k_weights(N, K, (17, split))
+    x = synth.normal_f32((B, K), (18, split))
+    y = _run(q4k, W, x, split_k=split)
+    assert_close(y, oracle.gemv(W, x, N, K), x, K, f"split={split}")
+
+
+def test_split_results_agree(env):
+    """Split-K on/off only re-associates fp32 sums: results agree within tolerance
+    and each configuration is deterministic run to run."""
+    q4k, oracle = env
+    N, K = 256, 3584
+    W = synth.q4k_weights(N, K, 19)
+    x = synth.normal_f32((1, K), 20)
+    ys = {s: _run(q4k, W, x, split_k=s) for s in (1, 2, 7)}
+    ref = oracle.gemv(W, x, N, K)
+    for s, y in ys.items():
+        assert_close(y, ref, x, K, f"split {s}")
+        assert np.array_equal(y, _run(q4k, W, x, split_k=s))
+
+
+def test_config0_4096(env):
+    """4096 x 4096, batch 1 (16 super-blocks per row), every output."""
+    q4k, oracle = env
+    N = K = 4096
+    W = synth.q4k_weights(N, K, (0, 0))
+    x = synth.normal_f32((1, K), (0, 1))
+    assert_close(_run(q4k, W, x), oracle.gemv(W, x, N, K), x, K, "config0")
+
+
+@pytest.mark.parametrize("B", [1, 2, 5, 9])
+def test_qwen_layer0_all_matrices(env, B):
+    """All seven Qwen2.5-7B-shaped matrices of layer 0, every output, batch 1/2/5/9."""
+    q4k, oracle = env
+    for name, N, K, W in synth.qwen_layer_weights(0):
+        x = synth.normal_f32((B, K), (0, 2, B, N, K))
+        assert_close(_run(q4k, W, x), oracle.gemv(W, x, N, K), x, K, f"{name} B={B}")
+
+
+def test_batch_rows_independent(env):
+    """Row b of a batch-5 product matches the batch-1 product of x[b]."""
+    q4k, oracle = env
+    N, K = 320, 3584
+    W = synth.q4k_weights(N, K, 23)
+    x = synth.normal_f32((5, K), 24)
+    y5 = _run(q4k, W, x)
+    ref = oracle.gemv(W, x, N, K)
+    for b in range(5):
+        y1 = _run(q4k, W, x[b:b + 1])
+        assert_close(y1, ref[b:b + 1], x[b:b + 1], K, f"b={b}")
+        assert_close(y5[b:b + 1], ref[b:b + 1], x[b:b + 1], K, f"b={b}")
+
+
+@pytest.mark.parametrize("scale", [1e-30, 1e-6, 1e6, 1e30])
+def test_extreme_activation_scales(env, scale):
+    """Any finite fp32 x works (power-of-two rescaling before the fp16 split)."""
+    q4k, oracle = env
+    N, K = 96, 1024
+    W = synth.q4k_weights(N, K, 25)
+    x = (synth.normal_f32((2, K), 26) * np.float32(scale)).astype(np.float32)
+    assert_close(_run(q4k, W, x), oracle.gemv(W, x, N, K), x, K, f"scale {scale}")
+
+
+def test_mixed_magnitudes_within_row(env):
+    """One huge entry next to normal ones in the same chunk."""
+    q4k, oracle = env
+    N, K = 64, 1024
+    W = synth.q4k_weights(N, K, 27)
+    x = synth.normal_f32((1, K), 28)
+    x[0, 300] = 3.0e4
+    assert_close(_run(q4k, W, x), oracle.gemv(W, x, N, K), x, K, "spike")
+
+
+def test_zero_and_one_hot(env):
+    q4k, oracle = env
+    N, K = 70, 768
+    W = synth.q4k_weights(N, K, 29)
+    y0 = _run(q4k, W, np.zeros((1, K), np.float32))
+    assert np.all(y0 == 0.0)
+    dense = oracle.dequant_matrix(W, N, K)
+    for c in (0, 31, 32, 255, 256, 767):
+        e = np.zeros((1, K), np.float32)
+        e[0, c] = 1.0
+        y = _run(q4k, W, e)[0]
+        np.testing.assert_allclose(y, dense[:, c], rtol=1e-6, atol=1e-7)
+
+
+def test_all_ones_row_sums(env):
+    q4k, oracle = env
+    N, K = 40, 1024
+    W = synth.q4k_weights(N, K, 30)
+    x = np.ones((1, K), np.float32)
+    assert_close(_run(q4k, W, x), oracle.gemv(W, x, N, K), x, K, "ones")
+
+
+def test_output_guards_untouched(env):
+    """Writes stay inside y (sentinels around the output are intact)."""
+    q4k, oracle = env
+    N, K, B = 77, 512, 3
+    W = _dev(synth.q4k_weights(N, K, 31))
+    x = _dev(synth.normal_f32((B, K), 32))
+    buf = torch.full((B * N + 2048,), 12345.0, dtype=torch.float32, device="cuda")
+    y = buf[1024:1024 + B * N].view(B, N)
+    q4k.gemv(W, x, y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:1024] == 12345.0) and torch.all(buf[1024 + B * N:] == 12345.0)
+
+
+def test_n_zero_is_noop(env):
+    q4k, _ = env
+    W = torch.empty((0, 144), dtype=torch.uint8, device="cuda")
+    x = torch.randn(1, 256, device="cuda")
+    y = torch.empty((1, 0), device="cuda")
+    q4k.gemv(W, x, y)
+
+
+def test_pdl_and_streams_bitwise_equal(env):
+    """The PDL launch path and a side stream give bitwise the same result."""
+    q4k, oracle = env
+    N, K = 512, 3584
+    W = _dev(synth.q4k_weights(N, K, 33))
+    x = _dev(synth.normal_f32((1, K), 34))
+    y_ref = q4k.gemv(W, x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        y_pdl = torch.empty_like(y_ref)
+        for _ in range(3):
+            q4k.gemv(W, x, y_pdl, pdl=True)
+    s.synchronize()
+    torch.cuda.synchronize()
+    assert torch.equal(y_ref, y_pdl)
+
+
+def test_graph_capture_replay(env):
+    """A chain of GEMVs captured in a CUDA graph replays to the eager results."""
+    q4k, oracle = env
+    mats = [(synth.q4k_weights(n, k, (35, i)), n, k) for i, (n, k) in enumerate([(512, 3584), (3584, 3584), (256, 1024)])]
+    Ws = [_dev(w) for w, _, _ in mats]
+    xs = [_dev(synth.normal_f32((1, k), (36, i))) for i, (_, _, k) in enumerate(mats)]
+    ys = [torch.empty((1, n), device="cuda") for _, n, _ in mats]
+    for W, x, y in zip(Ws, xs, ys):
+        q4k.gemv(W, x, y)
+    torch.cuda.synchronize()
+    eager = [y.clone() for y in ys]
+    for y in ys:
+        y.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for W, x, y in zip(Ws, xs, ys):
+                q4k.gemv(W, x, y, pdl=True)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, ys):
+        assert torch.equal(a, b)
+
+
+def test_device_error_flags_clear(env):
+    q4k, _ = env
+    torch.cuda.synchronize()
+    assert q4k.device_error_flags() == 0
