@@ -57,6 +57,24 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Largest value over all ranks of the default process group (itself when
+    there is none).  Timing is reported as the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, slowest_seconds: float) -> float:
+    """Units processed by all ranks (weak scaling: each rank does the same
+    work) divided by the slowest rank's time."""
+    return units_per_rank * world / slowest_seconds
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled while timed work runs."""
@@ -220,17 +238,36 @@ def run_ours(args):
     for layer in range(LAYERS):
         lw = synth.qwen_layer_weights(layer)
         Ws.append([torch.from_numpy(W).to(dev) for _, _, _, W in lw])
-    xs_by_layer = []
-    for layer in range(LAYERS):
-        # distinct activations per consumer: q/k/v share one, gate/up share one (as in a decoder layer)
-        xa = synth.normal_f32((16, 3584), (layer, 50))
-        xo = synth.normal_f32((16, 3584), (layer, 51))
-        xm = synth.normal_f32((16, 3584), (layer, 52))
-        xd = synth.normal_f32((16, 18944), (layer, 53))
-        xs_by_layer.append({"attn": torch.from_numpy(xa).to(dev), "o": torch.from_numpy(xo).to(dev),
-                            "mlp": torch.from_numpy(xm).to(dev), "down": torch.from_numpy(xd).to(dev)})
+    # Activations: q/k/v share one input, gate/up share one (as in a decoder
+    # layer); o and down have their own.  All live in one flat buffer per batch
+    # size so that the end-to-end run moves them with a single copy each way.
+    kinds = (("attn", 3584, 50), ("o", 3584, 51), ("mlp", 3584, 52), ("down", 18944, 53))
+    x_elems_per_row = LAYERS * sum(K for _, K, _ in kinds)
+    y_elems_per_row = LAYERS * sum(N for _, N, _ in shapes)
+    x_flat = torch.empty(16 * x_elems_per_row, dtype=torch.float32, device=dev)
+    y_flat = torch.empty(16 * y_elems_per_row, dtype=torch.float32, device=dev)
+
+    kind_base = {}
+    acc = 0
+    for kname, K, _ in kinds:
+        kind_base[kname] = (acc, K)
+        acc += LAYERS * K
+
+    def x_view(B, layer, kind):
+        """[B, K] activations of one (layer, consumer); contiguous, batch-major."""
+        base, K = kind_base[kind]
+        start = B * (base + layer * K)
+        return x_flat[start:start + B * K].view(B, K)
+
+    def y_view(B, layer, mi):
+        base = LAYERS * sum(N for _, N, _ in shapes[:mi])
+        N = shapes[mi][1]
+        start = B * (base + layer * N)
+        return y_flat[start:start + B * N].view(B, N)
+
+    g_x = synth.rng(7, 7)
+    x_flat.copy_(torch.from_numpy(g_x.standard_normal(x_flat.numel(), dtype=np.float32)))
     src = {"q": "attn", "k": "attn", "v": "attn", "o": "o", "gate": "mlp", "up": "mlp", "down": "down"}
-    ys = [[torch.empty((16, N), dtype=torch.float32, device=dev) for _, N, _ in shapes] for _ in range(LAYERS)]
     stream = torch.cuda.Stream(device=dev)
 
     def step_bytes(B):
@@ -239,8 +276,7 @@ def run_ours(args):
     def decode_step(B, pdl=True):
         for layer in range(LAYERS):
             for mi, (name, N, K) in enumerate(shapes):
-                x = xs_by_layer[layer][src[name]][:B]
-                q4k.gemv(Ws[layer][mi], x, ys[layer][mi][:B], stream=stream, pdl=pdl)
+                q4k.gemv(Ws[layer][mi], x_view(B, layer, src[name]), y_view(B, layer, mi), stream=stream, pdl=pdl)
 
     def capture(fn):
         g = torch.cuda.CUDAGraph()
@@ -253,26 +289,23 @@ def run_ours(args):
         return g
 
     def time_graph(g, steps, warmup):
-        for _ in range(warmup):
-            g.replay()
-        stream.synchronize()
-        barrier()
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            g.replay()
-        e1.record(stream)
+        # graph replays go to the current stream: make it the timed stream
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                g.replay()
+            stream.synchronize()
+            barrier()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                g.replay()
+            e1.record(stream)
         e1.synchronize()
         torch.cuda.synchronize()
         barrier()
-        ms = e0.elapsed_time(e1)
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(e0.elapsed_time(e1), device=dev)
         return ms / steps
 
     clocks = ClockSampler(local)
@@ -282,7 +315,7 @@ def run_ours(args):
     g1 = capture(lambda: decode_step(1))
     ms1 = time_graph(g1, args.steps, args.warmup)
     bytes1 = step_bytes(1)
-    value = bytes1 / (ms1 * 1e-3) / 1e9 * world
+    value = whole_job_rate(bytes1, world, ms1 * 1e-3) / 1e9
 
     # ---- VerifyBatch sweep (same weights)
     sweep = {}
@@ -308,6 +341,46 @@ def run_ours(args):
         del g
     del Wlm
 
+    # ---- end to end through the public API with host buffers (batch 1):
+    # one H2D copy of every activation of the step, the graph of 196 q4k_gemv
+    # calls, one D2H copy of every output.
+    nx1, ny1 = x_elems_per_row, y_elems_per_row
+    h_x = torch.empty(nx1, dtype=torch.float32).pin_memory()
+    h_x.copy_(x_flat[:nx1].cpu())
+    h_y = torch.empty(ny1, dtype=torch.float32).pin_memory()
+    h2d, d2h = nx1 * 4, ny1 * 4
+
+    def e2e_step():
+        x_flat[:nx1].copy_(h_x, non_blocking=True)
+        g1.replay()
+        h_y.copy_(y_flat[:ny1], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_step()
+        stream.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        e2e_steps = max(10, args.steps // 4)
+        for _ in range(e2e_steps):
+            e2e_step()
+        stream.synchronize()
+        e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_steps, device=dev)
+    e2e_val = whole_job_rate(bytes1, world, e2e_ms * 1e-3) / 1e9
+
+    # ---- roofline of the dominant kernel (the batch-1 GEMV; the step is only its launches)
+    launches_per_step = LAYERS * len(shapes)
+    achieved = bytes1 / (ms1 * 1e-3) / 1e9
+    tr = recorded_traffic()
+    traffic = None
+    if tr is not None:
+        traffic = tr["dram_bytes_per_weight_byte"] * bytes1 / launches_per_step
+    roof = {"kernel": "q4k_gemv_kernel<1,false>", "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+            "algorithmic_bytes_per_launch": bytes1 / launches_per_step,
+            "avg_launch_us": ms1 * 1e3 / launches_per_step,
+            "peak_source": pk["source"] + " (hbm copy bandwidth)"}
+
     # ---- prefill tiles (Llama-3-8B shapes)
     prefill = {}
     try:
@@ -331,47 +404,6 @@ def run_ours(args):
 
     ck = clocks.stop()
 
-    # ---- end to end through the public API with host buffers (batch 1)
-    h_in = {k: [xs_by_layer[l][k][:1].cpu().pin_memory() for l in range(LAYERS)] for k in ("attn", "o", "mlp", "down")}
-    h_out = [[torch.empty((1, N), dtype=torch.float32).pin_memory() for _, N, _ in shapes] for _ in range(LAYERS)]
-    h2d = sum(t.numel() * 4 for v in h_in.values() for t in v)
-    d2h = sum(t.numel() * 4 for row in h_out for t in row)
-
-    def e2e_step():
-        for k, lst in h_in.items():
-            for l in range(LAYERS):
-                xs_by_layer[l][k][:1].copy_(lst[l], non_blocking=True)
-        g1.replay()
-        for l in range(LAYERS):
-            for mi in range(len(shapes)):
-                h_out[l][mi].copy_(ys[l][mi][:1], non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            e2e_step()
-        stream.synchronize()
-        barrier()
-        t0 = time.perf_counter()
-        e2e_steps = max(10, args.steps // 4)
-        for _ in range(e2e_steps):
-            e2e_step()
-        stream.synchronize()
-        e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    e2e_val = bytes1 / (e2e_ms * 1e-3) / 1e9 * world
-
-    # ---- roofline of the dominant kernel (the batch-1 GEMV; the step is only its launches)
-    launches_per_step = LAYERS * len(shapes)
-    achieved = bytes1 / (ms1 * 1e-3) / 1e9
-    tr = recorded_traffic()
-    traffic = None
-    if tr is not None:
-        traffic = tr["dram_bytes_per_weight_byte"] * bytes1 / launches_per_step
-    roof = {"kernel": "q4k_gemv_kernel<1,false>", "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
-            "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-            "algorithmic_bytes_per_launch": bytes1 / launches_per_step,
-            "avg_launch_us": ms1 * 1e3 / launches_per_step,
-            "peak_source": pk["source"] + " (hbm copy bandwidth)"}
-
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms1, "higher_is_better": True, "scaling": "weak",
@@ -390,7 +422,7 @@ def run_ours(args):
         "prefill": prefill,
         "roofline": roof,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "path": "pinned host x -> H2D, graph of 196 q4k_gemv calls, D2H of all y"},
+                "ms_per_step": e2e_ms, "path": "one pinned H2D of all step activations, graph of 196 q4k_gemv calls, one D2H of all outputs"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": ck,
         "peaks": pk,
@@ -403,6 +435,38 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_profile_case(spec: str, iters: int):
+    """One op repeated `iters` times on seeded inputs, for ncu captures.
+    spec = gemv:N:K:B | argmax:N:K:B | prefill:N:K:T"""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    import q4_dequant_gemv_gb300 as q4k
+    import synth
+    __graft_entry__.build()
+    kind, N, K, B = spec.split(":")
+    N, K, B = int(N), int(K), int(B)
+    W = torch.from_numpy(synth.q4k_weights(N, K, (9, N, K))).cuda()
+    if kind == "prefill":
+        X = torch.from_numpy(synth.normal_bf16_bits((B, K), (9, B)).view(np.int16)).cuda().view(torch.bfloat16)
+        Y = torch.empty((B, N), dtype=torch.float32, device="cuda")
+        for _ in range(iters):
+            q4k.gemm_prefill(W, X, Y)
+    else:
+        x = torch.from_numpy(synth.normal_f32((B, K), (9, B))).cuda()
+        if kind == "gemv":
+            y = torch.empty((B, N), dtype=torch.float32, device="cuda")
+            for _ in range(iters):
+                q4k.gemv(W, x, y)
+        else:
+            idx = torch.empty(B, dtype=torch.int32, device="cuda")
+            for _ in range(iters):
+                q4k.gemv_argmax(W, x, idx)
+    torch.cuda.synchronize()
+    print(f"profile case {spec} x{iters} done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,7 +474,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--profile-case", default=None, help="gemv:N:K:B | argmax:N:K:B | prefill:N:K:T (ncu helper)")
+    ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
+    if args.profile_case:
+        run_profile_case(args.profile_case, args.iters)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

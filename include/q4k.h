@@ -87,8 +87,8 @@ int q4k_abi_version(void);
  *   W     uint8  [N][K/256*144]  Q4_K rows (layout above), 16-byte aligned
  *   x     fp32   [batch][K]      row-major, 16-byte aligned
  *   y     fp32   [batch][N]      row-major
- *   N >= 0 (N == 0 is a no-op), K a positive multiple of 256, K/256 < 2^24,
- *   1 <= batch <= 16.
+ *   N >= 0 (N == 0 is a no-op and W, y may then be NULL), K a positive multiple
+ *   of 256, K/256 < 2^24, 1 <= batch <= 16.
  * Accumulation is fp32.  Each weight super-block is read from memory once for
  * all batch rows.  x may hold any finite fp32 values.
  * Errors: INVALID_ARG (null pointer, N < 0, K <= 0 or K % 256 != 0, batch out
@@ -126,8 +126,8 @@ q4k_status q4k_gemv_argmax_debug(const void *W, const float *x, int32_t *idx, fl
  *   Y  fp32 [T][N] row-major
  * The weights are dequantized to bf16 (round to nearest even) in shared memory
  * and multiplied on the tcgen05 tensor cores with fp32 accumulation in tensor
- * memory.  Any T >= 0 is accepted (T == 0 or N == 0 is a no-op); the tensor
- * path is built for T >= 32.
+ * memory.  Any T >= 0 is accepted (T == 0 or N == 0 is a no-op, and the
+ * pointers may then be NULL); the tensor path is built for T >= 32.
  * Errors: INVALID_ARG, MISALIGNED (W or X), UNSUPPORTED_DEVICE, CUDA.
  */
 q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t N, int64_t K,
@@ -161,8 +161,9 @@ q4k_status q4k_gemv_ex(const void *W, const float *x, float *y, int64_t N, int64
 q4k_status q4k_gemv_plan(int64_t N, int64_t K, int batch, int out[4]);
 
 /* Sticky device-side error bits of the library's kernels, read synchronously
- * from the current device: bit 0 = a bounded wait inside a kernel timed out and
- * the kernel wound down early (its outputs are then invalid).  0 = no error. */
+ * from the current device: bit 0 = a bounded wait inside a GEMV/argmax kernel
+ * timed out, bit 1 = the same in the prefill kernel; the kernel then wound down
+ * early and its outputs are invalid.  0 = no error. */
 unsigned int q4k_device_error_flags(void);
 
 #ifdef __cplusplus

@@ -672,7 +672,8 @@ static cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_
 static q4k_status validate(const void *W, const void *x, const void *out, int64_t N, int64_t K, int batch,
                            bool argmax)
 {
-    if (!W || !x || !out) return Q4K_ERR_INVALID_ARG;
+    if (!x) return Q4K_ERR_INVALID_ARG;
+    if ((!W || !out) && !(N == 0 && !argmax)) return Q4K_ERR_INVALID_ARG;   // N == 0: W, y are never touched
     if (N < 0 || K <= 0 || (K % 256) != 0 || K / 256 >= (1ll << 24)) return Q4K_ERR_INVALID_ARG;
     if (batch < 1 || batch > Q4K_MAX_BATCH) return Q4K_ERR_INVALID_ARG;
     if (argmax && (N < 1 || N > 0x7FFFFFFFll)) return Q4K_ERR_INVALID_ARG;

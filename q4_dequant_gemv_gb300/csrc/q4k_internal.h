@@ -16,5 +16,6 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
 q4k_status gemv_plan_impl(int64_t N, int64_t K, int batch, int out[4]);
 q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream);
 unsigned int read_device_error();
+unsigned int read_prefill_error();
 
 }  // namespace q4k

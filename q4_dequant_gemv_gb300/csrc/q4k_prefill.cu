@@ -1,28 +1,436 @@
-// q4k_prefill.cu -- prefill entry point (the tcgen05 kernel follows in this file).
-#include <cstdint>
+// q4k_prefill.cu -- Q4_K prefill GEMM on the GB300 tcgen05 tensor cores.
+//
+// Y[t][n] = sum_k w[n][k] X[t][k] for a block of T prompt tokens: the dense
+// contraction that the dotLLM README's CUDA backend sends to "cuBLAS HGEMM for
+// prefill" after "on-the-fly weight dequantization" (News 2026-03).  Here the
+// weights are dequantized straight into shared memory as bf16 and multiplied
+// by hand-issued tcgen05.mma instructions, fp32 accumulation in tensor memory.
+//
+// CTA tile: 128 weight rows (the MMA M side) x TN*NTT tokens (the N side),
+// full K.  Per 64-wide K chunk (a quarter of a super-block):
+//   * warps 0-3 (one thread per weight row) read the row's sub-block pair from
+//     global memory, compute w = d*sc*q - dmin*m in fp32, round to bf16 (RNE)
+//     and store the 128-byte row in the 128-byte-swizzled K-major layout;
+//   * warp 4 loads the X tile [TN x 64] with a TMA tensor copy (128B swizzle);
+//   * warp 5 (one elected thread) issues 4 x NTT tcgen05.mma (K = 16 each)
+//     into the TMEM accumulators and commits to the stage's "empty" barrier.
+// A ring of NS stages overlaps the three.  The epilogue reads TMEM with
+// tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = weight rows) and writes Y
+// with coalesced stores.  Every mbarrier wait is bounded in time.
 
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "ptx.cuh"
 #include "q4k_internal.h"
 
 namespace q4k {
 
+__device__ unsigned int g_prefill_error = 0;   // bit 1: a bounded wait in the prefill kernel timed out
+
+unsigned int read_prefill_error()
+{
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_prefill_error, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+    return v;
+}
+
+namespace pf {
+
+constexpr int kRowsM = 128;          // MMA M
+constexpr int kChunk = 64;           // K elements per stage (one 128-byte swizzle row)
+constexpr int kThreads = 192;        // 4 dequant/epilogue warps + TMA warp + MMA warp
+constexpr int kAStageBytes = kRowsM * kChunk * 2;   // 16 KB
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms of
+// 1024 bytes (stride byte offset 1024), descriptor version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1) << 16;                 // leading byte offset (unused for this layout)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;         // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;                 // version
+    d |= static_cast<uint64_t>(2) << 61;                 // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+{
+    return (1u << 4)                                   // D format f32
+           | (1u << 7)                                 // A format bf16
+           | (1u << 10)                                // B format bf16
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+template <int TN, int NTT>
+struct Cfg {
+    static constexpr int kBBytes = TN * kChunk * 2;                       // one token subtile
+    static constexpr int kStageBytes = kAStageBytes + NTT * kBBytes;
+    static constexpr int kStages = (NTT * TN >= 512) ? 2 : 4;
+    static constexpr int kTmemCols = TN * NTT;                            // 32..512, power of two
+    static constexpr size_t kSmem = static_cast<size_t>(kStages) * kStageBytes + 1024 /*align*/ + 256;
+};
+
+template <int TN, int NTT>
+__global__ void __launch_bounds__(kThreads, 1)
+    q4k_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t *__restrict__ W, float *__restrict__ Y,
+                       int N, int K, int T)
+{
+    using C = Cfg<TN, NTT>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full_a[C::kStages], full_b[C::kStages], empty[C::kStages], done_bar;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int row0 = blockIdx.x * kRowsM;
+    const int t0 = blockIdx.y * TN * NTT;
+    const int nsub = min(NTT, (T - t0 + TN - 1) / TN);
+    const int nchunks = K / kChunk;
+    const size_t row_bytes = static_cast<size_t>(K / 256) * 144;
+
+    if (tid == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(&full_a[s]), 128);
+            mbar_init(smem_u32(&full_b[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(&done_bar), 1);
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(&tmem_base_s), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) prefetch_tmap(&tmX);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    if (warp < 4) {
+        // ------------------------------------------------ dequant producers
+        const int r = tid;                    // tile row 0..127
+        const int n = row0 + r;
+        const bool live = n < N;
+        const uint8_t *wrow = W + static_cast<size_t>(live ? n : 0) * row_bytes;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            const int blk = c >> 2, p = c & 3;
+            uint4 hdr = make_uint4(0, 0, 0, 0), qa = hdr, qb = hdr;
+            if (live) {
+                const uint8_t *bp = wrow + static_cast<size_t>(blk) * 144;
+                hdr = __ldg(reinterpret_cast<const uint4 *>(bp));
+                qa = __ldg(reinterpret_cast<const uint4 *>(bp + 16 + 32 * p));
+                qb = __ldg(reinterpret_cast<const uint4 *>(bp + 32 + 32 * p));
+            }
+            if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
+                atomicOr(&g_prefill_error, 2u);
+                s_abort = 1;
+            }
+            // scales of sub-blocks 2p (low nibbles) and 2p+1 (high nibbles)
+            const float d = half_lo_f32(hdr.x), dmin = half_hi_f32(hdr.x);
+            const uint32_t s0 = hdr.y, s1 = hdr.z, s2 = hdr.w;
+            auto byte_of = [](uint32_t w, int i) { return (w >> (8 * i)) & 0xFFu; };
+            int scE, mE, scO, mO;
+            {
+                const int j0 = 2 * p, j1 = 2 * p + 1;
+                auto sc_of = [&](int j) {
+                    return j < 4 ? static_cast<int>(byte_of(s0, j) & 63u)
+                                 : static_cast<int>((byte_of(s2, j - 4) & 15u) | ((byte_of(s0, j - 4) >> 6) << 4));
+                };
+                auto m_of = [&](int j) {
+                    return j < 4 ? static_cast<int>(byte_of(s1, j) & 63u)
+                                 : static_cast<int>((byte_of(s2, j - 4) >> 4) | ((byte_of(s1, j - 4) >> 6) << 4));
+                };
+                scE = sc_of(j0); mE = m_of(j0); scO = sc_of(j1); mO = m_of(j1);
+            }
+            const float dsE = d * static_cast<float>(scE), dmE = dmin * static_cast<float>(mE);
+            const float dsO16 = d * static_cast<float>(scO) * 0.0625f, dmO = dmin * static_cast<float>(mO);
+            const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+            uint8_t *arow = smem + stage * C::kStageBytes + r * 128;
+            const uint32_t k1024 = 0x64006400u;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {           // 0: low nibbles (k 0..31), 1: high (k 32..63)
+#pragma unroll
+                for (int c8 = 0; c8 < 4; ++c8) {             // 16-byte chunk: k = 32*half + 8*c8 .. +7
+                    uint32_t out[4];
+#pragma unroll
+                    for (int uu = 0; uu < 2; ++uu) {         // word u = 2*c8 + uu -> k offset 4u..4u+3
+                        const uint32_t w = words[2 * c8 + uu];
+                        const uint32_t mask = half ? 0x00F000F0u : 0x000F000Fu;
+                        // {q(4u), q(4u+2)} and {q(4u+1), q(4u+3)} (x16 for the high nibbles)
+                        const uint32_t h02 = hsub2_u32(and_or(w, mask, k1024), k1024);
+                        const uint32_t h13 = hsub2_u32(and_or(w >> 8, mask, k1024), k1024);
+                        const float ds = half ? dsO16 : dsE;
+                        const float dm = half ? dmO : dmE;
+                        const float w0 = fmaf(half_lo_f32(h02), ds, -dm);
+                        const float w2 = fmaf(half_hi_f32(h02), ds, -dm);
+                        const float w1 = fmaf(half_lo_f32(h13), ds, -dm);
+                        const float w3 = fmaf(half_hi_f32(h13), ds, -dm);
+                        out[2 * uu] = pack_bf16x2(w0, w1);
+                        out[2 * uu + 1] = pack_bf16x2(w2, w3);
+                    }
+                    const int chunk = 4 * half + c8;
+                    uint4 v = live ? make_uint4(out[0], out[1], out[2], out[3]) : make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) = v;
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&full_a[stage]));
+            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        }
+    } else if (warp == 4) {
+        // ------------------------------------------------ X tiles by TMA
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            const uint32_t bytes = static_cast<uint32_t>(nsub * C::kBBytes);
+            for (int c = 0; c < nchunks; ++c) {
+                if (!*(volatile int *)&s_abort &&
+                    !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
+                    atomicOr(&g_prefill_error, 2u);
+                    s_abort = 1;
+                }
+                if (!*(volatile int *)&s_abort) {
+                    mbar_arrive_expect_tx(smem_u32(&full_b[stage]), bytes);
+                    uint8_t *bbase = smem + stage * C::kStageBytes + kAStageBytes;
+                    for (int j = 0; j < nsub; ++j)
+                        tma_load_2d(smem_u32(bbase + j * C::kBBytes), &tmX, c * kChunk, t0 + j * TN,
+                                    smem_u32(&full_b[stage]));
+                    ++issued;
+                }
+                if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+            }
+            // After an abort, wait (bounded) for the copies still in flight so
+            // none lands after the CTA has exited.
+            if (*(volatile int *)&s_abort) {
+                for (int i = max(0, issued - C::kStages); i < issued; ++i)
+                    if (!mbar_wait_bounded(smem_u32(&full_b[i % C::kStages]), static_cast<uint32_t>((i / C::kStages) & 1),
+                                           kWaitLimitNs))
+                        break;
+            }
+        }
+    } else {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            constexpr uint32_t idesc = idesc_bf16(kRowsM, TN);
+            for (int c = 0; c < nchunks; ++c) {
+                bool ok = !*(volatile int *)&s_abort;
+                if (ok && !mbar_wait_bounded(smem_u32(&full_a[stage]), phase, kWaitLimitNs)) ok = false;
+                if (ok && !mbar_wait_bounded(smem_u32(&full_b[stage]), phase, kWaitLimitNs)) ok = false;
+                if (!ok && !*(volatile int *)&s_abort) {
+                    atomicOr(&g_prefill_error, 2u);
+                    s_abort = 1;
+                }
+                tc_fence_after();
+                if (ok) {
+                    const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
+                    const uint32_t b_addr = a_addr + kAStageBytes;
+#pragma unroll
+                    for (int j = 0; j < NTT; ++j) {
+                        if (j < nsub) {
+#pragma unroll
+                            for (int kk = 0; kk < kChunk / 16; ++kk) {
+                                const uint64_t ad = sw128_desc(a_addr + kk * 32);
+                                const uint64_t bd = sw128_desc(b_addr + j * C::kBBytes + kk * 32);
+                                umma_bf16(tmem + j * TN, ad, bd, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                    }
+                }
+                umma_commit(smem_u32(&empty[stage]));   // frees the stage once these MMAs finish
+                if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+            }
+            umma_commit(smem_u32(&done_bar));
+        }
+    }
+
+    // ---------------------------------------------------- epilogue (warps 0-3)
+    if (warp < 4) {
+        const bool ok = mbar_wait_bounded(smem_u32(&done_bar), 0u, kWaitLimitNs);
+        if (!ok) {
+            atomicOr(&g_prefill_error, 2u);
+            s_abort = 1;
+        }
+        tc_fence_after();
+        const int n = row0 + warp * 32 + lane;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        for (int j = 0; j < nsub; ++j) {
+#pragma unroll 1
+            for (int c0 = 0; c0 < TN; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld16(lane_addr + j * TN + c0, v);
+                tmem_wait_ld();
+                if (ok && n < N) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const int t = t0 + j * TN + c0 + i;
+                        if (t < T) Y[static_cast<size_t>(t) * N + n] = __uint_as_float(v[i]);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+}  // namespace pf
+
+// ------------------------------------------------------------------ host
 static q4k_status validate_prefill(const void *W, const void *X, const float *Y, int64_t N, int64_t K, int64_t T)
 {
-    if (!W || !X || !Y) return Q4K_ERR_INVALID_ARG;
+    const bool empty = (N == 0 || T == 0);       // nothing is read or written
+    if (!empty && (!W || !X || !Y)) return Q4K_ERR_INVALID_ARG;
     if (N < 0 || N > 0x7FFFFFFFll || T < 0 || T > 0x7FFFFFFFll) return Q4K_ERR_INVALID_ARG;
     if (K <= 0 || (K % 256) != 0 || K / 256 >= (1ll << 24)) return Q4K_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(W) & 15u) || (reinterpret_cast<uintptr_t>(X) & 15u)) return Q4K_ERR_MISALIGNED;
     return Q4K_OK;
 }
 
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+template <int TN, int NTT>
+static cudaError_t launch_prefill(const uint8_t *W, const void *X, float *Y, int N, int K, int T, cudaStream_t s)
+{
+    using C = pf::Cfg<TN, NTT>;
+    auto enc = get_encode();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap map;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(T)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(pf::kChunk), static_cast<cuuint32_t>(TN)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(X), gdim, gstride, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    auto kern = pf::q4k_prefill_kernel<TN, NTT>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&]() {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    dim3 grid((N + pf::kRowsM - 1) / pf::kRowsM, (T + TN * NTT - 1) / (TN * NTT), 1);
+    kern<<<grid, pf::kThreads, C::kSmem, s>>>(map, W, Y, N, K, T);
+    return cudaGetLastError();
+}
+
 q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream)
 {
-    (void)stream;
     q4k_status st = validate_prefill(W, X, Y, N, K, T);
     if (st != Q4K_OK) return st;
     st = check_device(nullptr);
     if (st != Q4K_OK) return st;
     if (N == 0 || T == 0) return Q4K_OK;
-    return Q4K_ERR_UNSUPPORTED_DEVICE;  // tensor-core kernel not wired yet
+    const auto *Wb = static_cast<const uint8_t *>(W);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int n = static_cast<int>(N), k = static_cast<int>(K), t = static_cast<int>(T);
+    cudaError_t e;
+    if (T <= 32) e = launch_prefill<32, 1>(Wb, X, Y, n, k, t, s);
+    else if (T <= 64) e = launch_prefill<64, 1>(Wb, X, Y, n, k, t, s);
+    else if (T <= 128) e = launch_prefill<128, 1>(Wb, X, Y, n, k, t, s);
+    else if (T <= 256) e = launch_prefill<256, 1>(Wb, X, Y, n, k, t, s);
+    else e = launch_prefill<256, 2>(Wb, X, Y, n, k, t, s);
+    return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
 }  // namespace q4k

@@ -1,0 +1,96 @@
+"""GPU parity of the tcgen05 prefill GEMM against the fp64 CPU oracle.
+
+The kernel rounds every weight to bf16 before the tensor-core product, so its
+error budget is the weight rounding (<= 2^-9 relative per term) plus fp32
+accumulation; the decode tolerances still bound it.  A second check compares
+against the oracle's bf16-weight diagnostic, which isolates the accumulation
+error and is much tighter."""
+import numpy as np
+import pytest
+
+import synth
+from parity import assert_close
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env():
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle
+    import q4_dequant_gemv_gb300 as q4k
+    torch.cuda.set_device(0)
+    return q4k, oracle
+
+
+def _run(q4k, W, X_bits):
+    Wd = torch.from_numpy(np.ascontiguousarray(W)).cuda()
+    Xd = torch.from_numpy(np.ascontiguousarray(X_bits).view(np.int16)).cuda().view(torch.bfloat16)
+    Y = q4k.gemm_prefill(Wd, Xd)
+    torch.cuda.synchronize()
+    return Y.cpu().numpy()
+
+
+def _check(q4k, oracle, N, K, T, seed, what):
+    W = synth.q4k_weights(N, K, (seed, 1))
+    X = synth.normal_bf16_bits((T, K), (seed, 2))
+    Y = _run(q4k, W, X)
+    Xf = synth.bf16_bits_to_f32(X)
+    ref = oracle.prefill(W, X, N, K)
+    assert_close(Y, ref, Xf, K, what)
+    # against the bf16-weight diagnostic: only fp32 accumulation error remains
+    ref_r = oracle.prefill(W, X, N, K, round_w=True)
+    bound = 1e-5 * (np.abs(Xf).astype(np.float64) @ np.abs(oracle.dequant_matrix(W, N, K)).T) + 1e-6
+    assert np.all(np.abs(Y - ref_r) <= bound * 4), f"{what}: beyond fp32 accumulation error"
+    return Y
+
+
+@pytest.mark.parametrize("N,K,T", [(128, 256, 32), (128, 512, 32), (256, 1024, 32), (200, 768, 33),
+                                   (130, 512, 1), (64, 256, 7), (384, 1024, 64), (256, 512, 128),
+                                   (128, 1024, 256), (256, 512, 300), (128, 768, 512), (100, 256, 600)])
+def test_prefill_shapes(env, N, K, T):
+    q4k, oracle = env
+    _check(q4k, oracle, N, K, T, N * 7 + K + T, f"N={N} K={K} T={T}")
+
+
+@pytest.mark.parametrize("T", [32, 512])
+def test_llama_shapes_sampled(env, T):
+    """Llama-3-8B-shaped matrices at full size; every output of a row sample is checked."""
+    q4k, oracle = env
+    for name, N, K in synth.llama3_8b_prefill_shapes():
+        W = synth.q4k_weights(N, K, (4, N, K))
+        X = synth.normal_bf16_bits((T, K), (4, T, K))
+        Y = _run(q4k, W, X)
+        g = np.random.default_rng(N + K + T)
+        rows = np.unique(np.concatenate([g.integers(0, N, 48), [0, N - 1, 127, 128]]))
+        Xf = synth.bf16_bits_to_f32(X)
+        ref = oracle.prefill(W[rows], X, rows.size, K)
+        assert_close(Y[:, rows], ref, Xf, K, f"{name} T={T}")
+
+
+def test_prefill_matches_gemv_within_tolerance(env):
+    """Prefill with T rows equals T decode GEMVs of the same (bf16-valued) activations."""
+    q4k, oracle = env
+    N, K, T = 256, 2048, 32
+    W = synth.q4k_weights(N, K, 61)
+    X = synth.normal_bf16_bits((T, K), 62)
+    Y = _run(q4k, W, X)
+    Xf = synth.bf16_bits_to_f32(X)
+    Wd = torch.from_numpy(W).cuda()
+    yg = q4k.gemv(Wd, torch.from_numpy(Xf[:16].copy()).cuda()).cpu().numpy()
+    assert_close(Y[:16], yg.astype(np.float64), Xf[:16], K, "prefill vs gemv")
+
+
+def test_prefill_guards_and_errors(env):
+    q4k, _ = env
+    N, K, T = 130, 512, 40
+    W = torch.from_numpy(synth.q4k_weights(N, K, 63)).cuda()
+    X = torch.from_numpy(synth.normal_bf16_bits((T, K), 64).view(np.int16)).cuda().view(torch.bfloat16)
+    buf = torch.full((T * N + 4096,), -777.0, device="cuda")
+    Y = buf[2048:2048 + T * N].view(T, N)
+    q4k.gemm_prefill(W, X, Y)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:2048] == -777.0) and torch.all(buf[2048 + T * N:] == -777.0)
+    assert q4k.device_error_flags() == 0
