@@ -104,9 +104,9 @@ q4k_status q4k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t 
  * leave the device: the only output is batch int32 values.
  *   idx   int32 [batch]
  *   1 <= N <= 2^31 - 1; other arguments as for q4k_gemv.
- * Scratch: 8*batch + 4 bytes taken from the stream-ordered allocator
- * (cudaMallocAsync / cudaFreeAsync on `stream`), so concurrent calls on
- * different streams are independent.
+ * Scratch: 144 bytes taken from the stream-ordered allocator (cudaMallocAsync,
+ * cleared with cudaMemsetAsync, released with cudaFreeAsync, all on `stream`),
+ * so concurrent calls on different streams are independent.
  */
 q4k_status q4k_gemv_argmax(const void *W, const float *x, int32_t *idx, int64_t N, int64_t K,
                            int batch, void *stream);

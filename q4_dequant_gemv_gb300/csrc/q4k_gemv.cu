@@ -38,8 +38,10 @@
 //     memory and combines CTAs with one 64-bit atomicMax per batch row plus a
 //     last-CTA ticket (no spin-waits).
 
-#include <cuda_runtime.h>
+#include <cuda.h>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstdint>
@@ -54,21 +56,19 @@
 namespace q4k {
 
 constexpr int kBlockBytes = 144;
-constexpr int kWarps = 4;                 // consumer warps per CTA
-constexpr int kRows = 16 * kWarps;        // rows per tile
+constexpr int kWarps = 8;                 // consumer warps per CTA
+constexpr int kRows = 16 * kWarps;        // rows per tile (128)
 constexpr int kThreads = 32 * (kWarps + 1);
 constexpr int kKsteps = 17;               // 16 k16 steps + 1 min-term step per super-block
-constexpr int kStages = 3;                // W ring depth
-constexpr int kStageBlocks = 2;           // super-blocks per row per stage
-constexpr int kRowStride = kStageBlocks * kBlockBytes + 16;   // padded (bank spread)
-constexpr int kStageBytes = kRows * kRowStride;
-constexpr size_t kSmemPerCta = 112 * 1024;   // two CTAs per SM
-constexpr uint64_t kWaitLimitNs = 2000000000ull;               // 2 s
+constexpr int kStages = 4;                // W ring depth
+constexpr int kStageBytes = kRows * kBlockBytes;   // one super-block of every tile row (18 KB)
+constexpr size_t kSmemPerCta2 = 110 * 1024;        // two CTAs per SM (batch <= 8)
+constexpr size_t kSmemPerCta1 = 200 * 1024;        // one CTA per SM (batch > 8)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
 __device__ unsigned int g_device_error = 0;   // bit 0: an mbarrier wait timed out
 
 struct GemvArgs {
-    const uint8_t *W;
     const float *x;
     float *y;            // may be null in the argmax variant (logits not wanted)
     int N;
@@ -88,16 +88,15 @@ __host__ __device__ inline size_t xfrag_bytes_per_block(int NT, int B)
     return static_cast<size_t>(kKsteps) * NT * frag_lanes(NT, B) * 8;
 }
 
+// Dynamic shared memory: [ring | x fragments | partial sums (split-K)].
+__host__ __device__ inline size_t xfrag_offset() { return static_cast<size_t>(kStages) * kStageBytes; }
+__host__ __device__ inline size_t red_offset(int NT, int B, int kc)
+{
+    return xfrag_offset() + ((xfrag_bytes_per_block(NT, B) * kc + 15) & ~size_t(15));
+}
 __host__ inline size_t gemv_smem_bytes(int NT, int B, int kc)
 {
-    size_t s = 0;
-    s += static_cast<size_t>(kStages) * kStageBytes;             // W ring
-    s += xfrag_bytes_per_block(NT, B) * kc;                      // x fragments
-    s += 2 * kStages * 8;                                        // mbarriers
-    s += 16 * 4 * 3;                                             // scale / unscale / amax per batch row
-    s += 16 * 8;                                                 // argmax keys
-    s += static_cast<size_t>(kRows) * 16 * 4;                    // split-K partials
-    return s + 256;                                              // alignment slack
+    return red_offset(NT, B, kc) + static_cast<size_t>(kRows) * 16 * 4;
 }
 
 // ---------------------------------------------------------------------------
@@ -233,28 +232,26 @@ __device__ __forceinline__ RowConsts decode_header(uint4 h, int t)
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.  Warps 0..3 consume (16 rows each), warp 4 produces.
+// The kernel.  Warps 0..7 consume (16 rows each), warp 8 produces.
 // grid = (row-tile CTAs, split) with cluster dims (1, split, 1) when split > 1.
+// W is read through a 2-D TMA tensor map: [N rows] x [K/256 * 18] 8-byte
+// words; one stage = one super-block of all 128 tile rows (rows beyond N are
+// zero-filled by the TMA unit).
 // ---------------------------------------------------------------------------
 template <int NT, bool ARGMAX>
-__global__ void __launch_bounds__(kThreads, 2) q4k_gemv_kernel(const GemvArgs args)
+__global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
+    q4k_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs args)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    uint8_t *ring = smem;
+    uint8_t *ring = smem_raw;
     const int B = args.B;
     const int LW = frag_lanes(NT, B);
-    uint2 *xf = reinterpret_cast<uint2 *>(ring + kStages * kStageBytes);
-    uint8_t *after_xf = reinterpret_cast<uint8_t *>(xf) + xfrag_bytes_per_block(NT, B) * args.kc;
-    uint64_t *bars = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(after_xf) + 7) & ~uintptr_t(7));
-    uint64_t *full = bars;
-    uint64_t *empty = bars + kStages;
-    float *s_scale = reinterpret_cast<float *>(bars + 2 * kStages);
-    float *s_unscale = s_scale + 16;
-    uint32_t *s_amax = reinterpret_cast<uint32_t *>(s_unscale + 16);
-    unsigned long long *s_best = reinterpret_cast<unsigned long long *>(
-        (reinterpret_cast<uintptr_t>(s_amax + 16) + 7) & ~uintptr_t(7));
-    float *s_red = reinterpret_cast<float *>(s_best + 16);
+    uint2 *xf = reinterpret_cast<uint2 *>(smem_raw + xfrag_offset());
+    float *s_red = reinterpret_cast<float *>(smem_raw + red_offset(NT, B, args.kc));
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
+    __shared__ float s_scale[16], s_unscale[16];
+    __shared__ uint32_t s_amax[16];
+    __shared__ unsigned long long s_best[16];
     __shared__ int s_abort;
     __shared__ int s_issued;
     __shared__ int s_cons[kWarps];
@@ -268,8 +265,6 @@ __global__ void __launch_bounds__(kThreads, 2) q4k_gemv_kernel(const GemvArgs ar
     const int kb_begin = static_cast<int>((static_cast<long long>(rank) * nb) / split);
     const int kb_end = static_cast<int>((static_cast<long long>(rank + 1) * nb) / split);
     const int ks = kb_end - kb_begin;
-    const int nstage_per_tile = (ks + kStageBlocks - 1) / kStageBlocks;
-    const size_t row_bytes = static_cast<size_t>(nb) * kBlockBytes;
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -282,62 +277,54 @@ __global__ void __launch_bounds__(kThreads, 2) q4k_gemv_kernel(const GemvArgs ar
         fence_barrier_init();
     }
     if (ARGMAX && tid < 16) s_best[tid] = 0ull;
+    if (warp == kWarps && lane == 0) prefetch_tensormap(&tmW);
     __syncthreads();
 
     pdl_launch_dependents();
 
     if (warp == kWarps) {
         // ------------------------------------------------------------ producer
-        const uint64_t policy = l2_policy_evict_first();
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued = 0;
-        for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
-            const int row0 = tile * kRows;
-            const int rows = min(kRows, args.N - row0);
-            for (int st = 0; st < nstage_per_tile; ++st) {
-                const int kb = kb_begin + st * kStageBlocks;
-                const int nblk = min(kStageBlocks, kb_end - kb);
-                // After an abort the producer keeps walking the schedule without
-                // waiting or copying, so nothing ever blocks on it.
-                if (!*(volatile int *)&s_abort &&
-                    !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
-                    atomicOr(&g_device_error, 1u);
-                    s_abort = 1;
-                }
-                if (*(volatile int *)&s_abort) {
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
+                    // After an abort the producer keeps walking the schedule
+                    // without waiting or copying, so nothing ever blocks on it.
+                    if (!*(volatile int *)&s_abort &&
+                        !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
+                        atomicOr(&g_device_error, 1u);
+                        s_abort = 1;
+                    }
+                    if (!*(volatile int *)&s_abort) {
+                        mbar_arrive_expect_tx(smem_u32(&full[stage]), kStageBytes);
+                        tma_load_2d_hint(smem_u32(ring + stage * kStageBytes), &tmW, kb * (kBlockBytes / 8),
+                                         tile * kRows, smem_u32(&full[stage]), policy);
+                        ++issued;
+                    }
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                    continue;
                 }
-                const uint32_t bytes = static_cast<uint32_t>(rows * nblk * kBlockBytes);
-                if (lane == 0) mbar_arrive_expect_tx(smem_u32(&full[stage]), bytes);
-                __syncwarp();
-                for (int r = lane; r < rows; r += 32) {
-                    const uint8_t *src = args.W + static_cast<size_t>(row0 + r) * row_bytes +
-                                         static_cast<size_t>(kb) * kBlockBytes;
-                    bulk_g2s(smem_u32(ring + stage * kStageBytes + r * kRowStride), src,
-                             static_cast<uint32_t>(nblk * kBlockBytes), smem_u32(&full[stage]), policy);
-                }
-                ++issued;
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
+            s_issued = issued;
         }
-        if (lane == 0) s_issued = issued;
     } else {
         // ------------------------------------------------------------ consumers
         const int g = lane >> 2;
         const int t = lane & 3;
-        const int ctid = tid;                   // 0..127
         pdl_wait();                             // x may come from the previous kernel
         const int nchunks = (ks + args.kc - 1) / args.kc;
         const bool single_chunk = (nchunks == 1);
-        if (single_chunk) {
-            convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_scale, s_unscale, s_amax, ctid,
-                                kWarps * 32);
-        }
+        if (single_chunk)
+            convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_scale, s_unscale, s_amax, tid, kWarps * 32);
+        bool live_col[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) live_col[nt] = (g + 8 * nt) < 2 * B;   // lane's column holds a batch row
         int stage = 0;
         uint32_t phase = 0;
         int consumed = 0;
+        const int row_off = (warp * 16 + g) * kBlockBytes;
         for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
             const int row0 = tile * kRows;
             float acc[NT][2];
@@ -345,20 +332,17 @@ __global__ void __launch_bounds__(kThreads, 2) q4k_gemv_kernel(const GemvArgs ar
             for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
             float unscale[NT];
             int chunk_end = -1;
-            bool reload_scale = false;
-            int blk_in_stage = 0;
-            const uint8_t *stage_base = nullptr;
+            bool reload_scale = true;
             for (int kbl = 0; kbl < ks; ++kbl) {
                 if (!single_chunk && kbl > chunk_end) {
-                    const int c0 = kbl;
-                    const int cn = min(args.kc, ks - c0);
+                    const int cn = min(args.kc, ks - kbl);
                     named_bar_sync(1, kWarps * 32);     // everyone done with the previous chunk
-                    convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + c0, cn, xf, s_scale, s_unscale, s_amax,
-                                        ctid, kWarps * 32);
-                    chunk_end = c0 + cn - 1;
+                    convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_scale, s_unscale, s_amax, tid,
+                                        kWarps * 32);
+                    chunk_end = kbl + cn - 1;
                     reload_scale = true;
                 }
-                if (kbl == 0 || reload_scale) {
+                if (reload_scale) {
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         const int b = t + 4 * nt;
@@ -366,83 +350,74 @@ __global__ void __launch_bounds__(kThreads, 2) q4k_gemv_kernel(const GemvArgs ar
                     }
                     reload_scale = false;
                 }
-                if (blk_in_stage == 0) {
-                    // After an abort the consumers keep walking the same schedule
-                    // (all named barriers are still reached) but stop waiting.
-                    if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs)) {
-                        atomicOr(&g_device_error, 1u);
-                        s_abort = 1;
-                    }
-                    stage_base = ring + stage * kStageBytes;
+                // After an abort the consumers keep walking the same schedule
+                // (every named barrier is still reached) but stop waiting.
+                if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs)) {
+                    atomicOr(&g_device_error, 1u);
+                    s_abort = 1;
                 }
-                const int xbl = single_chunk ? kbl : (kbl % args.kc);
-                {
-                    const uint8_t *rg = stage_base + (warp * 16 + g) * kRowStride + blk_in_stage * kBlockBytes;
-                    const uint8_t *rg8 = rg + 8 * kRowStride;
-                    const uint4 h0 = *reinterpret_cast<const uint4 *>(rg);
-                    const uint4 h1 = *reinterpret_cast<const uint4 *>(rg8);
-                    const uint4 qa0 = *reinterpret_cast<const uint4 *>(rg + 16 + 32 * t);
-                    const uint4 qb0 = *reinterpret_cast<const uint4 *>(rg + 32 + 32 * t);
-                    const uint4 qa1 = *reinterpret_cast<const uint4 *>(rg8 + 16 + 32 * t);
-                    const uint4 qb1 = *reinterpret_cast<const uint4 *>(rg8 + 32 + 32 * t);
-                    const RowConsts r0 = decode_header(h0, t);
-                    const RowConsts r1 = decode_header(h1, t);
-                    const uint32_t w0[8] = {qa0.x, qa0.y, qa0.z, qa0.w, qb0.x, qb0.y, qb0.z, qb0.w};
-                    const uint32_t w1[8] = {qa1.x, qa1.y, qa1.z, qa1.w, qb1.x, qb1.y, qb1.z, qb1.w};
-                    float cE[NT][4], cO[NT][4], cM[NT][4];
+                const uint8_t *ra = ring + stage * kStageBytes + row_off;   // row g of this warp
+                const uint8_t *rb = ra + 8 * kBlockBytes;                    // row g + 8
+                const uint2 *xrow = xf + static_cast<size_t>(single_chunk ? kbl : (kbl % args.kc)) * kKsteps * NT * LW;
+                const RowConsts r0 = decode_header(*reinterpret_cast<const uint4 *>(ra), t);
+                const RowConsts r1 = decode_header(*reinterpret_cast<const uint4 *>(rb), t);
+                float cE[2][NT][4], cO[2][NT][4], cM[NT][4];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) cE[nt][i] = cO[nt][i] = cM[nt][i] = 0.f;
-                    const uint2 *xrow = xf + static_cast<size_t>(xbl) * kKsteps * NT * LW;
+                    for (int i = 0; i < 4; ++i) cE[0][nt][i] = cE[1][nt][i] = cO[0][nt][i] = cO[1][nt][i] = cM[nt][i] = 0.f;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint32_t a = w0[u], a8 = a >> 8;
-                        const uint32_t c = w1[u], c8 = c >> 8;
-                        const uint32_t mask_lo = 0x000F000Fu, mask_hi = 0x00F000F0u, magic = 0x64006400u;
-                        const uint32_t e0 = hfma2_u32(and_or(a, mask_lo, magic), r0.mulE, r0.addE);
-                        const uint32_t e1 = hfma2_u32(and_or(a8, mask_lo, magic), r0.mulE, r0.addE);
-                        const uint32_t o0 = hfma2_u32(and_or(a, mask_hi, magic), r0.mulO, r0.addO);
-                        const uint32_t o1 = hfma2_u32(and_or(a8, mask_hi, magic), r0.mulO, r0.addO);
-                        const uint32_t f0 = hfma2_u32(and_or(c, mask_lo, magic), r1.mulE, r1.addE);
-                        const uint32_t f1 = hfma2_u32(and_or(c8, mask_lo, magic), r1.mulE, r1.addE);
-                        const uint32_t p0 = hfma2_u32(and_or(c, mask_hi, magic), r1.mulO, r1.addO);
-                        const uint32_t p1 = hfma2_u32(and_or(c8, mask_hi, magic), r1.mulO, r1.addO);
+                for (int half = 0; half < 2; ++half) {
+                    const uint4 qa = *reinterpret_cast<const uint4 *>(ra + 16 + 32 * t + 16 * half);
+                    const uint4 qb = *reinterpret_cast<const uint4 *>(rb + 16 + 32 * t + 16 * half);
+                    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+                    const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                    for (int uu = 0; uu < 4; ++uu) {
+                        const int u = 4 * half + uu;
+                        const uint32_t a = wa[uu], a8 = a >> 8;
+                        const uint32_t c = wb[uu], c8 = c >> 8;
+                        const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
+                        const uint32_t e0 = hfma2_u32(and_or(a, mlo, magic), r0.mulE, r0.addE);
+                        const uint32_t e1 = hfma2_u32(and_or(a8, mlo, magic), r0.mulE, r0.addE);
+                        const uint32_t o0 = hfma2_u32(and_or(a, mhi, magic), r0.mulO, r0.addO);
+                        const uint32_t o1 = hfma2_u32(and_or(a8, mhi, magic), r0.mulO, r0.addO);
+                        const uint32_t f0 = hfma2_u32(and_or(c, mlo, magic), r1.mulE, r1.addE);
+                        const uint32_t f1 = hfma2_u32(and_or(c8, mlo, magic), r1.mulE, r1.addE);
+                        const uint32_t p0 = hfma2_u32(and_or(c, mhi, magic), r1.mulO, r1.addO);
+                        const uint32_t p1 = hfma2_u32(and_or(c8, mhi, magic), r1.mulO, r1.addO);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const bool live = (g + 8 * nt) < 2 * B;   // lane's column holds a batch row
                             uint2 be = make_uint2(0u, 0u), bo = make_uint2(0u, 0u);
-                            if (live) {
+                            if (live_col[nt]) {
                                 be = xrow[(static_cast<size_t>(2 * u) * NT + nt) * LW + lane];
                                 bo = xrow[(static_cast<size_t>(2 * u + 1) * NT + nt) * LW + lane];
                             }
-                            mma_16816(cE[nt], e0, f0, e1, f1, be.x, be.y);
-                            mma_16816(cO[nt], o0, p0, o1, p1, bo.x, bo.y);
+                            mma_16816(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
+                            mma_16816(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
                         }
                     }
+                }
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const bool live = (g + 8 * nt) < 2 * B;
-                        uint2 bm = make_uint2(0u, 0u);
-                        if (live) bm = xrow[(static_cast<size_t>(16) * NT + nt) * LW + lane];
-                        mma_16816(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
-                        const float s0 = (cE[nt][0] + cO[nt][0]) + (cE[nt][1] + cO[nt][1]);
-                        const float s1 = (cE[nt][2] + cO[nt][2]) + (cE[nt][3] + cO[nt][3]);
-                        const float m0 = cM[nt][0] + cM[nt][1];
-                        const float m1 = cM[nt][2] + cM[nt][3];
-                        acc[nt][0] = fmaf(r0.d * unscale[nt], s0, acc[nt][0]);
-                        acc[nt][0] = fmaf(-r0.dmin * unscale[nt], m0, acc[nt][0]);
-                        acc[nt][1] = fmaf(r1.d * unscale[nt], s1, acc[nt][1]);
-                        acc[nt][1] = fmaf(-r1.dmin * unscale[nt], m1, acc[nt][1]);
-                    }
+                for (int nt = 0; nt < NT; ++nt) {
+                    uint2 bm = make_uint2(0u, 0u);
+                    if (live_col[nt]) bm = xrow[(static_cast<size_t>(16) * NT + nt) * LW + lane];
+                    mma_16816(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
+                    const float s0 = ((cE[0][nt][0] + cE[1][nt][0]) + (cO[0][nt][0] + cO[1][nt][0])) +
+                                     ((cE[0][nt][1] + cE[1][nt][1]) + (cO[0][nt][1] + cO[1][nt][1]));
+                    const float s1 = ((cE[0][nt][2] + cE[1][nt][2]) + (cO[0][nt][2] + cO[1][nt][2])) +
+                                     ((cE[0][nt][3] + cE[1][nt][3]) + (cO[0][nt][3] + cO[1][nt][3]));
+                    const float m0 = cM[nt][0] + cM[nt][1];
+                    const float m1 = cM[nt][2] + cM[nt][3];
+                    acc[nt][0] = fmaf(r0.d * unscale[nt], s0, acc[nt][0]);
+                    acc[nt][0] = fmaf(-r0.dmin * unscale[nt], m0, acc[nt][0]);
+                    acc[nt][1] = fmaf(r1.d * unscale[nt], s1, acc[nt][1]);
+                    acc[nt][1] = fmaf(-r1.dmin * unscale[nt], m1, acc[nt][1]);
                 }
-                if (++blk_in_stage == kStageBlocks || kbl == ks - 1) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
-                    ++consumed;
-                    blk_in_stage = 0;
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+                ++consumed;
+                if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
             // ---------------- tile epilogue
             if (split == 1 && !*(volatile int *)&s_abort) {
@@ -485,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 2) q4k_gemv_kernel(const GemvArgs ar
 
     if (split > 1) {
         // Deterministic cross-CTA reduction of the single row tile through
-        // distributed shared memory: rank r sums rows [r*64/split, (r+1)*64/split)
+        // distributed shared memory: rank r sums rows [r*128/split, (r+1)*128/split)
         // over ranks 0..split-1 in order.
         cluster_sync_all();
         if (!*(volatile int *)&s_abort) {
@@ -498,12 +473,12 @@ __global__ void __launch_bounds__(kThreads, 2) q4k_gemv_kernel(const GemvArgs ar
                 const int lr = lr0 + it / B;
                 const int b = it % B;
                 const uint32_t off = static_cast<uint32_t>((lr * B + b) * 4);
-                float s = 0.f;
-                for (int q = 0; q < split; ++q) s += ld_shared_cluster_f32(map_shared_rank(red_local + off, q));
+                float sum = 0.f;
+                for (int q = 0; q < split; ++q) sum += ld_shared_cluster_f32(map_shared_rank(red_local + off, q));
                 const int row = row0 + lr;
                 if (row < args.N) {
-                    if (args.y) args.y[static_cast<size_t>(b) * args.N + row] = s;
-                    if (ARGMAX && !isnan(s)) atomicMax(&s_best[b], argmax_key(s, static_cast<uint32_t>(row)));
+                    if (args.y) args.y[static_cast<size_t>(b) * args.N + row] = sum;
+                    if (ARGMAX && !isnan(sum)) atomicMax(&s_best[b], argmax_key(sum, static_cast<uint32_t>(row)));
                 }
             }
         }
@@ -605,11 +580,12 @@ static GemvPlan make_plan(int64_t N, int64_t K, int B, int sms, int forced_split
     const int ks_max = (nb + p.split - 1) / p.split;
     const size_t per_blk = xfrag_bytes_per_block(p.NT, B);
     const size_t fixed = gemv_smem_bytes(p.NT, B, 0);
-    int kc = static_cast<int>(std::max<size_t>(1, (kSmemPerCta - fixed) / per_blk));
+    const size_t budget = (p.NT <= 2) ? kSmemPerCta2 : kSmemPerCta1;
+    int kc = static_cast<int>(std::max<size_t>(1, (budget - fixed) / per_blk));
     p.kc = std::min(kc, ks_max);
     p.smem = gemv_smem_bytes(p.NT, B, p.kc);
     if (p.split == 1) {
-        const int ctas_per_sm = 2;
+        const int ctas_per_sm = (p.NT <= 2) ? 2 : 1;
         p.grid_x = std::min(p.tiles, sms * ctas_per_sm);
     } else {
         p.grid_x = p.tiles;
@@ -617,8 +593,41 @@ static GemvPlan make_plan(int64_t N, int64_t K, int B, int sms, int forced_split
     return p;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, []() {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// W as a 2-D tensor of 8-byte words: [N rows] x [K/256 * 18 words], box =
+// one super-block (18 words) of kRows rows.
+static bool encode_w_map(CUtensorMap *map, const void *W, int64_t N, int64_t K)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int64_t nb = K / 256;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(nb * (kBlockBytes / 8)), static_cast<cuuint64_t>(N)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(nb * kBlockBytes)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBlockBytes / 8), static_cast<cuuint32_t>(kRows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(W), gdim, gstride, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 template <int NT, bool ARGMAX>
-static cudaError_t launch_one(const GemvPlan &p, const GemvArgs &a, cudaStream_t stream, bool pdl)
+static cudaError_t launch_one(const GemvPlan &p, const CUtensorMap &map, const GemvArgs &a, cudaStream_t stream,
+                              bool pdl)
 {
     auto kern = q4k_gemv_kernel<NT, ARGMAX>;
     static std::mutex mu;
@@ -655,17 +664,20 @@ static cudaError_t launch_one(const GemvPlan &p, const GemvArgs &a, cudaStream_t
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, map, a);
 }
 
 template <bool ARGMAX>
-static cudaError_t launch_gemv(const GemvPlan &p, const GemvArgs &a, cudaStream_t s, bool pdl)
+static cudaError_t launch_gemv(const GemvPlan &p, const void *W, int64_t N, int64_t K, const GemvArgs &a,
+                               cudaStream_t s, bool pdl)
 {
+    CUtensorMap map;
+    if (!encode_w_map(&map, W, N, K)) return cudaErrorInvalidValue;
     switch (p.NT) {
-        case 1: return launch_one<1, ARGMAX>(p, a, s, pdl);
-        case 2: return launch_one<2, ARGMAX>(p, a, s, pdl);
-        case 3: return launch_one<3, ARGMAX>(p, a, s, pdl);
-        default: return launch_one<4, ARGMAX>(p, a, s, pdl);
+        case 1: return launch_one<1, ARGMAX>(p, map, a, s, pdl);
+        case 2: return launch_one<2, ARGMAX>(p, map, a, s, pdl);
+        case 3: return launch_one<3, ARGMAX>(p, map, a, s, pdl);
+        default: return launch_one<4, ARGMAX>(p, map, a, s, pdl);
     }
 }
 
@@ -695,7 +707,6 @@ q4k_status gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t
     if (forced < 0 || forced > 8) return Q4K_ERR_INVALID_ARG;
     GemvPlan p = make_plan(N, K, batch, sms, forced);
     GemvArgs a{};
-    a.W = static_cast<const uint8_t *>(W);
     a.x = x;
     a.y = y;
     a.N = static_cast<int>(N);
@@ -704,7 +715,7 @@ q4k_status gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t
     a.tiles = p.tiles;
     a.kc = p.kc;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
-    cudaError_t e = launch_gemv<false>(p, a, static_cast<cudaStream_t>(stream), pdl);
+    cudaError_t e = launch_gemv<false>(p, W, N, K, a, static_cast<cudaStream_t>(stream), pdl);
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
@@ -722,7 +733,6 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
     if (forced < 0 || forced > 8) return Q4K_ERR_INVALID_ARG;
     GemvPlan p = make_plan(N, K, batch, sms, forced);
     GemvArgs a{};
-    a.W = static_cast<const uint8_t *>(W);
     a.x = x;
     a.y = logits;
     a.N = static_cast<int>(N);
@@ -746,7 +756,7 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
         a.keys = scratch_keys;
         a.ticket = scratch_ticket;
     }
-    cudaError_t e = launch_gemv<true>(p, a, s, pdl && scratch_keys != nullptr);
+    cudaError_t e = launch_gemv<true>(p, W, N, K, a, s, pdl);
     if (buf) {
         cudaError_t e2 = cudaFreeAsync(buf, s);
         if (e == cudaSuccess) e = e2;

@@ -1,5 +1,8 @@
 // q4k_internal.h -- declarations shared by the translation units of the library.
 #pragma once
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdint>
 
 #include "../../include/q4k.h"
@@ -17,5 +20,7 @@ q4k_status gemv_plan_impl(int64_t N, int64_t K, int batch, int out[4]);
 q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream);
 unsigned int read_device_error();
 unsigned int read_prefill_error();
+// cuTensorMapEncodeTiled from the driver (null if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 }  // namespace q4k

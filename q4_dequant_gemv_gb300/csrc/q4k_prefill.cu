@@ -9,11 +9,15 @@
 // CTA tile: 128 weight rows (the MMA M side) x TN*NTT tokens (the N side),
 // full K.  Per 64-wide K chunk (a quarter of a super-block):
 //   * warps 0-3 (one thread per weight row) read the row's sub-block pair from
-//     global memory, compute w = d*sc*q - dmin*m in fp32, round to bf16 (RNE)
-//     and store the 128-byte row in the 128-byte-swizzled K-major layout;
+//     global memory, compute w = d*sc*q - dmin*m in fp32 and split it into two
+//     bf16 values, hi = bf16(w) and lo = bf16(w - hi) (|w - hi - lo| <=
+//     2^-17 |w|), stored as two 128-byte-swizzled K-major tiles.  A single
+//     bf16 rounding of w (8 significant bits) would put the product outside
+//     the decode path's error budget; the split keeps it at fp32 quality;
 //   * warp 4 loads the X tile [TN x 64] with a TMA tensor copy (128B swizzle);
-//   * warp 5 (one elected thread) issues 4 x NTT tcgen05.mma (K = 16 each)
-//     into the TMEM accumulators and commits to the stage's "empty" barrier.
+//   * warp 5 (one elected thread) issues 2 x 4 x NTT tcgen05.mma (K = 16
+//     each: hi tile, then lo tile, same accumulator) into TMEM and commits to
+//     the stage's "empty" barrier.
 // A ring of NS stages overlaps the three.  The epilogue reads TMEM with
 // tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = weight rows) and writes Y
 // with coalesced stores.  Every mbarrier wait is bounded in time.
@@ -44,7 +48,8 @@ namespace pf {
 constexpr int kRowsM = 128;          // MMA M
 constexpr int kChunk = 64;           // K elements per stage (one 128-byte swizzle row)
 constexpr int kThreads = 192;        // 4 dequant/epilogue warps + TMA warp + MMA warp
-constexpr int kAStageBytes = kRowsM * kChunk * 2;   // 16 KB
+constexpr int kATileBytes = kRowsM * kChunk * 2;    // 16 KB: one bf16 weight tile
+constexpr int kAStageBytes = 2 * kATileBytes;       // hi + lo tiles
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
@@ -126,6 +131,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+__device__ __forceinline__ float bf16_lo_f32(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;
@@ -137,9 +145,9 @@ template <int TN, int NTT>
 struct Cfg {
     static constexpr int kBBytes = TN * kChunk * 2;                       // one token subtile
     static constexpr int kStageBytes = kAStageBytes + NTT * kBBytes;
-    static constexpr int kStages = (NTT * TN >= 512) ? 2 : 4;
+    static constexpr int kStages = (200 * 1024 / kStageBytes) < 4 ? (200 * 1024 / kStageBytes) : 4;
     static constexpr int kTmemCols = TN * NTT;                            // 32..512, power of two
-    static constexpr size_t kSmem = static_cast<size_t>(kStages) * kStageBytes + 1024 /*align*/ + 256;
+    static constexpr size_t kSmem = static_cast<size_t>(kStages) * kStageBytes;
 };
 
 template <int TN, int NTT>
@@ -149,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 {
     using C = Cfg<TN, NTT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *smem = smem_raw;   // 1024-byte aligned: the 128B-swizzle atoms need it
     __shared__ __align__(8) uint64_t full_a[C::kStages], full_b[C::kStages], empty[C::kStages], done_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int s_abort;
@@ -230,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int half = 0; half < 2; ++half) {           // 0: low nibbles (k 0..31), 1: high (k 32..63)
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {             // 16-byte chunk: k = 32*half + 8*c8 .. +7
-                    uint32_t out[4];
+                    uint32_t out[4], outl[4];
 #pragma unroll
                     for (int uu = 0; uu < 2; ++uu) {         // word u = 2*c8 + uu -> k offset 4u..4u+3
                         const uint32_t w = words[2 * c8 + uu];
@@ -244,12 +252,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float w2 = fmaf(half_hi_f32(h02), ds, -dm);
                         const float w1 = fmaf(half_lo_f32(h13), ds, -dm);
                         const float w3 = fmaf(half_hi_f32(h13), ds, -dm);
-                        out[2 * uu] = pack_bf16x2(w0, w1);
-                        out[2 * uu + 1] = pack_bf16x2(w2, w3);
+                        const uint32_t h01 = pack_bf16x2(w0, w1), h23 = pack_bf16x2(w2, w3);
+                        out[2 * uu] = h01;
+                        out[2 * uu + 1] = h23;
+                        outl[2 * uu] = pack_bf16x2(w0 - bf16_lo_f32(h01), w1 - bf16_hi_f32(h01));
+                        outl[2 * uu + 1] = pack_bf16x2(w2 - bf16_lo_f32(h23), w3 - bf16_hi_f32(h23));
                     }
                     const int chunk = 4 * half + c8;
                     uint4 v = live ? make_uint4(out[0], out[1], out[2], out[3]) : make_uint4(0, 0, 0, 0);
+                    uint4 vl = live ? make_uint4(outl[0], outl[1], outl[2], outl[3]) : make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) = v;
+                    *reinterpret_cast<uint4 *>(arow + kATileBytes + ((chunk ^ (r & 7)) << 4)) = vl;
                 }
             }
             fence_proxy_async_smem();
@@ -311,9 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (j < nsub) {
 #pragma unroll
                             for (int kk = 0; kk < kChunk / 16; ++kk) {
-                                const uint64_t ad = sw128_desc(a_addr + kk * 32);
                                 const uint64_t bd = sw128_desc(b_addr + j * C::kBBytes + kk * 32);
-                                umma_bf16(tmem + j * TN, ad, bd, idesc, (c > 0 || kk > 0) ? 1u : 0u);
+                                umma_bf16(tmem + j * TN, sw128_desc(a_addr + kk * 32), bd, idesc,
+                                          (c > 0 || kk > 0) ? 1u : 0u);
+                                umma_bf16(tmem + j * TN, sw128_desc(a_addr + kATileBytes + kk * 32), bd, idesc, 1u);
                             }
                         }
                     }
@@ -372,26 +386,11 @@ static q4k_status validate_prefill(const void *W, const void *X, const float *Y,
     return Q4K_OK;
 }
 
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, []() {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 template <int TN, int NTT>
 static cudaError_t launch_prefill(const uint8_t *W, const void *X, float *Y, int N, int K, int T, cudaStream_t s)
 {
     using C = pf::Cfg<TN, NTT>;
-    auto enc = get_encode();
+    auto enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap map;
     cuuint64_t gdim[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(T)};
