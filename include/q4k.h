@@ -120,6 +120,28 @@ q4k_status q4k_gemv_argmax_debug(const void *W, const float *x, int32_t *idx, fl
                                  int64_t N, int64_t K, int batch, void *stream);
 
 /*
+ * Allocation-free q4k_gemv_argmax.  (No counterpart on the pages: this is an
+ * interface choice of this library.)  Same arguments, same result bit for bit.
+ * Meant for callers that must not allocate device memory while they run --
+ * code working from a fixed, pre-sized memory budget, real-time loops that
+ * forbid allocator calls, or processes whose stream-ordered allocator is
+ * unavailable or replaced.  Instead of cudaMallocAsync it uses a static device
+ * array of 16 keys + a ticket (144 bytes) that every GPU loading the library
+ * keeps until the process exits.
+ *   - batch must be <= 16 (the array's capacity); larger batches return
+ *     Q4K_ERR_INVALID_ARG.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Each call clears the array with cudaMemsetAsync on `stream` before its
+ *     kernel.  All calls share the array: calls that overlap on the GPU
+ *     (different streams, concurrently running graphs) race and may return
+ *     wrong indices.  Serialize them.
+ *   - Allocates nothing: no cudaMalloc, cudaMallocAsync or cudaFree.
+ */
+q4k_status q4k_gemv_argmax_noalloc(const void *W, const float *x, int32_t *idx, int64_t N, int64_t K,
+                                   int batch, void *stream);
+
+/*
  * Y[t][n] = sum_k w[n][k] * X[t][k]   for t < T, n < N (prefill).
  *   W  Q4_K rows as above (16-byte aligned)
  *   X  bf16 [T][K] row-major (16-byte aligned)

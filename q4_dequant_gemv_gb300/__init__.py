@@ -36,7 +36,7 @@ class LaunchOpts(ctypes.Structure):
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("q4k_status_string", "q4k_abi_version", "q4k_gemv", "q4k_gemv_argmax", "q4k_gemv_argmax_debug",
-           "q4k_gemm_prefill", "q4k_gemv_ex", "q4k_gemv_plan", "q4k_device_error_flags")
+           "q4k_gemv_argmax_noalloc", "q4k_gemm_prefill", "q4k_gemv_ex", "q4k_gemv_plan", "q4k_device_error_flags")
 
 
 def lib():
@@ -60,6 +60,8 @@ def lib():
         L.q4k_gemv_argmax.restype = I
         L.q4k_gemv_argmax_debug.argtypes = [P, P, P, P, I64, I64, I, P]
         L.q4k_gemv_argmax_debug.restype = I
+        L.q4k_gemv_argmax_noalloc.argtypes = [P, P, P, I64, I64, I, P]
+        L.q4k_gemv_argmax_noalloc.restype = I
         L.q4k_gemm_prefill.argtypes = [P, P, P, I64, I64, I64, P]
         L.q4k_gemm_prefill.restype = I
         L.q4k_gemv_plan.argtypes = [I64, I64, I, ctypes.POINTER(ctypes.c_int * 4)]

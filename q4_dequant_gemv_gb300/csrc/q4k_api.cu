@@ -44,6 +44,12 @@ q4k_status q4k_gemv_argmax_debug(const void *W, const float *x, int32_t *idx, fl
     return q4k::gemv_argmax_impl(W, x, idx, logits, N, K, batch, stream, nullptr, nullptr, nullptr);
 }
 
+q4k_status q4k_gemv_argmax_noalloc(const void *W, const float *x, int32_t *idx, int64_t N, int64_t K, int batch,
+                                   void *stream)
+{
+    return q4k::gemv_argmax_noalloc_impl(W, x, idx, N, K, batch, stream);
+}
+
 q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t N, int64_t K, int64_t T,
                             void *stream)
 {

@@ -60,7 +60,7 @@ constexpr int kWarps = 8;                 // consumer warps per CTA
 constexpr int kRows = 16 * kWarps;        // rows per tile (128)
 constexpr int kThreads = 32 * (kWarps + 1);
 constexpr int kKsteps = 17;               // 16 k16 steps + 1 min-term step per super-block
-constexpr int kStages = 4;                // W ring depth
+constexpr int kStages = 3;                // W ring depth
 constexpr int kStageBytes = kRows * kBlockBytes;   // one super-block of every tile row (18 KB)
 constexpr size_t kSmemPerCta2 = 110 * 1024;        // two CTAs per SM (batch <= 8)
 constexpr size_t kSmemPerCta1 = 200 * 1024;        // one CTA per SM (batch > 8)
@@ -318,9 +318,12 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
         const bool single_chunk = (nchunks == 1);
         if (single_chunk)
             convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_scale, s_unscale, s_amax, tid, kWarps * 32);
-        bool live_col[NT];
+        // B-fragment lane of each n-tile.  Lanes whose column holds no batch row
+        // read some other valid entry: MMA columns are independent, and those
+        // output columns are never used.
+        int blane[NT];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) live_col[nt] = (g + 8 * nt) < 2 * B;   // lane's column holds a batch row
+        for (int nt = 0; nt < NT; ++nt) blane[nt] = ((g + 8 * nt) < 2 * B) ? lane : (lane % LW);
         int stage = 0;
         uint32_t phase = 0;
         int consumed = 0;
@@ -363,10 +366,6 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
                 const RowConsts r1 = decode_header(*reinterpret_cast<const uint4 *>(rb), t);
                 float cE[2][NT][4], cO[2][NT][4], cM[NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) cE[0][nt][i] = cE[1][nt][i] = cO[0][nt][i] = cO[1][nt][i] = cM[nt][i] = 0.f;
-#pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     const uint4 qa = *reinterpret_cast<const uint4 *>(ra + 16 + 32 * t + 16 * half);
                     const uint4 qb = *reinterpret_cast<const uint4 *>(rb + 16 + 32 * t + 16 * half);
@@ -388,21 +387,22 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
                         const uint32_t p1 = hfma2_u32(and_or(c8, mhi, magic), r1.mulO, r1.addO);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            uint2 be = make_uint2(0u, 0u), bo = make_uint2(0u, 0u);
-                            if (live_col[nt]) {
-                                be = xrow[(static_cast<size_t>(2 * u) * NT + nt) * LW + lane];
-                                bo = xrow[(static_cast<size_t>(2 * u + 1) * NT + nt) * LW + lane];
+                            const uint2 be = xrow[(2 * u * NT + nt) * LW + blane[nt]];
+                            const uint2 bo = xrow[((2 * u + 1) * NT + nt) * LW + blane[nt]];
+                            if (u < 2) {   // first k-step of each accumulator chain
+                                mma_16816_z(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
+                                mma_16816_z(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
+                            } else {
+                                mma_16816(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
+                                mma_16816(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
                             }
-                            mma_16816(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
-                            mma_16816(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
                         }
                     }
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    uint2 bm = make_uint2(0u, 0u);
-                    if (live_col[nt]) bm = xrow[(static_cast<size_t>(16) * NT + nt) * LW + lane];
-                    mma_16816(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
+                    const uint2 bm = xrow[(16 * NT + nt) * LW + blane[nt]];
+                    mma_16816_z(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
                     const float s0 = ((cE[0][nt][0] + cE[1][nt][0]) + (cO[0][nt][0] + cO[1][nt][0])) +
                                      ((cE[0][nt][1] + cE[1][nt][1]) + (cO[0][nt][1] + cO[1][nt][1]));
                     const float s1 = ((cE[0][nt][2] + cE[1][nt][2]) + (cO[0][nt][2] + cO[1][nt][2])) +
@@ -566,13 +566,18 @@ static GemvPlan make_plan(int64_t N, int64_t K, int B, int sms, int forced_split
     if (forced_split > 0) {
         best_s = std::min(std::min(forced_split, nb), 8);
     } else {
+        // Cost = (units on the busiest SM) x (blocks per unit + per-CTA
+        // overhead) / (units that run concurrently on it, at most the CTAs per
+        // SM): a lone CTA is latency-bound and cannot use the whole SM.
+        const int cps = (p.NT <= 2) ? 2 : 1;
         double best = 1e30;
         const int smax = std::min(nb, 8);
         for (int s = 1; s <= smax; ++s) {
             const long long units = static_cast<long long>(p.tiles) * s;
             const long long per_sm = (units + sms - 1) / sms;
             const int per_unit = (nb + s - 1) / s;
-            const double cost = static_cast<double>(per_sm) * (per_unit + 0.5);
+            const double conc = static_cast<double>(std::min<long long>(per_sm, cps));
+            const double cost = static_cast<double>(per_sm) * (per_unit + 0.75) / conc;
             if (cost < best - 1e-9) { best = cost; best_s = s; }
         }
     }
@@ -762,6 +767,53 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
         if (e == cudaSuccess) e = e2;
     }
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the fused argmax.
+//
+// For callers that cannot allocate device memory while they run -- code that
+// works from a fixed, pre-sized memory budget, real-time loops that forbid any
+// allocator call, or processes whose stream-ordered allocator is unavailable
+// or replaced -- the argmax's small scratch (one 64-bit key per batch row plus
+// a CTA ticket) lives in this file-scope device array instead of coming from
+// cudaMallocAsync.  Every GPU that loads the library holds these bytes until
+// the process exits.  Host code cannot use the array's name as a device
+// address, so the address is looked up with cudaGetSymbolAddress once per
+// device (with that device current) on the first call there; make that first
+// call before any stream capture.  All calls share the array: it is cleared
+// with cudaMemsetAsync on the caller's stream before every launch, and calls
+// whose executions overlap on the GPU (different streams, concurrent graphs)
+// race on it.
+// ---------------------------------------------------------------------------
+constexpr int kNoAllocMaxBatch = 16;   // keys held by the static scratch
+__device__ __align__(256) static unsigned long long g_argmax_scratch[kNoAllocMaxBatch + 2];
+
+static unsigned long long *g_scratch_addr[64];
+static std::once_flag g_scratch_once[64];
+static cudaError_t g_scratch_err[64];
+
+q4k_status gemv_argmax_noalloc_impl(const void *W, const float *x, int32_t *idx, int64_t N, int64_t K, int batch,
+                                    void *stream)
+{
+    if (batch > kNoAllocMaxBatch) return Q4K_ERR_INVALID_ARG;   // beyond the static scratch
+    q4k_status st = validate(W, x, idx, N, K, batch, true);
+    if (st != Q4K_OK) return st;
+    st = check_device(nullptr);
+    if (st != Q4K_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4K_ERR_CUDA;
+    std::call_once(g_scratch_once[dev], [dev]() {
+        void *p = nullptr;
+        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_argmax_scratch);
+        g_scratch_addr[dev] = static_cast<unsigned long long *>(p);
+    });
+    if (g_scratch_err[dev] != cudaSuccess || g_scratch_addr[dev] == nullptr) return Q4K_ERR_CUDA;
+    unsigned long long *keys = g_scratch_addr[dev];
+    unsigned int *ticket = reinterpret_cast<unsigned int *>(keys + kNoAllocMaxBatch);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(keys, 0, sizeof(g_argmax_scratch), s) != cudaSuccess) return Q4K_ERR_CUDA;
+    return gemv_argmax_impl(W, x, idx, nullptr, N, K, batch, stream, keys, ticket, nullptr);
 }
 
 q4k_status gemv_plan_impl(int64_t N, int64_t K, int batch, int out[4])
