@@ -445,6 +445,20 @@ def run_profile_case(spec: str, iters: int):
     import q4_dequant_gemv_gb300 as q4k
     import synth
     __graft_entry__.build()
+    if spec.startswith("decode"):
+        # decode:L:B -- L Qwen2.5-7B-shaped layers (7 GEMVs each), eager launches
+        _, L, B = spec.split(":")
+        L, B = int(L), int(B)
+        layers = [[(N, K, torch.from_numpy(W).cuda()) for _, N, K, W in synth.qwen_layer_weights(l)] for l in range(L)]
+        xs = {K: torch.from_numpy(synth.normal_f32((B, K), (9, K))).cuda() for K in (3584, 18944)}
+        ys = [[torch.empty((B, N), device="cuda") for N, _, _ in lw] for lw in layers]
+        for _ in range(iters):
+            for lw, yl in zip(layers, ys):
+                for (N, K, W), y in zip(lw, yl):
+                    q4k.gemv(W, xs[K], y, pdl=True)
+        torch.cuda.synchronize()
+        print(f"profile case {spec} x{iters} done")
+        return
     kind, N, K, B = spec.split(":")
     N, K, B = int(N), int(K), int(B)
     W = torch.from_numpy(synth.q4k_weights(N, K, (9, N, K))).cuda()

@@ -88,11 +88,15 @@ __host__ __device__ inline size_t xfrag_bytes_per_block(int NT, int B)
     return static_cast<size_t>(kKsteps) * NT * frag_lanes(NT, B) * 8;
 }
 
-// Dynamic shared memory: [ring | x fragments | partial sums (split-K)].
+// Dynamic shared memory: [ring | x fragments | raw x chunk | partial sums (split-K)].
 __host__ __device__ inline size_t xfrag_offset() { return static_cast<size_t>(kStages) * kStageBytes; }
+__host__ __device__ inline size_t xraw_offset(int NT, int B, int kc)
+{
+    return xfrag_offset() + ((xfrag_bytes_per_block(NT, B) * kc + 127) & ~size_t(127));
+}
 __host__ __device__ inline size_t red_offset(int NT, int B, int kc)
 {
-    return xfrag_offset() + ((xfrag_bytes_per_block(NT, B) * kc + 15) & ~size_t(15));
+    return xraw_offset(NT, B, kc) + static_cast<size_t>(B) * kc * 1024;
 }
 __host__ inline size_t gemv_smem_bytes(int NT, int B, int kc)
 {
@@ -108,91 +112,112 @@ __host__ inline size_t gemv_smem_bytes(int NT, int B, int kc)
 // entries 4u..4u+3 of that sub-block ordered {4u, 4u+2 | 4u+1, 4u+3}.  Step 16
 // holds the sub-block sums of x for sub-blocks 2t, 2t+1 (the dmin*m term).
 // ---------------------------------------------------------------------------
+// Power-of-two scale 2^s with max|x| * 2^s in [2^9, 2^10) (s = 0 for an all
+// zero or non-finite chunk), clamped to the normal range.
+__device__ __forceinline__ int chunk_scale_exp(uint32_t amax_bits)
+{
+    const int E = static_cast<int>((amax_bits >> 23) & 255u);
+    int s = (amax_bits != 0u && E != 255) ? 136 - E : 0;
+    return max(-126, min(126, s));
+}
+
+struct XChunkState {
+    uint32_t parity;   // phase of the x mbarrier for the next chunk
+    int issued;        // thread 0: a copy into xraw has been issued
+};
+
+// The chunk of x (B rows x nblk*256 floats) is brought into shared memory by
+// one bulk copy per batch row, then converted there: per-row max -> scale,
+// fp16 hi/lo B fragments, sub-block sums.  Called by all consumer threads;
+// every caller must have finished reading the previous chunk's fragments
+// (the caller's named barrier) before it is entered.
 template <int NT>
 __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int kb0, int nblk, uint2 *xf,
-                                float *s_scale, float *s_unscale, uint32_t *s_amax, int tid, int nthr)
+                                const float *xraw, uint64_t *xbar, XChunkState &xs, float *s_unscale,
+                                uint32_t *s_amax, int *s_abort, int tid, int nthr)
 {
     const int LW = frag_lanes(NT, B);
-    // 1) per-batch-row max |x| over the chunk -> power-of-two scale
-    for (int b = tid; b < B; b += nthr) s_amax[b] = 0u;
-    named_bar_sync(1, nthr);
-    const int n4 = nblk * 64;  // float4 per batch row in the chunk
+    const int n = nblk * 256;                       // floats per batch row in the chunk
+    if (tid == 0) {
+        fence_proxy_async_smem();                   // prior generic reads of xraw happen first
+        mbar_arrive_expect_tx(smem_u32(xbar), static_cast<uint32_t>(B * n * 4));
+        for (int b = 0; b < B; ++b)
+            bulk_g2s(smem_u32(xraw + b * n), x + static_cast<size_t>(b) * K + static_cast<size_t>(kb0) * 256,
+                     static_cast<uint32_t>(n * 4), smem_u32(xbar), l2_policy_evict_last());
+        xs.issued = 1;
+    }
+    if (!*(volatile int *)s_abort && !mbar_wait_bounded(smem_u32(xbar), xs.parity, kWaitLimitNs)) {
+        atomicOr(&g_device_error, 1u);
+        *s_abort = 1;
+    }
+    xs.parity ^= 1u;
+    // 1) per-batch-row max |x|
     for (int b = 0; b < B; ++b) {
-        const float4 *xb = reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K + static_cast<size_t>(kb0) * 256);
+        const float4 *xb = reinterpret_cast<const float4 *>(xraw + b * n);
         uint32_t m = 0u;
-        for (int e = tid; e < n4; e += nthr) {
-            float4 v = __ldg(xb + e);
-            m = max(m, __float_as_uint(fabsf(v.x)));
-            m = max(m, __float_as_uint(fabsf(v.y)));
-            m = max(m, __float_as_uint(fabsf(v.z)));
-            m = max(m, __float_as_uint(fabsf(v.w)));
+        for (int e = tid; e < n / 4; e += nthr) {
+            const float4 v = xb[e];
+            m = max(m, max(max(__float_as_uint(fabsf(v.x)), __float_as_uint(fabsf(v.y))),
+                           max(__float_as_uint(fabsf(v.z)), __float_as_uint(fabsf(v.w)))));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
         if ((tid & 31) == 0 && m) atomicMax(&s_amax[b], m);
     }
     named_bar_sync(1, nthr);
-    for (int b = tid; b < B; b += nthr) {
-        uint32_t bits = s_amax[b];
-        int E = static_cast<int>((bits >> 23) & 255u);
-        int s = 0;
-        if (bits != 0u && E != 255) s = 136 - E;             // max|x| * 2^s in [2^9, 2^10)
-        s = max(-126, min(126, s));
-        s_scale[b] = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
-        s_unscale[b] = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-    }
-    named_bar_sync(1, nthr);
     // 2) main entries: items (bl, s<16, b, t)
     const int items = nblk * 16 * B * 4;
     for (int it = tid; it < items; it += nthr) {
-        int t = it & 3;
+        const int t = it & 3;
         int r = it >> 2;
-        int b = r % B;
+        const int b = r % B;
         r /= B;
-        int s = r & 15;
-        int bl = r >> 4;
-        int pos = (kb0 + bl) * 256 + 32 * (2 * t + (s & 1)) + 4 * (s >> 1);
-        float4 v = __ldg(reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K + pos));
-        const float sc = s_scale[b];
+        const int s = r & 15;
+        const int bl = r >> 4;
+        const float sc = __uint_as_float(static_cast<uint32_t>(chunk_scale_exp(s_amax[b]) + 127) << 23);
+        float4 v = *reinterpret_cast<const float4 *>(xraw + b * n + bl * 256 + 32 * (2 * t + (s & 1)) + 4 * (s >> 1));
         v.x *= sc; v.y *= sc; v.z *= sc; v.w *= sc;
-        uint32_t h01 = pack_half2(v.x, v.z);
-        uint32_t h23 = pack_half2(v.y, v.w);
-        uint32_t l01 = pack_half2(v.x - half_lo_f32(h01), v.z - half_hi_f32(h01));
-        uint32_t l23 = pack_half2(v.y - half_lo_f32(h23), v.w - half_hi_f32(h23));
+        const uint32_t h01 = pack_half2(v.x, v.z);
+        const uint32_t h23 = pack_half2(v.y, v.w);
+        const uint32_t l01 = pack_half2(v.x - half_lo_f32(h01), v.z - half_hi_f32(h01));
+        const uint32_t l23 = pack_half2(v.y - half_lo_f32(h23), v.w - half_hi_f32(h23));
         const int chi = 2 * b, clo = 2 * b + 1;
-        const size_t base = static_cast<size_t>(bl * kKsteps + s) * NT;
+        const int base = (bl * kKsteps + s) * NT;
         xf[(base + chi / 8) * LW + 4 * (chi % 8) + t] = make_uint2(h01, h23);
         xf[(base + clo / 8) * LW + 4 * (clo % 8) + t] = make_uint2(l01, l23);
     }
     // 3) min-term entries: items (bl, b, t): sums of sub-blocks 2t and 2t+1
     const int mitems = nblk * B * 4;
     for (int it = tid; it < mitems; it += nthr) {
-        int t = it & 3;
-        int r = it >> 2;
-        int b = r % B;
-        int bl = r / B;
-        const float sc = s_scale[b];
-        const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K +
-                                                           static_cast<size_t>(kb0 + bl) * 256 + 64 * t);
+        const int t = it & 3;
+        const int r = it >> 2;
+        const int b = r % B;
+        const int bl = r / B;
+        const float sc = __uint_as_float(static_cast<uint32_t>(chunk_scale_exp(s_amax[b]) + 127) << 23);
+        const float4 *p = reinterpret_cast<const float4 *>(xraw + b * n + bl * 256 + 64 * t);
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            float4 v = __ldg(p + e);
+            const float4 v = p[e];
             s0 += (v.x * sc + v.y * sc) + (v.z * sc + v.w * sc);
         }
 #pragma unroll
         for (int e = 8; e < 16; ++e) {
-            float4 v = __ldg(p + e);
+            const float4 v = p[e];
             s1 += (v.x * sc + v.y * sc) + (v.z * sc + v.w * sc);
         }
-        uint32_t h = pack_half2(s0, s1);
-        uint32_t l = pack_half2(s0 - half_lo_f32(h), s1 - half_hi_f32(h));
+        const uint32_t h = pack_half2(s0, s1);
+        const uint32_t l = pack_half2(s0 - half_lo_f32(h), s1 - half_hi_f32(h));
         const int chi = 2 * b, clo = 2 * b + 1;
-        const size_t base = static_cast<size_t>(bl * kKsteps + 16) * NT;
+        const int base = (bl * kKsteps + 16) * NT;
         xf[(base + chi / 8) * LW + 4 * (chi % 8) + t] = make_uint2(h, 0u);
         xf[(base + clo / 8) * LW + 4 * (clo % 8) + t] = make_uint2(l, 0u);
     }
+    for (int b = tid; b < B; b += nthr)
+        s_unscale[b] = __uint_as_float(static_cast<uint32_t>(127 - chunk_scale_exp(s_amax[b])) << 23);
     named_bar_sync(1, nthr);
+    // every thread has read s_amax: clear it for the next chunk
+    for (int b = tid; b < B; b += nthr) s_amax[b] = 0u;
 }
 
 // Scale/min constants of one row of a super-block for thread t (pair t).
@@ -248,8 +273,9 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
     const int LW = frag_lanes(NT, B);
     uint2 *xf = reinterpret_cast<uint2 *>(smem_raw + xfrag_offset());
     float *s_red = reinterpret_cast<float *>(smem_raw + red_offset(NT, B, args.kc));
-    __shared__ __align__(8) uint64_t full[kStages], empty[kStages];
-    __shared__ float s_scale[16], s_unscale[16];
+    const float *xraw = reinterpret_cast<const float *>(smem_raw + xraw_offset(NT, B, args.kc));
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], xbar;
+    __shared__ float s_unscale[16];
     __shared__ uint32_t s_amax[16];
     __shared__ unsigned long long s_best[16];
     __shared__ int s_abort;
@@ -271,12 +297,14 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
             mbar_init(smem_u32(&full[i]), 1);
             mbar_init(smem_u32(&empty[i]), kWarps);
         }
+        mbar_init(smem_u32(&xbar), 1);
         s_abort = 0;
         s_issued = 0;
         for (int w = 0; w < kWarps; ++w) s_cons[w] = 0;
         fence_barrier_init();
     }
     if (ARGMAX && tid < 16) s_best[tid] = 0ull;
+    if (tid < 16) s_amax[tid] = 0u;
     if (warp == kWarps && lane == 0) prefetch_tensormap(&tmW);
     __syncthreads();
 
@@ -316,8 +344,10 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
         pdl_wait();                             // x may come from the previous kernel
         const int nchunks = (ks + args.kc - 1) / args.kc;
         const bool single_chunk = (nchunks == 1);
+        XChunkState xs{0u, 0};
         if (single_chunk)
-            convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_scale, s_unscale, s_amax, tid, kWarps * 32);
+            convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, xraw, &xbar, xs, s_unscale, s_amax, &s_abort,
+                                tid, kWarps * 32);
         // B-fragment lane of each n-tile.  Lanes whose column holds no batch row
         // read some other valid entry: MMA columns are independent, and those
         // output columns are never used.
@@ -340,8 +370,8 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
                 if (!single_chunk && kbl > chunk_end) {
                     const int cn = min(args.kc, ks - kbl);
                     named_bar_sync(1, kWarps * 32);     // everyone done with the previous chunk
-                    convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_scale, s_unscale, s_amax, tid,
-                                        kWarps * 32);
+                    convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, xraw, &xbar, xs, s_unscale,
+                                        s_amax, &s_abort, tid, kWarps * 32);
                     chunk_end = kbl + cn - 1;
                     reload_scale = true;
                 }
@@ -445,6 +475,9 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
             }
         }
         if (lane == 0) s_cons[warp] = consumed;
+        // after an abort, wait (bounded) for this CTA's last x copy too
+        if (tid == 0 && xs.issued && *(volatile int *)&s_abort)
+            mbar_wait_bounded(smem_u32(&xbar), xs.parity ^ 1u, kWaitLimitNs);
     }
 
     // After a timed-out wait, wait (bounded) for the bulk copies this CTA issued
@@ -583,7 +616,7 @@ static GemvPlan make_plan(int64_t N, int64_t K, int B, int sms, int forced_split
     }
     p.split = best_s;
     const int ks_max = (nb + p.split - 1) / p.split;
-    const size_t per_blk = xfrag_bytes_per_block(p.NT, B);
+    const size_t per_blk = xfrag_bytes_per_block(p.NT, B) + static_cast<size_t>(B) * 1024;
     const size_t fixed = gemv_smem_bytes(p.NT, B, 0);
     const size_t budget = (p.NT <= 2) ? kSmemPerCta2 : kSmemPerCta1;
     int kc = static_cast<int>(std::max<size_t>(1, (budget - fixed) / per_blk));
