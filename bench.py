@@ -2,8 +2,9 @@
 
 Headline (the JSON line's `value`): weight-streaming throughput in GB/s of one
 decode step of a Qwen2.5-7B-shaped model -- 28 layers x 7 Q4_K GEMVs (q, k, v,
-o, gate, up, down), batch 1 -- with all inputs resident in HBM, the 196
-launches replayed from a CUDA graph.  Algorithmic bytes per step = the Q4_K
+o, gate, up, down), batch 1 -- with all inputs resident in HBM, the step's
+launches (q/k/v fused into one, gate/up into one: 4 per layer) replayed from a
+CUDA graph.  Algorithmic bytes per step = the Q4_K
 weights (4.5 bits/weight) + fp32 activations read + fp32 outputs written.
 
 The same line carries the batch-2/5/9 VerifyBatch sweep, the fused LM-head +
@@ -273,10 +274,19 @@ def run_ours(args):
     def step_bytes(B):
         return LAYERS * sum(N * (K // 256) * 144 + 4 * B * K + 4 * B * N for _, N, K in shapes)
 
-    def decode_step(B, pdl=True):
+    def decode_step(B, pdl=True, fused=True):
+        """One decode step: 28 layers x 7 GEMVs.  fused: q/k/v share one launch
+        and gate/up share one (4 launches per layer); otherwise 7 launches."""
         for layer in range(LAYERS):
-            for mi, (name, N, K) in enumerate(shapes):
-                q4k.gemv(Ws[layer][mi], x_view(B, layer, src[name]), y_view(B, layer, mi), stream=stream, pdl=pdl)
+            W, y = Ws[layer], (lambda mi: y_view(B, layer, mi))
+            if fused:
+                q4k.gemv_grouped(W[0:3], x_view(B, layer, "attn"), [y(0), y(1), y(2)], stream=stream, pdl=pdl)
+                q4k.gemv(W[3], x_view(B, layer, "o"), y(3), stream=stream, pdl=pdl)
+                q4k.gemv_grouped(W[4:6], x_view(B, layer, "mlp"), [y(4), y(5)], stream=stream, pdl=pdl)
+                q4k.gemv(W[6], x_view(B, layer, "down"), y(6), stream=stream, pdl=pdl)
+            else:
+                for mi, (name, N, K) in enumerate(shapes):
+                    q4k.gemv(W[mi], x_view(B, layer, src[name]), y(mi), stream=stream, pdl=pdl)
 
     def capture(fn):
         g = torch.cuda.CUDAGraph()
@@ -317,6 +327,12 @@ def run_ours(args):
     bytes1 = step_bytes(1)
     value = whole_job_rate(bytes1, world, ms1 * 1e-3) / 1e9
 
+    # ---- the same step with one launch per matrix (196 launches), for contrast
+    g1u = capture(lambda: decode_step(1, fused=False))
+    ms1u = time_graph(g1u, max(20, args.steps // 4), args.warmup)
+    del g1u
+    unfused = {"gbs": bytes1 / (ms1u * 1e-3) / 1e9, "us_per_step": ms1u * 1e3, "launches_per_step": LAYERS * 7}
+
     # ---- VerifyBatch sweep (same weights)
     sweep = {}
     for B in (2, 5, 9):
@@ -342,8 +358,8 @@ def run_ours(args):
     del Wlm
 
     # ---- end to end through the public API with host buffers (batch 1):
-    # one H2D copy of every activation of the step, the graph of 196 q4k_gemv
-    # calls, one D2H copy of every output.
+    # one H2D copy of every activation of the step, the graph of the step's
+    # launches, one D2H copy of every output.
     nx1, ny1 = x_elems_per_row, y_elems_per_row
     h_x = torch.empty(nx1, dtype=torch.float32).pin_memory()
     h_x.copy_(x_flat[:nx1].cpu())
@@ -369,7 +385,7 @@ def run_ours(args):
     e2e_val = whole_job_rate(bytes1, world, e2e_ms * 1e-3) / 1e9
 
     # ---- roofline of the dominant kernel (the batch-1 GEMV; the step is only its launches)
-    launches_per_step = LAYERS * len(shapes)
+    launches_per_step = LAYERS * 4
     achieved = bytes1 / (ms1 * 1e-3) / 1e9
     tr = recorded_traffic()
     traffic = None
@@ -412,17 +428,19 @@ def run_ours(args):
                                "gate/up 18944x3584, down 3584x18944), batch 1",
                    "batch": 1, "layers": LAYERS, "weight_bytes_per_step": LAYERS * sum(N * (K // 256) * 144 for _, N, K in shapes),
                    "algorithmic_bytes_per_step": bytes1, "cuda_graph": True, "pdl": True,
+                   "fused_dispatch": "q/k/v in one launch, gate/up in one launch (4 launches per layer)",
                    "l2": "inputs larger than L2 (3.67 GB of weights streamed per step)",
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": value / world / pk["hbm_gbs"],
         "us_per_layer": ms1 * 1e3 / LAYERS,
         "tok_per_s_equiv": 1e3 / ms1,
+        "unfused_one_launch_per_matrix": unfused,
         "verify_batch": sweep,
         "lm_head_argmax": lm,
         "prefill": prefill,
         "roofline": roof,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "path": "one pinned H2D of all step activations, graph of 196 q4k_gemv calls, one D2H of all outputs"},
+                "ms_per_step": e2e_ms, "path": "one pinned H2D of all step activations, graph of the 112 launches, one D2H of all outputs"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": ck,
         "peaks": pk,

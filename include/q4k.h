@@ -177,6 +177,27 @@ typedef struct {
 q4k_status q4k_gemv_ex(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch,
                        void *stream, const q4k_launch_opts *opts);
 
+/*
+ * Fused dispatch: up to 4 matrices that multiply the same x (the q/k/v
+ * projections of a layer, or its gate/up pair) in one launch, each with its
+ * own output.  Same numbers as calling q4k_gemv per matrix with the same
+ * split (the row tiles of all matrices share one grid, so the automatic split
+ * may differ from the per-matrix one).  The dotLLM README lists this fusion
+ * for its CPU decode (News 2026-03 "Fused decode dispatch": Q/K/V 3->1,
+ * Gate/Up 2->1).
+ *   groups[g].W  Q4_K [N_g][K/256*144] (16-byte aligned), groups[g].y fp32
+ *   [batch][N_g]; every matrix has the same K; 1 <= ngroups <= 4; opts may be
+ *   NULL.  A matrix with N_g == 0 is skipped.
+ */
+typedef struct {
+    const void *W;
+    float *y;
+    int64_t N;
+} q4k_gemv_group;
+
+q4k_status q4k_gemv_grouped(const q4k_gemv_group *groups, int ngroups, const float *x, int64_t K,
+                            int batch, void *stream, const q4k_launch_opts *opts);
+
 /* Launch plan the automatic heuristics pick for a shape (for tests and
  * reports): out[0] = split_k, out[1] = number of CTAs, out[2] = rows per CTA
  * tile, out[3] = K blocks per x chunk held in shared memory. */

@@ -34,9 +34,14 @@ class LaunchOpts(ctypes.Structure):
     _fields_ = [("split_k", ctypes.c_int), ("flags", ctypes.c_uint), ("reserved", ctypes.c_int * 6)]
 
 
+class GemvGroup(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int64)]
+
+
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("q4k_status_string", "q4k_abi_version", "q4k_gemv", "q4k_gemv_argmax", "q4k_gemv_argmax_debug",
-           "q4k_gemv_argmax_noalloc", "q4k_gemm_prefill", "q4k_gemv_ex", "q4k_gemv_plan", "q4k_device_error_flags")
+           "q4k_gemv_argmax_noalloc", "q4k_gemm_prefill", "q4k_gemv_ex", "q4k_gemv_grouped", "q4k_gemv_plan",
+           "q4k_device_error_flags")
 
 
 def lib():
@@ -56,6 +61,8 @@ def lib():
         L.q4k_gemv.restype = I
         L.q4k_gemv_ex.argtypes = [P, P, P, I64, I64, I, P, ctypes.POINTER(LaunchOpts)]
         L.q4k_gemv_ex.restype = I
+        L.q4k_gemv_grouped.argtypes = [ctypes.POINTER(GemvGroup), I, P, I64, I, P, ctypes.POINTER(LaunchOpts)]
+        L.q4k_gemv_grouped.restype = I
         L.q4k_gemv_argmax.argtypes = [P, P, P, I64, I64, I, P]
         L.q4k_gemv_argmax.restype = I
         L.q4k_gemv_argmax_debug.argtypes = [P, P, P, P, I64, I64, I, P]
@@ -130,6 +137,30 @@ def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False):
         st = L.q4k_gemv(W.data_ptr(), x2.data_ptr(), y.data_ptr(), N, K, B, _stream_ptr(stream))
         _check("q4k_gemv", st)
     return y.view(N) if squeeze and y.dim() == 2 else y
+
+
+def gemv_grouped(Ws, x, ys=None, *, stream=None, split_k: int = 0, pdl: bool = False):
+    """Several Q4_K matrices times the same x in one launch: returns [y_g [B, N_g]]."""
+    import torch
+    if not 1 <= len(Ws) <= 4:
+        raise ValueError("1 to 4 matrices")
+    _dev(x, "x", torch.float32)
+    x2 = x.view(1, -1) if x.dim() == 1 else x
+    B, K = x2.shape
+    if ys is None:
+        ys = [torch.empty((B, W.shape[0]), dtype=torch.float32, device=x.device) for W in Ws]
+    arr = (GemvGroup * len(Ws))()
+    for i, (W, y) in enumerate(zip(Ws, ys)):
+        _dev(W, "W", torch.uint8)
+        _dev(y, "y", torch.float32)
+        N = _shape_wk(W, K)
+        if y.numel() != B * N:
+            raise ValueError("y has the wrong size")
+        arr[i] = GemvGroup(W.data_ptr(), y.data_ptr(), N)
+    o = LaunchOpts(split_k, Q4K_FLAG_PDL if pdl else 0)
+    st = lib().q4k_gemv_grouped(arr, len(Ws), x2.data_ptr(), K, B, _stream_ptr(stream), ctypes.byref(o))
+    _check("q4k_gemv_grouped", st)
+    return ys
 
 
 def gemv_argmax(W, x, idx=None, *, logits=None, stream=None):

@@ -31,6 +31,12 @@ q4k_status q4k_gemv_ex(const void *W, const float *x, float *y, int64_t N, int64
     return q4k::gemv_impl(W, x, y, N, K, batch, stream, opts);
 }
 
+q4k_status q4k_gemv_grouped(const q4k_gemv_group *groups, int ngroups, const float *x, int64_t K, int batch,
+                            void *stream, const q4k_launch_opts *opts)
+{
+    return q4k::gemv_grouped_impl(groups, ngroups, x, K, batch, stream, opts);
+}
+
 q4k_status q4k_gemv_argmax(const void *W, const float *x, int32_t *idx, int64_t N, int64_t K, int batch,
                            void *stream)
 {

@@ -68,13 +68,17 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
 __device__ unsigned int g_device_error = 0;   // bit 0: an mbarrier wait timed out
 
+constexpr int kMaxGroups = 4;             // matrices sharing x in one launch
+
 struct GemvArgs {
     const float *x;
-    float *y;            // may be null in the argmax variant (logits not wanted)
-    int N;
+    float *y[kMaxGroups];           // outputs per matrix (null in the argmax variant without logits)
+    int N[kMaxGroups];              // rows per matrix
+    int tile_start[kMaxGroups + 1]; // first row tile of each matrix in the concatenated tile space
+    int ngroups;
     int nb;              // super-blocks per row
     int B;               // batch
-    int tiles;           // ceil(N / kRows)
+    int tiles;           // total row tiles over all matrices
     int kc;              // super-blocks per x chunk in shared memory
     unsigned long long *keys;  // argmax: [B] 64-bit keys (zeroed), null otherwise
     unsigned int *ticket;      // argmax: CTA ticket (zeroed)
@@ -83,9 +87,15 @@ struct GemvArgs {
 
 __host__ __device__ inline int frag_lanes(int NT, int B) { return NT == 1 ? 8 * B : 32; }
 
+// B fragments are stored lane-major: the 17*NT entries (uint2) of one lane for
+// one super-block are contiguous, so a consumer lane reads them at constant
+// offsets from one base.  The per-lane stride is odd in 8-byte units for even
+// NT so that the 16 lanes of a wavefront hit distinct bank pairs.
+__host__ __device__ constexpr int lane_stride(int NT) { return kKsteps * NT + ((NT & 1) ? 0 : 1); }
+
 __host__ __device__ inline size_t xfrag_bytes_per_block(int NT, int B)
 {
-    return static_cast<size_t>(kKsteps) * NT * frag_lanes(NT, B) * 8;
+    return static_cast<size_t>(lane_stride(NT)) * frag_lanes(NT, B) * 8;
 }
 
 // Dynamic shared memory: [ring | x fragments | raw x chunk | partial sums (split-K)].
@@ -182,9 +192,9 @@ __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int k
         const uint32_t l01 = pack_half2(v.x - half_lo_f32(h01), v.z - half_hi_f32(h01));
         const uint32_t l23 = pack_half2(v.y - half_lo_f32(h23), v.w - half_hi_f32(h23));
         const int chi = 2 * b, clo = 2 * b + 1;
-        const int base = (bl * kKsteps + s) * NT;
-        xf[(base + chi / 8) * LW + 4 * (chi % 8) + t] = make_uint2(h01, h23);
-        xf[(base + clo / 8) * LW + 4 * (clo % 8) + t] = make_uint2(l01, l23);
+        constexpr int LS = lane_stride(NT);
+        xf[(bl * LW + 4 * (chi % 8) + t) * LS + s * NT + chi / 8] = make_uint2(h01, h23);
+        xf[(bl * LW + 4 * (clo % 8) + t) * LS + s * NT + clo / 8] = make_uint2(l01, l23);
     }
     // 3) min-term entries: items (bl, b, t): sums of sub-blocks 2t and 2t+1
     const int mitems = nblk * B * 4;
@@ -209,9 +219,9 @@ __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int k
         const uint32_t h = pack_half2(s0, s1);
         const uint32_t l = pack_half2(s0 - half_lo_f32(h), s1 - half_hi_f32(h));
         const int chi = 2 * b, clo = 2 * b + 1;
-        const int base = (bl * kKsteps + 16) * NT;
-        xf[(base + chi / 8) * LW + 4 * (chi % 8) + t] = make_uint2(h, 0u);
-        xf[(base + clo / 8) * LW + 4 * (clo % 8) + t] = make_uint2(l, 0u);
+        constexpr int LS = lane_stride(NT);
+        xf[(bl * LW + 4 * (chi % 8) + t) * LS + 16 * NT + chi / 8] = make_uint2(h, 0u);
+        xf[(bl * LW + 4 * (clo % 8) + t) * LS + 16 * NT + clo / 8] = make_uint2(l, 0u);
     }
     for (int b = tid; b < B; b += nthr)
         s_unscale[b] = __uint_as_float(static_cast<uint32_t>(127 - chunk_scale_exp(s_amax[b])) << 23);
@@ -263,9 +273,38 @@ __device__ __forceinline__ RowConsts decode_header(uint4 h, int t)
 // words; one stage = one super-block of all 128 tile rows (rows beyond N are
 // zero-filled by the TMA unit).
 // ---------------------------------------------------------------------------
+// One tensor map per matrix of the launch.
+struct WMaps {
+    CUtensorMap m[kMaxGroups];
+};
+
+// Matrix of a row tile and its per-matrix data, selected with compile-time
+// indices only (no dynamically indexed parameter arrays, hence no local copy).
+struct TileInfo {
+    int grp;
+    int row0;     // first row of the tile within its matrix
+    int N;
+    float *y;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const GemvArgs &a, int tile)
+{
+    TileInfo ti{0, tile * kRows, a.N[0], a.y[0]};
+#pragma unroll
+    for (int i = 1; i < kMaxGroups; ++i) {
+        if (i < a.ngroups && tile >= a.tile_start[i]) {
+            ti.grp = i;
+            ti.row0 = (tile - a.tile_start[i]) * kRows;
+            ti.N = a.N[i];
+            ti.y = a.y[i];
+        }
+    }
+    return ti;
+}
+
 template <int NT, bool ARGMAX>
-__global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
-    q4k_gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs args)
+__global__ void __maxnreg__((NT <= 2) ? 112 : 224)
+    q4k_gemv_kernel(const __grid_constant__ WMaps maps, const GemvArgs args)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint8_t *ring = smem_raw;
@@ -305,7 +344,11 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
     }
     if (ARGMAX && tid < 16) s_best[tid] = 0ull;
     if (tid < 16) s_amax[tid] = 0u;
-    if (warp == kWarps && lane == 0) prefetch_tensormap(&tmW);
+    if (warp == kWarps && lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kMaxGroups; ++i)
+            if (i < args.ngroups) prefetch_tensormap(&maps.m[i]);
+    }
     __syncthreads();
 
     pdl_launch_dependents();
@@ -318,6 +361,12 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
             uint32_t phase = 0;
             int issued = 0;
             for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
+                const TileInfo ti = tile_info(args, tile);
+                const CUtensorMap *map = &maps.m[0];
+#pragma unroll
+                for (int i = 1; i < kMaxGroups; ++i)
+                    if (i == ti.grp) map = &maps.m[i];
+                const int lrow0 = ti.row0;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     // After an abort the producer keeps walking the schedule
                     // without waiting or copying, so nothing ever blocks on it.
@@ -328,8 +377,8 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
                     }
                     if (!*(volatile int *)&s_abort) {
                         mbar_arrive_expect_tx(smem_u32(&full[stage]), kStageBytes);
-                        tma_load_2d_hint(smem_u32(ring + stage * kStageBytes), &tmW, kb * (kBlockBytes / 8),
-                                         tile * kRows, smem_u32(&full[stage]), policy);
+                        tma_load_2d_hint(smem_u32(ring + stage * kStageBytes), map, kb * (kBlockBytes / 8), lrow0,
+                                         smem_u32(&full[stage]), policy);
                         ++issued;
                     }
                     if (++stage == kStages) { stage = 0; phase ^= 1u; }
@@ -351,15 +400,16 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
         // B-fragment lane of each n-tile.  Lanes whose column holds no batch row
         // read some other valid entry: MMA columns are independent, and those
         // output columns are never used.
-        int blane[NT];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) blane[nt] = ((g + 8 * nt) < 2 * B) ? lane : (lane % LW);
+        const int blane = (g < 2 * B) ? lane : (lane % LW);   // NT > 1: LW == 32, every lane is a valid slot
         int stage = 0;
         uint32_t phase = 0;
         int consumed = 0;
         const int row_off = (warp * 16 + g) * kBlockBytes;
         for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
-            const int row0 = tile * kRows;
+            const TileInfo ti = tile_info(args, tile);
+            const int row0 = ti.row0;   // within matrix ti.grp
+            const int Ng = ti.N;
+            float *yg = ti.y;
             float acc[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
@@ -391,7 +441,9 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
                 }
                 const uint8_t *ra = ring + stage * kStageBytes + row_off;   // row g of this warp
                 const uint8_t *rb = ra + 8 * kBlockBytes;                    // row g + 8
-                const uint2 *xrow = xf + static_cast<size_t>(single_chunk ? kbl : (kbl % args.kc)) * kKsteps * NT * LW;
+                // this lane's B fragments of this super-block (lane-major layout)
+                const uint2 *xl = xf + static_cast<size_t>((single_chunk ? kbl : (kbl % args.kc)) * LW + blane) *
+                                           lane_stride(NT);
                 const RowConsts r0 = decode_header(*reinterpret_cast<const uint4 *>(ra), t);
                 const RowConsts r1 = decode_header(*reinterpret_cast<const uint4 *>(rb), t);
                 float cE[2][NT][4], cO[2][NT][4], cM[NT][4];
@@ -417,8 +469,8 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
                         const uint32_t p1 = hfma2_u32(and_or(c8, mhi, magic), r1.mulO, r1.addO);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
-                            const uint2 be = xrow[(2 * u * NT + nt) * LW + blane[nt]];
-                            const uint2 bo = xrow[((2 * u + 1) * NT + nt) * LW + blane[nt]];
+                            const uint2 be = xl[2 * u * NT + nt];
+                            const uint2 bo = xl[(2 * u + 1) * NT + nt];
                             if (u < 2) {   // first k-step of each accumulator chain
                                 mma_16816_z(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
                                 mma_16816_z(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
@@ -431,7 +483,7 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
                 }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const uint2 bm = xrow[(16 * NT + nt) * LW + blane[nt]];
+                    const uint2 bm = xl[16 * NT + nt];
                     mma_16816_z(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
                     const float s0 = ((cE[0][nt][0] + cE[1][nt][0]) + (cO[0][nt][0] + cO[1][nt][0])) +
                                      ((cE[0][nt][1] + cE[1][nt][1]) + (cO[0][nt][1] + cO[1][nt][1]));
@@ -457,9 +509,9 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int row = row0 + warp * 16 + g + 8 * h;
-                        if (b < B && row < args.N) {
+                        if (b < B && row < Ng) {
                             const float v = acc[nt][h];
-                            if (args.y) args.y[static_cast<size_t>(b) * args.N + row] = v;
+                            if (yg) yg[static_cast<size_t>(b) * Ng + row] = v;
                             if (ARGMAX && !isnan(v)) atomicMax(&s_best[b], argmax_key(v, static_cast<uint32_t>(row)));
                         }
                     }
@@ -497,7 +549,10 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
         // over ranks 0..split-1 in order.
         cluster_sync_all();
         if (!*(volatile int *)&s_abort) {
-            const int row0 = blockIdx.x * kRows;
+            const TileInfo ti = tile_info(args, blockIdx.x);
+            const int row0 = ti.row0;
+            const int Ng = ti.N;
+            float *yg = ti.y;
             const int lr0 = (rank * kRows) / split;
             const int lr1 = ((rank + 1) * kRows) / split;
             const int items = (lr1 - lr0) * B;
@@ -509,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, (NT <= 2) ? 2 : 1)
                 float sum = 0.f;
                 for (int q = 0; q < split; ++q) sum += ld_shared_cluster_f32(map_shared_rank(red_local + off, q));
                 const int row = row0 + lr;
-                if (row < args.N) {
-                    if (args.y) args.y[static_cast<size_t>(b) * args.N + row] = sum;
+                if (row < Ng) {
+                    if (yg) yg[static_cast<size_t>(b) * Ng + row] = sum;
                     if (ARGMAX && !isnan(sum)) atomicMax(&s_best[b], argmax_key(sum, static_cast<uint32_t>(row)));
                 }
             }
@@ -589,12 +644,12 @@ static int batch_ntiles(int B) { return (2 * B + 7) / 8; }
 
 // Pick the K split: minimise (max row-tile units per SM) x (blocks per unit
 // + per-CTA overhead), preferring fewer CTAs on ties.
-static GemvPlan make_plan(int64_t N, int64_t K, int B, int sms, int forced_split)
+static GemvPlan make_plan(int tiles, int64_t K, int B, int sms, int forced_split)
 {
     GemvPlan p{};
     const int nb = static_cast<int>(K / 256);
     p.NT = batch_ntiles(B);
-    p.tiles = static_cast<int>((N + kRows - 1) / kRows);
+    p.tiles = tiles;
     int best_s = 1;
     if (forced_split > 0) {
         best_s = std::min(std::min(forced_split, nb), 8);
@@ -664,7 +719,7 @@ static bool encode_w_map(CUtensorMap *map, const void *W, int64_t N, int64_t K)
 }
 
 template <int NT, bool ARGMAX>
-static cudaError_t launch_one(const GemvPlan &p, const CUtensorMap &map, const GemvArgs &a, cudaStream_t stream,
+static cudaError_t launch_one(const GemvPlan &p, const WMaps &maps, const GemvArgs &a, cudaStream_t stream,
                               bool pdl)
 {
     auto kern = q4k_gemv_kernel<NT, ARGMAX>;
@@ -702,22 +757,26 @@ static cudaError_t launch_one(const GemvPlan &p, const CUtensorMap &map, const G
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, map, a);
+    return cudaLaunchKernelEx(&cfg, kern, maps, a);
 }
 
 template <bool ARGMAX>
-static cudaError_t launch_gemv(const GemvPlan &p, const void *W, int64_t N, int64_t K, const GemvArgs &a,
+static cudaError_t launch_gemv(const GemvPlan &p, const void *const *Ws, int64_t K, const GemvArgs &a,
                                cudaStream_t s, bool pdl)
 {
-    CUtensorMap map;
-    if (!encode_w_map(&map, W, N, K)) return cudaErrorInvalidValue;
+    WMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    for (int g = 0; g < a.ngroups; ++g)
+        if (!encode_w_map(&maps.m[g], Ws[g], a.N[g], K)) return cudaErrorInvalidValue;
     switch (p.NT) {
-        case 1: return launch_one<1, ARGMAX>(p, map, a, s, pdl);
-        case 2: return launch_one<2, ARGMAX>(p, map, a, s, pdl);
-        case 3: return launch_one<3, ARGMAX>(p, map, a, s, pdl);
-        default: return launch_one<4, ARGMAX>(p, map, a, s, pdl);
+        case 1: return launch_one<1, ARGMAX>(p, maps, a, s, pdl);
+        case 2: return launch_one<2, ARGMAX>(p, maps, a, s, pdl);
+        case 3: return launch_one<3, ARGMAX>(p, maps, a, s, pdl);
+        default: return launch_one<4, ARGMAX>(p, maps, a, s, pdl);
     }
 }
+
+static int row_tiles(int64_t N) { return static_cast<int>((N + kRows - 1) / kRows); }
 
 static q4k_status validate(const void *W, const void *x, const void *out, int64_t N, int64_t K, int batch,
                            bool argmax)
@@ -743,17 +802,61 @@ q4k_status gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t
     if (N == 0) return Q4K_OK;
     const int forced = opts ? opts->split_k : 0;
     if (forced < 0 || forced > 8) return Q4K_ERR_INVALID_ARG;
-    GemvPlan p = make_plan(N, K, batch, sms, forced);
+    GemvPlan p = make_plan(row_tiles(N), K, batch, sms, forced);
     GemvArgs a{};
     a.x = x;
-    a.y = y;
-    a.N = static_cast<int>(N);
+    a.y[0] = y;
+    a.N[0] = static_cast<int>(N);
+    a.ngroups = 1;
+    a.tile_start[0] = 0;
+    a.tile_start[1] = p.tiles;
     a.nb = static_cast<int>(K / 256);
     a.B = batch;
     a.tiles = p.tiles;
     a.kc = p.kc;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
-    cudaError_t e = launch_gemv<false>(p, W, N, K, a, static_cast<cudaStream_t>(stream), pdl);
+    cudaError_t e = launch_gemv<false>(p, &W, K, a, static_cast<cudaStream_t>(stream), pdl);
+    return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
+}
+
+q4k_status gemv_grouped_impl(const q4k_gemv_group *groups, int ngroups, const float *x, int64_t K, int batch,
+                             void *stream, const q4k_launch_opts *opts)
+{
+    if (!groups || ngroups < 1 || ngroups > kMaxGroups) return Q4K_ERR_INVALID_ARG;
+    int64_t total = 0;
+    for (int g = 0; g < ngroups; ++g) {
+        q4k_status st = validate(groups[g].W, x, groups[g].y, groups[g].N, K, batch, false);
+        if (st != Q4K_OK) return st;
+        total += groups[g].N;
+    }
+    int sms = 0;
+    q4k_status st = check_device(&sms);
+    if (st != Q4K_OK) return st;
+    const int forced = opts ? opts->split_k : 0;
+    if (forced < 0 || forced > 8) return Q4K_ERR_INVALID_ARG;
+    GemvArgs a{};
+    const void *Ws[kMaxGroups] = {nullptr, nullptr, nullptr, nullptr};
+    int tiles = 0;
+    for (int g = 0; g < ngroups; ++g) {
+        if (groups[g].N == 0) continue;          // empty matrices take no tiles
+        const int i = a.ngroups++;
+        Ws[i] = groups[g].W;
+        a.y[i] = groups[g].y;
+        a.N[i] = static_cast<int>(groups[g].N);
+        a.tile_start[i] = tiles;
+        tiles += row_tiles(groups[g].N);
+    }
+    if (a.ngroups == 0) return Q4K_OK;
+    a.tile_start[a.ngroups] = tiles;
+    (void)total;
+    GemvPlan p = make_plan(tiles, K, batch, sms, forced);
+    a.x = x;
+    a.nb = static_cast<int>(K / 256);
+    a.B = batch;
+    a.tiles = p.tiles;
+    a.kc = p.kc;
+    const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
+    cudaError_t e = launch_gemv<false>(p, Ws, K, a, static_cast<cudaStream_t>(stream), pdl);
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
@@ -769,11 +872,14 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int forced = opts ? opts->split_k : 0;
     if (forced < 0 || forced > 8) return Q4K_ERR_INVALID_ARG;
-    GemvPlan p = make_plan(N, K, batch, sms, forced);
+    GemvPlan p = make_plan(row_tiles(N), K, batch, sms, forced);
     GemvArgs a{};
     a.x = x;
-    a.y = logits;
-    a.N = static_cast<int>(N);
+    a.y[0] = logits;
+    a.N[0] = static_cast<int>(N);
+    a.ngroups = 1;
+    a.tile_start[0] = 0;
+    a.tile_start[1] = p.tiles;
     a.nb = static_cast<int>(K / 256);
     a.B = batch;
     a.tiles = p.tiles;
@@ -794,7 +900,7 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
         a.keys = scratch_keys;
         a.ticket = scratch_ticket;
     }
-    cudaError_t e = launch_gemv<true>(p, W, N, K, a, s, pdl);
+    cudaError_t e = launch_gemv<true>(p, &W, K, a, s, pdl);
     if (buf) {
         cudaError_t e2 = cudaFreeAsync(buf, s);
         if (e == cudaSuccess) e = e2;
@@ -855,7 +961,7 @@ q4k_status gemv_plan_impl(int64_t N, int64_t K, int batch, int out[4])
     int sms = 0;
     q4k_status st = check_device(&sms);
     if (st != Q4K_OK) return st;
-    GemvPlan p = make_plan(N, K, batch, sms, 0);
+    GemvPlan p = make_plan(row_tiles(N), K, batch, sms, 0);
     out[0] = p.split;
     out[1] = p.grid_x * p.split;
     out[2] = kRows;

@@ -17,6 +17,8 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
                             int batch, void *stream, unsigned long long *scratch_keys, unsigned int *scratch_ticket,
                             const q4k_launch_opts *opts);
 q4k_status gemv_plan_impl(int64_t N, int64_t K, int batch, int out[4]);
+q4k_status gemv_grouped_impl(const q4k_gemv_group *groups, int ngroups, const float *x, int64_t K, int batch,
+                             void *stream, const q4k_launch_opts *opts);
 q4k_status gemv_argmax_noalloc_impl(const void *W, const float *x, int32_t *idx, int64_t N, int64_t K, int batch,
                                     void *stream);
 q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream);
