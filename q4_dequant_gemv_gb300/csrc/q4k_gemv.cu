@@ -303,8 +303,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemvArgs &a, int tile)
 }
 
 template <int NT, bool ARGMAX>
-__global__ void __maxnreg__((NT <= 2) ? 112 : 224)
-    q4k_gemv_kernel(const __grid_constant__ WMaps maps, const GemvArgs args)
+__device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &args)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint8_t *ring = smem_raw;
@@ -592,6 +591,21 @@ __global__ void __maxnreg__((NT <= 2) ? 112 : 224)
     }
 }
 
+// Batch <= 8 (one or two n8 tiles): at most 112 registers, two CTAs per SM.
+template <int NT, bool ARGMAX>
+__global__ void __maxnreg__(112) q4k_gemv_kernel(const __grid_constant__ WMaps maps, const GemvArgs args)
+{
+    gemv_body<NT, ARGMAX>(maps, args);
+}
+
+// Batch 9..16 (three or four n8 tiles): one CTA per SM, registers as needed.
+template <int NT, bool ARGMAX>
+__global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel_wide(const __grid_constant__ WMaps maps,
+                                                                   const GemvArgs args)
+{
+    gemv_body<NT, ARGMAX>(maps, args);
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -722,7 +736,11 @@ template <int NT, bool ARGMAX>
 static cudaError_t launch_one(const GemvPlan &p, const WMaps &maps, const GemvArgs &a, cudaStream_t stream,
                               bool pdl)
 {
-    auto kern = q4k_gemv_kernel<NT, ARGMAX>;
+    void (*kern)(const WMaps, const GemvArgs);
+    if constexpr (NT <= 2)
+        kern = q4k_gemv_kernel<NT, ARGMAX>;
+    else
+        kern = q4k_gemv_kernel_wide<NT, ARGMAX>;
     static std::mutex mu;
     static int smem_set[64] = {0};   // per device: largest dynamic smem size already allowed
     int dev = 0;
@@ -757,7 +775,9 @@ static cudaError_t launch_one(const GemvPlan &p, const WMaps &maps, const GemvAr
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, maps, a);
+    e = cudaLaunchKernelEx(&cfg, kern, maps, a);
+    if (e != cudaSuccess) (void)cudaGetLastError();   // a failed launch leaves no sticky error behind
+    return e;
 }
 
 template <bool ARGMAX>
