@@ -149,7 +149,6 @@ __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int k
     const int LW = frag_lanes(NT, B);
     const int n = nblk * 256;                       // floats per batch row in the chunk
     if (tid == 0) {
-        fence_proxy_async_smem();                   // prior generic reads of xraw happen first
         mbar_arrive_expect_tx(smem_u32(xbar), static_cast<uint32_t>(B * n * 4));
         for (int b = 0; b < B; ++b)
             bulk_g2s(smem_u32(xraw + b * n), x + static_cast<size_t>(b) * K + static_cast<size_t>(kb0) * 256,
@@ -591,9 +590,10 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     }
 }
 
-// Batch <= 8 (one or two n8 tiles): at most 112 registers, two CTAs per SM.
+// Batch <= 8 (one or two n8 tiles): at most 104 registers, so that two CTAs of
+// 288 threads fit in the register file of an SM.
 template <int NT, bool ARGMAX>
-__global__ void __maxnreg__(112) q4k_gemv_kernel(const __grid_constant__ WMaps maps, const GemvArgs args)
+__global__ void __maxnreg__(104) q4k_gemv_kernel(const __grid_constant__ WMaps maps, const GemvArgs args)
 {
     gemv_body<NT, ARGMAX>(maps, args);
 }
@@ -750,6 +750,10 @@ static cudaError_t launch_one(const GemvPlan &p, const WMaps &maps, const GemvAr
         std::lock_guard<std::mutex> lk(mu);
         if (smem_set[dev & 63] < static_cast<int>(p.smem)) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(p.smem));
+            if (e != cudaSuccess) return e;
+            // all of the unified L1 / shared array as shared memory, so that two
+            // CTAs fit on an SM
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
             if (e != cudaSuccess) return e;
             smem_set[dev & 63] = static_cast<int>(p.smem);
         }
