@@ -56,9 +56,9 @@
 namespace q4k {
 
 constexpr int kBlockBytes = 144;
-constexpr int kWarps = 8;                 // consumer warps per CTA
+constexpr int kWarps = 8;                 // warps per CTA, 16 weight rows each
 constexpr int kRows = 16 * kWarps;        // rows per tile (128)
-constexpr int kThreads = 32 * (kWarps + 1);
+constexpr int kThreads = 32 * kWarps;
 constexpr int kKsteps = 17;               // 16 k16 steps + 1 min-term step per super-block
 constexpr int kStages = 3;                // W ring depth
 constexpr int kStageBytes = kRows * kBlockBytes;   // one super-block of every tile row (18 KB)
@@ -266,7 +266,11 @@ __device__ __forceinline__ RowConsts decode_header(uint4 h, int t)
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.  Warps 0..7 consume (16 rows each), warp 8 produces.
+// The kernel body.  All 8 warps consume (16 rows each); there is no producer
+// warp.  Thread 0 issues the first kStages weight stages right after
+// initialising the barriers; afterwards the last warp to finish reading a
+// stage (a shared-memory counter per ring slot) refills that slot with the
+// stage kStages ahead, so no thread ever waits for a slot to drain.
 // grid = (row-tile CTAs, split) with cluster dims (1, split, 1) when split > 1.
 // W is read through a 2-D TMA tensor map: [N rows] x [K/256 * 18] 8-byte
 // words; one stage = one super-block of all 128 tile rows (rows beyond N are
@@ -301,6 +305,31 @@ __device__ __forceinline__ TileInfo tile_info(const GemvArgs &a, int tile)
     return ti;
 }
 
+struct StageIssuer {
+    const WMaps *maps;
+    const GemvArgs *args;
+    int kb_begin, ks, total;    // this CTA's schedule: total = tiles_of_cta * ks stages
+    uint8_t *ring;
+    uint64_t *full;
+    uint64_t policy;
+
+    // Issue global stage i of this CTA's schedule into ring slot i % kStages.
+    __device__ __forceinline__ void issue(int i) const
+    {
+        const int tile = blockIdx.x + (i / ks) * gridDim.x;
+        const int kb = kb_begin + i % ks;
+        const TileInfo ti = tile_info(*args, tile);
+        const CUtensorMap *map = &maps->m[0];
+#pragma unroll
+        for (int g = 1; g < kMaxGroups; ++g)
+            if (g == ti.grp) map = &maps->m[g];
+        const int slot = i % kStages;
+        mbar_arrive_expect_tx(smem_u32(&full[slot]), kStageBytes);
+        tma_load_2d_hint(smem_u32(ring + slot * kStageBytes), map, kb * (kBlockBytes / 8), ti.row0,
+                         smem_u32(&full[slot]), policy);
+    }
+};
+
 template <int NT, bool ARGMAX>
 __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &args)
 {
@@ -311,12 +340,13 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     uint2 *xf = reinterpret_cast<uint2 *>(smem_raw + xfrag_offset());
     float *s_red = reinterpret_cast<float *>(smem_raw + red_offset(NT, B, args.kc));
     const float *xraw = reinterpret_cast<const float *>(smem_raw + xraw_offset(NT, B, args.kc));
-    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], xbar;
+    __shared__ __align__(8) uint64_t full[kStages], xbar;
     __shared__ float s_unscale[16];
     __shared__ uint32_t s_amax[16];
     __shared__ unsigned long long s_best[16];
     __shared__ int s_abort;
-    __shared__ int s_issued;
+    __shared__ int s_issued;                 // stages issued so far (for the abort drain)
+    __shared__ int s_slot_done[kStages];     // warp arrivals per ring slot (monotonic)
     __shared__ int s_cons[kWarps];
 
     const int tid = threadIdx.x;
@@ -328,229 +358,207 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     const int kb_begin = static_cast<int>((static_cast<long long>(rank) * nb) / split);
     const int kb_end = static_cast<int>((static_cast<long long>(rank + 1) * nb) / split);
     const int ks = kb_end - kb_begin;
+    const int my_tiles = (args.tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                         static_cast<int>(gridDim.x);
+    StageIssuer iss{&maps, &args, kb_begin, ks, my_tiles * ks, ring, full, 0ull};
 
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
-            mbar_init(smem_u32(&empty[i]), kWarps);
+            s_slot_done[i] = 0;
         }
         mbar_init(smem_u32(&xbar), 1);
         s_abort = 0;
-        s_issued = 0;
-        for (int w = 0; w < kWarps; ++w) s_cons[w] = 0;
         fence_barrier_init();
+#pragma unroll
+        for (int g = 0; g < kMaxGroups; ++g)
+            if (g < args.ngroups) prefetch_tensormap(&maps.m[g]);
+        // the first stages stream in while the CTA sets up (weights never
+        // depend on the previous kernel)
+        iss.policy = l2_policy_evict_first();
+        const int first = min(kStages, iss.total);
+        for (int i = 0; i < first; ++i) iss.issue(i);
+        s_issued = first;
     }
     if (ARGMAX && tid < 16) s_best[tid] = 0ull;
     if (tid < 16) s_amax[tid] = 0u;
-    if (warp == kWarps && lane == 0) {
-#pragma unroll
-        for (int i = 0; i < kMaxGroups; ++i)
-            if (i < args.ngroups) prefetch_tensormap(&maps.m[i]);
-    }
+    if (tid < kWarps) s_cons[tid] = 0;
     __syncthreads();
+    iss.policy = l2_policy_evict_first();
 
     pdl_launch_dependents();
+    pdl_wait();                             // x may come from the previous kernel
 
-    if (warp == kWarps) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_first();
-            int stage = 0;
-            uint32_t phase = 0;
-            int issued = 0;
-            for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
-                const TileInfo ti = tile_info(args, tile);
-                const CUtensorMap *map = &maps.m[0];
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int nchunks = (ks + args.kc - 1) / args.kc;
+    const bool single_chunk = (nchunks == 1);
+    XChunkState xs{0u, 0};
+    if (single_chunk)
+        convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, xraw, &xbar, xs, s_unscale, s_amax, &s_abort, tid,
+                            kThreads);
+    // B-fragment lane.  Lanes whose column holds no batch row read some other
+    // valid entry: MMA columns are independent, and those output columns are
+    // never used.
+    const int blane = (g < 2 * B) ? lane : (lane % LW);   // NT > 1: LW == 32, every lane is a valid slot
+    int consumed = 0;
+    const int row_off = (warp * 16 + g) * kBlockBytes;
+    for (int ti_idx = 0; ti_idx < my_tiles; ++ti_idx) {
+        const int tile = blockIdx.x + ti_idx * gridDim.x;
+        const TileInfo ti = tile_info(args, tile);
+        const int row0 = ti.row0;   // within matrix ti.grp
+        const int Ng = ti.N;
+        float *yg = ti.y;
+        float acc[NT][2];
 #pragma unroll
-                for (int i = 1; i < kMaxGroups; ++i)
-                    if (i == ti.grp) map = &maps.m[i];
-                const int lrow0 = ti.row0;
-                for (int kb = kb_begin; kb < kb_end; ++kb) {
-                    // After an abort the producer keeps walking the schedule
-                    // without waiting or copying, so nothing ever blocks on it.
-                    if (!*(volatile int *)&s_abort &&
-                        !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
-                        atomicOr(&g_device_error, 1u);
-                        s_abort = 1;
-                    }
-                    if (!*(volatile int *)&s_abort) {
-                        mbar_arrive_expect_tx(smem_u32(&full[stage]), kStageBytes);
-                        tma_load_2d_hint(smem_u32(ring + stage * kStageBytes), map, kb * (kBlockBytes / 8), lrow0,
-                                         smem_u32(&full[stage]), policy);
-                        ++issued;
-                    }
-                    if (++stage == kStages) { stage = 0; phase ^= 1u; }
-                }
+        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
+        float unscale[NT];
+        int chunk_end = -1;
+        bool reload_scale = true;
+        for (int kbl = 0; kbl < ks; ++kbl) {
+            if (!single_chunk && kbl > chunk_end) {
+                const int cn = min(args.kc, ks - kbl);
+                named_bar_sync(1, kThreads);     // everyone done with the previous chunk
+                convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, xraw, &xbar, xs, s_unscale, s_amax,
+                                    &s_abort, tid, kThreads);
+                chunk_end = kbl + cn - 1;
+                reload_scale = true;
             }
-            s_issued = issued;
-        }
-    } else {
-        // ------------------------------------------------------------ consumers
-        const int g = lane >> 2;
-        const int t = lane & 3;
-        pdl_wait();                             // x may come from the previous kernel
-        const int nchunks = (ks + args.kc - 1) / args.kc;
-        const bool single_chunk = (nchunks == 1);
-        XChunkState xs{0u, 0};
-        if (single_chunk)
-            convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, xraw, &xbar, xs, s_unscale, s_amax, &s_abort,
-                                tid, kWarps * 32);
-        // B-fragment lane of each n-tile.  Lanes whose column holds no batch row
-        // read some other valid entry: MMA columns are independent, and those
-        // output columns are never used.
-        const int blane = (g < 2 * B) ? lane : (lane % LW);   // NT > 1: LW == 32, every lane is a valid slot
-        int stage = 0;
-        uint32_t phase = 0;
-        int consumed = 0;
-        const int row_off = (warp * 16 + g) * kBlockBytes;
-        for (int tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
-            const TileInfo ti = tile_info(args, tile);
-            const int row0 = ti.row0;   // within matrix ti.grp
-            const int Ng = ti.N;
-            float *yg = ti.y;
-            float acc[NT][2];
+            if (reload_scale) {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
-            float unscale[NT];
-            int chunk_end = -1;
-            bool reload_scale = true;
-            for (int kbl = 0; kbl < ks; ++kbl) {
-                if (!single_chunk && kbl > chunk_end) {
-                    const int cn = min(args.kc, ks - kbl);
-                    named_bar_sync(1, kWarps * 32);     // everyone done with the previous chunk
-                    convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, xraw, &xbar, xs, s_unscale,
-                                        s_amax, &s_abort, tid, kWarps * 32);
-                    chunk_end = kbl + cn - 1;
-                    reload_scale = true;
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int b = t + 4 * nt;
+                    unscale[nt] = (b < B) ? s_unscale[b] : 0.f;
                 }
-                if (reload_scale) {
+                reload_scale = false;
+            }
+            const int slot = consumed % kStages;
+            const uint32_t phase = static_cast<uint32_t>((consumed / kStages) & 1);
+            // After an abort the warps keep walking the same schedule (every
+            // named barrier is still reached) but stop waiting.
+            if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), phase, kWaitLimitNs)) {
+                atomicOr(&g_device_error, 1u);
+                s_abort = 1;
+            }
+            const uint8_t *ra = ring + slot * kStageBytes + row_off;   // row g of this warp
+            const uint8_t *rb = ra + 8 * kBlockBytes;                   // row g + 8
+            // this lane's B fragments of this super-block (lane-major layout)
+            const uint2 *xl = xf + static_cast<size_t>((single_chunk ? kbl : (kbl % args.kc)) * LW + blane) *
+                                       lane_stride(NT);
+            const RowConsts r0 = decode_header(*reinterpret_cast<const uint4 *>(ra), t);
+            const RowConsts r1 = decode_header(*reinterpret_cast<const uint4 *>(rb), t);
+            float cE[2][NT][4], cO[2][NT][4], cM[NT][4];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const uint4 qa = *reinterpret_cast<const uint4 *>(ra + 16 + 32 * t + 16 * half);
+                const uint4 qb = *reinterpret_cast<const uint4 *>(rb + 16 + 32 * t + 16 * half);
+                const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+                const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+                for (int uu = 0; uu < 4; ++uu) {
+                    const int u = 4 * half + uu;
+                    const uint32_t a = wa[uu], a8 = a >> 8;
+                    const uint32_t c = wb[uu], c8 = c >> 8;
+                    const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
+                    const uint32_t e0 = hfma2_u32(and_or(a, mlo, magic), r0.mulE, r0.addE);
+                    const uint32_t e1 = hfma2_u32(and_or(a8, mlo, magic), r0.mulE, r0.addE);
+                    const uint32_t o0 = hfma2_u32(and_or(a, mhi, magic), r0.mulO, r0.addO);
+                    const uint32_t o1 = hfma2_u32(and_or(a8, mhi, magic), r0.mulO, r0.addO);
+                    const uint32_t f0 = hfma2_u32(and_or(c, mlo, magic), r1.mulE, r1.addE);
+                    const uint32_t f1 = hfma2_u32(and_or(c8, mlo, magic), r1.mulE, r1.addE);
+                    const uint32_t p0 = hfma2_u32(and_or(c, mhi, magic), r1.mulO, r1.addO);
+                    const uint32_t p1 = hfma2_u32(and_or(c8, mhi, magic), r1.mulO, r1.addO);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const int b = t + 4 * nt;
-                        unscale[nt] = (b < B) ? s_unscale[b] : 0.f;
-                    }
-                    reload_scale = false;
-                }
-                // After an abort the consumers keep walking the same schedule
-                // (every named barrier is still reached) but stop waiting.
-                if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[stage]), phase, kWaitLimitNs)) {
-                    atomicOr(&g_device_error, 1u);
-                    s_abort = 1;
-                }
-                const uint8_t *ra = ring + stage * kStageBytes + row_off;   // row g of this warp
-                const uint8_t *rb = ra + 8 * kBlockBytes;                    // row g + 8
-                // this lane's B fragments of this super-block (lane-major layout)
-                const uint2 *xl = xf + static_cast<size_t>((single_chunk ? kbl : (kbl % args.kc)) * LW + blane) *
-                                           lane_stride(NT);
-                const RowConsts r0 = decode_header(*reinterpret_cast<const uint4 *>(ra), t);
-                const RowConsts r1 = decode_header(*reinterpret_cast<const uint4 *>(rb), t);
-                float cE[2][NT][4], cO[2][NT][4], cM[NT][4];
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const uint4 qa = *reinterpret_cast<const uint4 *>(ra + 16 + 32 * t + 16 * half);
-                    const uint4 qb = *reinterpret_cast<const uint4 *>(rb + 16 + 32 * t + 16 * half);
-                    const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
-                    const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-                    for (int uu = 0; uu < 4; ++uu) {
-                        const int u = 4 * half + uu;
-                        const uint32_t a = wa[uu], a8 = a >> 8;
-                        const uint32_t c = wb[uu], c8 = c >> 8;
-                        const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
-                        const uint32_t e0 = hfma2_u32(and_or(a, mlo, magic), r0.mulE, r0.addE);
-                        const uint32_t e1 = hfma2_u32(and_or(a8, mlo, magic), r0.mulE, r0.addE);
-                        const uint32_t o0 = hfma2_u32(and_or(a, mhi, magic), r0.mulO, r0.addO);
-                        const uint32_t o1 = hfma2_u32(and_or(a8, mhi, magic), r0.mulO, r0.addO);
-                        const uint32_t f0 = hfma2_u32(and_or(c, mlo, magic), r1.mulE, r1.addE);
-                        const uint32_t f1 = hfma2_u32(and_or(c8, mlo, magic), r1.mulE, r1.addE);
-                        const uint32_t p0 = hfma2_u32(and_or(c, mhi, magic), r1.mulO, r1.addO);
-                        const uint32_t p1 = hfma2_u32(and_or(c8, mhi, magic), r1.mulO, r1.addO);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const uint2 be = xl[2 * u * NT + nt];
-                            const uint2 bo = xl[(2 * u + 1) * NT + nt];
-                            if (u < 2) {   // first k-step of each accumulator chain
-                                mma_16816_z(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
-                                mma_16816_z(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
-                            } else {
-                                mma_16816(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
-                                mma_16816(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
-                            }
+                        const uint2 be = xl[2 * u * NT + nt];
+                        const uint2 bo = xl[(2 * u + 1) * NT + nt];
+                        if (u < 2) {   // first k-step of each accumulator chain
+                            mma_16816_z(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
+                            mma_16816_z(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
+                        } else {
+                            mma_16816(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
+                            mma_16816(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
                         }
                     }
                 }
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const uint2 bm = xl[16 * NT + nt];
-                    mma_16816_z(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
-                    const float s0 = ((cE[0][nt][0] + cE[1][nt][0]) + (cO[0][nt][0] + cO[1][nt][0])) +
-                                     ((cE[0][nt][1] + cE[1][nt][1]) + (cO[0][nt][1] + cO[1][nt][1]));
-                    const float s1 = ((cE[0][nt][2] + cE[1][nt][2]) + (cO[0][nt][2] + cO[1][nt][2])) +
-                                     ((cE[0][nt][3] + cE[1][nt][3]) + (cO[0][nt][3] + cO[1][nt][3]));
-                    const float m0 = cM[nt][0] + cM[nt][1];
-                    const float m1 = cM[nt][2] + cM[nt][3];
-                    acc[nt][0] = fmaf(r0.d * unscale[nt], s0, acc[nt][0]);
-                    acc[nt][0] = fmaf(-r0.dmin * unscale[nt], m0, acc[nt][0]);
-                    acc[nt][1] = fmaf(r1.d * unscale[nt], s1, acc[nt][1]);
-                    acc[nt][1] = fmaf(-r1.dmin * unscale[nt], m1, acc[nt][1]);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
-                ++consumed;
-                if (++stage == kStages) { stage = 0; phase ^= 1u; }
             }
-            // ---------------- tile epilogue
-            if (split == 1 && !*(volatile int *)&s_abort) {
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int b = t + 4 * nt;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int row = row0 + warp * 16 + g + 8 * h;
-                        if (b < B && row < Ng) {
-                            const float v = acc[nt][h];
-                            if (yg) yg[static_cast<size_t>(b) * Ng + row] = v;
-                            if (ARGMAX && !isnan(v)) atomicMax(&s_best[b], argmax_key(v, static_cast<uint32_t>(row)));
-                        }
+            // This warp is done with the slot: the last warp to finish refills it.
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                // monotonic per-slot count: the kWarps-th arrival of each round is last
+                const int prev = atomicAdd(&s_slot_done[slot], 1);
+                if (prev % kWarps == kWarps - 1) {
+                    const int next = consumed + kStages;
+                    if (next < iss.total && !*(volatile int *)&s_abort) {
+                        iss.issue(next);
+                        atomicAdd(&s_issued, 1);
                     }
                 }
-            } else if (split > 1) {
+            }
+            ++consumed;
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int b = t + 4 * nt;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        if (b < B) s_red[(warp * 16 + g + 8 * h) * B + b] = acc[nt][h];
-                }
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint2 bm = xl[16 * NT + nt];
+                mma_16816_z(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
+                const float s0 = ((cE[0][nt][0] + cE[1][nt][0]) + (cO[0][nt][0] + cO[1][nt][0])) +
+                                 ((cE[0][nt][1] + cE[1][nt][1]) + (cO[0][nt][1] + cO[1][nt][1]));
+                const float s1 = ((cE[0][nt][2] + cE[1][nt][2]) + (cO[0][nt][2] + cO[1][nt][2])) +
+                                 ((cE[0][nt][3] + cE[1][nt][3]) + (cO[0][nt][3] + cO[1][nt][3]));
+                const float m0 = cM[nt][0] + cM[nt][1];
+                const float m1 = cM[nt][2] + cM[nt][3];
+                acc[nt][0] = fmaf(r0.d * unscale[nt], s0, acc[nt][0]);
+                acc[nt][0] = fmaf(-r0.dmin * unscale[nt], m0, acc[nt][0]);
+                acc[nt][1] = fmaf(r1.d * unscale[nt], s1, acc[nt][1]);
+                acc[nt][1] = fmaf(-r1.dmin * unscale[nt], m1, acc[nt][1]);
             }
         }
-        if (lane == 0) s_cons[warp] = consumed;
-        // after an abort, wait (bounded) for this CTA's last x copy too
-        if (tid == 0 && xs.issued && *(volatile int *)&s_abort)
-            mbar_wait_bounded(smem_u32(&xbar), xs.parity ^ 1u, kWaitLimitNs);
+        // ---------------- tile epilogue
+        if (split == 1 && !*(volatile int *)&s_abort) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int b = t + 4 * nt;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int row = row0 + warp * 16 + g + 8 * h;
+                    if (b < B && row < Ng) {
+                        const float v = acc[nt][h];
+                        if (yg) yg[static_cast<size_t>(b) * Ng + row] = v;
+                        if (ARGMAX && !isnan(v)) atomicMax(&s_best[b], argmax_key(v, static_cast<uint32_t>(row)));
+                    }
+                }
+            }
+        } else if (split > 1) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int b = t + 4 * nt;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    if (b < B) s_red[(warp * 16 + g + 8 * h) * B + b] = acc[nt][h];
+            }
+        }
     }
+    if (lane == 0) s_cons[warp] = consumed;
 
-    // After a timed-out wait, wait (bounded) for the bulk copies this CTA issued
-    // but did not consume, so that none of them lands after the CTA has exited.
+    // After a timed-out wait, wait (bounded) for the copies this CTA issued but
+    // did not consume, so that none of them lands after the CTA has exited.
     __syncthreads();
-    if (*(volatile int *)&s_abort && tid == kWarps * 32) {
+    if (*(volatile int *)&s_abort && tid == 0) {
         int lo = s_cons[0];
         for (int w = 1; w < kWarps; ++w) lo = min(lo, s_cons[w]);
         for (int i = lo; i < s_issued; ++i)
             if (!mbar_wait_bounded(smem_u32(&full[i % kStages]), static_cast<uint32_t>((i / kStages) & 1), kWaitLimitNs))
                 break;
+        if (xs.issued) mbar_wait_bounded(smem_u32(&xbar), xs.parity ^ 1u, kWaitLimitNs);
     }
 
     if (split > 1) {
         // Deterministic cross-CTA reduction of the single row tile through
         // distributed shared memory: rank r sums rows [r*128/split, (r+1)*128/split)
-        // over ranks 0..split-1 in order.
+        // over ranks 0..split-1 in order (all remote loads issued before the sum).
         cluster_sync_all();
         if (!*(volatile int *)&s_abort) {
             const TileInfo ti = tile_info(args, blockIdx.x);
-            const int row0 = ti.row0;
-            const int Ng = ti.N;
-            float *yg = ti.y;
             const int lr0 = (rank * kRows) / split;
             const int lr1 = ((rank + 1) * kRows) / split;
             const int items = (lr1 - lr0) * B;
@@ -559,11 +567,17 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
                 const int lr = lr0 + it / B;
                 const int b = it % B;
                 const uint32_t off = static_cast<uint32_t>((lr * B + b) * 4);
-                float sum = 0.f;
-                for (int q = 0; q < split; ++q) sum += ld_shared_cluster_f32(map_shared_rank(red_local + off, q));
-                const int row = row0 + lr;
-                if (row < Ng) {
-                    if (yg) yg[static_cast<size_t>(b) * Ng + row] = sum;
+                float v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    v[q] = (q < split) ? ld_shared_cluster_f32(map_shared_rank(red_local + off, q)) : 0.f;
+                float sum = v[0];
+#pragma unroll
+                for (int q = 1; q < 8; ++q)
+                    if (q < split) sum += v[q];
+                const int row = ti.row0 + lr;
+                if (row < ti.N) {
+                    if (ti.y) ti.y[static_cast<size_t>(b) * ti.N + row] = sum;
                     if (ARGMAX && !isnan(sum)) atomicMax(&s_best[b], argmax_key(sum, static_cast<uint32_t>(row)));
                 }
             }
@@ -590,10 +604,10 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     }
 }
 
-// Batch <= 8 (one or two n8 tiles): at most 104 registers, so that two CTAs of
-// 288 threads fit in the register file of an SM.
+// Batch <= 8 (one or two n8 tiles): at most 128 registers, so that two CTAs of
+// 8 warps (4 warps per SM sub-partition) fit in the register file.
 template <int NT, bool ARGMAX>
-__global__ void __maxnreg__(104) q4k_gemv_kernel(const __grid_constant__ WMaps maps, const GemvArgs args)
+__global__ void __maxnreg__(128) q4k_gemv_kernel(const __grid_constant__ WMaps maps, const GemvArgs args)
 {
     gemv_body<NT, ARGMAX>(maps, args);
 }

@@ -145,7 +145,9 @@ template <int TN, int NTT>
 struct Cfg {
     static constexpr int kBBytes = TN * kChunk * 2;                       // one token subtile
     static constexpr int kStageBytes = kAStageBytes + NTT * kBBytes;
-    static constexpr int kStages = (200 * 1024 / kStageBytes) < 4 ? (200 * 1024 / kStageBytes) : 4;
+    // 32-token tiles: three stages (two CTAs per SM); otherwise up to four.
+    static constexpr int kStages =
+        (TN * NTT <= 32) ? 3 : ((200 * 1024 / kStageBytes) < 4 ? (200 * 1024 / kStageBytes) : 4);
     static constexpr int kTmemCols = TN * NTT;                            // 32..512, power of two
     static constexpr size_t kSmem = static_cast<size_t>(kStages) * kStageBytes;
 };
@@ -168,7 +170,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row0 = blockIdx.x * kRowsM;
     const int t0 = blockIdx.y * TN * NTT;
     const int nsub = min(NTT, (T - t0 + TN - 1) / TN);
-    const int nchunks = K / kChunk;
+    // K split over the CTAs of a cluster along z (split == 1: whole K)
+    const int split = gridDim.z;
+    const int kz = blockIdx.z;
+    const int c_begin = static_cast<int>((static_cast<long long>(kz) * (K / kChunk)) / split);
+    const int c_end = static_cast<int>((static_cast<long long>(kz + 1) * (K / kChunk)) / split);
     const size_t row_bytes = static_cast<size_t>(K / 256) * 144;
 
     if (tid == 0) {
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t *wrow = W + static_cast<size_t>(live ? n : 0) * row_bytes;
         int stage = 0;
         uint32_t phase = 0;
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = c_begin; c < c_end; ++c) {
             const int blk = c >> 2, p = c & 3;
             uint4 hdr = make_uint4(0, 0, 0, 0), qa = hdr, qb = hdr;
             if (live) {
@@ -276,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int issued = 0;
             const uint32_t bytes = static_cast<uint32_t>(nsub * C::kBBytes);
-            for (int c = 0; c < nchunks; ++c) {
+            for (int c = c_begin; c < c_end; ++c) {
                 if (!*(volatile int *)&s_abort &&
                     !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
                     atomicOr(&g_prefill_error, 2u);
@@ -307,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             constexpr uint32_t idesc = idesc_bf16(kRowsM, TN);
-            for (int c = 0; c < nchunks; ++c) {
+            for (int c = c_begin; c < c_end; ++c) {
                 bool ok = !*(volatile int *)&s_abort;
                 if (ok && !mbar_wait_bounded(smem_u32(&full_a[stage]), phase, kWaitLimitNs)) ok = false;
                 if (ok && !mbar_wait_bounded(smem_u32(&full_b[stage]), phase, kWaitLimitNs)) ok = false;
@@ -326,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int kk = 0; kk < kChunk / 16; ++kk) {
                                 const uint64_t bd = sw128_desc(b_addr + j * C::kBBytes + kk * 32);
                                 umma_bf16(tmem + j * TN, sw128_desc(a_addr + kk * 32), bd, idesc,
-                                          (c > 0 || kk > 0) ? 1u : 0u);
+                                          (c > c_begin || kk > 0) ? 1u : 0u);
                                 umma_bf16(tmem + j * TN, sw128_desc(a_addr + kATileBytes + kk * 32), bd, idesc, 1u);
                             }
                         }
@@ -340,6 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------- epilogue (warps 0-3)
+    // Warp w reads TMEM lanes 32w..32w+31 (= tile rows).  With a K split the
+    // partial tile goes to this CTA's shared memory (column-major, so a warp's
+    // stores are consecutive); after a cluster barrier CTA rank z sums rows
+    // [z*128/split, (z+1)*128/split) over ranks 0..split-1 in order and writes Y.
+    float *part = reinterpret_cast<float *>(smem);   // pipeline buffers are idle by now
     if (warp < 4) {
         const bool ok = mbar_wait_bounded(smem_u32(&done_bar), 0u, kWaitLimitNs);
         if (!ok) {
@@ -347,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_abort = 1;
         }
         tc_fence_after();
-        const int n = row0 + warp * 32 + lane;
+        const int r = warp * 32 + lane;
+        const int n = row0 + r;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         for (int j = 0; j < nsub; ++j) {
 #pragma unroll 1
@@ -355,7 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[16];
                 tmem_ld16(lane_addr + j * TN + c0, v);
                 tmem_wait_ld();
-                if (ok && n < N) {
+                if (split > 1) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) part[(j * TN + c0 + i) * kRowsM + r] = __uint_as_float(v[i]);
+                } else if (ok && n < N) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int t = t0 + j * TN + c0 + i;
@@ -365,6 +380,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         tc_fence_before();
+    }
+    if (split > 1) {
+        __syncthreads();
+        cluster_sync_all();
+        if (!*(volatile int *)&s_abort) {
+            const int r0 = (kz * kRowsM) / split, r1 = ((kz + 1) * kRowsM) / split;
+            const int rows = r1 - r0;
+            const int cols = nsub * TN;
+            const uint32_t part_addr = smem_u32(part);
+            for (int it = tid; it < rows * cols; it += kThreads) {
+                const int c = it / rows;
+                const int r = r0 + it % rows;
+                const uint32_t off = static_cast<uint32_t>((c * kRowsM + r) * 4);
+                float sum = 0.f;
+                for (int q = 0; q < split; ++q) sum += ld_shared_cluster_f32(map_shared_rank(part_addr + off, q));
+                const int n = row0 + r, t = t0 + c;
+                if (n < N && t < T) Y[static_cast<size_t>(t) * N + n] = sum;
+            }
+        }
+        cluster_sync_all();
     }
     __syncthreads();
     if (warp == 5) {
@@ -387,9 +422,12 @@ static q4k_status validate_prefill(const void *W, const void *X, const float *Y,
 }
 
 template <int TN, int NTT>
-static cudaError_t launch_prefill(const uint8_t *W, const void *X, float *Y, int N, int K, int T, cudaStream_t s)
+static cudaError_t launch_prefill(const uint8_t *W, const void *X, float *Y, int N, int K, int T, int split,
+                                  cudaStream_t s)
 {
     using C = pf::Cfg<TN, NTT>;
+    // the split-K partial tile (128 x TN*NTT fp32) reuses the pipeline buffers
+    if (static_cast<size_t>(TN) * NTT * pf::kRowsM * 4 > C::kSmem) split = 1;
     auto enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap map;
@@ -408,27 +446,56 @@ static cudaError_t launch_prefill(const uint8_t *W, const void *X, float *Y, int
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
     });
     if (attr_err != cudaSuccess) return attr_err;
-    dim3 grid((N + pf::kRowsM - 1) / pf::kRowsM, (T + TN * NTT - 1) / (TN * NTT), 1);
-    kern<<<grid, pf::kThreads, C::kSmem, s>>>(map, W, Y, N, K, T);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + pf::kRowsM - 1) / pf::kRowsM, (T + TN * NTT - 1) / (TN * NTT), split);
+    cfg.blockDim = dim3(pf::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = split;
+    cfg.attrs = attr;
+    cfg.numAttrs = split > 1 ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, W, Y, N, K, T);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return e;
 }
 
 q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream)
 {
     q4k_status st = validate_prefill(W, X, Y, N, K, T);
     if (st != Q4K_OK) return st;
-    st = check_device(nullptr);
+    int sms = 0;
+    st = check_device(&sms);
     if (st != Q4K_OK) return st;
     if (N == 0 || T == 0) return Q4K_OK;
     const auto *Wb = static_cast<const uint8_t *>(W);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const int n = static_cast<int>(N), k = static_cast<int>(K), t = static_cast<int>(T);
+    const int mtiles = (n + pf::kRowsM - 1) / pf::kRowsM;
+    // Token tiling: one CTA covers up to 512 tokens (weights dequantized once)
+    // unless that leaves too few CTAs, then 256-token tiles.
+    int tn, ntt;
+    if (t <= 32) { tn = 32; ntt = 1; }
+    else if (t <= 64) { tn = 64; ntt = 1; }
+    else if (t <= 128) { tn = 128; ntt = 1; }
+    else if (t <= 256) { tn = 256; ntt = 1; }
+    else if (static_cast<long long>(mtiles) * ((t + 511) / 512) >= sms) { tn = 256; ntt = 2; }
+    else { tn = 256; ntt = 1; }
+    const long long ctas = static_cast<long long>(mtiles) * ((t + tn * ntt - 1) / (tn * ntt));
+    // K split over a cluster until the GPU is covered (at most 8, at least
+    // 8 chunks of 64 per CTA).
+    int split = 1;
+    while (ntt == 1 && split < 8 && ctas * split * 2 <= static_cast<long long>(sms) + sms / 2 && (k / 64) / (split * 2) >= 8)
+        split *= 2;
     cudaError_t e;
-    if (T <= 32) e = launch_prefill<32, 1>(Wb, X, Y, n, k, t, s);
-    else if (T <= 64) e = launch_prefill<64, 1>(Wb, X, Y, n, k, t, s);
-    else if (T <= 128) e = launch_prefill<128, 1>(Wb, X, Y, n, k, t, s);
-    else if (T <= 256) e = launch_prefill<256, 1>(Wb, X, Y, n, k, t, s);
-    else e = launch_prefill<256, 2>(Wb, X, Y, n, k, t, s);
+    if (tn == 32) e = launch_prefill<32, 1>(Wb, X, Y, n, k, t, split, s);
+    else if (tn == 64) e = launch_prefill<64, 1>(Wb, X, Y, n, k, t, split, s);
+    else if (tn == 128) e = launch_prefill<128, 1>(Wb, X, Y, n, k, t, split, s);
+    else if (ntt == 1) e = launch_prefill<256, 1>(Wb, X, Y, n, k, t, split, s);
+    else e = launch_prefill<256, 2>(Wb, X, Y, n, k, t, split, s);
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
