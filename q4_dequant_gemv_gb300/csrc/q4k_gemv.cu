@@ -60,7 +60,7 @@ constexpr int kWarps = 8;                 // warps per CTA, 16 weight rows each
 constexpr int kRows = 16 * kWarps;        // rows per tile (128)
 constexpr int kThreads = 32 * kWarps;
 constexpr int kKsteps = 17;               // 16 k16 steps + 1 min-term step per super-block
-constexpr int kStages = 3;                // W ring depth
+constexpr int kStages = 4;                // W ring depth
 constexpr int kStageBytes = kRows * kBlockBytes;   // one super-block of every tile row (18 KB)
 constexpr size_t kSmemPerCta2 = 110 * 1024;        // two CTAs per SM (batch <= 8)
 constexpr size_t kSmemPerCta1 = 200 * 1024;        // one CTA per SM (batch > 8)
@@ -98,19 +98,21 @@ __host__ __device__ inline size_t xfrag_bytes_per_block(int NT, int B)
     return static_cast<size_t>(lane_stride(NT)) * frag_lanes(NT, B) * 8;
 }
 
-// Dynamic shared memory: [ring | x fragments | raw x chunk | partial sums (split-K)].
+// Dynamic shared memory: [ring | x fragments | scratch].  The scratch holds
+// the raw x chunk while it is converted and, with a K split, the tile's partial
+// sums at the very end (after the last chunk has been converted), so the two
+// uses share it.
 __host__ __device__ inline size_t xfrag_offset() { return static_cast<size_t>(kStages) * kStageBytes; }
 __host__ __device__ inline size_t xraw_offset(int NT, int B, int kc)
 {
     return xfrag_offset() + ((xfrag_bytes_per_block(NT, B) * kc + 127) & ~size_t(127));
 }
-__host__ __device__ inline size_t red_offset(int NT, int B, int kc)
+__host__ __device__ inline size_t red_offset(int NT, int B, int kc) { return xraw_offset(NT, B, kc); }
+__host__ inline size_t gemv_smem_bytes(int NT, int B, int kc, int split)
 {
-    return xraw_offset(NT, B, kc) + static_cast<size_t>(B) * kc * 1024;
-}
-__host__ inline size_t gemv_smem_bytes(int NT, int B, int kc)
-{
-    return red_offset(NT, B, kc) + static_cast<size_t>(kRows) * 16 * 4;
+    const size_t xraw = static_cast<size_t>(B) * kc * 1024;
+    const size_t red = (split > 1) ? static_cast<size_t>(kRows) * B * 4 : 0;
+    return xraw_offset(NT, B, kc) + (xraw > red ? xraw : red);
 }
 
 // ---------------------------------------------------------------------------
@@ -700,11 +702,11 @@ static GemvPlan make_plan(int tiles, int64_t K, int B, int sms, int forced_split
     p.split = best_s;
     const int ks_max = (nb + p.split - 1) / p.split;
     const size_t per_blk = xfrag_bytes_per_block(p.NT, B) + static_cast<size_t>(B) * 1024;
-    const size_t fixed = gemv_smem_bytes(p.NT, B, 0);
+    const size_t fixed = gemv_smem_bytes(p.NT, B, 0, p.split) + 128;
     const size_t budget = (p.NT <= 2) ? kSmemPerCta2 : kSmemPerCta1;
     int kc = static_cast<int>(std::max<size_t>(1, (budget - fixed) / per_blk));
     p.kc = std::min(kc, ks_max);
-    p.smem = gemv_smem_bytes(p.NT, B, p.kc);
+    p.smem = gemv_smem_bytes(p.NT, B, p.kc, p.split);
     if (p.split == 1) {
         const int ctas_per_sm = (p.NT <= 2) ? 2 : 1;
         p.grid_x = std::min(p.tiles, sms * ctas_per_sm);
