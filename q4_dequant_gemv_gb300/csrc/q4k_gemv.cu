@@ -133,35 +133,28 @@ __device__ __forceinline__ int chunk_scale_exp(uint32_t amax_bits)
     return max(-126, min(126, s));
 }
 
-struct XChunkState {
-    uint32_t parity;   // phase of the x mbarrier for the next chunk
-    int issued;        // thread 0: a copy into xraw has been issued
-};
-
-// The chunk of x (B rows x nblk*256 floats) is brought into shared memory by
-// one bulk copy per batch row, then converted there: per-row max -> scale,
-// fp16 hi/lo B fragments, sub-block sums.  Called by all consumer threads;
-// every caller must have finished reading the previous chunk's fragments
-// (the caller's named barrier) before it is entered.
+// The chunk of x (B rows x nblk*256 floats) is copied into shared memory by
+// all threads with ordinary 16-byte loads (kept off the TMA queue, which is
+// busy streaming weights), then converted there: per-row max -> scale, fp16
+// hi/lo B fragments, sub-block sums.  Called by all threads; every caller must
+// have finished reading the previous chunk's fragments (the caller's named
+// barrier) before it is entered.
 template <int NT>
 __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int kb0, int nblk, uint2 *xf,
-                                const float *xraw, uint64_t *xbar, XChunkState &xs, float *s_unscale,
-                                uint32_t *s_amax, int *s_abort, int tid, int nthr)
+                                float *xraw, float *s_unscale, uint32_t *s_amax, int tid, int nthr)
 {
     const int LW = frag_lanes(NT, B);
     const int n = nblk * 256;                       // floats per batch row in the chunk
-    if (tid == 0) {
-        mbar_arrive_expect_tx(smem_u32(xbar), static_cast<uint32_t>(B * n * 4));
-        for (int b = 0; b < B; ++b)
-            bulk_g2s(smem_u32(xraw + b * n), x + static_cast<size_t>(b) * K + static_cast<size_t>(kb0) * 256,
-                     static_cast<uint32_t>(n * 4), smem_u32(xbar), l2_policy_evict_last());
-        xs.issued = 1;
+    {
+        const int n4 = n / 4;
+        for (int e = tid; e < B * n4; e += nthr) {
+            const int b = e / n4, i = e - b * n4;
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K +
+                                                                    static_cast<size_t>(kb0) * 256) + i);
+            reinterpret_cast<float4 *>(xraw + b * n)[i] = v;
+        }
+        named_bar_sync(1, nthr);
     }
-    if (!*(volatile int *)s_abort && !mbar_wait_bounded(smem_u32(xbar), xs.parity, kWaitLimitNs)) {
-        atomicOr(&g_device_error, 1u);
-        *s_abort = 1;
-    }
-    xs.parity ^= 1u;
     // 1) per-batch-row max |x|
     for (int b = 0; b < B; ++b) {
         const float4 *xb = reinterpret_cast<const float4 *>(xraw + b * n);
@@ -341,8 +334,8 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     const int LW = frag_lanes(NT, B);
     uint2 *xf = reinterpret_cast<uint2 *>(smem_raw + xfrag_offset());
     float *s_red = reinterpret_cast<float *>(smem_raw + red_offset(NT, B, args.kc));
-    const float *xraw = reinterpret_cast<const float *>(smem_raw + xraw_offset(NT, B, args.kc));
-    __shared__ __align__(8) uint64_t full[kStages], xbar;
+    float *xraw = reinterpret_cast<float *>(smem_raw + xraw_offset(NT, B, args.kc));
+    __shared__ __align__(8) uint64_t full[kStages];
     __shared__ float s_unscale[16];
     __shared__ uint32_t s_amax[16];
     __shared__ unsigned long long s_best[16];
@@ -369,7 +362,6 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             mbar_init(smem_u32(&full[i]), 1);
             s_slot_done[i] = 0;
         }
-        mbar_init(smem_u32(&xbar), 1);
         s_abort = 0;
         fence_barrier_init();
 #pragma unroll
@@ -395,10 +387,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     const int t = lane & 3;
     const int nchunks = (ks + args.kc - 1) / args.kc;
     const bool single_chunk = (nchunks == 1);
-    XChunkState xs{0u, 0};
-    if (single_chunk)
-        convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, xraw, &xbar, xs, s_unscale, s_amax, &s_abort, tid,
-                            kThreads);
+    if (single_chunk) convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, xraw, s_unscale, s_amax, tid, kThreads);
     // B-fragment lane.  Lanes whose column holds no batch row read some other
     // valid entry: MMA columns are independent, and those output columns are
     // never used.
@@ -421,8 +410,8 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             if (!single_chunk && kbl > chunk_end) {
                 const int cn = min(args.kc, ks - kbl);
                 named_bar_sync(1, kThreads);     // everyone done with the previous chunk
-                convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, xraw, &xbar, xs, s_unscale, s_amax,
-                                    &s_abort, tid, kThreads);
+                convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, xraw, s_unscale, s_amax, tid,
+                                    kThreads);
                 chunk_end = kbl + cn - 1;
                 reload_scale = true;
             }
@@ -551,7 +540,6 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
         for (int i = lo; i < s_issued; ++i)
             if (!mbar_wait_bounded(smem_u32(&full[i % kStages]), static_cast<uint32_t>((i / kStages) & 1), kWaitLimitNs))
                 break;
-        if (xs.issued) mbar_wait_bounded(smem_u32(&xbar), xs.parity ^ 1u, kWaitLimitNs);
     }
 
     if (split > 1) {
