@@ -98,21 +98,20 @@ __host__ __device__ inline size_t xfrag_bytes_per_block(int NT, int B)
     return static_cast<size_t>(lane_stride(NT)) * frag_lanes(NT, B) * 8;
 }
 
-// Dynamic shared memory: [ring | x fragments | scratch].  The scratch holds
-// the raw x chunk while it is converted and, with a K split, the tile's partial
-// sums at the very end (after the last chunk has been converted), so the two
-// uses share it.
+// Dynamic shared memory: [ring | x fragments | raw x chunk | split-K receive
+// buffer (split slots of at most ceil(128/split) rows x B, only with a split)].
 __host__ __device__ inline size_t xfrag_offset() { return static_cast<size_t>(kStages) * kStageBytes; }
 __host__ __device__ inline size_t xraw_offset(int NT, int B, int kc)
 {
     return xfrag_offset() + ((xfrag_bytes_per_block(NT, B) * kc + 127) & ~size_t(127));
 }
-__host__ __device__ inline size_t red_offset(int NT, int B, int kc) { return xraw_offset(NT, B, kc); }
+__host__ __device__ inline size_t red_offset(int NT, int B, int kc)
+{
+    return xraw_offset(NT, B, kc) + static_cast<size_t>(B) * kc * 1024;
+}
 __host__ inline size_t gemv_smem_bytes(int NT, int B, int kc, int split)
 {
-    const size_t xraw = static_cast<size_t>(B) * kc * 1024;
-    const size_t red = (split > 1) ? static_cast<size_t>(kRows) * B * 4 : 0;
-    return xraw_offset(NT, B, kc) + (xraw > red ? xraw : red);
+    return red_offset(NT, B, kc) + ((split > 1) ? static_cast<size_t>(kRows + 8) * B * 4 : 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -379,6 +378,9 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     if (tid < kWarps) s_cons[tid] = 0;
     __syncthreads();
     iss.policy = l2_policy_evict_first();
+    // every CTA of a cluster has started once this phase completes; it is
+    // waited for only before the first remote store, at the very end
+    if (split > 1) cluster_arrive_relaxed();
 
     pdl_launch_dependents();
     pdl_wait();                             // x may come from the previous kernel
@@ -520,12 +522,26 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
                 }
             }
         } else if (split > 1) {
+            // Push this CTA's partial rows into the shared memory of the rank
+            // that owns them: rank r owns tile rows [r*128/split, (r+1)*128/split)
+            // and keeps one slot per source rank in its receive buffer.  The
+            // wait completes the start-of-kernel phase (all CTAs running); the
+            // barrier after the tile loop orders the stores before the sums.
+            cluster_wait_acquire();
+            const uint32_t red_base = smem_u32(s_red);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int b = t + 4 * nt;
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    if (b < B) s_red[(warp * 16 + g + 8 * h) * B + b] = acc[nt][h];
+                for (int h = 0; h < 2; ++h) {
+                    const int row = warp * 16 + g + 8 * h;
+                    const int owner = (row * split + split - 1) / kRows;
+                    const int o0 = (owner * kRows) / split, o1 = ((owner + 1) * kRows) / split;
+                    if (b < B && !*(volatile int *)&s_abort) {
+                        const uint32_t off = static_cast<uint32_t>(((rank * (o1 - o0) + (row - o0)) * B + b) * 4);
+                        st_shared_cluster_f32(map_shared_rank(red_base + off, owner), acc[nt][h]);
+                    }
+                }
             }
         }
     }
@@ -543,36 +559,27 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     }
 
     if (split > 1) {
-        // Deterministic cross-CTA reduction of the single row tile through
-        // distributed shared memory: rank r sums rows [r*128/split, (r+1)*128/split)
-        // over ranks 0..split-1 in order (all remote loads issued before the sum).
-        cluster_sync_all();
+        // Deterministic cross-CTA reduction: after this cluster barrier every
+        // rank holds the partials of its own rows from all ranks and adds them
+        // in rank order.
+        cluster_arrive_release();
+        cluster_wait_acquire();
         if (!*(volatile int *)&s_abort) {
             const TileInfo ti = tile_info(args, blockIdx.x);
             const int lr0 = (rank * kRows) / split;
-            const int lr1 = ((rank + 1) * kRows) / split;
-            const int items = (lr1 - lr0) * B;
-            const uint32_t red_local = smem_u32(s_red);
-            for (int it = tid; it < items; it += kThreads) {
-                const int lr = lr0 + it / B;
-                const int b = it % B;
-                const uint32_t off = static_cast<uint32_t>((lr * B + b) * 4);
-                float v[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    v[q] = (q < split) ? ld_shared_cluster_f32(map_shared_rank(red_local + off, q)) : 0.f;
-                float sum = v[0];
-#pragma unroll
-                for (int q = 1; q < 8; ++q)
-                    if (q < split) sum += v[q];
-                const int row = ti.row0 + lr;
+            const int rows = ((rank + 1) * kRows) / split - lr0;
+            for (int it = tid; it < rows * B; it += kThreads) {
+                const int lr = it / B;
+                const int b = it - lr * B;
+                float sum = s_red[lr * B + b];
+                for (int q = 1; q < split; ++q) sum += s_red[(q * rows + lr) * B + b];
+                const int row = ti.row0 + lr0 + lr;
                 if (row < ti.N) {
                     if (ti.y) ti.y[static_cast<size_t>(b) * ti.N + row] = sum;
                     if (ARGMAX && !isnan(sum)) atomicMax(&s_best[b], argmax_key(sum, static_cast<uint32_t>(row)));
                 }
             }
         }
-        cluster_sync_all();
     }
 
     if (ARGMAX) {
