@@ -138,19 +138,39 @@ __device__ __forceinline__ int chunk_scale_exp(uint32_t amax_bits)
 // hi/lo B fragments, sub-block sums.  Called by all threads; every caller must
 // have finished reading the previous chunk's fragments (the caller's named
 // barrier) before it is entered.
-template <int NT>
+template <int NT, typename AfterLoads>
 __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int kb0, int nblk, uint2 *xf,
-                                float *xraw, float *s_unscale, uint32_t *s_amax, int tid, int nthr)
+                                float *xraw, float *s_unscale, uint32_t *s_amax, int tid, int nthr,
+                                const AfterLoads &after_loads)
 {
     const int LW = frag_lanes(NT, B);
     const int n = nblk * 256;                       // floats per batch row in the chunk
     {
+        // all loads are issued before any is used (up to 8 per thread in
+        // flight), then after_loads runs (it issues the next weight stages,
+        // which must not overtake x at the SM's memory port), then the stores
         const int n4 = n / 4;
-        for (int e = tid; e < B * n4; e += nthr) {
-            const int b = e / n4, i = e - b * n4;
-            const float4 v = __ldg(reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K +
-                                                                    static_cast<size_t>(kb0) * 256) + i);
-            reinterpret_cast<float4 *>(xraw + b * n)[i] = v;
+        const int total = B * n4;
+        for (int base = 0; base < total; base += 8 * nthr) {
+            float4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = base + j * nthr + tid;
+                if (e < total) {
+                    const int b = e / n4, i = e - b * n4;
+                    v[j] = __ldg(reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K +
+                                                                  static_cast<size_t>(kb0) * 256) + i);
+                }
+            }
+            if (base == 0) after_loads();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int e = base + j * nthr + tid;
+                if (e < total) {
+                    const int b = e / n4, i = e - b * n4;
+                    reinterpret_cast<float4 *>(xraw + b * n)[i] = v[j];
+                }
+            }
         }
         named_bar_sync(1, nthr);
     }
@@ -366,10 +386,12 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
 #pragma unroll
         for (int g = 0; g < kMaxGroups; ++g)
             if (g < args.ngroups) prefetch_tensormap(&maps.m[g]);
-        // the first stages stream in while the CTA sets up (weights never
-        // depend on the previous kernel)
+        // The first stage streams in while the CTA sets up and, under PDL,
+        // while the previous kernel finishes (weights never depend on it).
+        // Only one: x is loaded after the dependency wait and must not queue
+        // behind a full ring of weight data at the SM's memory port.
         iss.policy = l2_policy_evict_first();
-        const int first = min(kStages, iss.total);
+        const int first = min(1, iss.total);
         for (int i = 0; i < first; ++i) iss.issue(i);
         s_issued = first;
     }
@@ -389,7 +411,19 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     const int t = lane & 3;
     const int nchunks = (ks + args.kc - 1) / args.kc;
     const bool single_chunk = (nchunks == 1);
-    if (single_chunk) convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, xraw, s_unscale, s_amax, tid, kThreads);
+    // the rest of the initial ring is issued once this thread's x loads are out
+    auto fill_ring = [&]() {
+        if (tid == 0) {
+            const int upto = min(kStages, iss.total);
+            for (int i = 1; i < upto; ++i) iss.issue(i);
+            atomicAdd(&s_issued, max(0, upto - 1));
+        }
+    };
+    auto nothing = []() {};
+    if (single_chunk)
+        convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, xraw, s_unscale, s_amax, tid, kThreads, fill_ring);
+    else
+        fill_ring();
     // B-fragment lane.  Lanes whose column holds no batch row read some other
     // valid entry: MMA columns are independent, and those output columns are
     // never used.
@@ -413,7 +447,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
                 const int cn = min(args.kc, ks - kbl);
                 named_bar_sync(1, kThreads);     // everyone done with the previous chunk
                 convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, xraw, s_unscale, s_amax, tid,
-                                    kThreads);
+                                    kThreads, nothing);
                 chunk_end = kbl + cn - 1;
                 reload_scale = true;
             }
