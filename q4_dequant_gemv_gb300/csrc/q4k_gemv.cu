@@ -98,16 +98,12 @@ __host__ __device__ inline size_t xfrag_bytes_per_block(int NT, int B)
     return static_cast<size_t>(lane_stride(NT)) * frag_lanes(NT, B) * 8;
 }
 
-// Dynamic shared memory: [ring | x fragments | raw x chunk | split-K receive
-// buffer (split slots of at most ceil(128/split) rows x B, only with a split)].
+// Dynamic shared memory: [ring | x fragments | split-K receive buffer (split
+// slots of at most ceil(128/split) rows x B, only with a split)].
 __host__ __device__ inline size_t xfrag_offset() { return static_cast<size_t>(kStages) * kStageBytes; }
-__host__ __device__ inline size_t xraw_offset(int NT, int B, int kc)
-{
-    return xfrag_offset() + ((xfrag_bytes_per_block(NT, B) * kc + 127) & ~size_t(127));
-}
 __host__ __device__ inline size_t red_offset(int NT, int B, int kc)
 {
-    return xraw_offset(NT, B, kc) + static_cast<size_t>(B) * kc * 1024;
+    return xfrag_offset() + ((xfrag_bytes_per_block(NT, B) * kc + 127) & ~size_t(127));
 }
 __host__ inline size_t gemv_smem_bytes(int NT, int B, int kc, int split)
 {
@@ -132,109 +128,85 @@ __device__ __forceinline__ int chunk_scale_exp(uint32_t amax_bits)
     return max(-126, min(126, s));
 }
 
-// The chunk of x (B rows x nblk*256 floats) is copied into shared memory by
-// all threads with ordinary 16-byte loads (kept off the TMA queue, which is
-// busy streaming weights), then converted there: per-row max -> scale, fp16
-// hi/lo B fragments, sub-block sums.  Called by all threads; every caller must
-// have finished reading the previous chunk's fragments (the caller's named
-// barrier) before it is entered.
+// A chunk of x (B rows x nblk*256 floats, at most 8 float4 per thread) is
+// loaded into registers with 16-byte loads, the per-row max comes from warp
+// reductions plus one shared atomic per warp, and after a single barrier every
+// thread converts its own values: power-of-two scale, fp16 hi/lo B fragments,
+// sub-block sums (8-lane shuffles).  Float4 number i of a batch row covers
+// elements 4i..4i+3, i.e. super-block i/64, sub-block j = (i/8)%8 (pair t = j/2,
+// half h = j%2), word u = i%8 -> k-step s = 2u + h of pair t.  Called by all
+// threads; the caller must have finished reading the previous chunk's
+// fragments (its named barrier) before it is entered.
 template <int NT, typename AfterLoads>
 __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int kb0, int nblk, uint2 *xf,
-                                float *xraw, float *s_unscale, uint32_t *s_amax, int tid, int nthr,
-                                const AfterLoads &after_loads)
+                                float *s_unscale, uint32_t *s_amax, int tid, int nthr, const AfterLoads &after_loads)
 {
     const int LW = frag_lanes(NT, B);
-    const int n = nblk * 256;                       // floats per batch row in the chunk
-    {
-        // all loads are issued before any is used (up to 8 per thread in
-        // flight), then after_loads runs (it issues the next weight stages,
-        // which must not overtake x at the SM's memory port), then the stores
-        const int n4 = n / 4;
-        const int total = B * n4;
-        for (int base = 0; base < total; base += 8 * nthr) {
-            float4 v[8];
+    constexpr int LS = lane_stride(NT);
+    const int n4 = nblk * 64;                 // float4 per batch row in the chunk (a multiple of 64)
+    const int total = B * n4;                 // <= 8 * nthr (chunk size chosen by the host)
+    float4 v[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = base + j * nthr + tid;
-                if (e < total) {
-                    const int b = e / n4, i = e - b * n4;
-                    v[j] = __ldg(reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K +
-                                                                  static_cast<size_t>(kb0) * 256) + i);
-                }
-            }
-            if (base == 0) after_loads();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int e = base + j * nthr + tid;
-                if (e < total) {
-                    const int b = e / n4, i = e - b * n4;
-                    reinterpret_cast<float4 *>(xraw + b * n)[i] = v[j];
-                }
-            }
+    for (int j = 0; j < 8; ++j) {
+        const int e = j * nthr + tid;
+        if (e < total) {
+            const int b = e / n4, i = e - b * n4;
+            v[j] = __ldg(reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K +
+                                                          static_cast<size_t>(kb0) * 256) + i);
         }
-        named_bar_sync(1, nthr);
     }
-    // 1) per-batch-row max |x|
-    for (int b = 0; b < B; ++b) {
-        const float4 *xb = reinterpret_cast<const float4 *>(xraw + b * n);
-        uint32_t m = 0u;
-        for (int e = tid; e < n / 4; e += nthr) {
-            const float4 v = xb[e];
-            m = max(m, max(max(__float_as_uint(fabsf(v.x)), __float_as_uint(fabsf(v.y))),
-                           max(__float_as_uint(fabsf(v.z)), __float_as_uint(fabsf(v.w)))));
-        }
+    after_loads();
+    // per-row max |x|: the 32 lanes of a warp hold 32 consecutive float4 of one row
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if ((tid & 31) == 0 && m) atomicMax(&s_amax[b], m);
+    for (int j = 0; j < 8; ++j) {
+        const int e0 = j * nthr + (tid & ~31);
+        if (e0 < total) {
+            const int e = j * nthr + tid;
+            uint32_t m = 0u;
+            if (e < total)
+                m = max(max(__float_as_uint(fabsf(v[j].x)), __float_as_uint(fabsf(v[j].y))),
+                        max(__float_as_uint(fabsf(v[j].z)), __float_as_uint(fabsf(v[j].w))));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+            if ((tid & 31) == 0 && m) atomicMax(&s_amax[e0 / n4], m);
+        }
     }
     named_bar_sync(1, nthr);
-    // 2) main entries: items (bl, s<16, b, t)
-    const int items = nblk * 16 * B * 4;
-    for (int it = tid; it < items; it += nthr) {
-        const int t = it & 3;
-        int r = it >> 2;
-        const int b = r % B;
-        r /= B;
-        const int s = r & 15;
-        const int bl = r >> 4;
-        const float sc = __uint_as_float(static_cast<uint32_t>(chunk_scale_exp(s_amax[b]) + 127) << 23);
-        float4 v = *reinterpret_cast<const float4 *>(xraw + b * n + bl * 256 + 32 * (2 * t + (s & 1)) + 4 * (s >> 1));
-        v.x *= sc; v.y *= sc; v.z *= sc; v.w *= sc;
-        const uint32_t h01 = pack_half2(v.x, v.z);
-        const uint32_t h23 = pack_half2(v.y, v.w);
-        const uint32_t l01 = pack_half2(v.x - half_lo_f32(h01), v.z - half_hi_f32(h01));
-        const uint32_t l23 = pack_half2(v.y - half_lo_f32(h23), v.w - half_hi_f32(h23));
-        const int chi = 2 * b, clo = 2 * b + 1;
-        constexpr int LS = lane_stride(NT);
-        xf[(bl * LW + 4 * (chi % 8) + t) * LS + s * NT + chi / 8] = make_uint2(h01, h23);
-        xf[(bl * LW + 4 * (clo % 8) + t) * LS + s * NT + clo / 8] = make_uint2(l01, l23);
-    }
-    // 3) min-term entries: items (bl, b, t): sums of sub-blocks 2t and 2t+1
-    const int mitems = nblk * B * 4;
-    for (int it = tid; it < mitems; it += nthr) {
-        const int t = it & 3;
-        const int r = it >> 2;
-        const int b = r % B;
-        const int bl = r / B;
-        const float sc = __uint_as_float(static_cast<uint32_t>(chunk_scale_exp(s_amax[b]) + 127) << 23);
-        const float4 *p = reinterpret_cast<const float4 *>(xraw + b * n + bl * 256 + 64 * t);
-        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float4 v = p[e];
-            s0 += (v.x * sc + v.y * sc) + (v.z * sc + v.w * sc);
-        }
-#pragma unroll
-        for (int e = 8; e < 16; ++e) {
-            const float4 v = p[e];
-            s1 += (v.x * sc + v.y * sc) + (v.z * sc + v.w * sc);
-        }
-        const uint32_t h = pack_half2(s0, s1);
-        const uint32_t l = pack_half2(s0 - half_lo_f32(h), s1 - half_hi_f32(h));
+    for (int j = 0; j < 8; ++j) {
+        const int e0 = j * nthr + (tid & ~31);
+        if (e0 >= total) continue;            // warp-uniform
+        const int e = j * nthr + tid;
+        const bool live = e < total;
+        const int b = e0 / n4;                // the whole warp is in one row
+        const int i = e - b * n4;
+        const float sc = __uint_as_float(static_cast<uint32_t>(chunk_scale_exp(s_amax[b]) + 127) << 23);
+        float4 w = live ? v[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        w.x *= sc; w.y *= sc; w.z *= sc; w.w *= sc;
+        const int bl = i >> 6, sb = (i >> 3) & 7, u = i & 7;
+        const int t = sb >> 1, h = sb & 1, s = 2 * u + h;
         const int chi = 2 * b, clo = 2 * b + 1;
-        constexpr int LS = lane_stride(NT);
-        xf[(bl * LW + 4 * (chi % 8) + t) * LS + 16 * NT + chi / 8] = make_uint2(h, 0u);
-        xf[(bl * LW + 4 * (clo % 8) + t) * LS + 16 * NT + clo / 8] = make_uint2(l, 0u);
+        if (live) {
+            const uint32_t h01 = pack_half2(w.x, w.z);
+            const uint32_t h23 = pack_half2(w.y, w.w);
+            const uint32_t l01 = pack_half2(w.x - half_lo_f32(h01), w.z - half_hi_f32(h01));
+            const uint32_t l23 = pack_half2(w.y - half_lo_f32(h23), w.w - half_hi_f32(h23));
+            xf[(bl * LW + 4 * (chi % 8) + t) * LS + s * NT + chi / 8] = make_uint2(h01, h23);
+            xf[(bl * LW + 4 * (clo % 8) + t) * LS + s * NT + clo / 8] = make_uint2(l01, l23);
+        }
+        // sub-block sum over the 8 lanes holding it, then pair it with the
+        // odd sub-block held by the next 8 lanes
+        float sum = (w.x + w.y) + (w.z + w.w);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        const float sum_odd = __shfl_down_sync(0xffffffffu, sum, 8);
+        if (live && u == 0 && h == 0) {
+            const uint32_t hs = pack_half2(sum, sum_odd);
+            const uint32_t ls = pack_half2(sum - half_lo_f32(hs), sum_odd - half_hi_f32(hs));
+            xf[(bl * LW + 4 * (chi % 8) + t) * LS + 16 * NT + chi / 8] = make_uint2(hs, 0u);
+            xf[(bl * LW + 4 * (clo % 8) + t) * LS + 16 * NT + clo / 8] = make_uint2(ls, 0u);
+        }
     }
     for (int b = tid; b < B; b += nthr)
         s_unscale[b] = __uint_as_float(static_cast<uint32_t>(127 - chunk_scale_exp(s_amax[b])) << 23);
@@ -353,7 +325,6 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     const int LW = frag_lanes(NT, B);
     uint2 *xf = reinterpret_cast<uint2 *>(smem_raw + xfrag_offset());
     float *s_red = reinterpret_cast<float *>(smem_raw + red_offset(NT, B, args.kc));
-    float *xraw = reinterpret_cast<float *>(smem_raw + xraw_offset(NT, B, args.kc));
     __shared__ __align__(8) uint64_t full[kStages];
     __shared__ float s_unscale[16];
     __shared__ uint32_t s_amax[16];
@@ -421,7 +392,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     };
     auto nothing = []() {};
     if (single_chunk)
-        convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, xraw, s_unscale, s_amax, tid, kThreads, fill_ring);
+        convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_unscale, s_amax, tid, kThreads, fill_ring);
     else
         fill_ring();
     // B-fragment lane.  Lanes whose column holds no batch row read some other
@@ -446,8 +417,8 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             if (!single_chunk && kbl > chunk_end) {
                 const int cn = min(args.kc, ks - kbl);
                 named_bar_sync(1, kThreads);     // everyone done with the previous chunk
-                convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, xraw, s_unscale, s_amax, tid,
-                                    kThreads, nothing);
+                convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, s_amax, tid, kThreads,
+                                    nothing);
                 chunk_end = kbl + cn - 1;
                 reload_scale = true;
             }
@@ -730,10 +701,12 @@ static GemvPlan make_plan(int tiles, int64_t K, int B, int sms, int forced_split
     }
     p.split = best_s;
     const int ks_max = (nb + p.split - 1) / p.split;
-    const size_t per_blk = xfrag_bytes_per_block(p.NT, B) + static_cast<size_t>(B) * 1024;
+    const size_t per_blk = xfrag_bytes_per_block(p.NT, B);
     const size_t fixed = gemv_smem_bytes(p.NT, B, 0, p.split) + 128;
     const size_t budget = (p.NT <= 2) ? kSmemPerCta2 : kSmemPerCta1;
     int kc = static_cast<int>(std::max<size_t>(1, (budget - fixed) / per_blk));
+    // the conversion holds at most 8 float4 of x per thread: B * kc * 64 <= 8 * 256
+    kc = std::min(kc, std::max(1, 32 / B));
     p.kc = std::min(kc, ks_max);
     p.smem = gemv_smem_bytes(p.NT, B, p.kc, p.split);
     if (p.split == 1) {
