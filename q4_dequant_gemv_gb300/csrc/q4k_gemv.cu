@@ -145,14 +145,21 @@ __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int k
     constexpr int LS = lane_stride(NT);
     const int n4 = nblk * 64;                 // float4 per batch row in the chunk (a multiple of 64)
     const int total = B * n4;                 // <= 8 * nthr (chunk size chosen by the host)
+    // row of float4 number e: e / n4 = (e >> 6) / nblk, by multiplication with a
+    // rounded-up 16-bit reciprocal; exact because e >> 6 < B * nblk <= 32 (the
+    // host keeps B * kc <= 32), checked for every nblk up to 4096 and quotient
+    // below 64
+    const uint32_t inv_nblk = (65536u + static_cast<uint32_t>(nblk) - 1u) / static_cast<uint32_t>(nblk);
+    auto row_of = [&](int e) { return static_cast<int>(((static_cast<uint32_t>(e) >> 6) * inv_nblk) >> 16); };
+    const float4 *xs = reinterpret_cast<const float4 *>(x + static_cast<size_t>(kb0) * 256);
+    const int K4 = K / 4;
     float4 v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int e = j * nthr + tid;
         if (e < total) {
-            const int b = e / n4, i = e - b * n4;
-            v[j] = __ldg(reinterpret_cast<const float4 *>(x + static_cast<size_t>(b) * K +
-                                                          static_cast<size_t>(kb0) * 256) + i);
+            const int b = row_of(e);
+            v[j] = __ldg(xs + b * K4 + (e - b * n4));
         }
     }
     after_loads();
@@ -168,7 +175,7 @@ __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int k
                         max(__float_as_uint(fabsf(v[j].z)), __float_as_uint(fabsf(v[j].w))));
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if ((tid & 31) == 0 && m) atomicMax(&s_amax[e0 / n4], m);
+            if ((tid & 31) == 0 && m) atomicMax(&s_amax[row_of(e0)], m);
         }
     }
     named_bar_sync(1, nthr);
@@ -178,7 +185,7 @@ __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int k
         if (e0 >= total) continue;            // warp-uniform
         const int e = j * nthr + tid;
         const bool live = e < total;
-        const int b = e0 / n4;                // the whole warp is in one row
+        const int b = row_of(e0);             // the whole warp is in one row
         const int i = e - b * n4;
         const float sc = __uint_as_float(static_cast<uint32_t>(chunk_scale_exp(s_amax[b]) + 127) << 23);
         float4 w = live ? v[j] : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -357,12 +364,10 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
 #pragma unroll
         for (int g = 0; g < kMaxGroups; ++g)
             if (g < args.ngroups) prefetch_tensormap(&maps.m[g]);
-        // The first stage streams in while the CTA sets up and, under PDL,
+        // The first stages stream in while the CTA sets up and, under PDL,
         // while the previous kernel finishes (weights never depend on it).
-        // Only one: x is loaded after the dependency wait and must not queue
-        // behind a full ring of weight data at the SM's memory port.
         iss.policy = l2_policy_evict_first();
-        const int first = min(1, iss.total);
+        const int first = min(kStages, iss.total);
         for (int i = 0; i < first; ++i) iss.issue(i);
         s_issued = first;
     }
@@ -382,19 +387,8 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     const int t = lane & 3;
     const int nchunks = (ks + args.kc - 1) / args.kc;
     const bool single_chunk = (nchunks == 1);
-    // the rest of the initial ring is issued once this thread's x loads are out
-    auto fill_ring = [&]() {
-        if (tid == 0) {
-            const int upto = min(kStages, iss.total);
-            for (int i = 1; i < upto; ++i) iss.issue(i);
-            atomicAdd(&s_issued, max(0, upto - 1));
-        }
-    };
     auto nothing = []() {};
-    if (single_chunk)
-        convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_unscale, s_amax, tid, kThreads, fill_ring);
-    else
-        fill_ring();
+    if (single_chunk) convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_unscale, s_amax, tid, kThreads, nothing);
     // B-fragment lane.  Lanes whose column holds no batch row read some other
     // valid entry: MMA columns are independent, and those output columns are
     // never used.
