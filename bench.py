@@ -198,17 +198,22 @@ def kernel_source_hash():
 
 
 def recorded_traffic():
-    """DRAM bytes per weight byte from a committed ncu capture of the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "gemv_traffic.json")
+    """DRAM bytes per algorithmic byte of the batch-1 GEMV kernel, from the
+    committed ncu summary, if it was captured from the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "gemv_traffic.txt")
     if not os.path.exists(p):
         return None
-    try:
-        d = json.load(open(p))
-    except Exception:
-        return None
+    d = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            d[k.strip()] = v.strip()
     if d.get("source_hash") != kernel_source_hash():
         return None
-    return d
+    try:
+        return {"dram_bytes_per_weight_byte": float(d["dram_bytes_per_algorithmic_byte"])}
+    except (KeyError, ValueError):
+        return None
 
 
 def run_ours(args):
