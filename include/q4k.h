@@ -198,6 +198,51 @@ typedef struct {
 q4k_status q4k_gemv_grouped(const q4k_gemv_group *groups, int ngroups, const float *x, int64_t K,
                             int batch, void *stream, const q4k_launch_opts *opts);
 
+/*
+ * Chains: a fixed sequence of GEMV steps run by ONE persistent kernel launch.
+ * Each step is what one q4k_gemv_grouped call computes (1..4 matrices that
+ * multiply the same x).  The semantics are those of issuing the steps one
+ * after the other on a stream: step s+1 reads its x only after every output
+ * of steps 0..s has been written, so a step may read an earlier step's
+ * output, and an output may overwrite an earlier step's input.  The gain over
+ * separate launches is that the weights of step s+1 already stream into the
+ * GPU while step s finishes, and no CTA has to be launched or drained between
+ * steps.  This extends the pages' fused decode dispatch (dotLLM README, News
+ * 2026-03: fewer dispatches per decode step) to a whole decode step; the
+ * pages have no chain API of their own, this is an interface choice of this
+ * library.
+ *
+ * q4k_chain_create validates the steps, picks each step's split and encodes
+ * its tensor maps into device memory allocated with cudaMalloc on the current
+ * device (synchronous: call it outside stream capture).  The chain keeps the
+ * pointers it was given: the weights, x and y buffers must stay allocated and
+ * at the same addresses while the chain is used; their contents may change
+ * between runs.  q4k_chain_run launches the whole sequence on `stream`
+ * (capturable in a CUDA graph): two stream-ordered memsets of the chain's
+ * small counters, then one cooperative kernel launch; runs of the same chain
+ * must not overlap on the GPU.  q4k_chain_destroy frees the device memory
+ * (synchronous; no run may still be pending).
+ *   steps[s].x       fp32 [batch][K], 16-byte aligned
+ *   steps[s].K       multiple of 256 (same for the step's matrices)
+ *   steps[s].ngroups 1..4; groups as in q4k_gemv_grouped (N == 0 skipped)
+ *   nsteps           1..4096 (the step table must also fit in shared memory:
+ *                    Q4K_ERR_INVALID_ARG if it does not)
+ *   batch            1..16
+ */
+#define Q4K_CHAIN_MAX_STEPS 4096
+typedef struct {
+    const float *x;
+    int64_t K;
+    int ngroups;
+    q4k_gemv_group groups[4];
+} q4k_chain_step;
+
+typedef struct q4k_chain q4k_chain;
+
+q4k_status q4k_chain_create(const q4k_chain_step *steps, int nsteps, int batch, q4k_chain **chain);
+q4k_status q4k_chain_run(const q4k_chain *chain, void *stream);
+q4k_status q4k_chain_destroy(q4k_chain *chain);
+
 /* Launch plan the automatic heuristics pick for a shape (for tests and
  * reports): out[0] = split_k, out[1] = number of CTAs, out[2] = rows per CTA
  * tile, out[3] = K blocks per x chunk held in shared memory. */

@@ -38,10 +38,15 @@ class GemvGroup(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int64)]
 
 
+class ChainStep(ctypes.Structure):
+    _fields_ = [("x", ctypes.c_void_p), ("K", ctypes.c_int64), ("ngroups", ctypes.c_int),
+                ("groups", GemvGroup * 4)]
+
+
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("q4k_status_string", "q4k_abi_version", "q4k_gemv", "q4k_gemv_argmax", "q4k_gemv_argmax_debug",
            "q4k_gemv_argmax_noalloc", "q4k_gemm_prefill", "q4k_gemv_ex", "q4k_gemv_grouped", "q4k_gemv_plan",
-           "q4k_device_error_flags")
+           "q4k_device_error_flags", "q4k_chain_create", "q4k_chain_run", "q4k_chain_destroy")
 
 
 def lib():
@@ -74,6 +79,12 @@ def lib():
         L.q4k_gemv_plan.argtypes = [I64, I64, I, ctypes.POINTER(ctypes.c_int * 4)]
         L.q4k_gemv_plan.restype = I
         L.q4k_device_error_flags.restype = ctypes.c_uint
+        L.q4k_chain_create.argtypes = [ctypes.POINTER(ChainStep), I, I, ctypes.POINTER(ctypes.c_void_p)]
+        L.q4k_chain_create.restype = I
+        L.q4k_chain_run.argtypes = [P, P]
+        L.q4k_chain_run.restype = I
+        L.q4k_chain_destroy.argtypes = [P]
+        L.q4k_chain_destroy.restype = I
         _lib = L
         return L
 
@@ -199,6 +210,62 @@ def gemm_prefill(W, X, Y=None, *, stream=None):
     st = lib().q4k_gemm_prefill(W.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, _stream_ptr(stream))
     _check("q4k_gemm_prefill", st)
     return Y
+
+
+class Chain:
+    """A fixed sequence of GEMV steps run by one persistent launch (q4k_chain_*).
+
+    steps: list of (x, [(W, y), ...]) with x fp32 [batch, K] and per matrix W
+    uint8 [N, K/256*144], y fp32 [batch, N] (1..4 matrices per step).  Step s+1
+    reads its x only after all outputs of the earlier steps are written, so x of
+    a later step may be the y of an earlier one.  The chain keeps the tensors'
+    addresses: they stay referenced by this object."""
+
+    def __init__(self, steps, batch: int):
+        import torch
+        L = lib()
+        self._keep = []
+        arr = (ChainStep * len(steps))()
+        for i, (x, groups) in enumerate(steps):
+            _dev(x, "x", torch.float32)
+            x2 = x.view(1, -1) if x.dim() == 1 else x
+            if x2.shape[0] != batch:
+                raise ValueError(f"step {i}: x has {x2.shape[0]} rows, batch is {batch}")
+            K = x2.shape[1]
+            if not 1 <= len(groups) <= 4:
+                raise ValueError(f"step {i}: 1 to 4 matrices")
+            arr[i].x = x2.data_ptr()
+            arr[i].K = K
+            arr[i].ngroups = len(groups)
+            for g, (W, y) in enumerate(groups):
+                _dev(W, "W", torch.uint8)
+                _dev(y, "y", torch.float32)
+                N = _shape_wk(W, K)
+                if y.numel() != batch * N:
+                    raise ValueError(f"step {i}: y has the wrong size")
+                arr[i].groups[g] = GemvGroup(W.data_ptr(), y.data_ptr(), N)
+                self._keep += [W, y]
+            self._keep.append(x)
+        h = ctypes.c_void_p()
+        _check("q4k_chain_create", L.q4k_chain_create(arr, len(steps), batch, ctypes.byref(h)))
+        self._h = h
+        self._lib = L
+
+    def run(self, stream=None):
+        if self._h is None:
+            raise RuntimeError("chain is closed")
+        _check("q4k_chain_run", self._lib.q4k_chain_run(self._h, _stream_ptr(stream)))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            self._lib.q4k_chain_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def gemv_plan(N: int, K: int, batch: int):

@@ -62,6 +62,15 @@ q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t
     return q4k::prefill_impl(W, X_bf16, Y, N, K, T, stream);
 }
 
+q4k_status q4k_chain_create(const q4k_chain_step *steps, int nsteps, int batch, q4k_chain **chain)
+{
+    return q4k::chain_create_impl(steps, nsteps, batch, chain);
+}
+
+q4k_status q4k_chain_run(const q4k_chain *chain, void *stream) { return q4k::chain_run_impl(chain, stream); }
+
+q4k_status q4k_chain_destroy(q4k_chain *chain) { return q4k::chain_destroy_impl(chain); }
+
 q4k_status q4k_gemv_plan(int64_t N, int64_t K, int batch, int out[4])
 {
     return q4k::gemv_plan_impl(N, K, batch, out);

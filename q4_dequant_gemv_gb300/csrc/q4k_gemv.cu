@@ -48,6 +48,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <new>
+#include <vector>
 
 #include "../../include/q4k.h"
 #include "ptx.cuh"
@@ -137,7 +139,7 @@ __device__ __forceinline__ int chunk_scale_exp(uint32_t amax_bits)
 // half h = j%2), word u = i%8 -> k-step s = 2u + h of pair t.  Called by all
 // threads; the caller must have finished reading the previous chunk's
 // fragments (its named barrier) before it is entered.
-template <int NT, typename AfterLoads>
+template <int NT, typename AfterLoads, bool L2ONLY = false>
 __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int kb0, int nblk, uint2 *xf,
                                 float *s_unscale, uint32_t *s_amax, int tid, int nthr, const AfterLoads &after_loads)
 {
@@ -159,7 +161,7 @@ __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int k
         const int e = j * nthr + tid;
         if (e < total) {
             const int b = row_of(e);
-            v[j] = __ldg(xs + b * K4 + (e - b * n4));
+            v[j] = L2ONLY ? __ldcg(xs + b * K4 + (e - b * n4)) : __ldg(xs + b * K4 + (e - b * n4));
         }
     }
     after_loads();
@@ -222,6 +224,18 @@ __device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int k
     for (int b = tid; b < B; b += nthr) s_amax[b] = 0u;
 }
 
+// Warm L2 with x[b][kb0*256, kb1*256) for every batch row (one 128-byte line
+// per thread and round).  Safe before the dependency wait: L2 is where the
+// previous kernel's writes land, so the loads after the wait still see them.
+__device__ __forceinline__ void prefetch_x_l2(const float *x, int K, int B, int kb0, int kb1, int tid, int nthr)
+{
+    const int lines = (kb1 - kb0) * 8;   // 1 KB of floats per super-block
+    for (int i = tid; i < B * lines; i += nthr) {
+        const int b = i / lines;
+        prefetch_l2(x + static_cast<size_t>(b) * K + static_cast<size_t>(kb0) * 256 + (i - b * lines) * 32);
+    }
+}
+
 // Scale/min constants of one row of a super-block for thread t (pair t).
 struct RowConsts {
     uint32_t mulE, addE, mulO, addO;  // f16x2 (sc_2t), (-1024 sc_2t), (sc_2t+1 / 16), (-64 sc_2t+1)
@@ -258,6 +272,76 @@ __device__ __forceinline__ RowConsts decode_header(uint4 h, int t)
     return rc;
 }
 
+// One super-block of this warp's 16 rows (rows g and g + 8 for thread (g, t)):
+// dequantize into A fragments, run the k16 steps against the x fragments at
+// xl, call release() once the slot's bytes have been read, then fold the
+// super-block into acc as d*C - dmin*Cmin.  NC accumulator chains per
+// sub-block parity (2: shorter dependency chains; 1: fewer registers).
+template <int NT, int NC, typename Release>
+__device__ __forceinline__ void stage_compute(const uint8_t *ra, const uint8_t *rb, const uint2 *xl, int t,
+                                              const float (&unscale)[NT], float (&acc)[NT][2], Release &&release)
+{
+    const RowConsts r0 = decode_header(*reinterpret_cast<const uint4 *>(ra), t);
+    const RowConsts r1 = decode_header(*reinterpret_cast<const uint4 *>(rb), t);
+    float cE[NC][NT][4], cO[NC][NT][4], cM[NT][4];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const uint4 qa = *reinterpret_cast<const uint4 *>(ra + 16 + 32 * t + 16 * half);
+        const uint4 qb = *reinterpret_cast<const uint4 *>(rb + 16 + 32 * t + 16 * half);
+        const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+        const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+            const int u = 4 * half + uu;
+            const uint32_t a = wa[uu], a8 = a >> 8;
+            const uint32_t c = wb[uu], c8 = c >> 8;
+            const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
+            const uint32_t e0 = hfma2_u32(and_or(a, mlo, magic), r0.mulE, r0.addE);
+            const uint32_t e1 = hfma2_u32(and_or(a8, mlo, magic), r0.mulE, r0.addE);
+            const uint32_t o0 = hfma2_u32(and_or(a, mhi, magic), r0.mulO, r0.addO);
+            const uint32_t o1 = hfma2_u32(and_or(a8, mhi, magic), r0.mulO, r0.addO);
+            const uint32_t f0 = hfma2_u32(and_or(c, mlo, magic), r1.mulE, r1.addE);
+            const uint32_t f1 = hfma2_u32(and_or(c8, mlo, magic), r1.mulE, r1.addE);
+            const uint32_t p0 = hfma2_u32(and_or(c, mhi, magic), r1.mulO, r1.addO);
+            const uint32_t p1 = hfma2_u32(and_or(c8, mhi, magic), r1.mulO, r1.addO);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint2 be = xl[2 * u * NT + nt];
+                const uint2 bo = xl[(2 * u + 1) * NT + nt];
+                if (u < NC) {   // first k-step of each accumulator chain
+                    mma_16816_z(cE[uu % NC][nt], e0, f0, e1, f1, be.x, be.y);
+                    mma_16816_z(cO[uu % NC][nt], o0, p0, o1, p1, bo.x, bo.y);
+                } else {
+                    mma_16816(cE[uu % NC][nt], e0, f0, e1, f1, be.x, be.y);
+                    mma_16816(cO[uu % NC][nt], o0, p0, o1, p1, bo.x, bo.y);
+                }
+            }
+        }
+    }
+    release();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const uint2 bm = xl[16 * NT + nt];
+        mma_16816_z(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
+        float s0, s1;
+        if constexpr (NC == 2) {
+            s0 = ((cE[0][nt][0] + cE[1][nt][0]) + (cO[0][nt][0] + cO[1][nt][0])) +
+                 ((cE[0][nt][1] + cE[1][nt][1]) + (cO[0][nt][1] + cO[1][nt][1]));
+            s1 = ((cE[0][nt][2] + cE[1][nt][2]) + (cO[0][nt][2] + cO[1][nt][2])) +
+                 ((cE[0][nt][3] + cE[1][nt][3]) + (cO[0][nt][3] + cO[1][nt][3]));
+        } else {
+            s0 = (cE[0][nt][0] + cO[0][nt][0]) + (cE[0][nt][1] + cO[0][nt][1]);
+            s1 = (cE[0][nt][2] + cO[0][nt][2]) + (cE[0][nt][3] + cO[0][nt][3]);
+        }
+        const float m0 = cM[nt][0] + cM[nt][1];
+        const float m1 = cM[nt][2] + cM[nt][3];
+        acc[nt][0] = fmaf(r0.d * unscale[nt], s0, acc[nt][0]);
+        acc[nt][0] = fmaf(-r0.dmin * unscale[nt], m0, acc[nt][0]);
+        acc[nt][1] = fmaf(r1.d * unscale[nt], s1, acc[nt][1]);
+        acc[nt][1] = fmaf(-r1.dmin * unscale[nt], m1, acc[nt][1]);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel body.  All 8 warps consume (16 rows each); there is no producer
 // warp.  Thread 0 issues the first kStages weight stages right after
@@ -283,7 +367,8 @@ struct TileInfo {
     float *y;
 };
 
-__device__ __forceinline__ TileInfo tile_info(const GemvArgs &a, int tile)
+template <typename Desc>
+__device__ __forceinline__ TileInfo tile_info(const Desc &a, int tile)
 {
     TileInfo ti{0, tile * kRows, a.N[0], a.y[0]};
 #pragma unroll
@@ -437,73 +522,23 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             // this lane's B fragments of this super-block (lane-major layout)
             const uint2 *xl = xf + static_cast<size_t>((single_chunk ? kbl : (kbl % args.kc)) * LW + blane) *
                                        lane_stride(NT);
-            const RowConsts r0 = decode_header(*reinterpret_cast<const uint4 *>(ra), t);
-            const RowConsts r1 = decode_header(*reinterpret_cast<const uint4 *>(rb), t);
-            float cE[2][NT][4], cO[2][NT][4], cM[NT][4];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const uint4 qa = *reinterpret_cast<const uint4 *>(ra + 16 + 32 * t + 16 * half);
-                const uint4 qb = *reinterpret_cast<const uint4 *>(rb + 16 + 32 * t + 16 * half);
-                const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
-                const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-                for (int uu = 0; uu < 4; ++uu) {
-                    const int u = 4 * half + uu;
-                    const uint32_t a = wa[uu], a8 = a >> 8;
-                    const uint32_t c = wb[uu], c8 = c >> 8;
-                    const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
-                    const uint32_t e0 = hfma2_u32(and_or(a, mlo, magic), r0.mulE, r0.addE);
-                    const uint32_t e1 = hfma2_u32(and_or(a8, mlo, magic), r0.mulE, r0.addE);
-                    const uint32_t o0 = hfma2_u32(and_or(a, mhi, magic), r0.mulO, r0.addO);
-                    const uint32_t o1 = hfma2_u32(and_or(a8, mhi, magic), r0.mulO, r0.addO);
-                    const uint32_t f0 = hfma2_u32(and_or(c, mlo, magic), r1.mulE, r1.addE);
-                    const uint32_t f1 = hfma2_u32(and_or(c8, mlo, magic), r1.mulE, r1.addE);
-                    const uint32_t p0 = hfma2_u32(and_or(c, mhi, magic), r1.mulO, r1.addO);
-                    const uint32_t p1 = hfma2_u32(and_or(c8, mhi, magic), r1.mulO, r1.addO);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const uint2 be = xl[2 * u * NT + nt];
-                        const uint2 bo = xl[(2 * u + 1) * NT + nt];
-                        if (u < 2) {   // first k-step of each accumulator chain
-                            mma_16816_z(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
-                            mma_16816_z(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
-                        } else {
-                            mma_16816(cE[uu & 1][nt], e0, f0, e1, f1, be.x, be.y);
-                            mma_16816(cO[uu & 1][nt], o0, p0, o1, p1, bo.x, bo.y);
+            stage_compute<NT, 2>(ra, rb, xl, t, unscale, acc, [&]() {
+                // This warp is done with the slot: the last warp to finish refills it.
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence_block();
+                    // monotonic per-slot count: the kWarps-th arrival of each round is last
+                    const int prev = atomicAdd(&s_slot_done[slot], 1);
+                    if (prev % kWarps == kWarps - 1) {
+                        const int next = consumed + kStages;
+                        if (next < iss.total && !*(volatile int *)&s_abort) {
+                            iss.issue(next);
+                            atomicAdd(&s_issued, 1);
                         }
                     }
                 }
-            }
-            // This warp is done with the slot: the last warp to finish refills it.
-            __syncwarp();
-            if (lane == 0) {
-                __threadfence_block();
-                // monotonic per-slot count: the kWarps-th arrival of each round is last
-                const int prev = atomicAdd(&s_slot_done[slot], 1);
-                if (prev % kWarps == kWarps - 1) {
-                    const int next = consumed + kStages;
-                    if (next < iss.total && !*(volatile int *)&s_abort) {
-                        iss.issue(next);
-                        atomicAdd(&s_issued, 1);
-                    }
-                }
-            }
-            ++consumed;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const uint2 bm = xl[16 * NT + nt];
-                mma_16816_z(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
-                const float s0 = ((cE[0][nt][0] + cE[1][nt][0]) + (cO[0][nt][0] + cO[1][nt][0])) +
-                                 ((cE[0][nt][1] + cE[1][nt][1]) + (cO[0][nt][1] + cO[1][nt][1]));
-                const float s1 = ((cE[0][nt][2] + cE[1][nt][2]) + (cO[0][nt][2] + cO[1][nt][2])) +
-                                 ((cE[0][nt][3] + cE[1][nt][3]) + (cO[0][nt][3] + cO[1][nt][3]));
-                const float m0 = cM[nt][0] + cM[nt][1];
-                const float m1 = cM[nt][2] + cM[nt][3];
-                acc[nt][0] = fmaf(r0.d * unscale[nt], s0, acc[nt][0]);
-                acc[nt][0] = fmaf(-r0.dmin * unscale[nt], m0, acc[nt][0]);
-                acc[nt][1] = fmaf(r1.d * unscale[nt], s1, acc[nt][1]);
-                acc[nt][1] = fmaf(-r1.dmin * unscale[nt], m1, acc[nt][1]);
-            }
+                ++consumed;
+            });
         }
         // ---------------- tile epilogue
         if (split == 1 && !*(volatile int *)&s_abort) {
@@ -614,6 +649,347 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel_wide(const __grid
                                                                    const GemvArgs args)
 {
     gemv_body<NT, ARGMAX>(maps, args);
+}
+
+// ---------------------------------------------------------------------------
+// Chain: a sequence of GEMV steps (each one grouped GEMV: up to four matrices
+// sharing one x) in ONE persistent launch.
+//
+// The CTAs of a cooperative grid stay resident across steps.  Each CTA works
+// through a fixed share of every step (work unit = row tile x K slice; with
+// G CTAs, unit u goes to CTA u mod G) and streams its weight stages through
+// one ring for the whole chain, so the stages of step s+1 are already in
+// flight while step s finishes: the same last-arriver refill as above, with
+// the stage -> (step, unit, super-block) map looked up in a per-CTA table.
+// Step s+1 reads x only after every CTA has finished step s (a counter in
+// global memory, bounded spin), so a step may consume the output of an
+// earlier one.  A K split over CTAs (a power of two dividing G, so that a
+// CTA's K slice is the same for all its units of a step) is reduced without
+// clusters: each slice writes its partial rows to a scratch area and the last
+// slice of the tile (global ticket) adds them in slice order.
+// ---------------------------------------------------------------------------
+// One step as the kernel reads it from device memory (the tensor maps make it
+// 128-byte aligned).
+struct ChainStep {
+    CUtensorMap maps[kMaxGroups];
+    const float *x;
+    float *y[kMaxGroups];
+    int N[kMaxGroups];
+    int tile_start[kMaxGroups + 1];
+    int ngroups;
+    int nb;      // super-blocks per row
+    int tiles;   // row tiles of all matrices
+    int split;   // K slices per tile (power of two dividing the grid)
+    int kc;      // super-blocks per x chunk
+};
+
+// The copy each CTA keeps in shared memory, with its own K slice and unit count.
+struct ChainStepS {
+    float *y[kMaxGroups];
+    const float *x;
+    int N[kMaxGroups];
+    int tile_start[kMaxGroups + 1];
+    int ngroups, nb, split, kc;
+    int kb0, ks, mine;   // this CTA: first super-block and length of its K slice, units
+};
+
+struct ChainArgs {
+    const ChainStep *steps;
+    int nsteps;
+    int B;
+    int kc_max;                 // x chunk capacity of the shared-memory layout
+    float *partials;            // split-K partial rows [tile][slice][B][128]
+    unsigned int *tickets;      // per row tile, zero between uses
+    unsigned int *bar;          // arrivals of all CTAs, zeroed before the launch
+};
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p)
+{
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Wait until *bar >= target (bounded; gives up early once any kernel of the
+// library has flagged an error).
+__device__ __forceinline__ bool grid_wait(const unsigned int *bar, unsigned int target)
+{
+    if (ld_acquire_u32(bar) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        __nanosleep(64);
+        if (ld_acquire_u32(bar) >= target) return true;
+        if (*(volatile unsigned int *)&g_device_error) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+__host__ __device__ inline size_t chain_xf_bytes(int NT, int B, int kc_max)
+{
+    return (xfrag_bytes_per_block(NT, B) * kc_max + 127) & ~size_t(127);
+}
+
+// Issue global stage i of this CTA's chain schedule into ring slot i % kStages.
+// The slot's next stage is always kStages further on, so its step is found by
+// walking forward from the step of the slot's previous stage (cursor[slot]).
+__device__ __forceinline__ void chain_issue(const ChainArgs &args, const ChainStepS *s_steps, const int *s_start,
+                                            int *cursor, uint8_t *ring, uint64_t *full, int i)
+{
+    const int slot = i % kStages;
+    int si = cursor[slot];
+    while (s_start[si + 1] <= i) ++si;
+    cursor[slot] = si;
+    const ChainStepS &st = s_steps[si];
+    const int local = i - s_start[si];
+    const int ul = local / st.ks;
+    const int kb = st.kb0 + (local - ul * st.ks);
+    const int tile = (static_cast<int>(blockIdx.x) + ul * static_cast<int>(gridDim.x)) / st.split;
+    const TileInfo ti = tile_info(st, tile);
+    mbar_arrive_expect_tx(smem_u32(&full[slot]), kStageBytes);
+    tma_load_2d_hint(smem_u32(ring + slot * kStageBytes), &args.steps[si].maps[ti.grp], kb * (kBlockBytes / 8),
+                     ti.row0, smem_u32(&full[slot]), l2_policy_evict_first());
+}
+
+template <int NT>
+__device__ __forceinline__ void chain_body(const ChainArgs &args)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *ring = smem_raw;
+    const int B = args.B;
+    const int LW = frag_lanes(NT, B);
+    uint2 *xf = reinterpret_cast<uint2 *>(smem_raw + xfrag_offset());
+    ChainStepS *s_steps = reinterpret_cast<ChainStepS *>(smem_raw + xfrag_offset() + chain_xf_bytes(NT, B, args.kc_max));
+    int *s_start = reinterpret_cast<int *>(s_steps + args.nsteps);   // [nsteps + 1]
+    __shared__ __align__(8) uint64_t full[kStages];
+    __shared__ float s_unscale[16];
+    __shared__ uint32_t s_amax[16];
+    __shared__ int s_abort;
+    __shared__ int s_issued;
+    __shared__ int s_last;
+    __shared__ int s_slot_done[kStages];
+    __shared__ int s_cons[kWarps];
+    __shared__ int s_cursor[kStages];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int G = gridDim.x;
+    const int c = blockIdx.x;
+    const int nsteps = args.nsteps;
+
+    // this CTA's copy of the steps and its number of stages per step
+    for (int si = tid; si < nsteps; si += kThreads) {
+        const ChainStep &st = args.steps[si];
+        ChainStepS &d = s_steps[si];
+#pragma unroll
+        for (int g = 0; g < kMaxGroups; ++g) {
+            d.y[g] = st.y[g];
+            d.N[g] = st.N[g];
+            d.tile_start[g] = st.tile_start[g];
+        }
+        d.tile_start[kMaxGroups] = st.tile_start[kMaxGroups];
+        d.x = st.x;
+        d.ngroups = st.ngroups;
+        d.nb = st.nb;
+        d.split = st.split;
+        d.kc = st.kc;
+        const int units = st.tiles * st.split;
+        const int rank = c & (st.split - 1);
+        d.mine = (c < units) ? (units - c + G - 1) / G : 0;
+        d.kb0 = (rank * st.nb) / st.split;
+        d.ks = ((rank + 1) * st.nb) / st.split - d.kb0;
+        s_start[si + 1] = d.mine * d.ks;
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            s_slot_done[i] = 0;
+            s_cursor[i] = 0;
+        }
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (tid < 16) s_amax[tid] = 0u;
+    if (tid < kWarps) s_cons[tid] = 0;
+    __syncthreads();
+    if (tid == 0) {
+        s_start[0] = 0;
+        for (int si = 0; si < nsteps; ++si) s_start[si + 1] += s_start[si];
+    }
+    __syncthreads();
+    const int total = s_start[nsteps];
+    auto issue = [&](int i) { chain_issue(args, s_steps, s_start, s_cursor, ring, full, i); };
+
+    if (tid == 0) {
+        // the TMA unit reads the tensor maps from global memory: warm its
+        // descriptor cache for the first two steps before the first copies
+        for (int si = 0; si < min(nsteps, 2); ++si)
+            for (int g = 0; g < s_steps[si].ngroups; ++g) prefetch_tensormap(&args.steps[si].maps[g]);
+        const int first = min(kStages, total);
+        for (int i = 0; i < first; ++i) issue(i);
+        s_issued = first;
+    }
+
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int blane = (g < 2 * B) ? lane : (lane % LW);
+    const int row_off = (warp * 16 + g) * kBlockBytes;
+    int consumed = 0;
+    auto nothing = []() {};
+
+    for (int si = 0; si < nsteps; ++si) {
+        const ChainStepS &st = s_steps[si];
+        const int split = st.split;
+        const int rank = c & (split - 1);
+        const int kb_begin = st.kb0;
+        const int ks = st.ks;
+        const int mine = st.mine;
+        // x of this step may be an output of an earlier step: wait until
+        // every CTA has finished step si - 1
+        if (tid == 32 && si + 2 < nsteps)   // maps of the step after next (its copies start during step si + 1)
+            for (int gi = 0; gi < s_steps[si + 2].ngroups; ++gi) prefetch_tensormap(&args.steps[si + 2].maps[gi]);
+        if (mine > 0) prefetch_x_l2(st.x, st.nb * 256, B, kb_begin, kb_begin + ks, tid, kThreads);
+        if (si > 0) {
+            if (tid == 0 && !*(volatile int *)&s_abort && !grid_wait(args.bar, static_cast<unsigned>(si * G))) {
+                atomicOr(&g_device_error, 1u);
+                s_abort = 1;
+            }
+            __syncthreads();
+        }
+        if (mine > 0 && !*(volatile int *)&s_abort) {
+            const int kc = st.kc;
+            const bool single_chunk = ks <= kc;
+            if (single_chunk)
+                convert_x_chunk<NT, decltype(nothing), true>(st.x, st.nb * 256, B, kb_begin, ks, xf, s_unscale,
+                                                              s_amax, tid, kThreads, nothing);
+            for (int ul = 0; ul < mine; ++ul) {
+                float acc[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
+                float unscale[NT];
+                int chunk_end = -1;
+                bool reload_scale = true;
+                for (int kbl = 0; kbl < ks; ++kbl) {
+                    if (!single_chunk && kbl > chunk_end) {
+                        const int cn = min(kc, ks - kbl);
+                        named_bar_sync(1, kThreads);   // everyone done with the previous chunk
+                        convert_x_chunk<NT, decltype(nothing), true>(st.x, st.nb * 256, B, kb_begin + kbl, cn, xf,
+                                                                      s_unscale, s_amax, tid, kThreads, nothing);
+                        chunk_end = kbl + cn - 1;
+                        reload_scale = true;
+                    }
+                    if (reload_scale) {
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const int b = t + 4 * nt;
+                            unscale[nt] = (b < B) ? s_unscale[b] : 0.f;
+                        }
+                        reload_scale = false;
+                    }
+                    const int slot = consumed % kStages;
+                    const uint32_t phase = static_cast<uint32_t>((consumed / kStages) & 1);
+                    if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), phase, kWaitLimitNs)) {
+                        atomicOr(&g_device_error, 1u);
+                        s_abort = 1;
+                    }
+                    const uint8_t *ra = ring + slot * kStageBytes + row_off;
+                    const uint8_t *rb = ra + 8 * kBlockBytes;
+                    const uint2 *xl =
+                        xf + static_cast<size_t>((single_chunk ? kbl : (kbl % kc)) * LW + blane) * lane_stride(NT);
+                    // the refill runs after the stage (fewer live registers than
+                    // inside it: the stage-to-step lookup is longer here)
+                    stage_compute<NT, 1>(ra, rb, xl, t, unscale, acc, []() {});
+                    __syncwarp();
+                    if (lane == 0) {
+                        __threadfence_block();
+                        const int prev = atomicAdd(&s_slot_done[slot], 1);
+                        if (prev % kWarps == kWarps - 1) {
+                            const int next = consumed + kStages;
+                            if (next < total && !*(volatile int *)&s_abort) {
+                                issue(next);
+                                atomicAdd(&s_issued, 1);
+                            }
+                        }
+                    }
+                    ++consumed;
+                }
+                // ---------------- unit epilogue
+                const int tile = (c + ul * G) / split;
+                const TileInfo ti = tile_info(st, tile);
+                if (split == 1) {
+                    if (!*(volatile int *)&s_abort) {
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            const int b = t + 4 * nt;
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int row = ti.row0 + warp * 16 + g + 8 * h;
+                                if (b < B && row < ti.N) ti.y[static_cast<size_t>(b) * ti.N + row] = acc[nt][h];
+                            }
+                        }
+                    }
+                } else {
+                    float *part = args.partials + static_cast<size_t>(tile * split + rank) * B * kRows;
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int b = t + 4 * nt;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            if (b < B) part[b * kRows + warp * 16 + g + 8 * h] = acc[nt][h];
+                    }
+                    __syncthreads();
+                    if (tid == 0) {
+                        __threadfence();
+                        const unsigned prev = atomicAdd(&args.tickets[tile], 1u);
+                        s_last = (prev == static_cast<unsigned>(split - 1));
+                    }
+                    __syncthreads();
+                    if (s_last) {
+                        // every slice of the tile is in: add them in slice order
+                        __threadfence();
+                        const float *p0 = args.partials + static_cast<size_t>(tile * split) * B * kRows;
+                        for (int idx = tid; idx < B * kRows; idx += kThreads) {
+                            float sum = __ldcg(p0 + idx);
+                            for (int q = 1; q < split; ++q) sum += __ldcg(p0 + static_cast<size_t>(q) * B * kRows + idx);
+                            const int b = idx / kRows;
+                            const int row = ti.row0 + (idx - b * kRows);
+                            if (row < ti.N && !*(volatile int *)&s_abort) ti.y[static_cast<size_t>(b) * ti.N + row] = sum;
+                        }
+                        if (tid == 0) args.tickets[tile] = 0u;
+                    }
+                }
+            }
+        }
+        // this CTA's share of step si is done: its outputs are written and its x is read
+        __syncthreads();
+        if (tid == 0) {
+            __threadfence();
+            atomicAdd(args.bar, 1u);
+        }
+    }
+    if (lane == 0) s_cons[warp] = consumed;
+
+    // After a timed-out wait: wait (bounded) for the copies issued but not consumed.
+    __syncthreads();
+    if (*(volatile int *)&s_abort && tid == 0) {
+        int lo = s_cons[0];
+        for (int w = 1; w < kWarps; ++w) lo = min(lo, s_cons[w]);
+        for (int i = lo; i < s_issued; ++i)
+            if (!mbar_wait_bounded(smem_u32(&full[i % kStages]), static_cast<uint32_t>((i / kStages) & 1), kWaitLimitNs))
+                break;
+    }
+}
+
+template <int NT>
+__global__ void __maxnreg__(128) q4k_chain_kernel(const __grid_constant__ ChainArgs args)
+{
+    chain_body<NT>(args);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1) q4k_chain_kernel_wide(const __grid_constant__ ChainArgs args)
+{
+    chain_body<NT>(args);
 }
 
 // ---------------------------------------------------------------------------
@@ -1003,6 +1379,219 @@ q4k_status gemv_plan_impl(int64_t N, int64_t K, int batch, int out[4])
     out[2] = kRows;
     out[3] = p.kc;
     return Q4K_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Chains (host side)
+// ---------------------------------------------------------------------------
+// K split of one chain step: a power of two dividing the grid (so that a CTA's
+// K slice is the same for all its units), chosen to minimise (units on the
+// busiest CTA) x (super-blocks per unit + per-unit overhead), with a small
+// charge for the partial-sum fix-up.
+static int chain_split(int tiles, int nb, int G)
+{
+    int best = 1;
+    double best_cost = 1e30;
+    for (int s = 1; s <= 16 && s <= nb; s *= 2) {
+        if (G % s) break;
+        const long long units = static_cast<long long>(tiles) * s;
+        const long long per_cta = (units + G - 1) / G;
+        const int per_unit = (nb + s - 1) / s;
+        const double cost = static_cast<double>(per_cta) * (per_unit + 0.75) + (s > 1 ? 0.25 : 0.0);
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = s;
+        }
+    }
+    return best;
+}
+
+template <int NT>
+static void (*chain_kernel())(const ChainArgs)
+{
+    if constexpr (NT <= 2)
+        return q4k_chain_kernel<NT>;
+    else
+        return q4k_chain_kernel_wide<NT>;
+}
+
+static void (*chain_kernel_for(int NT))(const ChainArgs)
+{
+    switch (NT) {
+        case 1: return chain_kernel<1>();
+        case 2: return chain_kernel<2>();
+        case 3: return chain_kernel<3>();
+        default: return chain_kernel<4>();
+    }
+}
+
+}  // namespace q4k
+
+struct q4k_chain {
+    int dev;
+    int NT;
+    int grid;
+    size_t smem;
+    size_t counter_bytes;   // tickets + barrier counter, cleared before every run
+    void *dmem;
+    q4k::ChainArgs args;
+};
+
+namespace q4k {
+
+q4k_status chain_create_impl(const q4k_chain_step *steps, int nsteps, int batch, q4k_chain **chain)
+{
+    if (!chain) return Q4K_ERR_INVALID_ARG;
+    *chain = nullptr;
+    if (!steps || nsteps < 1 || nsteps > Q4K_CHAIN_MAX_STEPS || batch < 1 || batch > Q4K_MAX_BATCH)
+        return Q4K_ERR_INVALID_ARG;
+    for (int si = 0; si < nsteps; ++si) {
+        const q4k_chain_step &st = steps[si];
+        if (!st.x || st.ngroups < 1 || st.ngroups > kMaxGroups) return Q4K_ERR_INVALID_ARG;
+        if (st.K <= 0 || (st.K % 256) != 0 || st.K / 256 >= (1ll << 24)) return Q4K_ERR_INVALID_ARG;
+        if (reinterpret_cast<uintptr_t>(st.x) & 15u) return Q4K_ERR_MISALIGNED;
+        for (int g = 0; g < st.ngroups; ++g) {
+            const q4k_gemv_group &gr = st.groups[g];
+            if (gr.N < 0 || gr.N > 0x7FFFFFFFll) return Q4K_ERR_INVALID_ARG;
+            if (gr.N == 0) continue;
+            if (!gr.W || !gr.y) return Q4K_ERR_INVALID_ARG;
+            if (reinterpret_cast<uintptr_t>(gr.W) & 15u) return Q4K_ERR_MISALIGNED;
+        }
+    }
+    int sms = 0;
+    q4k_status st = check_device(&sms);
+    if (st != Q4K_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4K_ERR_CUDA;
+
+    const int NT = batch_ntiles(batch);
+    const int cps = (NT <= 2) ? 2 : 1;
+    // shared memory: W ring | x chunk | step table
+    const size_t table = static_cast<size_t>(nsteps) * sizeof(ChainStepS) + static_cast<size_t>(nsteps + 1) * 4;
+    const size_t budget = (NT <= 2) ? kSmemPerCta2 : kSmemPerCta1;
+    const size_t per_blk = xfrag_bytes_per_block(NT, batch);
+    if (xfrag_offset() + table + chain_xf_bytes(NT, batch, 1) > budget) return Q4K_ERR_INVALID_ARG;
+    int kc_need = 1;
+    for (int si = 0; si < nsteps; ++si) kc_need = std::max(kc_need, static_cast<int>(steps[si].K / 256));
+    int kc_max = static_cast<int>((budget - xfrag_offset() - table) / per_blk);
+    while (kc_max > 1 && xfrag_offset() + table + chain_xf_bytes(NT, batch, kc_max) > budget) --kc_max;
+    kc_max = std::max(1, std::min(std::min(kc_max, 32 / batch), kc_need));
+    const size_t smem = xfrag_offset() + chain_xf_bytes(NT, batch, kc_max) + table;
+
+    void (*kern)(const ChainArgs) = chain_kernel_for(NT);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return Q4K_ERR_CUDA;
+    }
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess || occ < 1) {
+        (void)cudaGetLastError();
+        return Q4K_ERR_CUDA;
+    }
+    const int G = sms * std::min(occ, cps);
+
+    // the device-side step table
+    std::vector<ChainStep> hs(nsteps);
+    size_t partial_floats = 0;
+    int max_tiles = 1;
+    for (int si = 0; si < nsteps; ++si) {
+        const q4k_chain_step &in = steps[si];
+        ChainStep &d = hs[si];
+        memset(&d, 0, sizeof(d));
+        d.x = in.x;
+        d.nb = static_cast<int>(in.K / 256);
+        int tiles = 0;
+        for (int g = 0; g < in.ngroups; ++g) {
+            const q4k_gemv_group &gr = in.groups[g];
+            if (gr.N == 0) continue;
+            const int i = d.ngroups++;
+            d.y[i] = gr.y;
+            d.N[i] = static_cast<int>(gr.N);
+            d.tile_start[i] = tiles;
+            tiles += row_tiles(gr.N);
+            if (!encode_w_map(&d.maps[i], gr.W, gr.N, in.K)) return Q4K_ERR_CUDA;
+        }
+        for (int g = d.ngroups; g <= kMaxGroups; ++g) d.tile_start[g] = tiles;
+        d.tiles = tiles;
+        d.split = tiles > 0 ? chain_split(tiles, d.nb, G) : 1;
+        const int ks_max = (d.nb + d.split - 1) / d.split;
+        d.kc = std::min(kc_max, ks_max);
+        if (d.split > 1) {
+            partial_floats = std::max(partial_floats, static_cast<size_t>(tiles) * d.split * batch * kRows);
+            max_tiles = std::max(max_tiles, tiles);
+        }
+    }
+    // one allocation: steps | partial rows | tickets | barrier counter
+    const size_t steps_bytes = (static_cast<size_t>(nsteps) * sizeof(ChainStep) + 255) & ~size_t(255);
+    const size_t part_bytes = (partial_floats * 4 + 255) & ~size_t(255);
+    const size_t counter_bytes = static_cast<size_t>(max_tiles + 1) * 4;
+    void *dmem = nullptr;
+    if (cudaMalloc(&dmem, steps_bytes + part_bytes + counter_bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return Q4K_ERR_CUDA;
+    }
+    uint8_t *base = static_cast<uint8_t *>(dmem);
+    if (cudaMemcpy(base, hs.data(), static_cast<size_t>(nsteps) * sizeof(ChainStep), cudaMemcpyHostToDevice) !=
+        cudaSuccess) {
+        cudaFree(dmem);
+        return Q4K_ERR_CUDA;
+    }
+    q4k_chain *ch = new (std::nothrow) q4k_chain;
+    if (!ch) {
+        cudaFree(dmem);
+        return Q4K_ERR_CUDA;
+    }
+    ch->dev = dev;
+    ch->NT = NT;
+    ch->grid = G;
+    ch->smem = smem;
+    ch->counter_bytes = counter_bytes;
+    ch->dmem = dmem;
+    ch->args.steps = reinterpret_cast<const ChainStep *>(base);
+    ch->args.nsteps = nsteps;
+    ch->args.B = batch;
+    ch->args.kc_max = kc_max;
+    ch->args.partials = reinterpret_cast<float *>(base + steps_bytes);
+    ch->args.tickets = reinterpret_cast<unsigned int *>(base + steps_bytes + part_bytes);
+    ch->args.bar = ch->args.tickets + max_tiles;
+    *chain = ch;
+    return Q4K_OK;
+}
+
+q4k_status chain_run_impl(const q4k_chain *ch, void *stream)
+{
+    if (!ch) return Q4K_ERR_INVALID_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return Q4K_ERR_CUDA;
+    if (dev != ch->dev) return Q4K_ERR_INVALID_ARG;   // the chain's memory lives on another device
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ch->args.tickets, 0, ch->counter_bytes, s) != cudaSuccess) return Q4K_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ch->grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = ch->smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: they wait for one another between steps
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel_for(ch->NT), ch->args);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return Q4K_ERR_CUDA;
+    }
+    return Q4K_OK;
+}
+
+q4k_status chain_destroy_impl(q4k_chain *ch)
+{
+    if (!ch) return Q4K_OK;
+    const cudaError_t e = cudaFree(ch->dmem);
+    delete ch;
+    return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
 unsigned int read_device_error()
