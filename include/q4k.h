@@ -158,9 +158,10 @@ q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t
 /*
  * Extended launch control (tests and benchmarks).  Zero-initialised options
  * reproduce the plain entry points exactly.
- *   split_k  0 = automatic; 1 <= s <= 8 forces the K range of every row tile to
- *            be split over s cooperating CTAs of a thread-block cluster
- *            (clamped to K/256).
+ *   split_k  0 = automatic (up to 16 CTAs per tile for batch <= 8, when all
+ *            clusters fit on the GPU at once); 1 <= s <= 8 forces the K range
+ *            of every row tile to be split over s cooperating CTAs of a
+ *            thread-block cluster (clamped to K/256).
  *   flags    Q4K_FLAG_PDL: launch with programmatic dependent launch, so the
  *            kernel may start streaming W while the previous kernel on the
  *            stream is still running.  W must then not be written by that

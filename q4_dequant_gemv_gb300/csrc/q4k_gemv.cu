@@ -107,9 +107,12 @@ __host__ __device__ inline size_t red_offset(int NT, int B, int kc)
 {
     return xfrag_offset() + ((xfrag_bytes_per_block(NT, B) * kc + 127) & ~size_t(127));
 }
+// Split-K receive buffer: the owner of ceil(128 / split) rows keeps one slot
+// per source rank, split * ceil(128 / split) <= 128 + 15 rows for split <= 16.
+constexpr int kRedRows = kRows + 16;
 __host__ inline size_t gemv_smem_bytes(int NT, int B, int kc, int split)
 {
-    return red_offset(NT, B, kc) + ((split > 1) ? static_cast<size_t>(kRows + 8) * B * 4 : 0);
+    return red_offset(NT, B, kc) + ((split > 1) ? static_cast<size_t>(kRedRows) * B * 4 : 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -1044,6 +1047,42 @@ static int batch_ntiles(int B) { return (2 * B + 7) / 8; }
 
 // Pick the K split: minimise (max row-tile units per SM) x (blocks per unit
 // + per-CTA overhead), preferring fewer CTAs on ties.
+// How many thread-block clusters of `size` CTAs (1..16; above 8 only with the
+// non-portable opt-in) the batch <= 8 GEMV kernels can keep resident at once
+// on the current device, at their largest shared-memory footprint (two CTAs
+// per SM).  The planner uses it to keep a K split within one wave.
+static int max_resident_clusters(int size)
+{
+    static int table[64][17];
+    static std::once_flag once[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::call_once(once[dev], [dev]() {
+        void (*kern)(const WMaps, const GemvArgs) = q4k_gemv_kernel<1, false>;
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemPerCta2));
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        for (int c = 1; c <= 16; ++c) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(1, c, 1);
+            cfg.blockDim = dim3(kThreads, 1, 1);
+            cfg.dynamicSmemBytes = kSmemPerCta2;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 1;
+            attr[0].val.clusterDim.y = c;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+            table[dev][c] = n;
+        }
+        (void)cudaGetLastError();
+    });
+    return table[dev][size];
+}
+
 static GemvPlan make_plan(int tiles, int64_t K, int B, int sms, int forced_split)
 {
     GemvPlan p{};
@@ -1057,10 +1096,13 @@ static GemvPlan make_plan(int tiles, int64_t K, int B, int sms, int forced_split
         // Cost = (units on the busiest SM) x (blocks per unit + per-CTA
         // overhead) / (units that run concurrently on it, at most the CTAs per
         // SM): a lone CTA is latency-bound and cannot use the whole SM.
+        // Splits above 8 (non-portable cluster sizes, batch <= 8 kernels) only
+        // when all of the tile's clusters stay resident in one wave.
         const int cps = (p.NT <= 2) ? 2 : 1;
         double best = 1e30;
-        const int smax = std::min(nb, 8);
+        const int smax = std::min(nb, p.NT <= 2 ? 16 : 8);
         for (int s = 1; s <= smax; ++s) {
+            if (s > 8 && max_resident_clusters(s) < p.tiles) continue;
             const long long units = static_cast<long long>(p.tiles) * s;
             const long long per_sm = (units + sms - 1) / sms;
             const int per_unit = (nb + s - 1) / s;
@@ -1143,6 +1185,11 @@ static cudaError_t launch_one(const GemvPlan &p, const WMaps &maps, const GemvAr
             // CTAs fit on an SM
             e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
             if (e != cudaSuccess) return e;
+            // K splits over up to 16 CTAs (clusters above 8 are non-portable)
+            if (NT <= 2) {
+                e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                if (e != cudaSuccess) return e;
+            }
             smem_set[dev & 63] = static_cast<int>(p.smem);
         }
     }

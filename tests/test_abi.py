@@ -155,3 +155,24 @@ def test_chain_host_validation(q4k):
     assert create(steps(W=0, y=0, N=0)) in (0, 3, 4)   # empty matrices need no pointers
     assert L.q4k_chain_run(None, None) == 1
     assert L.q4k_chain_destroy(None) == 0
+
+
+def test_split_receive_slots_fit():
+    """The GEMV's split-K reduction (one row tile over `split` CTAs of a cluster):
+    rank r owns tile rows [r*128/split, (r+1)*128/split) and receives one slot per
+    source rank for each of them at offset src*(rows owned) + (row - first row).
+    Every offset it writes or reads stays below the 144 rows of the buffer for
+    every split up to 16 (the same formulas as the kernel's epilogue)."""
+    k_rows, buf_rows = 128, 144
+    for split in range(1, 17):
+        top = 0
+        for src in range(split):
+            for row in range(k_rows):
+                owner = (row * split + split - 1) // k_rows
+                o0, o1 = owner * k_rows // split, (owner + 1) * k_rows // split
+                assert o0 <= row < o1
+                top = max(top, src * (o1 - o0) + (row - o0))
+        for rank in range(split):
+            rows = (rank + 1) * k_rows // split - rank * k_rows // split
+            top = max(top, (split - 1) * rows + rows - 1)
+        assert top < buf_rows, (split, top)

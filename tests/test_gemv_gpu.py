@@ -252,3 +252,20 @@ def test_device_error_flags_clear(env):
     q4k, _ = env
     torch.cuda.synchronize()
     assert q4k.device_error_flags() == 0
+
+
+def test_auto_split_above_eight(env):
+    """Few row tiles and a long K: the planner may split K over up to 16 CTAs
+    (non-portable cluster sizes); results stay within the tolerance."""
+    q4k, oracle = env
+    N, K = 3584, 18944
+    plan = q4k.gemv_plan(N, K, 1)
+    assert 1 <= plan["split_k"] <= 16
+    W = synth.q4k_weights(N, K, (96, 1))
+    for B in (1, 3, 6):
+        x = synth.normal_f32((B, K), (96, 2, B))
+        assert_close(_run(q4k, W, x), oracle.gemv(W, x, N, K), x, K, f"down-shaped B={B} split {plan['split_k']}")
+    N2 = 600
+    W2 = W[:N2]
+    x = synth.normal_f32((2, K), (96, 3))
+    assert_close(_run(q4k, W2, x), oracle.gemv(W2, x, N2, K), x, K, "5 tiles, long K")
