@@ -338,6 +338,25 @@ def run_ours(args):
     del g1u
     unfused = {"gbs": bytes1 / (ms1u * 1e-3) / 1e9, "us_per_step": ms1u * 1e3, "launches_per_step": LAYERS * 7}
 
+    # ---- the same step as one chain (one persistent launch for all 112 steps)
+    def chain_steps(B):
+        st = []
+        for layer in range(LAYERS):
+            W, y = Ws[layer], (lambda mi: y_view(B, layer, mi))
+            st += [(x_view(B, layer, "attn"), [(W[0], y(0)), (W[1], y(1)), (W[2], y(2))]),
+                   (x_view(B, layer, "o"), [(W[3], y(3))]),
+                   (x_view(B, layer, "mlp"), [(W[4], y(4)), (W[5], y(5))]),
+                   (x_view(B, layer, "down"), [(W[6], y(6))])]
+        return st
+    chain_res = {}
+    for B in (1, 5):
+        ch = q4k.Chain(chain_steps(B), B)
+        gc = capture(lambda: ch.run(stream=stream))
+        msc = time_graph(gc, max(10, args.steps // 4), args.warmup)
+        del gc
+        ch.close()
+        chain_res[f"batch{B}"] = {"gbs": step_bytes(B) / (msc * 1e-3) / 1e9, "us_per_step": msc * 1e3}
+
     # ---- VerifyBatch sweep (same weights)
     sweep = {}
     for B in (2, 5, 9):
@@ -440,6 +459,7 @@ def run_ours(args):
         "us_per_layer": ms1 * 1e3 / LAYERS,
         "tok_per_s_equiv": 1e3 / ms1,
         "unfused_one_launch_per_matrix": unfused,
+        "chain_one_launch_per_step": chain_res,
         "verify_batch": sweep,
         "lm_head_argmax": lm,
         "prefill": prefill,
@@ -468,6 +488,25 @@ def run_profile_case(spec: str, iters: int):
     import q4_dequant_gemv_gb300 as q4k
     import synth
     __graft_entry__.build()
+    if spec.startswith("chain"):
+        # chain:L:B -- L Qwen2.5-7B-shaped layers as one chain (4 steps per layer)
+        _, L, B = spec.split(":")
+        L, B = int(L), int(B)
+        layers = [[torch.from_numpy(W).cuda() for _, _, _, W in synth.qwen_layer_weights(l)] for l in range(L)]
+        shapes = synth.qwen25_7b_shapes()
+        xs = {K: torch.from_numpy(synth.normal_f32((B, K), (9, K))).cuda() for K in (3584, 18944)}
+        ys = [[torch.empty((B, N), device="cuda") for _, N, _ in shapes] for _ in range(L)]
+        steps = []
+        for W, y in zip(layers, ys):
+            steps += [(xs[3584], [(W[0], y[0]), (W[1], y[1]), (W[2], y[2])]), (xs[3584], [(W[3], y[3])]),
+                      (xs[3584], [(W[4], y[4]), (W[5], y[5])]), (xs[18944], [(W[6], y[6])])]
+        ch = q4k.Chain(steps, B)
+        for _ in range(iters):
+            ch.run()
+        torch.cuda.synchronize()
+        ch.close()
+        print(f"profile case {spec} x{iters} done")
+        return
     if spec.startswith("decode"):
         # decode:L:B -- L Qwen2.5-7B-shaped layers (7 GEMVs each), eager launches
         _, L, B = spec.split(":")
@@ -511,7 +550,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
-    ap.add_argument("--profile-case", default=None, help="gemv:N:K:B | argmax:N:K:B | prefill:N:K:T (ncu helper)")
+    ap.add_argument("--profile-case", default=None, help="gemv:N:K:B | argmax:N:K:B | prefill:N:K:T | decode:L:B | chain:L:B (ncu helper)")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:
