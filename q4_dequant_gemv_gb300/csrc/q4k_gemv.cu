@@ -133,103 +133,89 @@ __device__ __forceinline__ int chunk_scale_exp(uint32_t amax_bits)
     return max(-126, min(126, s));
 }
 
-// A chunk of x (B rows x nblk*256 floats, at most 8 float4 per thread) is
-// loaded into registers with 16-byte loads, the per-row max comes from warp
-// reductions plus one shared atomic per warp, and after a single barrier every
-// thread converts its own values: power-of-two scale, fp16 hi/lo B fragments,
-// sub-block sums (8-lane shuffles).  Float4 number i of a batch row covers
-// elements 4i..4i+3, i.e. super-block i/64, sub-block j = (i/8)%8 (pair t = j/2,
-// half h = j%2), word u = i%8 -> k-step s = 2u + h of pair t.  Called by all
-// threads; the caller must have finished reading the previous chunk's
-// fragments (its named barrier) before it is entered.
-template <int NT, typename AfterLoads, bool L2ONLY = false>
-__device__ void convert_x_chunk(const float *__restrict__ x, int K, int B, int kb0, int nblk, uint2 *xf,
-                                float *s_unscale, uint32_t *s_amax, int tid, int nthr, const AfterLoads &after_loads)
+// A chunk of x (B rows x nblk super-blocks, B * nblk <= 32) -> B fragments in
+// shared memory.  One warp converts one (batch row, super-block) item per
+// round; lane l holds float4 l and l + 32 of the super-block (elements
+// 4i..4i+3, sub-block i/8, word i%8).  All loads of all rounds are issued
+// first.  Each item gets its own power-of-two scale from a warp-level max
+// (no shared-memory max, no barrier in between), stored as s_unscale[bl*B + b];
+// then the fp16 hi/lo fragments and the sub-block sums (8-lane shuffles).
+// Float4 i is sub-block j = i/8 (pair t = j/2, half h = j%2), word u = i%8 ->
+// k-step s = 2u + h of pair t.  Ends with a barrier over all nthr threads; the
+// caller must have finished reading the previous chunk's fragments and scales.
+template <int NT, bool L2ONLY = false>
+__device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int kb0, int nblk, uint2 *xf,
+                                 float *s_unscale, int tid, int nthr)
 {
     const int LW = frag_lanes(NT, B);
     constexpr int LS = lane_stride(NT);
-    const int n4 = nblk * 64;                 // float4 per batch row in the chunk (a multiple of 64)
-    const int total = B * n4;                 // <= 8 * nthr (chunk size chosen by the host)
-    // row of float4 number e: e / n4 = (e >> 6) / nblk, by multiplication with a
-    // rounded-up 16-bit reciprocal; exact because e >> 6 < B * nblk <= 32 (the
-    // host keeps B * kc <= 32), checked for every nblk up to 4096 and quotient
-    // below 64
-    const uint32_t inv_nblk = (65536u + static_cast<uint32_t>(nblk) - 1u) / static_cast<uint32_t>(nblk);
-    auto row_of = [&](int e) { return static_cast<int>(((static_cast<uint32_t>(e) >> 6) * inv_nblk) >> 16); };
-    const float4 *xs = reinterpret_cast<const float4 *>(x + static_cast<size_t>(kb0) * 256);
-    const int K4 = K / 4;
-    float4 v[8];
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    const int items = B * nblk;   // <= 32: at most 4 rounds of 8 warps
+    float4 v[4][2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int e = j * nthr + tid;
-        if (e < total) {
-            const int b = row_of(e);
-            v[j] = L2ONLY ? __ldcg(xs + b * K4 + (e - b * n4)) : __ldg(xs + b * K4 + (e - b * n4));
+    for (int r = 0; r < 4; ++r) {
+        const int it = warp + r * nwarps;
+        if (it < items) {   // warp-uniform
+            const int b = it / nblk;
+            const float4 *src = reinterpret_cast<const float4 *>(
+                x + static_cast<size_t>(b) * K + static_cast<size_t>(kb0 + (it - b * nblk)) * 256);
+            v[r][0] = L2ONLY ? __ldcg(src + lane) : __ldg(src + lane);
+            v[r][1] = L2ONLY ? __ldcg(src + 32 + lane) : __ldg(src + 32 + lane);
         }
     }
-    after_loads();
-    // per-row max |x|: the 32 lanes of a warp hold 32 consecutive float4 of one row
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int e0 = j * nthr + (tid & ~31);
-        if (e0 < total) {
-            const int e = j * nthr + tid;
-            uint32_t m = 0u;
-            if (e < total)
-                m = max(max(__float_as_uint(fabsf(v[j].x)), __float_as_uint(fabsf(v[j].y))),
-                        max(__float_as_uint(fabsf(v[j].z)), __float_as_uint(fabsf(v[j].w))));
+    for (int r = 0; r < 4; ++r) {
+        const int it = warp + r * nwarps;
+        if (it >= items) continue;   // warp-uniform
+        const int b = it / nblk;
+        const int bl = it - b * nblk;
+        uint32_t m = 0u;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-            if ((tid & 31) == 0 && m) atomicMax(&s_amax[row_of(e0)], m);
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const float4 w = v[r][h2];
+            m = max(m, max(max(__float_as_uint(fabsf(w.x)), __float_as_uint(fabsf(w.y))),
+                           max(__float_as_uint(fabsf(w.z)), __float_as_uint(fabsf(w.w)))));
         }
-    }
-    named_bar_sync(1, nthr);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int e0 = j * nthr + (tid & ~31);
-        if (e0 >= total) continue;            // warp-uniform
-        const int e = j * nthr + tid;
-        const bool live = e < total;
-        const int b = row_of(e0);             // the whole warp is in one row
-        const int i = e - b * n4;
-        const float sc = __uint_as_float(static_cast<uint32_t>(chunk_scale_exp(s_amax[b]) + 127) << 23);
-        float4 w = live ? v[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-        w.x *= sc; w.y *= sc; w.z *= sc; w.w *= sc;
-        const int bl = i >> 6, sb = (i >> 3) & 7, u = i & 7;
-        const int t = sb >> 1, h = sb & 1, s = 2 * u + h;
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const int e = chunk_scale_exp(m);
+        const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+        if (lane == 0) s_unscale[bl * B + b] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
         const int chi = 2 * b, clo = 2 * b + 1;
-        if (live) {
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int i = lane + 32 * h2;
+            float4 w = v[r][h2];
+            w.x *= sc; w.y *= sc; w.z *= sc; w.w *= sc;
+            const int sb = i >> 3, u = i & 7;
+            const int t = sb >> 1, s = 2 * u + (sb & 1);
             const uint32_t h01 = pack_half2(w.x, w.z);
             const uint32_t h23 = pack_half2(w.y, w.w);
             const uint32_t l01 = pack_half2(w.x - half_lo_f32(h01), w.z - half_hi_f32(h01));
             const uint32_t l23 = pack_half2(w.y - half_lo_f32(h23), w.w - half_hi_f32(h23));
             xf[(bl * LW + 4 * (chi % 8) + t) * LS + s * NT + chi / 8] = make_uint2(h01, h23);
             xf[(bl * LW + 4 * (clo % 8) + t) * LS + s * NT + clo / 8] = make_uint2(l01, l23);
-        }
-        // sub-block sum over the 8 lanes holding it, then pair it with the
-        // odd sub-block held by the next 8 lanes
-        float sum = (w.x + w.y) + (w.z + w.w);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        const float sum_odd = __shfl_down_sync(0xffffffffu, sum, 8);
-        if (live && u == 0 && h == 0) {
-            const uint32_t hs = pack_half2(sum, sum_odd);
-            const uint32_t ls = pack_half2(sum - half_lo_f32(hs), sum_odd - half_hi_f32(hs));
-            xf[(bl * LW + 4 * (chi % 8) + t) * LS + 16 * NT + chi / 8] = make_uint2(hs, 0u);
-            xf[(bl * LW + 4 * (clo % 8) + t) * LS + 16 * NT + clo / 8] = make_uint2(ls, 0u);
+            // sub-block sum over the 8 lanes holding it, then pair it with the
+            // odd sub-block held by the next 8 lanes
+            float sum = (w.x + w.y) + (w.z + w.w);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            const float sum_odd = __shfl_down_sync(0xffffffffu, sum, 8);
+            if ((i & 15) == 0) {
+                const uint32_t hs = pack_half2(sum, sum_odd);
+                const uint32_t ls = pack_half2(sum - half_lo_f32(hs), sum_odd - half_hi_f32(hs));
+                xf[(bl * LW + 4 * (chi % 8) + t) * LS + 16 * NT + chi / 8] = make_uint2(hs, 0u);
+                xf[(bl * LW + 4 * (clo % 8) + t) * LS + 16 * NT + clo / 8] = make_uint2(ls, 0u);
+            }
         }
     }
-    for (int b = tid; b < B; b += nthr)
-        s_unscale[b] = __uint_as_float(static_cast<uint32_t>(127 - chunk_scale_exp(s_amax[b])) << 23);
     named_bar_sync(1, nthr);
-    // every thread has read s_amax: clear it for the next chunk
-    for (int b = tid; b < B; b += nthr) s_amax[b] = 0u;
 }
 
 // Warm L2 with x[b][kb0*256, kb1*256) for every batch row (one 128-byte line
-// per thread and round).  Safe before the dependency wait: L2 is where the
-// previous kernel's writes land, so the loads after the wait still see them.
+// per thread and round).  Safe before a dependency wait: L2 is where the
+// earlier writes land, so the loads after the wait still see them.
 __device__ __forceinline__ void prefetch_x_l2(const float *x, int K, int B, int kb0, int kb1, int tid, int nthr)
 {
     const int lines = (kb1 - kb0) * 8;   // 1 KB of floats per super-block
@@ -421,8 +407,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     uint2 *xf = reinterpret_cast<uint2 *>(smem_raw + xfrag_offset());
     float *s_red = reinterpret_cast<float *>(smem_raw + red_offset(NT, B, args.kc));
     __shared__ __align__(8) uint64_t full[kStages];
-    __shared__ float s_unscale[16];
-    __shared__ uint32_t s_amax[16];
+    __shared__ float s_unscale[32];   // per (super-block of the chunk, batch row)
     __shared__ unsigned long long s_best[16];
     __shared__ int s_abort;
     __shared__ int s_issued;                 // stages issued so far (for the abort drain)
@@ -460,7 +445,6 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
         s_issued = first;
     }
     if (ARGMAX && tid < 16) s_best[tid] = 0ull;
-    if (tid < 16) s_amax[tid] = 0u;
     if (tid < kWarps) s_cons[tid] = 0;
     __syncthreads();
     iss.policy = l2_policy_evict_first();
@@ -475,8 +459,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     const int t = lane & 3;
     const int nchunks = (ks + args.kc - 1) / args.kc;
     const bool single_chunk = (nchunks == 1);
-    auto nothing = []() {};
-    if (single_chunk) convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_unscale, s_amax, tid, kThreads, nothing);
+    if (single_chunk) convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_unscale, tid, kThreads);
     // B-fragment lane.  Lanes whose column holds no batch row read some other
     // valid entry: MMA columns are independent, and those output columns are
     // never used.
@@ -494,23 +477,19 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
         for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
         float unscale[NT];
         int chunk_end = -1;
-        bool reload_scale = true;
         for (int kbl = 0; kbl < ks; ++kbl) {
             if (!single_chunk && kbl > chunk_end) {
                 const int cn = min(args.kc, ks - kbl);
                 named_bar_sync(1, kThreads);     // everyone done with the previous chunk
-                convert_x_chunk<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, s_amax, tid, kThreads,
-                                    nothing);
+                convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, tid, kThreads);
                 chunk_end = kbl + cn - 1;
-                reload_scale = true;
             }
-            if (reload_scale) {
+            // this super-block's x scale per batch row
+            const int blk = single_chunk ? kbl : (kbl % args.kc);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int b = t + 4 * nt;
-                    unscale[nt] = (b < B) ? s_unscale[b] : 0.f;
-                }
-                reload_scale = false;
+            for (int nt = 0; nt < NT; ++nt) {
+                const int b = t + 4 * nt;
+                unscale[nt] = (b < B) ? s_unscale[blk * B + b] : 0.f;
             }
             const int slot = consumed % kStages;
             const uint32_t phase = static_cast<uint32_t>((consumed / kStages) & 1);
@@ -764,8 +743,7 @@ __device__ __forceinline__ void chain_body(const ChainArgs &args)
     ChainStepS *s_steps = reinterpret_cast<ChainStepS *>(smem_raw + xfrag_offset() + chain_xf_bytes(NT, B, args.kc_max));
     int *s_start = reinterpret_cast<int *>(s_steps + args.nsteps);   // [nsteps + 1]
     __shared__ __align__(8) uint64_t full[kStages];
-    __shared__ float s_unscale[16];
-    __shared__ uint32_t s_amax[16];
+    __shared__ float s_unscale[32];   // per (super-block of the chunk, batch row)
     __shared__ int s_abort;
     __shared__ int s_issued;
     __shared__ int s_last;
@@ -812,7 +790,6 @@ __device__ __forceinline__ void chain_body(const ChainArgs &args)
         s_abort = 0;
         fence_barrier_init();
     }
-    if (tid < 16) s_amax[tid] = 0u;
     if (tid < kWarps) s_cons[tid] = 0;
     __syncthreads();
     if (tid == 0) {
@@ -838,7 +815,6 @@ __device__ __forceinline__ void chain_body(const ChainArgs &args)
     const int blane = (g < 2 * B) ? lane : (lane % LW);
     const int row_off = (warp * 16 + g) * kBlockBytes;
     int consumed = 0;
-    auto nothing = []() {};
 
     for (int si = 0; si < nsteps; ++si) {
         const ChainStepS &st = s_steps[si];
@@ -862,32 +838,26 @@ __device__ __forceinline__ void chain_body(const ChainArgs &args)
         if (mine > 0 && !*(volatile int *)&s_abort) {
             const int kc = st.kc;
             const bool single_chunk = ks <= kc;
-            if (single_chunk)
-                convert_x_chunk<NT, decltype(nothing), true>(st.x, st.nb * 256, B, kb_begin, ks, xf, s_unscale,
-                                                              s_amax, tid, kThreads, nothing);
+            if (single_chunk) convert_x_blocks<NT, true>(st.x, st.nb * 256, B, kb_begin, ks, xf, s_unscale, tid, kThreads);
             for (int ul = 0; ul < mine; ++ul) {
                 float acc[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
                 float unscale[NT];
                 int chunk_end = -1;
-                bool reload_scale = true;
                 for (int kbl = 0; kbl < ks; ++kbl) {
                     if (!single_chunk && kbl > chunk_end) {
                         const int cn = min(kc, ks - kbl);
                         named_bar_sync(1, kThreads);   // everyone done with the previous chunk
-                        convert_x_chunk<NT, decltype(nothing), true>(st.x, st.nb * 256, B, kb_begin + kbl, cn, xf,
-                                                                      s_unscale, s_amax, tid, kThreads, nothing);
+                        convert_x_blocks<NT, true>(st.x, st.nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, tid,
+                                                   kThreads);
                         chunk_end = kbl + cn - 1;
-                        reload_scale = true;
                     }
-                    if (reload_scale) {
+                    const int blk = single_chunk ? kbl : (kbl % kc);
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const int b = t + 4 * nt;
-                            unscale[nt] = (b < B) ? s_unscale[b] : 0.f;
-                        }
-                        reload_scale = false;
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int b = t + 4 * nt;
+                        unscale[nt] = (b < B) ? s_unscale[blk * B + b] : 0.f;
                     }
                     const int slot = consumed % kStages;
                     const uint32_t phase = static_cast<uint32_t>((consumed / kStages) & 1);
