@@ -93,7 +93,14 @@ __host__ __device__ inline int frag_lanes(int NT, int B) { return NT == 1 ? 8 * 
 // one super-block are contiguous, so a consumer lane reads them at constant
 // offsets from one base.  The per-lane stride is odd in 8-byte units for even
 // NT so that the 16 lanes of a wavefront hit distinct bank pairs.
-__host__ __device__ constexpr int lane_stride(int NT) { return kKsteps * NT + ((NT & 1) ? 0 : 1); }
+__host__ __device__ constexpr int lane_stride(int NT)
+{
+    // even (16-byte aligned lanes: a k-step's even and odd fragments load as one
+    // 16-byte access; lane L starts at bank 4L mod 32 for NT = 1, 2, 4, so the
+    // eight lanes of a 16-byte wavefront hit distinct banks); NT = 3 loads
+    // 8-byte fragments and keeps an odd stride
+    return NT == 3 ? kKsteps * NT : kKsteps * NT + ((kKsteps * NT) & 1);
+}
 
 __host__ __device__ inline size_t xfrag_bytes_per_block(int NT, int B)
 {
@@ -295,8 +302,20 @@ __device__ __forceinline__ void stage_compute(const uint8_t *ra, const uint8_t *
             const uint32_t p1 = hfma2_u32(and_or(c8, mhi, magic), r1.mulO, r1.addO);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const uint2 be = xl[2 * u * NT + nt];
-                const uint2 bo = xl[(2 * u + 1) * NT + nt];
+                uint2 be, bo;
+                if constexpr (NT == 1) {   // even and odd fragment of k-step pair u: one 16-byte load
+                    const uint4 q = *reinterpret_cast<const uint4 *>(&xl[2 * u]);
+                    be = make_uint2(q.x, q.y);
+                    bo = make_uint2(q.z, q.w);
+                } else if constexpr ((NT & 1) == 0) {   // two n-tiles per 16-byte load
+                    const uint4 qe = *reinterpret_cast<const uint4 *>(&xl[2 * u * NT + (nt & ~1)]);
+                    const uint4 qo = *reinterpret_cast<const uint4 *>(&xl[(2 * u + 1) * NT + (nt & ~1)]);
+                    be = (nt & 1) ? make_uint2(qe.z, qe.w) : make_uint2(qe.x, qe.y);
+                    bo = (nt & 1) ? make_uint2(qo.z, qo.w) : make_uint2(qo.x, qo.y);
+                } else {
+                    be = xl[2 * u * NT + nt];
+                    bo = xl[(2 * u + 1) * NT + nt];
+                }
                 if (u < NC) {   // first k-step of each accumulator chain
                     mma_16816_z(cE[uu % NC][nt], e0, f0, e1, f1, be.x, be.y);
                     mma_16816_z(cO[uu % NC][nt], o0, p0, o1, p1, bo.x, bo.y);
@@ -504,7 +523,8 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             // this lane's B fragments of this super-block (lane-major layout)
             const uint2 *xl = xf + static_cast<size_t>((single_chunk ? kbl : (kbl % args.kc)) * LW + blane) *
                                        lane_stride(NT);
-            stage_compute<NT, 2>(ra, rb, xl, t, unscale, acc, [&]() {
+            // two accumulator chains per parity at batch <= 4 (shorter chains), one above (fewer registers)
+            stage_compute<NT, NT == 1 ? 2 : 1>(ra, rb, xl, t, unscale, acc, [&]() {
                 // This warp is done with the slot: the last warp to finish refills it.
                 __syncwarp();
                 if (lane == 0) {
