@@ -51,6 +51,7 @@ constexpr int kThreads = 192;        // 4 dequant/epilogue warps + TMA warp + MM
 constexpr int kATileBytes = kRowsM * kChunk * 2;    // 16 KB: one bf16 weight tile
 constexpr int kAStageBytes = 2 * kATileBytes;       // hi + lo tiles
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kPrefetch = 3;        // chunks of weight loads in flight per dequant thread
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
@@ -205,15 +206,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t *wrow = W + static_cast<size_t>(live ? n : 0) * row_bytes;
         int stage = 0;
         uint32_t phase = 0;
-        for (int c = c_begin; c < c_end; ++c) {
-            const int blk = c >> 2, p = c & 3;
-            uint4 hdr = make_uint4(0, 0, 0, 0), qa = hdr, qb = hdr;
-            if (live) {
-                const uint8_t *bp = wrow + static_cast<size_t>(blk) * 144;
-                hdr = __ldg(reinterpret_cast<const uint4 *>(bp));
-                qa = __ldg(reinterpret_cast<const uint4 *>(bp + 16 + 32 * p));
-                qb = __ldg(reinterpret_cast<const uint4 *>(bp + 32 + 32 * p));
+        // The row's global loads run kPrefetch chunks ahead of the dequant, so
+        // the memory latency overlaps the work on the chunks in between.
+        uint4 nh[kPrefetch], na[kPrefetch], nb[kPrefetch];
+        auto load_chunk = [&](int c, uint4 &h, uint4 &a, uint4 &b) {
+            h = a = b = make_uint4(0, 0, 0, 0);
+            if (live && c < c_end) {
+                const uint8_t *bp = wrow + static_cast<size_t>(c >> 2) * 144;
+                const int p = c & 3;
+                h = __ldg(reinterpret_cast<const uint4 *>(bp));
+                a = __ldg(reinterpret_cast<const uint4 *>(bp + 16 + 32 * p));
+                b = __ldg(reinterpret_cast<const uint4 *>(bp + 32 + 32 * p));
             }
+        };
+#pragma unroll
+        for (int i = 0; i < kPrefetch; ++i) load_chunk(c_begin + i, nh[i], na[i], nb[i]);
+        for (int c = c_begin; c < c_end; ++c) {
+            const int p = c & 3;
+            const uint4 hdr = nh[0], qa = na[0], qb = nb[0];
+#pragma unroll
+            for (int i = 0; i + 1 < kPrefetch; ++i) { nh[i] = nh[i + 1]; na[i] = na[i + 1]; nb[i] = nb[i + 1]; }
+            load_chunk(c + kPrefetch, nh[kPrefetch - 1], na[kPrefetch - 1], nb[kPrefetch - 1]);
             if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
                 atomicOr(&g_prefill_error, 2u);
                 s_abort = 1;
@@ -482,7 +495,11 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     else if (t <= 64) { tn = 64; ntt = 1; }
     else if (t <= 128) { tn = 128; ntt = 1; }
     else if (t <= 256) { tn = 256; ntt = 1; }
-    else if (static_cast<long long>(mtiles) * ((t + 511) / 512) >= sms) { tn = 256; ntt = 2; }
+    // 512-token tiles dequantize each weight tile half as often; they pay
+    // once they fill at least 70 % of the SMs (14336 rows: 112 tiles on 152
+    // SMs take about three quarters of the time of two waves of 256-token
+    // tiles)
+    else if (static_cast<long long>(mtiles) * ((t + 511) / 512) * 10 >= static_cast<long long>(sms) * 7) { tn = 256; ntt = 2; }
     else { tn = 256; ntt = 1; }
     const long long ctas = static_cast<long long>(mtiles) * ((t + tn * ntt - 1) / (tn * ntt));
     // K split over a cluster until the GPU is covered (at most 8, at least

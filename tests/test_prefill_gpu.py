@@ -63,7 +63,9 @@ def test_single_bf16_rounding_would_not_do(env):
 @pytest.mark.parametrize("N,K,T", [(128, 256, 32), (128, 512, 32), (256, 1024, 32), (200, 768, 33),
                                    (130, 512, 1), (64, 256, 7), (384, 1024, 64), (256, 512, 128),
                                    (128, 1024, 256), (256, 512, 300), (128, 768, 512), (100, 256, 600),
-                                   (128, 4096, 32), (256, 4096, 512), (1000, 2048, 40), (128, 8192, 300)])
+                                   (128, 4096, 32), (256, 4096, 512), (1000, 2048, 40), (128, 8192, 300),
+                                   # enough row tiles for 512-token tiles; ragged last token tile
+                                   (13696, 256, 520), (14336, 512, 1030)])
 def test_prefill_shapes(env, N, K, T):
     q4k, oracle = env
     _check(q4k, oracle, N, K, T, N * 7 + K + T, f"N={N} K={K} T={T}")
