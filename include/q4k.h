@@ -90,7 +90,15 @@ int q4k_abi_version(void);
  *   N >= 0 (N == 0 is a no-op and W, y may then be NULL), K a positive multiple
  *   of 256, K/256 < 2^24, 1 <= batch <= 16.
  * Accumulation is fp32.  Each weight super-block is read from memory once for
- * all batch rows.  x may hold any finite fp32 values.
+ * all batch rows.  x may hold any finite fp32 values.  Inside, each
+ * super-block of x is carried in one of two forms:
+ *   - batch 1: two int8 parts, x ~= (a/32258)(254 xh + xl) with a = max|x| of
+ *     the super-block (error <= a (1/64516 + 2^-16)); the weight nibbles are
+ *     multiplied with them by integer dot products (dp4a), exact in int32,
+ *     and the scales applied per super-block in fp32;
+ *   - batch >= 2 (and batch 1 with Q4K_FLAG_TENSOR_CORE): two fp16 parts after
+ *     a power-of-two scale (error <= 2^-22 |x|), multiplied with the weights as
+ *     exact fp16 integers on the tensor cores (mma.sync), fp32 accumulation.
  * Errors: INVALID_ARG (null pointer, N < 0, K <= 0 or K % 256 != 0, batch out
  * of range), MISALIGNED (W or x), UNSUPPORTED_DEVICE, CUDA.
  */
@@ -166,9 +174,14 @@ q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t
  *            kernel may start streaming W while the previous kernel on the
  *            stream is still running.  W must then not be written by that
  *            previous kernel (weights are constant during decode); x is still
- *            read only after the previous kernel has completed.
+ *            read only after the previous kernel has completed.  Batch-1
+ *            launches whose K split exceeds 8 CTAs ignore it (their clusters,
+ *            placed beside the previous kernel's CTAs, ran slower).
+ *            Q4K_FLAG_TENSOR_CORE: batch 1 uses the tensor-core inner product
+ *            of the larger batches instead of the integer one.
  */
 #define Q4K_FLAG_PDL 1u
+#define Q4K_FLAG_TENSOR_CORE 2u
 typedef struct {
     int split_k;
     unsigned flags;

@@ -10,6 +10,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// c + sum over the four bytes of a (unsigned) times the four bytes of b
+// (signed), in one instruction.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int r;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
 // (a & b) | c in one LOP3.
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c)
 {

@@ -220,6 +220,92 @@ __device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int 
     named_bar_sync(1, nthr);
 }
 
+// ---------------------------------------------------------------------------
+// Batch 1, integer inner product: x of one super-block as two int8 parts per
+// element,  x ~= (dx / 254) * (254 * xh + xl)  with dx = max|x| / 127,
+// q = x * (127 / max|x|), xh = rint(q) and xl = rint((q - xh) * 254), all in
+// fp32 (x and max|x| first scaled by 2^64 when max|x| < 2^-64), so that
+// |x - (dx / 254)(254 xh + xl)| <= dx (1/508 + 2^-16).  Per local
+// super-block bl, at byte offset bl * blk_bytes of the fragment area:
+//   [0, 256)    xh in k order       [256, 512)  xl in k order
+//   [512, 544)  int32 per sub-block j: 254 * sum(xh) + sum(xl) over its 32 k
+// and s_unscale[bl] * s_pre[bl] = dx / 254, with s_unscale[bl] kept in the
+// normal range (s_pre = 2^-64 for the scaled blocks, else 1); s_unscale is 0
+// for an all-zero super-block and the non-finite max itself when x holds an
+// inf or NaN, so that the result is not finite.
+// One warp per super-block; lane l holds float4 l and l + 32 (k = 4l..4l+3 and
+// 128 + 4l..).  Ends with a barrier over all nthr threads.
+// ---------------------------------------------------------------------------
+constexpr int kI8Bytes = 544;
+static_assert(kI8Bytes <= lane_stride(1) * 8 * 8, "batch-1 fragment area holds the int8 parts");
+
+template <bool L2ONLY = false>
+__device__ void convert_x_i8_blocks(const float *__restrict__ x, int kb0, int nblk, uint8_t *xb, int blk_bytes,
+                                    float *s_unscale, float *s_pre, int tid, int nthr)
+{
+    const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    float4 v[4][2];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int it = warp + r * nwarps;
+        if (it < nblk) {   // warp-uniform
+            const float4 *src = reinterpret_cast<const float4 *>(x + static_cast<size_t>(kb0 + it) * 256);
+            v[r][0] = L2ONLY ? __ldcg(src + lane) : __ldg(src + lane);
+            v[r][1] = L2ONLY ? __ldcg(src + 32 + lane) : __ldg(src + 32 + lane);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int it = warp + r * nwarps;
+        if (it >= nblk) continue;   // warp-uniform
+        uint32_t m = 0u;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const float4 w = v[r][h2];
+            m = max(m, max(max(__float_as_uint(fabsf(w.x)), __float_as_uint(fabsf(w.y))),
+                           max(__float_as_uint(fabsf(w.z)), __float_as_uint(fabsf(w.w)))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float amax = __uint_as_float(m);
+        const bool ok = m != 0u && m < 0x7F800000u;   // finite and not all zero
+        // below 2^-64 the reciprocal is taken of the max scaled by 2^64 (exact)
+        // and x is scaled alike, so that it stays finite
+        const float pre = (m < 0x1F800000u) ? 0x1p64f : 1.0f;
+        const float inv = ok ? 127.0f / (amax * pre) : 0.0f;
+        uint8_t *base = xb + static_cast<size_t>(it) * blk_bytes;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const float4 w = v[r][h2];
+            const float e[4] = {w.x, w.y, w.z, w.w};
+            uint32_t hw = 0u, lw = 0u;
+            int sum = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float q = (e[j] * pre) * inv;
+                const float hq = rintf(q);
+                const float lq = rintf((q - hq) * 254.0f);
+                const int hi = static_cast<int>(hq), lo = static_cast<int>(lq);
+                hw |= (static_cast<uint32_t>(hi) & 0xFFu) << (8 * j);
+                lw |= (static_cast<uint32_t>(lo) & 0xFFu) << (8 * j);
+                sum += 254 * hi + lo;
+            }
+            const int i = lane + 32 * h2;   // float4 index: k = 4i..4i+3, sub-block i/8
+            *reinterpret_cast<uint32_t *>(base + 4 * i) = hw;
+            *reinterpret_cast<uint32_t *>(base + 256 + 4 * i) = lw;
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            if ((i & 7) == 0) reinterpret_cast<int *>(base + 512)[i >> 3] = sum;
+        }
+        if (lane == 0) {
+            s_unscale[it] = ok ? (amax * pre) / 127.0f / 254.0f : (m == 0u ? 0.0f : amax);
+            s_pre[it] = 1.0f / pre;
+        }
+    }
+    named_bar_sync(1, nthr);
+}
+
 // Warm L2 with x[b][kb0*256, kb1*256) for every batch row (one 128-byte line
 // per thread and round).  Safe before a dependency wait: L2 is where the
 // earlier writes land, so the loads after the wait still see them.
@@ -266,6 +352,95 @@ __device__ __forceinline__ RowConsts decode_header(uint4 h, int t)
     rc.mulO = hmul2_u32(hi2, 0x2C002C00u);        // * 1/16
     rc.addO = hmul2_u32(hi2, 0xD400D400u);        // * -64
     return rc;
+}
+
+// Integer scale/min constants of one row for thread t (sub-blocks 2t, 2t+1).
+struct RowConstsI {
+    int scE, scO, mE, mO;
+    float d, dmin;
+};
+__device__ __forceinline__ RowConstsI decode_header_i(uint4 h, int t)
+{
+    RowConstsI rc;
+    rc.d = half_lo_f32(h.x);
+    rc.dmin = half_hi_f32(h.x);
+    const uint32_t sh = (t & 1) ? 16u : 0u;
+    const uint32_t a0 = (h.y >> sh) & 0xFFFFu;   // s[2(t&1)], s[2(t&1)+1]
+    const uint32_t a1 = (h.z >> sh) & 0xFFFFu;   // s[4+...]
+    const uint32_t a2 = (h.w >> sh) & 0xFFFFu;   // s[8+...]
+    uint32_t scp, mp;
+    if (t < 2) {
+        scp = a0 & 0x3F3Fu;
+        mp = a1 & 0x3F3Fu;
+    } else {
+        scp = (a2 & 0x0F0Fu) | ((a0 >> 2) & 0x3030u);
+        mp = ((a2 >> 4) & 0x0F0Fu) | ((a1 >> 2) & 0x3030u);
+    }
+    rc.scE = static_cast<int>(scp & 0xFFu);
+    rc.scO = static_cast<int>(scp >> 8);
+    rc.mE = static_cast<int>(mp & 0xFFu);
+    rc.mO = static_cast<int>(mp >> 8);
+    return rc;
+}
+
+// Batch 1, integer inner product of one super-block for thread (g, t): rows g
+// (ra) and g + 8 (rb), sub-block pair t.  Byte i of the pair's 32 quant bytes
+// holds q of weight i of sub-block 2t (low nibble) and of 2t+1 (high nibble);
+// dp4a multiplies four of them with four int8 parts of x at a time.  Low
+// nibbles go in as q, high nibbles in place as 16 q (one exact shift per sum
+// afterwards).  Per row the sums are exact in int32:
+//   T = 254 (scE SEh + scO SOh) + (scE SEl + scO SOl)    (|T| < 1.96e9)
+//   M = mE BS_2t + mO BS_2t+1                            (|M| < 1.4e8)
+// and y += ((d T - dmin M) u) pre with u pre = dx / 254 for this super-block
+// (every intermediate in the normal range, whatever the size of x).
+template <typename Release>
+__device__ __forceinline__ void stage_compute_i8(const uint8_t *ra, const uint8_t *rb, const uint8_t *xb, int t,
+                                                 float u, float pre, float (&acc)[1][2], Release &&release)
+{
+    const RowConstsI r0 = decode_header_i(*reinterpret_cast<const uint4 *>(ra), t);
+    const RowConstsI r1 = decode_header_i(*reinterpret_cast<const uint4 *>(rb), t);
+    int eh0 = 0, el0 = 0, oh0 = 0, ol0 = 0, eh1 = 0, el1 = 0, oh1 = 0, ol1 = 0;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const uint4 qa = *reinterpret_cast<const uint4 *>(ra + 16 + 32 * t + 16 * half);
+        const uint4 qb = *reinterpret_cast<const uint4 *>(rb + 16 + 32 * t + 16 * half);
+        // x parts of k = 64t + 16 half + 0..15 (sub-block 2t) and + 32 (2t+1)
+        const uint4 xhE = *reinterpret_cast<const uint4 *>(xb + 64 * t + 16 * half);
+        const uint4 xhO = *reinterpret_cast<const uint4 *>(xb + 64 * t + 32 + 16 * half);
+        const uint4 xlE = *reinterpret_cast<const uint4 *>(xb + 256 + 64 * t + 16 * half);
+        const uint4 xlO = *reinterpret_cast<const uint4 *>(xb + 256 + 64 * t + 32 + 16 * half);
+        const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
+        const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
+        const uint32_t he[4] = {xhE.x, xhE.y, xhE.z, xhE.w};
+        const uint32_t ho[4] = {xhO.x, xhO.y, xhO.z, xhO.w};
+        const uint32_t le[4] = {xlE.x, xlE.y, xlE.z, xlE.w};
+        const uint32_t lo[4] = {xlO.x, xlO.y, xlO.z, xlO.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t aE = wa[j] & 0x0F0F0F0Fu, aO = wa[j] & 0xF0F0F0F0u;
+            const uint32_t bE = wb[j] & 0x0F0F0F0Fu, bO = wb[j] & 0xF0F0F0F0u;
+            eh0 = dp4a_us(aE, he[j], eh0);
+            el0 = dp4a_us(aE, le[j], el0);
+            oh0 = dp4a_us(aO, ho[j], oh0);
+            ol0 = dp4a_us(aO, lo[j], ol0);
+            eh1 = dp4a_us(bE, he[j], eh1);
+            el1 = dp4a_us(bE, le[j], el1);
+            oh1 = dp4a_us(bO, ho[j], oh1);
+            ol1 = dp4a_us(bO, lo[j], ol1);
+        }
+    }
+    release();
+    const int2 bs = *reinterpret_cast<const int2 *>(xb + 512 + 8 * t);
+    // the high-nibble sums are multiples of 16: exact shifts
+    oh0 >>= 4; ol0 >>= 4; oh1 >>= 4; ol1 >>= 4;
+    const int T0 = 254 * (r0.scE * eh0 + r0.scO * oh0) + (r0.scE * el0 + r0.scO * ol0);
+    const int T1 = 254 * (r1.scE * eh1 + r1.scO * oh1) + (r1.scE * el1 + r1.scO * ol1);
+    const int M0 = r0.mE * bs.x + r0.mO * bs.y;
+    const int M1 = r1.mE * bs.x + r1.mO * bs.y;
+    const float v0 = fmaf(r0.d, static_cast<float>(T0), -r0.dmin * static_cast<float>(M0));
+    const float v1 = fmaf(r1.d, static_cast<float>(T1), -r1.dmin * static_cast<float>(M1));
+    acc[0][0] = fmaf(v0 * u, pre, acc[0][0]);
+    acc[0][1] = fmaf(v1 * u, pre, acc[0][1]);
 }
 
 // One super-block of this warp's 16 rows (rows g and g + 8 for thread (g, t)):
@@ -416,7 +591,7 @@ struct StageIssuer {
     }
 };
 
-template <int NT, bool ARGMAX>
+template <int NT, bool ARGMAX, bool I8>
 __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &args)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -427,6 +602,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     float *s_red = reinterpret_cast<float *>(smem_raw + red_offset(NT, B, args.kc));
     __shared__ __align__(8) uint64_t full[kStages];
     __shared__ float s_unscale[32];   // per (super-block of the chunk, batch row)
+    __shared__ float s_pre[32];       // integer path: power-of-two factor per super-block
     __shared__ unsigned long long s_best[16];
     __shared__ int s_abort;
     __shared__ int s_issued;                 // stages issued so far (for the abort drain)
@@ -478,7 +654,16 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     const int t = lane & 3;
     const int nchunks = (ks + args.kc - 1) / args.kc;
     const bool single_chunk = (nchunks == 1);
-    if (single_chunk) convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_unscale, tid, kThreads);
+    // batch 1 on the integer path: int8 x parts, one block of the fragment area per super-block
+    static_assert(!I8 || NT == 1, "the integer path is batch 1 only");
+    uint8_t *xb = reinterpret_cast<uint8_t *>(xf);
+    const int blk_bytes = static_cast<int>(xfrag_bytes_per_block(1, 1));
+    if (single_chunk) {
+        if constexpr (I8)
+            convert_x_i8_blocks(args.x, kb_begin, ks, xb, blk_bytes, s_unscale, s_pre, tid, kThreads);
+        else
+            convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_unscale, tid, kThreads);
+    }
     // B-fragment lane.  Lanes whose column holds no batch row read some other
     // valid entry: MMA columns are independent, and those output columns are
     // never used.
@@ -500,7 +685,10 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             if (!single_chunk && kbl > chunk_end) {
                 const int cn = min(args.kc, ks - kbl);
                 named_bar_sync(1, kThreads);     // everyone done with the previous chunk
-                convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, tid, kThreads);
+                if constexpr (I8)
+                    convert_x_i8_blocks(args.x, kb_begin + kbl, cn, xb, blk_bytes, s_unscale, s_pre, tid, kThreads);
+                else
+                    convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, tid, kThreads);
                 chunk_end = kbl + cn - 1;
             }
             // this super-block's x scale per batch row
@@ -508,7 +696,8 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int b = t + 4 * nt;
-                unscale[nt] = (b < B) ? s_unscale[blk * B + b] : 0.f;
+                // integer path: all four pair lanes of a row work on batch row 0
+                unscale[nt] = I8 ? s_unscale[blk] : ((b < B) ? s_unscale[blk * B + b] : 0.f);
             }
             const int slot = consumed % kStages;
             const uint32_t phase = static_cast<uint32_t>((consumed / kStages) & 1);
@@ -524,7 +713,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             const uint2 *xl = xf + static_cast<size_t>((single_chunk ? kbl : (kbl % args.kc)) * LW + blane) *
                                        lane_stride(NT);
             // two accumulator chains per parity at batch <= 4 (shorter chains), one above (fewer registers)
-            stage_compute<NT, NT == 1 ? 2 : 1>(ra, rb, xl, t, unscale, acc, [&]() {
+            auto release = [&]() {
                 // This warp is done with the slot: the last warp to finish refills it.
                 __syncwarp();
                 if (lane == 0) {
@@ -540,9 +729,20 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
                     }
                 }
                 ++consumed;
-            });
+            };
+            if constexpr (I8)
+                stage_compute_i8(ra, rb, xb + blk * blk_bytes, t, unscale[0], s_pre[blk], acc, release);
+            else
+                stage_compute<NT, NT == 1 ? 2 : 1>(ra, rb, xl, t, unscale, acc, release);
         }
         // ---------------- tile epilogue
+        if constexpr (I8) {   // sum the four sub-block-pair lanes of each row
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                acc[0][h] += __shfl_xor_sync(0xffffffffu, acc[0][h], 1);
+                acc[0][h] += __shfl_xor_sync(0xffffffffu, acc[0][h], 2);
+            }
+        }
         if (split == 1 && !*(volatile int *)&s_abort) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
@@ -639,10 +839,10 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
 
 // Batch <= 8 (one or two n8 tiles): at most 128 registers, so that two CTAs of
 // 8 warps (4 warps per SM sub-partition) fit in the register file.
-template <int NT, bool ARGMAX>
+template <int NT, bool ARGMAX, bool I8 = false>
 __global__ void __maxnreg__(128) q4k_gemv_kernel(const __grid_constant__ WMaps maps, const GemvArgs args)
 {
-    gemv_body<NT, ARGMAX>(maps, args);
+    gemv_body<NT, ARGMAX, I8>(maps, args);
 }
 
 // Batch 9..16 (three or four n8 tiles): one CTA per SM, registers as needed.
@@ -650,7 +850,7 @@ template <int NT, bool ARGMAX>
 __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel_wide(const __grid_constant__ WMaps maps,
                                                                    const GemvArgs args)
 {
-    gemv_body<NT, ARGMAX>(maps, args);
+    gemv_body<NT, ARGMAX, false>(maps, args);
 }
 
 // ---------------------------------------------------------------------------
@@ -1026,6 +1226,7 @@ q4k_status check_device(int *sms_out)
 
 struct GemvPlan {
     int NT;
+    bool i8;        // batch 1 on the integer (dp4a) inner product
     int split;
     int grid_x;
     int tiles;
@@ -1078,6 +1279,7 @@ static GemvPlan make_plan(int tiles, int64_t K, int B, int sms, int forced_split
     GemvPlan p{};
     const int nb = static_cast<int>(K / 256);
     p.NT = batch_ntiles(B);
+    p.i8 = (B == 1);
     p.tiles = tiles;
     int best_s = 1;
     if (forced_split > 0) {
@@ -1152,13 +1354,13 @@ static bool encode_w_map(CUtensorMap *map, const void *W, int64_t N, int64_t K)
     return r == CUDA_SUCCESS;
 }
 
-template <int NT, bool ARGMAX>
+template <int NT, bool ARGMAX, bool I8 = false>
 static cudaError_t launch_one(const GemvPlan &p, const WMaps &maps, const GemvArgs &a, cudaStream_t stream,
                               bool pdl)
 {
     void (*kern)(const WMaps, const GemvArgs);
     if constexpr (NT <= 2)
-        kern = q4k_gemv_kernel<NT, ARGMAX>;
+        kern = q4k_gemv_kernel<NT, ARGMAX, I8>;
     else
         kern = q4k_gemv_kernel_wide<NT, ARGMAX>;
     static std::mutex mu;
@@ -1197,7 +1399,11 @@ static cudaError_t launch_one(const GemvPlan &p, const WMaps &maps, const GemvAr
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
-    if (pdl) {
+    // Batch-1 launches with clusters above 8 CTAs go without PDL: placed early
+    // beside the previous kernel's CTAs, not all of their clusters found room
+    // at once (measured: the down projection after gate/up, 15.9 us with PDL,
+    // 13.8 us without; the tensor-core kernels gain from PDL there).
+    if (pdl && !(I8 && p.split > 8)) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
@@ -1218,7 +1424,7 @@ static cudaError_t launch_gemv(const GemvPlan &p, const void *const *Ws, int64_t
     for (int g = 0; g < a.ngroups; ++g)
         if (!encode_w_map(&maps.m[g], Ws[g], a.N[g], K)) return cudaErrorInvalidValue;
     switch (p.NT) {
-        case 1: return launch_one<1, ARGMAX>(p, maps, a, s, pdl);
+        case 1: return p.i8 ? launch_one<1, ARGMAX, true>(p, maps, a, s, pdl) : launch_one<1, ARGMAX>(p, maps, a, s, pdl);
         case 2: return launch_one<2, ARGMAX>(p, maps, a, s, pdl);
         case 3: return launch_one<3, ARGMAX>(p, maps, a, s, pdl);
         default: return launch_one<4, ARGMAX>(p, maps, a, s, pdl);
@@ -1264,6 +1470,7 @@ q4k_status gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t
     a.tiles = p.tiles;
     a.kc = p.kc;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
+    if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.i8 = false;
     cudaError_t e = launch_gemv<false>(p, &W, K, a, static_cast<cudaStream_t>(stream), pdl);
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
@@ -1305,6 +1512,7 @@ q4k_status gemv_grouped_impl(const q4k_gemv_group *groups, int ngroups, const fl
     a.tiles = p.tiles;
     a.kc = p.kc;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
+    if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.i8 = false;
     cudaError_t e = launch_gemv<false>(p, Ws, K, a, static_cast<cudaStream_t>(stream), pdl);
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
@@ -1335,6 +1543,7 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
     a.kc = p.kc;
     a.idx = idx;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
+    if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.i8 = false;
     void *buf = nullptr;
     const size_t bytes = 8 * 16 + 16;
     if (scratch_keys == nullptr) {

@@ -106,14 +106,61 @@ def test_batch_rows_independent(env):
         assert_close(y5[b:b + 1], ref[b:b + 1], x[b:b + 1], K, f"b={b}")
 
 
-@pytest.mark.parametrize("scale", [1e-30, 1e-6, 1e6, 1e30])
-def test_extreme_activation_scales(env, scale):
-    """Any finite fp32 x works (power-of-two rescaling before the fp16 split)."""
+@pytest.mark.parametrize("B", [1, 2])
+@pytest.mark.parametrize("scale", [1e-37, 1e-30, 1e-6, 1e6, 1e30])
+def test_extreme_activation_scales(env, scale, B):
+    """Any finite fp32 x works: batch 2 rescales by a power of two before the
+    fp16 split, batch 1 quantizes against each super-block's own max|x|."""
     q4k, oracle = env
     N, K = 96, 1024
     W = synth.q4k_weights(N, K, 25)
-    x = (synth.normal_f32((2, K), 26) * np.float32(scale)).astype(np.float32)
-    assert_close(_run(q4k, W, x), oracle.gemv(W, x, N, K), x, K, f"scale {scale}")
+    x = (synth.normal_f32((B, K), 26) * np.float32(scale)).astype(np.float32)
+    assert_close(_run(q4k, W, x), oracle.gemv(W, x, N, K), x, K, f"scale {scale} B={B}")
+
+
+def _int8_parts(x):
+    """The batch-1 integer path's representation of x, retaken in numpy fp32:
+    per super-block a = max|x| (with x and a scaled by p = 2^64 below 2^-64, else
+    p = 1), q = (p x) * (127 / (p a)), xh = rint(q), xl = rint((q - xh) * 254);
+    returns x~ = ((p a) / 127 / 254)(254 xh + xl) / p in fp64."""
+    K = x.size
+    blocks = x.reshape(K // 256, 256).astype(np.float32)
+    out = np.zeros((K // 256, 256), np.float64)
+    for i, v in enumerate(blocks):
+        a = np.float32(np.max(np.abs(v)))
+        if a == 0:
+            continue
+        pre = np.float32(2.0 ** 64) if a < np.float32(2.0 ** -64) else np.float32(1)
+        inv = np.float32(127) / np.float32(a * pre)
+        q = (v * pre).astype(np.float32) * inv
+        xh = np.rint(q)
+        xl = np.rint((q - xh).astype(np.float32) * np.float32(254))
+        u = np.float32(np.float32(np.float32(a * pre) / np.float32(127)) / np.float32(254))
+        out[i] = np.float64(u) / np.float64(pre) * (254.0 * xh.astype(np.float64) + xl.astype(np.float64))
+    return out.reshape(K)
+
+
+@pytest.mark.parametrize("N,K,seed", [(300, 3584, 41), (129, 18944, 42), (640, 4096, 43)])
+def test_batch1_integer_path_is_exact(env, N, K, seed):
+    """Batch 1 runs integer dot products on int8 parts of x.  Given the same
+    parts (retaken in numpy), the kernel's result must equal the fp64 product
+    of the dequantized weights with them up to fp32 rounding of the
+    per-super-block combine: |dy| <= 1e-5 sum_k |w||x~| (an integer overflow or a
+    misplaced part would be off by far more)."""
+    q4k, oracle = env
+    W = synth.q4k_weights(N, K, (seed, 1))
+    x = synth.normal_f32((1, K), (seed, 2))
+    x[0, 5] = 40.0          # one super-block with a large max, so most parts are small
+    x[0, 512:768] = 0.0     # an all-zero super-block
+    xt = _int8_parts(x[0])
+    D = oracle.dequant_matrix(W, N, K)
+    ref = D @ xt
+    bound = 1e-5 * (np.abs(D) @ np.abs(xt)) + 1e-30
+    y = _run(q4k, W, x)[0]
+    assert np.all(np.abs(y - ref) <= bound), f"max excess {np.max(np.abs(y - ref) - bound)}"
+    # and the tensor-core path on the same input stays within the stated tolerance
+    yt = _run(q4k, W, x, tensor_core=True)
+    assert_close(yt[None, :] if yt.ndim == 1 else yt, oracle.gemv(W, x, N, K), x, K, "tensor-core batch 1")
 
 
 def test_mixed_magnitudes_within_row(env):
