@@ -78,6 +78,8 @@ def _load():
         lib.oracle_argmax_f32.argtypes = [P, I64]
         lib.oracle_argmax_f32.restype = I64
         lib.oracle_prefill.argtypes = [P, P, P, I64, I64, I64, I, I]
+        lib.oracle_q8k_quantize.argtypes = [P, I64, P, P]
+        lib.oracle_gemv_q8k.argtypes = [P, P, P, P, I64, I64, I]
         lib.oracle_max_threads.restype = I
         _lib = lib
         return lib
@@ -194,3 +196,24 @@ def prefill(W: np.ndarray, X_bf16_bits: np.ndarray, N: int, K: int, round_w: boo
     Y = np.zeros((T, N), np.float64)
     _load().oracle_prefill(_ptr(W), _ptr(X), _ptr(Y), N, K, T, 1 if round_w else 0, threads)
     return Y
+
+
+def q8k_quantize(x: np.ndarray, K: int):
+    """Q8_K activation quantization of one row x fp32 [K]: int8 codes q [K] and
+    float32 block scales d [K/256] (rule: oracle_q8k_quantize in q4k_oracle.c)."""
+    x1 = _c(x, np.float32).reshape(K)
+    q = np.zeros(K, np.int8)
+    d = np.zeros(K // QK, np.float32)
+    _load().oracle_q8k_quantize(_ptr(x1), K, _ptr(q), _ptr(d))
+    return q, d
+
+
+def gemv_q8k(W: np.ndarray, q: np.ndarray, d: np.ndarray, N: int, K: int, threads: int = 0) -> np.ndarray:
+    """fp64 y [N] = W_deq . (d_block * q): the Q4_K x Q8_K product, batch 1."""
+    W = _c(W, np.uint8)
+    q = _c(q, np.int8)
+    d = _c(d, np.float32)
+    assert W.size == N * (K // QK) * QBYTES and q.size == K and d.size == K // QK
+    y = np.zeros(N, np.float64)
+    _load().oracle_gemv_q8k(_ptr(W), _ptr(q), _ptr(d), _ptr(y), N, K, threads)
+    return y

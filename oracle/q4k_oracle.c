@@ -20,6 +20,10 @@
  *   - the prefill product with bf16 activations ("cuBLAS HGEMM for prefill",
  *     dotLLM README, News 2026-03 "CUDA GPU backend"): same fp64 sum with the
  *     bf16 activations decoded exactly.
+ *   - Q8_K activation quantization and the Q4_K x Q8_K product (dotLLM README,
+ *     News 2026-03 "Mixed quantization + Q8_K"): the int8 codes and block
+ *     scales by the rule written at oracle_q8k_quantize, then the same fp64
+ *     sum over the dequantized activations.
  *
  * The Q4_K super-block (the pages name the format -- Q4_K / Q4_K_M -- but never
  * print its bytes; the reading used here is the GGUF packing):
@@ -226,6 +230,57 @@ void oracle_gemv_rows(const uint8_t *W, const float *x, double *y, int64_t N, in
                 for (int64_t k = 0; k < K; ++k) acc += buf[k] * (double)xb[k];
                 y[(int64_t)b * R + r] = acc;
             }
+        }
+        free(buf);
+    }
+}
+
+/*
+ * Q8_K-style activation quantization.  The dotLLM README (News 2026-03, "Mixed
+ * quantization + Q8_K") describes x quantized in 256-element blocks with a
+ * float32 scale, int8 codes and precomputed block sums, feeding a fused
+ * Q4_K x Q8_K GEMV.  It fixes the block size, the float32 scale and the int8
+ * codes but no rounding rule; this oracle takes the plainest one, in fp32:
+ *   a = max |x| over the block,  d = a / 127,
+ *   q = rint(x * (127 / a))   (round half to even; |q| <= 127),
+ * an all-zero block giving d = 0, q = 0.  When a < 2^-64 the same fp32 values
+ * are formed as (x * 2^64) * (127 / (a * 2^64)), so that the reciprocal stays
+ * finite for every finite x (scaling by 2^64 is exact).  Finite x only.
+ */
+void oracle_q8k_quantize(const float *x, int64_t K, int8_t *q, float *d)
+{
+    for (int64_t b = 0; b < K / QK; ++b) {
+        const float *xb = x + b * QK;
+        float a = 0.0f;
+        for (int i = 0; i < QK; ++i) {
+            const float v = fabsf(xb[i]);
+            if (v > a) a = v;
+        }
+        d[b] = a / 127.0f;
+        const float pre = (a < 0x1p-64f) ? 0x1p64f : 1.0f;
+        const float inv = (a > 0.0f) ? 127.0f / (a * pre) : 0.0f;
+        for (int i = 0; i < QK; ++i) {
+            const float t = (xb[i] * pre) * inv;
+            q[b * QK + i] = (int8_t)rintf(t);
+        }
+    }
+}
+
+/* y[n] = sum_k w[n][k] * (d_{k/256} * q[k]) in fp64, k order: the product of
+ * the dequantized weights with the dequantized Q8_K activations (batch 1). */
+void oracle_gemv_q8k(const uint8_t *W, const int8_t *q, const float *d, double *y, int64_t N, int64_t K,
+                     int threads)
+{
+    set_threads(threads);
+#pragma omp parallel
+    {
+        double *buf = (double *)malloc((size_t)K * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t n = 0; n < N; ++n) {
+            dequant_row(W, n, K, buf);
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) acc += buf[k] * ((double)d[k / QK] * (double)q[k]);
+            y[n] = acc;
         }
         free(buf);
     }

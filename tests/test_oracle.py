@@ -389,3 +389,134 @@ def test_pins_catch_planted_mistakes(oracle_mod, tmp_path):
         lib.oracle_dequant_block(good.ctypes.data_as(ctypes.c_void_p), w.ctypes.data_as(ctypes.c_void_p))
         caught[name] = not np.array_equal(w, exp)
     assert all(caught.values()), caught
+
+
+# ---------------------------------------------------------------- Q8_K activations
+def _q8k_golden():
+    blocks, cur = [], None
+    for line in open(os.path.join(GOLDEN, "q8k_blocks.txt")):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        key, rest = line.split(None, 1)
+        if key == "name":
+            cur = {"name": rest}
+            blocks.append(cur)
+        elif key in ("x", "q"):
+            cur[key] = [float(v) for v in rest.split()]
+        elif key == "d":
+            cur["d"] = rest
+    return blocks
+
+
+@pytest.mark.parametrize("blk", _q8k_golden(), ids=lambda b: b["name"])
+def test_q8k_golden_blocks(oracle_mod, blk):
+    """Hand-derived codes and scales (tests/golden/q8k_blocks.txt)."""
+    x = np.zeros(256, np.float32)
+    x[:len(blk["x"])] = blk["x"]
+    q, d = oracle_mod.q8k_quantize(x, 256)
+    assert list(q[:len(blk["q"])]) == [int(v) for v in blk["q"]]
+    assert np.all(q[len(blk["q"]):] == 0)
+    if "/" in blk["d"]:
+        num, den = blk["d"].split("/")
+        want = np.float32(num) / np.float32(den)   # IEEE single division (numpy)
+    else:
+        want = np.float32(blk["d"])
+    assert d[0] == want
+
+
+def test_q8k_invariants(oracle_mod):
+    """|q| <= 127, the largest |x| maps to +-127 with its sign, every code is
+    within half a step of x/d, and the signs agree."""
+    g = np.random.default_rng(11)
+    K = 256 * 8
+    x = (g.standard_normal(K) * np.repeat(10.0 ** g.uniform(-20, 20, K // 256), 256)).astype(np.float32)
+    q, d = oracle_mod.q8k_quantize(x, K)
+    assert np.all(np.abs(q.astype(int)) <= 127)
+    for b in range(K // 256):
+        xb, qb = x[256 * b:256 * (b + 1)].astype(np.float64), q[256 * b:256 * (b + 1)].astype(np.float64)
+        i = int(np.argmax(np.abs(xb)))
+        assert qb[i] == 127 * np.sign(xb[i])
+        assert np.all(np.abs(xb / np.float64(d[b]) - qb) <= 0.5 + 1e-5)
+        assert np.all(qb * xb >= 0)
+
+
+@pytest.mark.parametrize("e", [-90, -70, -3, 5, 60])
+def test_q8k_power_of_two_scaling(oracle_mod, e):
+    """Scaling a block by 2^e leaves every code unchanged and scales d by 2^e
+    exactly -- including blocks whose max drops below 2^-64."""
+    g = np.random.default_rng(12)
+    x = g.standard_normal(512).astype(np.float32)
+    q0, d0 = oracle_mod.q8k_quantize(x, 512)
+    xs = (x.astype(np.float64) * 2.0 ** e).astype(np.float32)
+    assert np.array_equal(xs.astype(np.float64), x.astype(np.float64) * 2.0 ** e)   # exact scaling
+    q1, d1 = oracle_mod.q8k_quantize(xs, 512)
+    assert np.array_equal(q0, q1)
+    assert np.array_equal(d1.astype(np.float64), d0.astype(np.float64) * 2.0 ** e)
+
+
+def test_q8k_product_brute_force(oracle_mod):
+    """The Q4_K x Q8_K product equals the library matmul of the dequantized
+    weights with the dequantized codes, and stays within the quantization
+    bound sum_k |w| d/2 of the exact product with x."""
+    N, K = 6, 768
+    W = synth.q4k_weights(N, K, 13)
+    x = synth.normal_f32((1, K), 14)[0]
+    q, d = oracle_mod.q8k_quantize(x, K)
+    xt = np.repeat(d.astype(np.float64), 256) * q.astype(np.float64)
+    D = oracle_mod.dequant_matrix(W, N, K)
+    y = oracle_mod.gemv_q8k(W, q, d, N, K)
+    np.testing.assert_allclose(y, D @ xt, rtol=1e-12, atol=1e-12)
+    exact = oracle_mod.gemv(W, x, N, K)[0]
+    bound = np.abs(D) @ (np.repeat(d.astype(np.float64), 256) / 2) * (1 + 1e-6)
+    assert np.all(np.abs(y - exact) <= bound)
+    assert np.any(y != exact)
+
+
+def test_q8k_pins_catch_planted_mistakes(oracle_mod, tmp_path):
+    """Plausible mistakes planted into a copy of the quantizer are caught by
+    the golden blocks or the scaling pin."""
+    import ctypes
+    import subprocess
+    src = open(os.path.join(os.path.dirname(oracle_mod.__file__), "q4k_oracle.c")).read()
+    mutants = {
+        "half away from zero": ("q[b * QK + i] = (int8_t)rintf(t);", "q[b * QK + i] = (int8_t)roundf(t);"),
+        "128 levels": ("127.0f / (a * pre)", "128.0f / (a * pre)"),
+        "scale 1/128": ("d[b] = a / 127.0f;", "d[b] = a / 128.0f;"),
+        "signed max": ("const float v = fabsf(xb[i]);", "const float v = xb[i];"),
+        "unscaled x": ("const float t = (xb[i] * pre) * inv;", "const float t = xb[i] * inv;"),
+    }
+    blocks = _q8k_golden()
+    g = np.random.default_rng(15)
+    xs = g.standard_normal(256).astype(np.float32)
+    caught = {}
+    for name, (a, b) in mutants.items():
+        assert a in src, name
+        path = tmp_path / f"q8_{abs(hash(name))}.c"
+        path.write_text(src.replace(a, b))
+        so = str(path) + ".so"
+        subprocess.run(["gcc", "-O1", "-fPIC", "-shared", str(path), "-o", so, "-lm"], check=True)
+        lib = ctypes.CDLL(so)
+        lib.oracle_q8k_quantize.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+
+        def quant(x):
+            q = np.zeros(256, np.int8)
+            d = np.zeros(1, np.float32)
+            x = np.ascontiguousarray(x, np.float32)
+            lib.oracle_q8k_quantize(x.ctypes.data_as(ctypes.c_void_p), 256, q.ctypes.data_as(ctypes.c_void_p),
+                                    d.ctypes.data_as(ctypes.c_void_p))
+            return q, d
+
+        bad = False
+        for blk in blocks:
+            x = np.zeros(256, np.float32)
+            x[:len(blk["x"])] = blk["x"]
+            q, d = quant(x)
+            bad |= list(q[:len(blk["q"])]) != [int(v) for v in blk["q"]]
+            if "/" not in blk["d"]:
+                bad |= d[0] != np.float32(blk["d"])
+        q0, _ = quant(xs)
+        q1, _ = quant((xs.astype(np.float64) * 2.0 ** -90).astype(np.float32))
+        bad |= not np.array_equal(q0, q1)
+        caught[name] = bad
+    assert all(caught.values()), caught
