@@ -287,19 +287,20 @@ def run_ours(args):
     def step_bytes(B):
         return LAYERS * sum(N * (K // 256) * 144 + 4 * B * K + 4 * B * N for _, N, K in shapes)
 
-    def decode_step(B, pdl=True, fused=True, tc=False):
+    def decode_step(B, pdl=True, fused=True, tc=False, q8=False):
         """One decode step: 28 layers x 7 GEMVs.  fused: q/k/v share one launch
         and gate/up share one (4 launches per layer); otherwise 7 launches.
-        tc: batch 1 on the tensor-core inner product instead of the integer one."""
+        tc: batch 1 on the tensor-core inner product instead of the integer one.
+        q8: batch 1 with x quantized Q8_K style (its own error bound)."""
         for layer in range(LAYERS):
             W, y = Ws[layer], (lambda mi: y_view(B, layer, mi))
             if fused:
                 q4k.gemv_grouped(W[0:3], x_view(B, layer, "attn"), [y(0), y(1), y(2)], stream=stream, pdl=pdl,
-                                 tensor_core=tc)
-                q4k.gemv(W[3], x_view(B, layer, "o"), y(3), stream=stream, pdl=pdl, tensor_core=tc)
+                                 tensor_core=tc, q8k=q8)
+                q4k.gemv(W[3], x_view(B, layer, "o"), y(3), stream=stream, pdl=pdl, tensor_core=tc, q8k=q8)
                 q4k.gemv_grouped(W[4:6], x_view(B, layer, "mlp"), [y(4), y(5)], stream=stream, pdl=pdl,
-                                 tensor_core=tc)
-                q4k.gemv(W[6], x_view(B, layer, "down"), y(6), stream=stream, pdl=pdl, tensor_core=tc)
+                                 tensor_core=tc, q8k=q8)
+                q4k.gemv(W[6], x_view(B, layer, "down"), y(6), stream=stream, pdl=pdl, tensor_core=tc, q8k=q8)
             else:
                 for mi, (name, N, K) in enumerate(shapes):
                     q4k.gemv(W[mi], x_view(B, layer, src[name]), y(mi), stream=stream, pdl=pdl, tensor_core=tc)
@@ -354,7 +355,15 @@ def run_ours(args):
     ms1t = time_graph(g1t, max(20, args.steps // 4), args.warmup)
     del g1t
     tensor_core_b1 = {"gbs": bytes1 / (ms1t * 1e-3) / 1e9, "us_per_step": ms1t * 1e3,
-                      "kernel": "q4k_gemv_kernel<1,false,false> (mma.sync m16n8k16, x as fp16 hi+lo)"}
+                      "kernel": "q4k_gemv_kernel<1,false,0> (mma.sync m16n8k16, x as fp16 hi+lo)"}
+
+    # ---- the same step with x quantized Q8_K style (one int8 code per element; own error bound)
+    g1q = capture(lambda: decode_step(1, q8=True))
+    ms1q = time_graph(g1q, max(20, args.steps // 4), args.warmup)
+    del g1q
+    q8k_b1 = {"gbs": bytes1 / (ms1q * 1e-3) / 1e9, "us_per_step": ms1q * 1e3,
+              "kernel": "q4k_gemv_kernel<1,false,2> (dp4a, x as Q8_K int8 codes per 256-block)",
+              "numerics": "W times the Q8_K-quantized x: differs from W x by <= sum|w| d/2 per row"}
 
     # ---- the same step as one chain (one persistent launch for all 112 steps)
     def chain_steps(B):
@@ -475,7 +484,7 @@ def run_ours(args):
     traffic = None
     if tr is not None:
         traffic = tr["dram_bytes_per_weight_byte"] * bytes1 / launches_per_step
-    roof = {"kernel": "q4k_gemv_kernel<1,false,true> (batch 1, integer dp4a inner product)", "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+    roof = {"kernel": "q4k_gemv_kernel<1,false,1> (batch 1, integer dp4a inner product)", "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
             "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
             "algorithmic_bytes_per_launch": bytes1 / launches_per_step,
             "avg_launch_us": ms1 * 1e3 / launches_per_step,
@@ -529,6 +538,7 @@ def run_ours(args):
         "tok_per_s_equiv": 1e3 / ms1,
         "unfused_one_launch_per_matrix": unfused,
         "batch1_tensor_core_path": tensor_core_b1,
+        "batch1_q8k_activations": q8k_b1,
         "chain_one_launch_per_step": chain_res,
         "verify_batch": sweep,
         "lm_head_argmax": lm,

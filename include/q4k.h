@@ -179,9 +179,19 @@ q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t
  *            placed beside the previous kernel's CTAs, ran slower).
  *            Q4K_FLAG_TENSOR_CORE: batch 1 uses the tensor-core inner product
  *            of the larger batches instead of the integer one.
+ *            Q4K_FLAG_Q8K_X: batch 1 with x quantized Q8_K style (dotLLM README,
+ *            News 2026-03 "Mixed quantization + Q8_K": 256-element blocks, a
+ *            float32 scale, int8 codes, precomputed block sums): per block
+ *            a = max|x|, d = a/127, q = rint(x * (127/a)) in fp32 (round half
+ *            to even); the result is the product of W with d*q (exact integer
+ *            dot products, fp32 per block), so it differs from W x by at most
+ *            sum_k |w_k| d/2 per row -- its own tolerance, not the one stated
+ *            for q4k_gemv.  Returns Q4K_ERR_INVALID_ARG with batch > 1 or
+ *            together with Q4K_FLAG_TENSOR_CORE.
  */
 #define Q4K_FLAG_PDL 1u
 #define Q4K_FLAG_TENSOR_CORE 2u
+#define Q4K_FLAG_Q8K_X 4u
 typedef struct {
     int split_k;
     unsigned flags;

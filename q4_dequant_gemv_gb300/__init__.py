@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(HERE, "libq4k.so")
 Q4K_OK = 0
 Q4K_FLAG_PDL = 1
 Q4K_FLAG_TENSOR_CORE = 2
+Q4K_FLAG_Q8K_X = 4
 QK = 256
 QBYTES = 144
 MAX_BATCH = 16
@@ -126,13 +127,16 @@ def _shape_wk(W, K):
     return N
 
 
-def _flags(pdl: bool, tensor_core: bool) -> int:
-    return (Q4K_FLAG_PDL if pdl else 0) | (Q4K_FLAG_TENSOR_CORE if tensor_core else 0)
+def _flags(pdl: bool, tensor_core: bool, q8k: bool = False) -> int:
+    return ((Q4K_FLAG_PDL if pdl else 0) | (Q4K_FLAG_TENSOR_CORE if tensor_core else 0)
+            | (Q4K_FLAG_Q8K_X if q8k else 0))
 
 
-def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False, tensor_core: bool = False):
+def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False, tensor_core: bool = False,
+         q8k: bool = False):
     """y [B, N] (fp32) = W_q4k [N, K] . x [B, K] (fp32); x may also be [K].
-    tensor_core: batch 1 on the tensor-core inner product instead of the integer one."""
+    tensor_core: batch 1 on the tensor-core inner product instead of the integer one.
+    q8k: batch 1 with x quantized Q8_K style (int8 codes per 256-block), its own error bound."""
     import torch
     _dev(W, "W", torch.uint8)
     _dev(x, "x", torch.float32)
@@ -146,8 +150,8 @@ def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False, tens
     if y.numel() != B * N:
         raise ValueError("y has the wrong size")
     L = lib()
-    if split_k or pdl or tensor_core:
-        o = LaunchOpts(split_k, _flags(pdl, tensor_core))
+    if split_k or pdl or tensor_core or q8k:
+        o = LaunchOpts(split_k, _flags(pdl, tensor_core, q8k))
         st = L.q4k_gemv_ex(W.data_ptr(), x2.data_ptr(), y.data_ptr(), N, K, B, _stream_ptr(stream), ctypes.byref(o))
         _check("q4k_gemv_ex", st)
     else:
@@ -156,7 +160,8 @@ def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False, tens
     return y.view(N) if squeeze and y.dim() == 2 else y
 
 
-def gemv_grouped(Ws, x, ys=None, *, stream=None, split_k: int = 0, pdl: bool = False, tensor_core: bool = False):
+def gemv_grouped(Ws, x, ys=None, *, stream=None, split_k: int = 0, pdl: bool = False, tensor_core: bool = False,
+                 q8k: bool = False):
     """Several Q4_K matrices times the same x in one launch: returns [y_g [B, N_g]]."""
     import torch
     if not 1 <= len(Ws) <= 4:
@@ -174,7 +179,7 @@ def gemv_grouped(Ws, x, ys=None, *, stream=None, split_k: int = 0, pdl: bool = F
         if y.numel() != B * N:
             raise ValueError("y has the wrong size")
         arr[i] = GemvGroup(W.data_ptr(), y.data_ptr(), N)
-    o = LaunchOpts(split_k, _flags(pdl, tensor_core))
+    o = LaunchOpts(split_k, _flags(pdl, tensor_core, q8k))
     st = lib().q4k_gemv_grouped(arr, len(Ws), x2.data_ptr(), K, B, _stream_ptr(stream), ctypes.byref(o))
     _check("q4k_gemv_grouped", st)
     return ys

@@ -239,7 +239,7 @@ __device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int 
 constexpr int kI8Bytes = 544;
 static_assert(kI8Bytes <= lane_stride(1) * 8 * 8, "batch-1 fragment area holds the int8 parts");
 
-template <bool L2ONLY = false>
+template <bool Q8, bool L2ONLY = false>
 __device__ void convert_x_i8_blocks(const float *__restrict__ x, int kb0, int nblk, uint8_t *xb, int blk_bytes,
                                     float *s_unscale, float *s_pre, int tid, int nthr)
 {
@@ -284,22 +284,27 @@ __device__ void convert_x_i8_blocks(const float *__restrict__ x, int kb0, int nb
             for (int j = 0; j < 4; ++j) {
                 const float q = (e[j] * pre) * inv;
                 const float hq = rintf(q);
-                const float lq = rintf((q - hq) * 254.0f);
-                const int hi = static_cast<int>(hq), lo = static_cast<int>(lq);
+                const int hi = static_cast<int>(hq);
                 hw |= (static_cast<uint32_t>(hi) & 0xFFu) << (8 * j);
-                lw |= (static_cast<uint32_t>(lo) & 0xFFu) << (8 * j);
-                sum += 254 * hi + lo;
+                if constexpr (Q8) {
+                    sum += hi;
+                } else {
+                    const int lo = static_cast<int>(rintf((q - hq) * 254.0f));
+                    lw |= (static_cast<uint32_t>(lo) & 0xFFu) << (8 * j);
+                    sum += 254 * hi + lo;
+                }
             }
             const int i = lane + 32 * h2;   // float4 index: k = 4i..4i+3, sub-block i/8
             *reinterpret_cast<uint32_t *>(base + 4 * i) = hw;
-            *reinterpret_cast<uint32_t *>(base + 256 + 4 * i) = lw;
+            if constexpr (!Q8) *reinterpret_cast<uint32_t *>(base + 256 + 4 * i) = lw;
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             sum += __shfl_xor_sync(0xffffffffu, sum, 4);
             if ((i & 7) == 0) reinterpret_cast<int *>(base + 512)[i >> 3] = sum;
         }
         if (lane == 0) {
-            s_unscale[it] = ok ? (amax * pre) / 127.0f / 254.0f : (m == 0u ? 0.0f : amax);
+            s_unscale[it] = ok ? (Q8 ? (amax * pre) / 127.0f : (amax * pre) / 127.0f / 254.0f)
+                               : (m == 0u ? 0.0f : amax);
             s_pre[it] = 1.0f / pre;
         }
     }
@@ -393,7 +398,7 @@ __device__ __forceinline__ RowConstsI decode_header_i(uint4 h, int t)
 //   M = mE BS_2t + mO BS_2t+1                            (|M| < 1.4e8)
 // and y += ((d T - dmin M) u) pre with u pre = dx / 254 for this super-block
 // (every intermediate in the normal range, whatever the size of x).
-template <typename Release>
+template <bool Q8, typename Release>
 __device__ __forceinline__ void stage_compute_i8(const uint8_t *ra, const uint8_t *rb, const uint8_t *xb, int t,
                                                  float u, float pre, float (&acc)[1][2], Release &&release)
 {
@@ -407,8 +412,9 @@ __device__ __forceinline__ void stage_compute_i8(const uint8_t *ra, const uint8_
         // x parts of k = 64t + 16 half + 0..15 (sub-block 2t) and + 32 (2t+1)
         const uint4 xhE = *reinterpret_cast<const uint4 *>(xb + 64 * t + 16 * half);
         const uint4 xhO = *reinterpret_cast<const uint4 *>(xb + 64 * t + 32 + 16 * half);
-        const uint4 xlE = *reinterpret_cast<const uint4 *>(xb + 256 + 64 * t + 16 * half);
-        const uint4 xlO = *reinterpret_cast<const uint4 *>(xb + 256 + 64 * t + 32 + 16 * half);
+        const uint4 xlE = Q8 ? make_uint4(0, 0, 0, 0) : *reinterpret_cast<const uint4 *>(xb + 256 + 64 * t + 16 * half);
+        const uint4 xlO = Q8 ? make_uint4(0, 0, 0, 0)
+                             : *reinterpret_cast<const uint4 *>(xb + 256 + 64 * t + 32 + 16 * half);
         const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
         const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
         const uint32_t he[4] = {xhE.x, xhE.y, xhE.z, xhE.w};
@@ -420,21 +426,23 @@ __device__ __forceinline__ void stage_compute_i8(const uint8_t *ra, const uint8_
             const uint32_t aE = wa[j] & 0x0F0F0F0Fu, aO = wa[j] & 0xF0F0F0F0u;
             const uint32_t bE = wb[j] & 0x0F0F0F0Fu, bO = wb[j] & 0xF0F0F0F0u;
             eh0 = dp4a_us(aE, he[j], eh0);
-            el0 = dp4a_us(aE, le[j], el0);
             oh0 = dp4a_us(aO, ho[j], oh0);
-            ol0 = dp4a_us(aO, lo[j], ol0);
             eh1 = dp4a_us(bE, he[j], eh1);
-            el1 = dp4a_us(bE, le[j], el1);
             oh1 = dp4a_us(bO, ho[j], oh1);
-            ol1 = dp4a_us(bO, lo[j], ol1);
+            if constexpr (!Q8) {
+                el0 = dp4a_us(aE, le[j], el0);
+                ol0 = dp4a_us(aO, lo[j], ol0);
+                el1 = dp4a_us(bE, le[j], el1);
+                ol1 = dp4a_us(bO, lo[j], ol1);
+            }
         }
     }
     release();
     const int2 bs = *reinterpret_cast<const int2 *>(xb + 512 + 8 * t);
     // the high-nibble sums are multiples of 16: exact shifts
     oh0 >>= 4; ol0 >>= 4; oh1 >>= 4; ol1 >>= 4;
-    const int T0 = 254 * (r0.scE * eh0 + r0.scO * oh0) + (r0.scE * el0 + r0.scO * ol0);
-    const int T1 = 254 * (r1.scE * eh1 + r1.scO * oh1) + (r1.scE * el1 + r1.scO * ol1);
+    const int T0 = Q8 ? r0.scE * eh0 + r0.scO * oh0 : 254 * (r0.scE * eh0 + r0.scO * oh0) + (r0.scE * el0 + r0.scO * ol0);
+    const int T1 = Q8 ? r1.scE * eh1 + r1.scO * oh1 : 254 * (r1.scE * eh1 + r1.scO * oh1) + (r1.scE * el1 + r1.scO * ol1);
     const int M0 = r0.mE * bs.x + r0.mO * bs.y;
     const int M1 = r1.mE * bs.x + r1.mO * bs.y;
     const float v0 = fmaf(r0.d, static_cast<float>(T0), -r0.dmin * static_cast<float>(M0));
@@ -591,9 +599,14 @@ struct StageIssuer {
     }
 };
 
-template <int NT, bool ARGMAX, bool I8>
+// XM: how x enters the inner product.  0: fp16 hi/lo parts on the tensor cores
+// (any batch); 1: two int8 parts per element and dp4a (batch 1); 2: one int8
+// code per element, Q8_K style, and dp4a (batch 1, on request).
+template <int NT, bool ARGMAX, int XM>
 __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &args)
 {
+    constexpr bool I8 = XM != 0;
+    constexpr bool Q8 = XM == 2;
     extern __shared__ __align__(128) uint8_t smem_raw[];
     uint8_t *ring = smem_raw;
     const int B = args.B;
@@ -660,7 +673,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     const int blk_bytes = static_cast<int>(xfrag_bytes_per_block(1, 1));
     if (single_chunk) {
         if constexpr (I8)
-            convert_x_i8_blocks(args.x, kb_begin, ks, xb, blk_bytes, s_unscale, s_pre, tid, kThreads);
+            convert_x_i8_blocks<Q8>(args.x, kb_begin, ks, xb, blk_bytes, s_unscale, s_pre, tid, kThreads);
         else
             convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_unscale, tid, kThreads);
     }
@@ -686,7 +699,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
                 const int cn = min(args.kc, ks - kbl);
                 named_bar_sync(1, kThreads);     // everyone done with the previous chunk
                 if constexpr (I8)
-                    convert_x_i8_blocks(args.x, kb_begin + kbl, cn, xb, blk_bytes, s_unscale, s_pre, tid, kThreads);
+                    convert_x_i8_blocks<Q8>(args.x, kb_begin + kbl, cn, xb, blk_bytes, s_unscale, s_pre, tid, kThreads);
                 else
                     convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, tid, kThreads);
                 chunk_end = kbl + cn - 1;
@@ -731,7 +744,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
                 ++consumed;
             };
             if constexpr (I8)
-                stage_compute_i8(ra, rb, xb + blk * blk_bytes, t, unscale[0], s_pre[blk], acc, release);
+                stage_compute_i8<Q8>(ra, rb, xb + blk * blk_bytes, t, unscale[0], s_pre[blk], acc, release);
             else
                 stage_compute<NT, NT == 1 ? 2 : 1>(ra, rb, xl, t, unscale, acc, release);
         }
@@ -839,10 +852,10 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
 
 // Batch <= 8 (one or two n8 tiles): at most 128 registers, so that two CTAs of
 // 8 warps (4 warps per SM sub-partition) fit in the register file.
-template <int NT, bool ARGMAX, bool I8 = false>
+template <int NT, bool ARGMAX, int XM = 0>
 __global__ void __maxnreg__(128) q4k_gemv_kernel(const __grid_constant__ WMaps maps, const GemvArgs args)
 {
-    gemv_body<NT, ARGMAX, I8>(maps, args);
+    gemv_body<NT, ARGMAX, XM>(maps, args);
 }
 
 // Batch 9..16 (three or four n8 tiles): one CTA per SM, registers as needed.
@@ -850,7 +863,7 @@ template <int NT, bool ARGMAX>
 __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel_wide(const __grid_constant__ WMaps maps,
                                                                    const GemvArgs args)
 {
-    gemv_body<NT, ARGMAX, false>(maps, args);
+    gemv_body<NT, ARGMAX, 0>(maps, args);
 }
 
 // ---------------------------------------------------------------------------
@@ -1226,7 +1239,7 @@ q4k_status check_device(int *sms_out)
 
 struct GemvPlan {
     int NT;
-    bool i8;        // batch 1 on the integer (dp4a) inner product
+    int xm;         // x mode of the batch-1 kernel: 0 tensor cores, 1 two int8 parts, 2 Q8_K codes
     int split;
     int grid_x;
     int tiles;
@@ -1279,7 +1292,7 @@ static GemvPlan make_plan(int tiles, int64_t K, int B, int sms, int forced_split
     GemvPlan p{};
     const int nb = static_cast<int>(K / 256);
     p.NT = batch_ntiles(B);
-    p.i8 = (B == 1);
+    p.xm = (B == 1) ? 1 : 0;
     p.tiles = tiles;
     int best_s = 1;
     if (forced_split > 0) {
@@ -1354,13 +1367,13 @@ static bool encode_w_map(CUtensorMap *map, const void *W, int64_t N, int64_t K)
     return r == CUDA_SUCCESS;
 }
 
-template <int NT, bool ARGMAX, bool I8 = false>
+template <int NT, bool ARGMAX, int XM = 0>
 static cudaError_t launch_one(const GemvPlan &p, const WMaps &maps, const GemvArgs &a, cudaStream_t stream,
                               bool pdl)
 {
     void (*kern)(const WMaps, const GemvArgs);
     if constexpr (NT <= 2)
-        kern = q4k_gemv_kernel<NT, ARGMAX, I8>;
+        kern = q4k_gemv_kernel<NT, ARGMAX, XM>;
     else
         kern = q4k_gemv_kernel_wide<NT, ARGMAX>;
     static std::mutex mu;
@@ -1403,7 +1416,7 @@ static cudaError_t launch_one(const GemvPlan &p, const WMaps &maps, const GemvAr
     // beside the previous kernel's CTAs, not all of their clusters found room
     // at once (measured: the down projection after gate/up, 15.9 us with PDL,
     // 13.8 us without; the tensor-core kernels gain from PDL there).
-    if (pdl && !(I8 && p.split > 8)) {
+    if (pdl && !(XM != 0 && p.split > 8)) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
@@ -1424,7 +1437,10 @@ static cudaError_t launch_gemv(const GemvPlan &p, const void *const *Ws, int64_t
     for (int g = 0; g < a.ngroups; ++g)
         if (!encode_w_map(&maps.m[g], Ws[g], a.N[g], K)) return cudaErrorInvalidValue;
     switch (p.NT) {
-        case 1: return p.i8 ? launch_one<1, ARGMAX, true>(p, maps, a, s, pdl) : launch_one<1, ARGMAX>(p, maps, a, s, pdl);
+        case 1:
+            if (p.xm == 1) return launch_one<1, ARGMAX, 1>(p, maps, a, s, pdl);
+            if (p.xm == 2) return launch_one<1, ARGMAX, 2>(p, maps, a, s, pdl);
+            return launch_one<1, ARGMAX, 0>(p, maps, a, s, pdl);
         case 2: return launch_one<2, ARGMAX>(p, maps, a, s, pdl);
         case 3: return launch_one<3, ARGMAX>(p, maps, a, s, pdl);
         default: return launch_one<4, ARGMAX>(p, maps, a, s, pdl);
@@ -1470,7 +1486,11 @@ q4k_status gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t
     a.tiles = p.tiles;
     a.kc = p.kc;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
-    if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.i8 = false;
+    if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.xm = 0;
+    if (opts && (opts->flags & Q4K_FLAG_Q8K_X)) {
+        if (batch != 1 || (opts->flags & Q4K_FLAG_TENSOR_CORE)) return Q4K_ERR_INVALID_ARG;
+        p.xm = 2;
+    }
     cudaError_t e = launch_gemv<false>(p, &W, K, a, static_cast<cudaStream_t>(stream), pdl);
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
@@ -1512,7 +1532,11 @@ q4k_status gemv_grouped_impl(const q4k_gemv_group *groups, int ngroups, const fl
     a.tiles = p.tiles;
     a.kc = p.kc;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
-    if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.i8 = false;
+    if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.xm = 0;
+    if (opts && (opts->flags & Q4K_FLAG_Q8K_X)) {
+        if (batch != 1 || (opts->flags & Q4K_FLAG_TENSOR_CORE)) return Q4K_ERR_INVALID_ARG;
+        p.xm = 2;
+    }
     cudaError_t e = launch_gemv<false>(p, Ws, K, a, static_cast<cudaStream_t>(stream), pdl);
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
@@ -1543,7 +1567,11 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
     a.kc = p.kc;
     a.idx = idx;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
-    if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.i8 = false;
+    if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.xm = 0;
+    if (opts && (opts->flags & Q4K_FLAG_Q8K_X)) {
+        if (batch != 1 || (opts->flags & Q4K_FLAG_TENSOR_CORE)) return Q4K_ERR_INVALID_ARG;
+        p.xm = 2;
+    }
     void *buf = nullptr;
     const size_t bytes = 8 * 16 + 16;
     if (scratch_keys == nullptr) {

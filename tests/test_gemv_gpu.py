@@ -316,3 +316,55 @@ def test_auto_split_above_eight(env):
     W2 = W[:N2]
     x = synth.normal_f32((2, K), (96, 3))
     assert_close(_run(q4k, W2, x), oracle.gemv(W2, x, N2, K), x, K, "5 tiles, long K")
+
+
+# ---------------------------------------------------------------- Q8_K activations (batch 1, on request)
+def _q8k_input(K, seed):
+    x = synth.normal_f32((1, K), (seed, 2))
+    x[0, 0:256] *= np.float32(1e-30)        # a tiny block
+    x[0, 256:512] = 0.0                     # an all-zero block
+    x[0, 700] = 55.0                        # a block with one large entry
+    x[0, 1024:1280] = np.float32(127.0) * np.round(x[0, 1024:1280])   # codes on exact integers
+    return x
+
+
+@pytest.mark.parametrize("N,K,seed", [(300, 3584, 51), (129, 18944, 52), (640, 4096, 53), (1, 1536, 54)])
+def test_q8k_matches_oracle(env, N, K, seed):
+    """Q4K_FLAG_Q8K_X: the kernel quantizes x with the oracle's rule (same fp32
+    decisions) and multiplies exactly in integers; against the oracle's
+    Q4_K x Q8_K product it may differ only by fp32 rounding of the
+    per-block combine, and against the exact product by the quantization bound
+    sum_k |w| d/2."""
+    q4k, oracle = env
+    W = synth.q4k_weights(N, K, (seed, 1))
+    x = _q8k_input(K, seed)
+    y = _run(q4k, W, x, q8k=True)[0]
+    q, d = oracle.q8k_quantize(x[0], K)
+    ref = oracle.gemv_q8k(W, q, d, N, K)
+    D = oracle.dequant_matrix(W, N, K)
+    xt = np.repeat(d.astype(np.float64), 256) * q.astype(np.float64)
+    assert np.all(np.abs(y - ref) <= 1e-5 * (np.abs(D) @ np.abs(xt)) + 1e-30)
+    exact = oracle.gemv(W, x, N, K)[0]
+    bound = (np.abs(D) @ (np.repeat(d.astype(np.float64), 256) / 2)) * (1 + 1e-4) + 1e-5 * (np.abs(D) @ np.abs(xt))
+    assert np.all(np.abs(y - exact) <= bound)
+
+
+def test_q8k_grouped_and_guards(env):
+    q4k, oracle = env
+    K = 3584
+    Ws = [synth.q4k_weights(N, K, (55, N)) for N in (256, 129)]
+    x = _q8k_input(K, 56)
+    ys = q4k.gemv_grouped([_dev(W) for W in Ws], _dev(x), q8k=True)
+    torch.cuda.synchronize()
+    q, d = oracle.q8k_quantize(x[0], K)
+    for W, yg in zip(Ws, ys):
+        N = W.shape[0]
+        ref = oracle.gemv_q8k(W, q, d, N, K)
+        D = oracle.dequant_matrix(W, N, K)
+        xt = np.repeat(d.astype(np.float64), 256) * q.astype(np.float64)
+        assert np.all(np.abs(yg.cpu().numpy()[0] - ref) <= 1e-5 * (np.abs(D) @ np.abs(xt)) + 1e-30)
+    W = _dev(Ws[0])
+    with pytest.raises(q4k.Q4KError):
+        q4k.gemv(W, _dev(synth.normal_f32((2, K), 57)), q8k=True)          # batch 1 only
+    with pytest.raises(q4k.Q4KError):
+        q4k.gemv(W, _dev(x), q8k=True, tensor_core=True)                   # one inner product at a time
