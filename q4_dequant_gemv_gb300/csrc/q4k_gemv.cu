@@ -227,8 +227,11 @@ __device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int 
 // fp32 (x and max|x| first scaled by 2^64 when max|x| < 2^-64), so that
 // |x - (dx / 254)(254 xh + xl)| <= dx (1/508 + 2^-16).  Per local
 // super-block bl, at byte offset bl * blk_bytes of the fragment area:
-//   [0, 256)    xh in k order       [256, 512)  xl in k order
-//   [512, 544)  int32 per sub-block j: 254 * sum(xh) + sum(xl) over its 32 k
+//   [0, 320)    xh: the 64 values of sub-block pair t at 80 t, in k order
+//   [320, 640)  xl: the same at 320 + 80 t
+//   [640, 672)  int32 per sub-block j: 254 * sum(xh) + sum(xl) over its 32 k
+// (the 16-byte pad per pair puts the four pairs' 16-byte loads of one
+// quarter-warp on distinct banks)
 // and s_unscale[bl] * s_pre[bl] = dx / 254, with s_unscale[bl] kept in the
 // normal range (s_pre = 2^-64 for the scaled blocks, else 1); s_unscale is 0
 // for an all-zero super-block and the non-finite max itself when x holds an
@@ -236,7 +239,8 @@ __device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int 
 // One warp per super-block; lane l holds float4 l and l + 32 (k = 4l..4l+3 and
 // 128 + 4l..).  Ends with a barrier over all nthr threads.
 // ---------------------------------------------------------------------------
-constexpr int kI8Bytes = 544;
+constexpr int kI8Bytes = 672;
+constexpr int kI8Pair = 80;        // bytes per sub-block pair in each part
 static_assert(kI8Bytes <= lane_stride(1) * 8 * 8, "batch-1 fragment area holds the int8 parts");
 
 template <bool Q8, bool L2ONLY = false>
@@ -294,13 +298,14 @@ __device__ void convert_x_i8_blocks(const float *__restrict__ x, int kb0, int nb
                     sum += 254 * hi + lo;
                 }
             }
-            const int i = lane + 32 * h2;   // float4 index: k = 4i..4i+3, sub-block i/8
-            *reinterpret_cast<uint32_t *>(base + 4 * i) = hw;
-            if constexpr (!Q8) *reinterpret_cast<uint32_t *>(base + 256 + 4 * i) = lw;
+            const int i = lane + 32 * h2;   // float4 index: k = 4i..4i+3, sub-block i/8, pair i/16
+            const int off = kI8Pair * (i >> 4) + 4 * (i & 15);
+            *reinterpret_cast<uint32_t *>(base + off) = hw;
+            if constexpr (!Q8) *reinterpret_cast<uint32_t *>(base + 4 * kI8Pair + off) = lw;
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
             sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            if ((i & 7) == 0) reinterpret_cast<int *>(base + 512)[i >> 3] = sum;
+            if ((i & 7) == 0) reinterpret_cast<int *>(base + 8 * kI8Pair)[i >> 3] = sum;
         }
         if (lane == 0) {
             s_unscale[it] = ok ? (Q8 ? (amax * pre) / 127.0f : (amax * pre) / 127.0f / 254.0f)
@@ -410,11 +415,11 @@ __device__ __forceinline__ void stage_compute_i8(const uint8_t *ra, const uint8_
         const uint4 qa = *reinterpret_cast<const uint4 *>(ra + 16 + 32 * t + 16 * half);
         const uint4 qb = *reinterpret_cast<const uint4 *>(rb + 16 + 32 * t + 16 * half);
         // x parts of k = 64t + 16 half + 0..15 (sub-block 2t) and + 32 (2t+1)
-        const uint4 xhE = *reinterpret_cast<const uint4 *>(xb + 64 * t + 16 * half);
-        const uint4 xhO = *reinterpret_cast<const uint4 *>(xb + 64 * t + 32 + 16 * half);
-        const uint4 xlE = Q8 ? make_uint4(0, 0, 0, 0) : *reinterpret_cast<const uint4 *>(xb + 256 + 64 * t + 16 * half);
-        const uint4 xlO = Q8 ? make_uint4(0, 0, 0, 0)
-                             : *reinterpret_cast<const uint4 *>(xb + 256 + 64 * t + 32 + 16 * half);
+        const uint8_t *xh = xb + kI8Pair * t + 16 * half;
+        const uint4 xhE = *reinterpret_cast<const uint4 *>(xh);
+        const uint4 xhO = *reinterpret_cast<const uint4 *>(xh + 32);
+        const uint4 xlE = Q8 ? make_uint4(0, 0, 0, 0) : *reinterpret_cast<const uint4 *>(xh + 4 * kI8Pair);
+        const uint4 xlO = Q8 ? make_uint4(0, 0, 0, 0) : *reinterpret_cast<const uint4 *>(xh + 4 * kI8Pair + 32);
         const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
         const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
         const uint32_t he[4] = {xhE.x, xhE.y, xhE.z, xhE.w};
@@ -438,7 +443,7 @@ __device__ __forceinline__ void stage_compute_i8(const uint8_t *ra, const uint8_
         }
     }
     release();
-    const int2 bs = *reinterpret_cast<const int2 *>(xb + 512 + 8 * t);
+    const int2 bs = *reinterpret_cast<const int2 *>(xb + 8 * kI8Pair + 8 * t);
     // the high-nibble sums are multiples of 16: exact shifts
     oh0 >>= 4; ol0 >>= 4; oh1 >>= 4; ol1 >>= 4;
     const int T0 = Q8 ? r0.scE * eh0 + r0.scO * oh0 : 254 * (r0.scE * eh0 + r0.scO * oh0) + (r0.scE * el0 + r0.scO * ol0);
