@@ -80,6 +80,9 @@ def _load():
         lib.oracle_prefill.argtypes = [P, P, P, I64, I64, I64, I, I]
         lib.oracle_q8k_quantize.argtypes = [P, I64, P, P]
         lib.oracle_gemv_q8k.argtypes = [P, P, P, P, I64, I64, I]
+        lib.oracle_q6k_dequant_block.argtypes = [P, P]
+        lib.oracle_q6k_gemv.argtypes = [P, P, P, I64, I64, I, I]
+        lib.oracle_q6k_gemv_rows.argtypes = [P, P, P, I64, I, P, I64, I]
         lib.oracle_max_threads.restype = I
         _lib = lib
         return lib
@@ -216,4 +219,44 @@ def gemv_q8k(W: np.ndarray, q: np.ndarray, d: np.ndarray, N: int, K: int, thread
     assert W.size == N * (K // QK) * QBYTES and q.size == K and d.size == K // QK
     y = np.zeros(N, np.float64)
     _load().oracle_gemv_q8k(_ptr(W), _ptr(q), _ptr(d), _ptr(y), N, K, threads)
+    return y
+
+
+Q6BYTES = 210
+
+
+def q6k_dequant_block(blk) -> np.ndarray:
+    """The 256 weights (fp64) of one 210-byte Q6_K block."""
+    b = _c(np.frombuffer(bytes(blk), np.uint8) if isinstance(blk, (bytes, bytearray)) else blk, np.uint8)
+    assert b.size == Q6BYTES
+    w = np.zeros(QK, np.float64)
+    _load().oracle_q6k_dequant_block(_ptr(b), _ptr(w))
+    return w
+
+
+def q6k_dequant_matrix(W: np.ndarray, N: int, K: int) -> np.ndarray:
+    W = _c(W, np.uint8).reshape(N * (K // QK), Q6BYTES)
+    return np.stack([q6k_dequant_block(W[i]) for i in range(W.shape[0])]).reshape(N, K) if N else np.zeros((0, K))
+
+
+def q6k_gemv(W: np.ndarray, x: np.ndarray, N: int, K: int, threads: int = 0) -> np.ndarray:
+    """fp64 y [B][N] = W_q6k_deq [N][K] . x[b] for x fp32 [B][K] (or [K])."""
+    W = _c(W, np.uint8)
+    x2 = _c(x, np.float32).reshape(-1, K)
+    B = x2.shape[0]
+    assert W.size == N * (K // QK) * Q6BYTES
+    y = np.zeros((B, N), np.float64)
+    _load().oracle_q6k_gemv(_ptr(W), _ptr(x2), _ptr(y), N, K, B, threads)
+    return y
+
+
+def q6k_gemv_rows(W: np.ndarray, x: np.ndarray, N: int, K: int, rows, threads: int = 0) -> np.ndarray:
+    """fp64 y [B][len(rows)] for a subset of rows of a Q6_K matrix times x."""
+    W = _c(W, np.uint8)
+    x2 = _c(x, np.float32).reshape(-1, K)
+    B = x2.shape[0]
+    r = _c(rows, np.int64)
+    assert W.size == N * (K // QK) * Q6BYTES and (r.size == 0 or (r.min() >= 0 and r.max() < N))
+    y = np.zeros((B, r.size), np.float64)
+    _load().oracle_q6k_gemv_rows(_ptr(W), _ptr(x2), _ptr(y), K, B, _ptr(r), r.size, threads)
     return y

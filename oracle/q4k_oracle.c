@@ -20,6 +20,9 @@
  *   - the prefill product with bf16 activations ("cuBLAS HGEMM for prefill",
  *     dotLLM README, News 2026-03 "CUDA GPU backend"): same fp64 sum with the
  *     bf16 activations decoded exactly.
+ *   - the Q6_K GEMV (dotLLM README, News 2026-03 "CUDA GPU backend": "custom
+ *     quantized GEMV for decode (Q8_0, Q4_K, Q6_K)"): the same plain fp64
+ *     product over the Q6_K weights, layout at oracle_q6k_dequant_block.
  *   - Q8_K activation quantization and the Q4_K x Q8_K product (dotLLM README,
  *     News 2026-03 "Mixed quantization + Q8_K"): the int8 codes and block
  *     scales by the rule written at oracle_q8k_quantize, then the same fp64
@@ -281,6 +284,87 @@ void oracle_gemv_q8k(const uint8_t *W, const int8_t *q, const float *d, double *
             double acc = 0.0;
             for (int64_t k = 0; k < K; ++k) acc += buf[k] * ((double)d[k / QK] * (double)q[k]);
             y[n] = acc;
+        }
+        free(buf);
+    }
+}
+
+/*
+ * Q6_K, the other block format of Q4_K_M files ("custom quantized GEMV for
+ * decode (Q8_0, Q4_K, Q6_K)", dotLLM README, News 2026-03 "CUDA GPU
+ * backend"; the pages print no bytes, the reading used here is the GGUF Q6_K
+ * packing):  210 bytes hold 256 weights in 16 sub-blocks of 16.
+ *   bytes   0..127  ql[128]  low 4 bits of the 6-bit codes
+ *   bytes 128..191  qh[64]   high 2 bits of the codes
+ *   bytes 192..207  sc[16]   int8 scale of each 16 weights
+ *   bytes 208..209  d        IEEE binary16, little-endian
+ * For weight k = 128 h + 32 c + l  (h < 2, c < 4, l < 32):
+ *   low  = ql[64 h + 32 (c & 1) + l]: its low nibble when c < 2, else its high
+ *   high = (qh[32 h + l] >> (2 c)) & 3
+ *   q = low + 16 high  (0..63),   w = d * sc[k / 16] * (q - 32)
+ * (d * sc * (q - 32) has at most 11 + 8 + 6 significant bits: exact in fp64.)
+ */
+#define Q6BYTES 210
+
+void oracle_q6k_dequant_block(const uint8_t blk[Q6BYTES], double w[QK])
+{
+    const uint8_t *ql = blk, *qh = blk + 128;
+    const int8_t *sc = (const int8_t *)(blk + 192);
+    const double d = oracle_fp16_to_double((uint16_t)(blk[208] | (blk[209] << 8)));
+    for (int k = 0; k < QK; ++k) {
+        const int h = k / 128, c = (k % 128) / 32, l = k % 32;
+        const int byte = ql[64 * h + 32 * (c & 1) + l];
+        const int low = (c < 2) ? (byte & 15) : (byte >> 4);
+        const int high = (qh[32 * h + l] >> (2 * c)) & 3;
+        const int q = low + 16 * high;
+        w[k] = d * (double)sc[k / 16] * (double)(q - 32);
+    }
+}
+
+static void q6k_dequant_row(const uint8_t *W, int64_t n, int64_t K, double *buf)
+{
+    const int64_t nb = K / QK;
+    for (int64_t b = 0; b < nb; ++b) oracle_q6k_dequant_block(W + (n * nb + b) * Q6BYTES, buf + b * QK);
+}
+
+/* y[b][n] = sum_k w[n][k] * x[b][k] for a Q6_K matrix; x fp32 [B][K], y fp64 [B][N]. */
+void oracle_q6k_gemv(const uint8_t *W, const float *x, double *y, int64_t N, int64_t K, int B, int threads)
+{
+    set_threads(threads);
+#pragma omp parallel
+    {
+        double *buf = (double *)malloc((size_t)K * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t n = 0; n < N; ++n) {
+            q6k_dequant_row(W, n, K, buf);
+            for (int b = 0; b < B; ++b) {
+                const float *xb = x + (int64_t)b * K;
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k) acc += buf[k] * (double)xb[k];
+                y[(int64_t)b * N + n] = acc;
+            }
+        }
+        free(buf);
+    }
+}
+
+/* The same for an explicit row subset (rows[r] -> y[b][r]); y is [B][R]. */
+void oracle_q6k_gemv_rows(const uint8_t *W, const float *x, double *y, int64_t K, int B, const int64_t *rows,
+                          int64_t R, int threads)
+{
+    set_threads(threads);
+#pragma omp parallel
+    {
+        double *buf = (double *)malloc((size_t)K * sizeof(double));
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < R; ++r) {
+            q6k_dequant_row(W, rows[r], K, buf);
+            for (int b = 0; b < B; ++b) {
+                const float *xb = x + (int64_t)b * K;
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k) acc += buf[k] * (double)xb[k];
+                y[(int64_t)b * R + r] = acc;
+            }
         }
         free(buf);
     }

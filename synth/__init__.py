@@ -48,6 +48,25 @@ def q4k_weights(N: int, K: int, seed, d_lo: float = 2e-4, d_hi: float = 2e-3) ->
     return out.reshape(N, nb * QBYTES)
 
 
+Q6BYTES = 210
+
+
+def q6k_weights(N: int, K: int, seed, d_lo: float = 2e-4, d_hi: float = 2e-3) -> np.ndarray:
+    """Random Q6_K matrix, uint8 [N, K/256*210]: uniform bytes for the 6-bit
+    codes and the int8 scales (all signs), d ~ U[d_lo, d_hi] rounded to fp16."""
+    assert K % QK == 0 and K > 0 and N >= 0
+    nb = K // QK
+    g = rng(*(seed if isinstance(seed, tuple) else (seed,)))
+    nblk = N * nb
+    out = np.empty((nblk, Q6BYTES), np.uint8)
+    if nblk:
+        raw = g.bit_generator.random_raw((nblk * 208 + 7) // 8)
+        out[:, :208] = raw.view(np.uint8)[: nblk * 208].reshape(nblk, 208)
+        d = g.uniform(d_lo, d_hi, size=nblk).astype(np.float16)
+        out[:, 208:210] = d.view(np.uint8).reshape(nblk, 2)
+    return out.reshape(N, nb * Q6BYTES)
+
+
 def normal_f32(shape, seed) -> np.ndarray:
     """N(0, 1) float32 samples."""
     g = rng(*(seed if isinstance(seed, tuple) else (seed,)))
