@@ -150,6 +150,32 @@ q4k_status q4k_gemv_argmax_noalloc(const void *W, const float *x, int32_t *idx, 
                                    int batch, void *stream);
 
 /*
+ * ---------------------------------------------------------------------------
+ * Q6_K super-block (210 bytes, 256 weights, 6.5625 bits per weight), the other
+ * block format of Q4_K_M files ("custom quantized GEMV for decode (Q8_0, Q4_K,
+ * Q6_K)", dotLLM README, News 2026-03 "CUDA GPU backend").  The pages print no
+ * bytes; this library fixes the GGUF Q6_K packing:
+ *   bytes   0..127  ql[128] low 4 bits of the 6-bit codes
+ *   bytes 128..191  qh[64]  high 2 bits of the codes
+ *   bytes 192..207  sc[16]  int8 scale of each 16 weights
+ *   bytes 208..209  d       IEEE binary16, little-endian
+ *   weight k = 128h + 32c + l (h < 2, c < 4, l < 32):
+ *     low  = ql[64h + 32(c & 1) + l], its low nibble for c < 2, high for c >= 2
+ *     high = (qh[32h + l] >> 2c) & 3,   q = low + 16 high (0..63)
+ *     w = d * sc[k / 16] * (q - 32)
+ * Rows hold K/256 consecutive blocks (row n at byte n * (K/256) * 210); blocks
+ * are therefore only 2-byte aligned.
+ * ---------------------------------------------------------------------------
+ * y[b][n] = sum_k w[n][k] * x[b][k] for a Q6_K matrix W, b < batch, n < N.
+ *   W uint8 [N][K/256*210] (16-byte aligned), x fp32 [batch][K] (16-byte
+ *   aligned), y fp32 [batch][N]; N >= 0 (0: no-op), K a positive multiple of
+ *   256, 1 <= batch <= 16.  fp32 accumulation; each block is read once for all
+ *   batch rows; deterministic.
+ * Errors: INVALID_ARG, MISALIGNED (W or x), UNSUPPORTED_DEVICE, CUDA.
+ */
+q4k_status q6k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream);
+
+/*
  * Y[t][n] = sum_k w[n][k] * X[t][k]   for t < T, n < N (prefill).
  *   W  Q4_K rows as above (16-byte aligned)
  *   X  bf16 [T][K] row-major (16-byte aligned)

@@ -48,7 +48,7 @@ class ChainStep(ctypes.Structure):
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("q4k_status_string", "q4k_abi_version", "q4k_gemv", "q4k_gemv_argmax", "q4k_gemv_argmax_debug",
            "q4k_gemv_argmax_noalloc", "q4k_gemm_prefill", "q4k_gemv_ex", "q4k_gemv_grouped", "q4k_gemv_plan",
-           "q4k_device_error_flags", "q4k_chain_create", "q4k_chain_run", "q4k_chain_destroy")
+           "q4k_device_error_flags", "q4k_chain_create", "q4k_chain_run", "q4k_chain_destroy", "q6k_gemv")
 
 
 def lib():
@@ -77,6 +77,8 @@ def lib():
         L.q4k_gemv_argmax_noalloc.argtypes = [P, P, P, I64, I64, I, P]
         L.q4k_gemv_argmax_noalloc.restype = I
         L.q4k_gemm_prefill.argtypes = [P, P, P, I64, I64, I64, P]
+        L.q6k_gemv.argtypes = [P, P, P, I64, I64, I, P]
+        L.q6k_gemv.restype = I
         L.q4k_gemm_prefill.restype = I
         L.q4k_gemv_plan.argtypes = [I64, I64, I, ctypes.POINTER(ctypes.c_int * 4)]
         L.q4k_gemv_plan.restype = I
@@ -157,6 +159,27 @@ def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False, tens
     else:
         st = L.q4k_gemv(W.data_ptr(), x2.data_ptr(), y.data_ptr(), N, K, B, _stream_ptr(stream))
         _check("q4k_gemv", st)
+    return y.view(N) if squeeze and y.dim() == 2 else y
+
+
+def q6k_gemv(W, x, y=None, *, stream=None):
+    """y [B, N] (fp32) = W_q6k [N, K] . x [B, K] (fp32); x may also be [K]."""
+    import torch
+    _dev(W, "W", torch.uint8)
+    _dev(x, "x", torch.float32)
+    squeeze = x.dim() == 1
+    x2 = x.view(1, -1) if squeeze else x
+    B, K = x2.shape
+    if K % 256 or W.dim() != 2 or W.shape[1] != (K // 256) * 210:
+        raise ValueError(f"W must be [N, {(K // 256) * 210}] uint8 for K={K}")
+    N = W.shape[0]
+    if y is None:
+        y = torch.empty((B, N), dtype=torch.float32, device=x.device)
+    _dev(y, "y", torch.float32)
+    if y.numel() != B * N:
+        raise ValueError("y has the wrong size")
+    st = lib().q6k_gemv(W.data_ptr(), x2.data_ptr(), y.data_ptr(), N, K, B, _stream_ptr(stream))
+    _check("q6k_gemv", st)
     return y.view(N) if squeeze and y.dim() == 2 else y
 
 

@@ -25,6 +25,11 @@ q4k_status q4k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t 
     return q4k::gemv_impl(W, x, y, N, K, batch, stream, nullptr);
 }
 
+q4k_status q6k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream)
+{
+    return q4k::q6k_gemv_impl(W, x, y, N, K, batch, stream);
+}
+
 q4k_status q4k_gemv_ex(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream,
                        const q4k_launch_opts *opts)
 {

@@ -1,0 +1,147 @@
+// q6k_gemv.cu -- Q6_K decode GEMV on GB300: y[b] = W x[b] for the other block
+// format of Q4_K_M files ("custom quantized GEMV for decode (Q8_0, Q4_K,
+// Q6_K)", dotLLM README, News 2026-03 "CUDA GPU backend"; the GGUF Q6_K
+// packing is written out in include/q4k.h).
+//
+// A 210-byte block is only 2-byte aligned inside a row (rows of K/256 blocks
+// follow one another), so neither TMA boxes nor 16-byte loads can address it.
+// A warp decodes one block at a time straight from global memory: lane L takes
+// quant bytes ql[4L..4L+3] (two 16-bit loads), i.e. four weights of sub-block
+// pair c1 = (L/8)&1 and four of c1+2, the matching four qh bytes, and the two
+// int8 scales of those weights.  Per 32-bit word the four 6-bit codes are
+// assembled with a few integer ops; each code becomes q - 32 in fp32 by one
+// byte permute (2^23 + q) and one exact subtraction; x is read as float4s
+// (the row's x slice stays in L1 across rows).  fp32 accumulation, one warp
+// reduction per row; when a matrix has few rows, the 8 warps of a CTA split a
+// row's blocks and their partial sums are added in warp order (deterministic).
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "q4k_internal.h"
+
+namespace q4k {
+namespace q6 {
+
+constexpr int kBytes = 210;
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kMaxB = 16;
+
+__device__ __forceinline__ uint32_t ld_u16(const uint8_t *p)   // 2-byte aligned
+{
+    return static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(p)));
+}
+
+// grid: one CTA per kWarps / wpr rows; warp w works on row (w / wpr) of the
+// CTA and on the blocks b with b % wpr == w % wpr.
+__global__ void __launch_bounds__(kThreads) q6k_gemv_kernel(const uint8_t *__restrict__ W, const float *__restrict__ x,
+                                                           float *__restrict__ y, int N, int nb, int B, int wpr)
+{
+    __shared__ float part[kWarps][kMaxB];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rows_per_cta = kWarps / wpr;
+    const int row = blockIdx.x * rows_per_cta + warp / wpr;
+    const int slice = warp % wpr;
+    // this lane's share of a block
+    const int h = lane >> 4, c1 = (lane >> 3) & 1, l0 = 4 * (lane & 7);
+    const int ql_off = 4 * lane;                          // = 64 h + 32 c1 + l0
+    const int qh_off = 128 + 32 * h + l0;
+    const int sc_off = 192 + 8 * h + 2 * c1 + (l0 >> 4);   // scale of the low-nibble weights; +4 for the high ones
+    const int k_lo = 128 * h + 32 * c1 + l0;              // their first weight; +64 for the high ones
+    const int K = nb * 256;
+    float acc[kMaxB];
+#pragma unroll
+    for (int b = 0; b < kMaxB; ++b) acc[b] = 0.f;
+    if (row < N) {
+        const uint8_t *wrow = W + static_cast<size_t>(row) * nb * kBytes;
+        for (int blk = slice; blk < nb; blk += wpr) {
+            const uint8_t *A = wrow + static_cast<size_t>(blk) * kBytes;
+            const uint32_t ql = ld_u16(A + ql_off) | (ld_u16(A + ql_off + 2) << 16);
+            const uint32_t qh = ld_u16(A + qh_off) | (ld_u16(A + qh_off + 2) << 16);
+            const float sc_lo = static_cast<float>(static_cast<int8_t>(__ldg(A + sc_off)));
+            const float sc_hi = static_cast<float>(static_cast<int8_t>(__ldg(A + sc_off + 4)));
+            const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(ld_u16(A + 208))));
+            // four 6-bit codes per word: low nibble | high bit pair << 4
+            const uint32_t q_lo = (ql & 0x0F0F0F0Fu) | (((qh >> (2 * c1)) & 0x03030303u) << 4);
+            const uint32_t q_hi = ((ql >> 4) & 0x0F0F0F0Fu) | (((qh >> (2 * c1 + 4)) & 0x03030303u) << 4);
+            float w_lo[4], w_hi[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {   // 2^23 + q - (2^23 + 32) = q - 32, exact
+                w_lo[j] = __uint_as_float(__byte_perm(q_lo, 0x4B000000u, 0x7440u | j)) - 8388640.0f;
+                w_hi[j] = __uint_as_float(__byte_perm(q_hi, 0x4B000000u, 0x7440u | j)) - 8388640.0f;
+            }
+            const float s_lo = d * sc_lo, s_hi = d * sc_hi;   // exact: 11 x 8 significant bits
+            const float *xb = x + static_cast<size_t>(blk) * 256 + k_lo;
+#pragma unroll
+            for (int b = 0; b < kMaxB; ++b) {
+                if (b >= B) break;
+                const float4 xa = __ldg(reinterpret_cast<const float4 *>(xb + static_cast<size_t>(b) * K));
+                const float4 xc = __ldg(reinterpret_cast<const float4 *>(xb + static_cast<size_t>(b) * K + 64));
+                float t_lo = w_lo[0] * xa.x;
+                t_lo = fmaf(w_lo[1], xa.y, t_lo);
+                t_lo = fmaf(w_lo[2], xa.z, t_lo);
+                t_lo = fmaf(w_lo[3], xa.w, t_lo);
+                float t_hi = w_hi[0] * xc.x;
+                t_hi = fmaf(w_hi[1], xc.y, t_hi);
+                t_hi = fmaf(w_hi[2], xc.z, t_hi);
+                t_hi = fmaf(w_hi[3], xc.w, t_hi);
+                acc[b] = fmaf(s_lo, t_lo, fmaf(s_hi, t_hi, acc[b]));
+            }
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < kMaxB; ++b) {
+        if (b >= B) break;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], o);
+        if (lane == 0) part[warp][b] = acc[b];
+    }
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) < rows_per_cta * B) {
+        const int rr = threadIdx.x / B, b = threadIdx.x - rr * B;
+        const int r = blockIdx.x * rows_per_cta + rr;
+        if (r < N) {
+            float s = part[rr * wpr][b];
+            for (int q = 1; q < wpr; ++q) s += part[rr * wpr + q][b];
+            y[static_cast<size_t>(b) * N + r] = s;
+        }
+    }
+}
+
+}  // namespace q6
+
+// Warps per row: enough warps in flight for the GPU (about 48 per SM), at
+// most 8 (one CTA) and at most one per block.
+static int q6k_warps_per_row(int64_t N, int nb, int sms)
+{
+    const long long want = static_cast<long long>(sms) * 48;
+    int wpr = 1;
+    while (wpr < 8 && wpr * 2 <= nb && static_cast<long long>(N) * wpr < want) wpr *= 2;
+    return wpr;
+}
+
+q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream)
+{
+    if (!x) return Q4K_ERR_INVALID_ARG;
+    if ((!W || !y) && N != 0) return Q4K_ERR_INVALID_ARG;
+    if (N < 0 || N > 0x7FFFFFFFll || K <= 0 || (K % 256) != 0 || K / 256 >= (1ll << 24)) return Q4K_ERR_INVALID_ARG;
+    if (batch < 1 || batch > q6::kMaxB) return Q4K_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W) & 15u) || (reinterpret_cast<uintptr_t>(x) & 15u)) return Q4K_ERR_MISALIGNED;
+    int sms = 0;
+    const q4k_status st = check_device(&sms);
+    if (st != Q4K_OK) return st;
+    if (N == 0) return Q4K_OK;
+    const int nb = static_cast<int>(K / 256);
+    const int wpr = q6k_warps_per_row(N, nb, sms);
+    const int rows_per_cta = q6::kWarps / wpr;
+    const long long grid = (N + rows_per_cta - 1) / rows_per_cta;
+    if (grid > 0x7FFFFFFFll) return Q4K_ERR_INVALID_ARG;
+    q6::q6k_gemv_kernel<<<static_cast<unsigned>(grid), q6::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(W), x, y, static_cast<int>(N), nb, batch, wpr);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
+}
+
+}  // namespace q4k

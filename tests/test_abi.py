@@ -23,7 +23,7 @@ def q4k():
 def _declared():
     src = open(os.path.join(ROOT, "include", "q4k.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(q4k_[a-z_0-9]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b((?:q4k|q6k)_[a-z_0-9]+)\s*\(", src)))
 
 
 def test_header_symbols_exported(q4k):
