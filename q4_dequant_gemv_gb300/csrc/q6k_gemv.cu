@@ -17,6 +17,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "q4k_internal.h"
@@ -34,15 +35,19 @@ __device__ __forceinline__ uint32_t ld_u16(const uint8_t *p)   // 2-byte aligned
     return static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short *>(p)));
 }
 
-// grid: one CTA per kWarps / wpr rows; warp w works on row (w / wpr) of the
-// CTA and on the blocks b with b % wpr == w % wpr.
+// Persistent CTAs over groups of kWarps / wpr rows: warp w works on row
+// (w / wpr) of the group and on the blocks b with b % wpr == w % wpr.  XS: x
+// (B x K fp32) is staged in shared memory once per CTA; otherwise it is read
+// from global memory (L1).
+template <int BMAX, bool XS>
 __global__ void __launch_bounds__(kThreads) q6k_gemv_kernel(const uint8_t *__restrict__ W, const float *__restrict__ x,
-                                                           float *__restrict__ y, int N, int nb, int B, int wpr)
+                                                           float *__restrict__ y, int N, int nb, int B, int wpr,
+                                                           int groups)
 {
-    __shared__ float part[kWarps][kMaxB];
+    extern __shared__ __align__(16) float xs[];
+    __shared__ float part[kWarps][BMAX];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows_per_cta = kWarps / wpr;
-    const int row = blockIdx.x * rows_per_cta + warp / wpr;
     const int slice = warp % wpr;
     // this lane's share of a block
     const int h = lane >> 4, c1 = (lane >> 3) & 1, l0 = 4 * (lane & 7);
@@ -51,62 +56,79 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_kernel(const uint8_t *__res
     const int sc_off = 192 + 8 * h + 2 * c1 + (l0 >> 4);   // scale of the low-nibble weights; +4 for the high ones
     const int k_lo = 128 * h + 32 * c1 + l0;              // their first weight; +64 for the high ones
     const int K = nb * 256;
-    float acc[kMaxB];
+    if constexpr (XS) {
+        const float4 *src = reinterpret_cast<const float4 *>(x);
+        float4 *dst = reinterpret_cast<float4 *>(xs);
+        for (int i = threadIdx.x; i < B * K / 4; i += kThreads) dst[i] = __ldg(src + i);
+        __syncthreads();
+    }
+    const float *xv = XS ? xs : x;
+    for (int grp = blockIdx.x; grp < groups; grp += gridDim.x) {
+        const int row = grp * rows_per_cta + warp / wpr;
+        float acc[BMAX];
 #pragma unroll
-    for (int b = 0; b < kMaxB; ++b) acc[b] = 0.f;
-    if (row < N) {
-        const uint8_t *wrow = W + static_cast<size_t>(row) * nb * kBytes;
-        for (int blk = slice; blk < nb; blk += wpr) {
-            const uint8_t *A = wrow + static_cast<size_t>(blk) * kBytes;
-            const uint32_t ql = ld_u16(A + ql_off) | (ld_u16(A + ql_off + 2) << 16);
-            const uint32_t qh = ld_u16(A + qh_off) | (ld_u16(A + qh_off + 2) << 16);
-            const float sc_lo = static_cast<float>(static_cast<int8_t>(__ldg(A + sc_off)));
-            const float sc_hi = static_cast<float>(static_cast<int8_t>(__ldg(A + sc_off + 4)));
-            const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(ld_u16(A + 208))));
-            // four 6-bit codes per word: low nibble | high bit pair << 4
-            const uint32_t q_lo = (ql & 0x0F0F0F0Fu) | (((qh >> (2 * c1)) & 0x03030303u) << 4);
-            const uint32_t q_hi = ((ql >> 4) & 0x0F0F0F0Fu) | (((qh >> (2 * c1 + 4)) & 0x03030303u) << 4);
-            float w_lo[4], w_hi[4];
+        for (int b = 0; b < BMAX; ++b) acc[b] = 0.f;
+        if (row < N) {
+            const uint8_t *wrow = W + static_cast<size_t>(row) * nb * kBytes;
+            for (int blk = slice; blk < nb; blk += wpr) {
+                const uint8_t *A = wrow + static_cast<size_t>(blk) * kBytes;
+                const uint32_t ql = ld_u16(A + ql_off) | (ld_u16(A + ql_off + 2) << 16);
+                const uint32_t qh = ld_u16(A + qh_off) | (ld_u16(A + qh_off + 2) << 16);
+                const float sc_lo = static_cast<float>(static_cast<int8_t>(__ldg(A + sc_off)));
+                const float sc_hi = static_cast<float>(static_cast<int8_t>(__ldg(A + sc_off + 4)));
+                const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(ld_u16(A + 208))));
+                // four 6-bit codes per word: low nibble | high bit pair << 4
+                const uint32_t q_lo = (ql & 0x0F0F0F0Fu) | (((qh >> (2 * c1)) & 0x03030303u) << 4);
+                const uint32_t q_hi = ((ql >> 4) & 0x0F0F0F0Fu) | (((qh >> (2 * c1 + 4)) & 0x03030303u) << 4);
+                float w_lo[4], w_hi[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {   // 2^23 + q - (2^23 + 32) = q - 32, exact
-                w_lo[j] = __uint_as_float(__byte_perm(q_lo, 0x4B000000u, 0x7440u | j)) - 8388640.0f;
-                w_hi[j] = __uint_as_float(__byte_perm(q_hi, 0x4B000000u, 0x7440u | j)) - 8388640.0f;
-            }
-            const float s_lo = d * sc_lo, s_hi = d * sc_hi;   // exact: 11 x 8 significant bits
-            const float *xb = x + static_cast<size_t>(blk) * 256 + k_lo;
+                for (int j = 0; j < 4; ++j) {   // 2^23 + q - (2^23 + 32) = q - 32, exact
+                    w_lo[j] = __uint_as_float(__byte_perm(q_lo, 0x4B000000u, 0x7440u | j)) - 8388640.0f;
+                    w_hi[j] = __uint_as_float(__byte_perm(q_hi, 0x4B000000u, 0x7440u | j)) - 8388640.0f;
+                }
+                const float s_lo = d * sc_lo, s_hi = d * sc_hi;   // exact: 11 x 8 significant bits
+                const float *xb = xv + static_cast<size_t>(blk) * 256 + k_lo;
 #pragma unroll
-            for (int b = 0; b < kMaxB; ++b) {
-                if (b >= B) break;
-                const float4 xa = __ldg(reinterpret_cast<const float4 *>(xb + static_cast<size_t>(b) * K));
-                const float4 xc = __ldg(reinterpret_cast<const float4 *>(xb + static_cast<size_t>(b) * K + 64));
-                float t_lo = w_lo[0] * xa.x;
-                t_lo = fmaf(w_lo[1], xa.y, t_lo);
-                t_lo = fmaf(w_lo[2], xa.z, t_lo);
-                t_lo = fmaf(w_lo[3], xa.w, t_lo);
-                float t_hi = w_hi[0] * xc.x;
-                t_hi = fmaf(w_hi[1], xc.y, t_hi);
-                t_hi = fmaf(w_hi[2], xc.z, t_hi);
-                t_hi = fmaf(w_hi[3], xc.w, t_hi);
-                acc[b] = fmaf(s_lo, t_lo, fmaf(s_hi, t_hi, acc[b]));
+                for (int b = 0; b < BMAX; ++b) {
+                    if (b >= B) break;
+                    float4 xa, xc;
+                    if constexpr (XS) {
+                        xa = *reinterpret_cast<const float4 *>(xb + static_cast<size_t>(b) * K);
+                        xc = *reinterpret_cast<const float4 *>(xb + static_cast<size_t>(b) * K + 64);
+                    } else {
+                        xa = __ldg(reinterpret_cast<const float4 *>(xb + static_cast<size_t>(b) * K));
+                        xc = __ldg(reinterpret_cast<const float4 *>(xb + static_cast<size_t>(b) * K + 64));
+                    }
+                    float t_lo = w_lo[0] * xa.x;
+                    t_lo = fmaf(w_lo[1], xa.y, t_lo);
+                    t_lo = fmaf(w_lo[2], xa.z, t_lo);
+                    t_lo = fmaf(w_lo[3], xa.w, t_lo);
+                    float t_hi = w_hi[0] * xc.x;
+                    t_hi = fmaf(w_hi[1], xc.y, t_hi);
+                    t_hi = fmaf(w_hi[2], xc.z, t_hi);
+                    t_hi = fmaf(w_hi[3], xc.w, t_hi);
+                    acc[b] = fmaf(s_lo, t_lo, fmaf(s_hi, t_hi, acc[b]));
+                }
             }
         }
-    }
 #pragma unroll
-    for (int b = 0; b < kMaxB; ++b) {
-        if (b >= B) break;
+        for (int b = 0; b < BMAX; ++b) {
+            if (b >= B) break;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], o);
-        if (lane == 0) part[warp][b] = acc[b];
-    }
-    __syncthreads();
-    if (static_cast<int>(threadIdx.x) < rows_per_cta * B) {
-        const int rr = threadIdx.x / B, b = threadIdx.x - rr * B;
-        const int r = blockIdx.x * rows_per_cta + rr;
-        if (r < N) {
-            float s = part[rr * wpr][b];
-            for (int q = 1; q < wpr; ++q) s += part[rr * wpr + q][b];
-            y[static_cast<size_t>(b) * N + r] = s;
+            for (int o = 16; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], o);
+            if (lane == 0) part[warp][b] = acc[b];
         }
+        __syncthreads();
+        if (static_cast<int>(threadIdx.x) < rows_per_cta * B) {
+            const int rr = threadIdx.x / B, b = threadIdx.x - rr * B;
+            const int r = grp * rows_per_cta + rr;
+            if (r < N) {
+                float sum = part[rr * wpr][b];
+                for (int q = 1; q < wpr; ++q) sum += part[rr * wpr + q][b];
+                y[static_cast<size_t>(b) * N + r] = sum;
+            }
+        }
+        __syncthreads();   // part[] is rewritten by the next group
     }
 }
 
@@ -120,6 +142,26 @@ static int q6k_warps_per_row(int64_t N, int nb, int sms)
     int wpr = 1;
     while (wpr < 8 && wpr * 2 <= nb && static_cast<long long>(N) * wpr < want) wpr *= 2;
     return wpr;
+}
+
+// Persistent grid: as many CTAs as fit on the GPU at once (occupancy for this
+// shared-memory size), at most one per row group.
+template <int BMAX, bool XS>
+static cudaError_t q6k_launch(const uint8_t *W, const float *x, float *y, int N, int nb, int B, int wpr, int groups,
+                              int sms, size_t smem, cudaStream_t s)
+{
+    auto kern = q6::q6k_gemv_kernel<BMAX, XS>;
+    cudaError_t e;
+    if (XS) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, q6::kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = static_cast<int>(std::min<long long>(groups, static_cast<long long>(sms) * std::max(occ, 1)));
+    kern<<<grid, q6::kThreads, smem, s>>>(W, x, y, N, nb, B, wpr, groups);
+    return cudaGetLastError();
 }
 
 q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream)
@@ -136,12 +178,31 @@ q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int
     const int nb = static_cast<int>(K / 256);
     const int wpr = q6k_warps_per_row(N, nb, sms);
     const int rows_per_cta = q6::kWarps / wpr;
-    const long long grid = (N + rows_per_cta - 1) / rows_per_cta;
-    if (grid > 0x7FFFFFFFll) return Q4K_ERR_INVALID_ARG;
-    q6::q6k_gemv_kernel<<<static_cast<unsigned>(grid), q6::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint8_t *>(W), x, y, static_cast<int>(N), nb, batch, wpr);
-    const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
+    const long long groups = (N + rows_per_cta - 1) / rows_per_cta;
+    // x staged in shared memory when it is small enough to leave room for six
+    // or more CTAs per SM (a larger x there cost more in latency hiding than
+    // it saved in loads: measured); persistent CTAs then load it once each
+    const size_t xbytes = static_cast<size_t>(batch) * static_cast<size_t>(K) * 4;
+    const bool xs = xbytes <= 32 * 1024;
+    if (groups > 0x7FFFFFFFll) return Q4K_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const uint8_t *Wb = static_cast<const uint8_t *>(W);
+    const int n = static_cast<int>(N), g = static_cast<int>(groups), gr = sms;
+    cudaError_t e;
+    if (batch == 1)
+        e = xs ? q6k_launch<1, true>(Wb, x, y, n, nb, batch, wpr, g, gr, xbytes, s)
+               : q6k_launch<1, false>(Wb, x, y, n, nb, batch, wpr, g, gr, 0, s);
+    else if (batch <= 4)
+        e = xs ? q6k_launch<4, true>(Wb, x, y, n, nb, batch, wpr, g, gr, xbytes, s)
+               : q6k_launch<4, false>(Wb, x, y, n, nb, batch, wpr, g, gr, 0, s);
+    else
+        e = xs ? q6k_launch<16, true>(Wb, x, y, n, nb, batch, wpr, g, gr, xbytes, s)
+               : q6k_launch<16, false>(Wb, x, y, n, nb, batch, wpr, g, gr, 0, s);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return Q4K_ERR_CUDA;
+    }
+    return Q4K_OK;
 }
 
 }  // namespace q4k
