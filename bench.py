@@ -15,7 +15,7 @@ the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-`--impl reference` times the CPU oracle (the reference arm of this build) on a
+`--impl reference` times the CPU oracle (the reference arm) on a
 bounded sample of the same workload and prints the same kind of line.
 """
 from __future__ import annotations
