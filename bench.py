@@ -580,7 +580,7 @@ def run_ours(args):
 
 def run_profile_case(spec: str, iters: int):
     """One op repeated `iters` times on seeded inputs, for ncu captures.
-    spec = gemv:N:K:B | argmax:N:K:B | prefill:N:K:T"""
+    spec = gemv:N:K:B | argmax:N:K:B | prefill:N:K:T | q6k:N:K:B"""
     import numpy as np
     import torch
 
@@ -623,6 +623,16 @@ def run_profile_case(spec: str, iters: int):
         return
     kind, N, K, B = spec.split(":")
     N, K, B = int(N), int(K), int(B)
+    if kind == "q6k":
+        # q6k:N:K:B -- the Q6_K GEMV
+        W6 = torch.from_numpy(synth.q6k_weights(N, K, (9, N, K))).cuda()
+        x = torch.from_numpy(synth.normal_f32((B, K), (9, B))).cuda()
+        y = torch.empty((B, N), dtype=torch.float32, device="cuda")
+        for _ in range(iters):
+            q4k.q6k_gemv(W6, x, y)
+        torch.cuda.synchronize()
+        print(f"profile case {spec} x{iters} done")
+        return
     W = torch.from_numpy(synth.q4k_weights(N, K, (9, N, K))).cuda()
     if kind == "prefill":
         X = torch.from_numpy(synth.normal_bf16_bits((B, K), (9, B)).view(np.int16)).cuda().view(torch.bfloat16)
@@ -650,7 +660,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
-    ap.add_argument("--profile-case", default=None, help="gemv:N:K:B | argmax:N:K:B | prefill:N:K:T | decode:L:B | chain:L:B (ncu helper)")
+    ap.add_argument("--profile-case", default=None, help="gemv:N:K:B | argmax:N:K:B | prefill:N:K:T | q6k:N:K:B | decode:L:B | chain:L:B (ncu helper)")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:
