@@ -17,6 +17,9 @@
  *   - q4k_gemm_prefill the prefill product with bf16 activations ("cuBLAS HGEMM
  *                      for prefill", dotLLM README, News 2026-03), here on the
  *                      tcgen05 tensor cores after a dequantize-to-bf16 step.
+ *   - q6k_gemv         y = W x for a Q6_K matrix, the other block format of
+ *                      Q4_K_M files ("custom quantized GEMV for decode (Q8_0,
+ *                      Q4_K, Q6_K)", same page and item).
  *
  * ---------------------------------------------------------------------------
  * Q4_K super-block (144 bytes, 256 weights, 4.5 bits per weight)
