@@ -303,7 +303,7 @@ q4k_status q4k_gemv_plan(int64_t N, int64_t K, int batch, int out[4]);
 
 /* Sticky device-side error bits of the library's kernels, read synchronously
  * from the current device: bit 0 = a bounded wait inside a GEMV/argmax kernel
- * timed out, bit 1 = the same in the prefill kernel; the kernel then wound down
+ * (Q4_K or Q6_K) timed out, bit 1 = the same in the prefill kernel; the kernel then wound down
  * early and its outputs are invalid.  0 = no error. */
 unsigned int q4k_device_error_flags(void);
 

@@ -83,6 +83,9 @@ q4k_status q4k_gemv_plan(int64_t N, int64_t K, int batch, int out[4])
 
 /* Sticky device-side error bits (bit 0: a bounded wait inside a kernel timed
  * out and the kernel wound down early).  Synchronous; 0 means no error. */
-unsigned int q4k_device_error_flags(void) { return q4k::read_device_error() | q4k::read_prefill_error(); }
+unsigned int q4k_device_error_flags(void)
+{
+    return q4k::read_device_error() | q4k::read_prefill_error() | q4k::read_q6k_error();
+}
 
 }  // extern "C"

@@ -28,6 +28,7 @@ q4k_status chain_run_impl(const q4k_chain *chain, void *stream);
 q4k_status chain_destroy_impl(q4k_chain *chain);
 unsigned int read_device_error();
 unsigned int read_prefill_error();
+unsigned int read_q6k_error();
 // cuTensorMapEncodeTiled from the CUDA driver API (null if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 

@@ -22,6 +22,7 @@
 #include <algorithm>
 #include <cstdint>
 
+#include "ptx.cuh"
 #include "q4k_internal.h"
 
 namespace q4k {
@@ -46,8 +47,8 @@ __device__ __forceinline__ uint32_t ld_u16(const uint8_t *p)   // 2-byte aligned
 // from global memory (L1).
 template <int BMAX, bool XS>
 __global__ void __launch_bounds__(kThreads) q6k_gemv_kernel(const uint8_t *__restrict__ W, const float *__restrict__ x,
-                                                           float *__restrict__ y, int N, int nb, int B, int wpr,
-                                                           int groups)
+                                                           float *__restrict__ y, int N, int ldy, int nb, int B,
+                                                           int wpr, int groups)
 {
     extern __shared__ __align__(16) float xs[];
     __shared__ float part[kWarps][RPW][BMAX];
@@ -147,10 +148,151 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_kernel(const uint8_t *__res
             if (row < N) {
                 float sum = part[wr * wpr][r][b];
                 for (int q = 1; q < wpr; ++q) sum += part[wr * wpr + q][r][b];
-                y[static_cast<size_t>(b) * N + row] = sum;
+                y[static_cast<size_t>(b) * ldy + row] = sum;
             }
         }
         __syncthreads();   // part[] is rewritten by the next group
+    }
+}
+
+
+// ---------------------------------------------------------------------------
+// Staged variant for rows of up to kStageMax / 8 bytes: 8 consecutive rows are
+// one contiguous byte range starting on a 16-byte boundary (8 x an even row
+// length), so one bulk async copy fills a ring stage with a whole tile of 8
+// rows; warp w decodes row w of the tile from shared memory (16-bit loads at
+// low latency instead of global ones).  Persistent CTAs over the full tiles;
+// the last warp to finish a stage issues the tile kStages ahead into it.  Every
+// wait is bounded: on a timeout the CTA flags g_q6k_error, keeps walking its
+// schedule without waiting, and waits (bounded) for its copies in flight
+// before it exits.
+// ---------------------------------------------------------------------------
+constexpr int kStages = 4;
+constexpr int kStageMax = 32 * 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+__device__ unsigned int g_q6k_error = 0;   // bit 0: a bounded wait of the staged kernel timed out
+
+__device__ __forceinline__ uint32_t lds_u16(const uint8_t *p) { return *reinterpret_cast<const unsigned short *>(p); }
+
+template <int BMAX>
+__global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__restrict__ W, const float *__restrict__ x,
+                                                           float *__restrict__ y, int N, int nb, int B, int tiles)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full[kStages];
+    __shared__ int s_done[kStages];
+    __shared__ int s_abort;
+    __shared__ int s_issued;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int K = nb * 256;
+    const int RB = nb * kBytes;                 // row bytes
+    const int stage_bytes = 8 * RB;             // a multiple of 16
+    float *xs = reinterpret_cast<float *>(smem + kStages * stage_bytes);
+    const int my_tiles = (tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                         static_cast<int>(gridDim.x);
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int i) {   // tile i of this CTA's schedule into slot i % kStages
+        const int slot = i % kStages;
+        const size_t tile = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(i) * gridDim.x;
+        mbar_arrive_expect_tx(smem_u32(&full[slot]), static_cast<uint32_t>(stage_bytes));
+        bulk_g2s(smem_u32(smem + slot * stage_bytes), W + tile * stage_bytes, static_cast<uint32_t>(stage_bytes),
+                 smem_u32(&full[slot]), policy);
+    };
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            s_done[i] = 0;
+        }
+        s_abort = 0;
+        fence_barrier_init();
+        const int first = min(kStages, my_tiles);
+        for (int i = 0; i < first; ++i) issue(i);
+        s_issued = first;
+    }
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(x);
+        float4 *dst = reinterpret_cast<float4 *>(xs);
+        for (int i = tid; i < B * K / 4; i += kThreads) dst[i] = __ldg(src + i);
+    }
+    __syncthreads();
+    const int h = lane >> 4, c1 = (lane >> 3) & 1, l0 = 4 * (lane & 7);
+    const int ql_off = 4 * lane;
+    const int qh_off = 128 + 32 * h + l0;
+    const int sc_off = 192 + 8 * h + 2 * c1 + (l0 >> 4);
+    const int k_lo = 128 * h + 32 * c1 + l0;
+    for (int i = 0; i < my_tiles; ++i) {
+        const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+        const int slot = i % kStages;
+        const uint32_t phase = static_cast<uint32_t>((i / kStages) & 1);
+        if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), phase, kWaitLimitNs)) {
+            atomicOr(&g_q6k_error, 1u);
+            s_abort = 1;
+        }
+        const uint8_t *rowp = smem + slot * stage_bytes + warp * RB;
+        float acc[BMAX];
+#pragma unroll
+        for (int b = 0; b < BMAX; ++b) acc[b] = 0.f;
+        for (int blk = 0; blk < nb; ++blk) {
+            const uint8_t *A = rowp + blk * kBytes;
+            const uint32_t ql = lds_u16(A + ql_off) | (lds_u16(A + ql_off + 2) << 16);
+            const uint32_t qh = lds_u16(A + qh_off) | (lds_u16(A + qh_off + 2) << 16);
+            const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(lds_u16(A + 208))));
+            const float s_lo = d * static_cast<float>(static_cast<int8_t>(A[sc_off]));
+            const float s_hi = d * static_cast<float>(static_cast<int8_t>(A[sc_off + 4]));
+            const uint32_t q_lo = (ql & 0x0F0F0F0Fu) | (((qh >> (2 * c1)) & 0x03030303u) << 4);
+            const uint32_t q_hi = ((ql >> 4) & 0x0F0F0F0Fu) | (((qh >> (2 * c1 + 4)) & 0x03030303u) << 4);
+            float w_lo[4], w_hi[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {   // 2^23 + q - (2^23 + 32) = q - 32, exact
+                w_lo[j] = __uint_as_float(__byte_perm(q_lo, 0x4B000000u, 0x7440u | j)) - 8388640.0f;
+                w_hi[j] = __uint_as_float(__byte_perm(q_hi, 0x4B000000u, 0x7440u | j)) - 8388640.0f;
+            }
+            const float *xb = xs + blk * 256 + k_lo;
+#pragma unroll
+            for (int b = 0; b < BMAX; ++b) {
+                if (b >= B) break;
+                const float4 xa = *reinterpret_cast<const float4 *>(xb + b * K);
+                const float4 xc = *reinterpret_cast<const float4 *>(xb + b * K + 64);
+                float t_lo = w_lo[0] * xa.x;
+                t_lo = fmaf(w_lo[1], xa.y, t_lo);
+                t_lo = fmaf(w_lo[2], xa.z, t_lo);
+                t_lo = fmaf(w_lo[3], xa.w, t_lo);
+                float t_hi = w_hi[0] * xc.x;
+                t_hi = fmaf(w_hi[1], xc.y, t_hi);
+                t_hi = fmaf(w_hi[2], xc.z, t_hi);
+                t_hi = fmaf(w_hi[3], xc.w, t_hi);
+                acc[b] = fmaf(s_lo, t_lo, fmaf(s_hi, t_hi, acc[b]));
+            }
+        }
+        // this warp is done with the slot: the last warp to finish refills it
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            const int prev = atomicAdd(&s_done[slot], 1);
+            if (prev % kWarps == kWarps - 1) {
+                const int next = i + kStages;
+                if (next < my_tiles && !*(volatile int *)&s_abort) {
+                    issue(next);
+                    atomicAdd(&s_issued, 1);
+                }
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < BMAX; ++b) {
+            if (b >= B) break;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], o);
+            if (lane == 0 && !*(volatile int *)&s_abort) y[static_cast<size_t>(b) * N + tile * 8 + warp] = acc[b];
+        }
+    }
+    // After a timed-out wait, wait (bounded) for the copies issued but not
+    // consumed, so that none lands after the CTA has exited.
+    __syncthreads();
+    if (*(volatile int *)&s_abort && tid == 0) {
+        for (int i = max(0, s_issued - kStages); i < s_issued; ++i)
+            if (!mbar_wait_bounded(smem_u32(&full[i % kStages]), static_cast<uint32_t>((i / kStages) & 1), kWaitLimitNs))
+                break;
     }
 }
 
@@ -169,8 +311,8 @@ static int q6k_warps_per_row(int64_t N, int nb, int sms)
 // Persistent grid: as many CTAs as fit on the GPU at once (occupancy for this
 // shared-memory size), at most one per row group.
 template <int BMAX, bool XS>
-static cudaError_t q6k_launch(const uint8_t *W, const float *x, float *y, int N, int nb, int B, int wpr, int groups,
-                              int sms, size_t smem, cudaStream_t s)
+static cudaError_t q6k_launch(const uint8_t *W, const float *x, float *y, int N, int ldy, int nb, int B, int wpr,
+                              int groups, int sms, size_t smem, cudaStream_t s)
 {
     auto kern = q6::q6k_gemv_kernel<BMAX, XS>;
     cudaError_t e;
@@ -182,8 +324,52 @@ static cudaError_t q6k_launch(const uint8_t *W, const float *x, float *y, int N,
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, q6::kThreads, smem);
     if (e != cudaSuccess) return e;
     const int grid = static_cast<int>(std::min<long long>(groups, static_cast<long long>(sms) * std::max(occ, 1)));
-    kern<<<grid, q6::kThreads, smem, s>>>(W, x, y, N, nb, B, wpr, groups);
+    kern<<<grid, q6::kThreads, smem, s>>>(W, x, y, N, ldy, nb, B, wpr, groups);
     return cudaGetLastError();
+}
+
+template <int BMAX>
+static cudaError_t q6k_launch_staged(const uint8_t *W, const float *x, float *y, int N, int nb, int B, int tiles,
+                                     int sms, size_t smem, cudaStream_t s)
+{
+    auto kern = q6::q6k_gemv_staged<BMAX>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, q6::kThreads, smem);
+    if (e != cudaSuccess) return e;
+    const int grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(sms) * std::max(occ, 1)));
+    kern<<<grid, q6::kThreads, smem, s>>>(W, x, y, N, nb, B, tiles);
+    return cudaGetLastError();
+}
+
+// The direct kernel on rows [0, N) of W, output rows with stride ldy.
+static cudaError_t q6k_direct(const uint8_t *W, const float *x, float *y, int N, int ldy, int nb, int batch, int sms,
+                              cudaStream_t s)
+{
+    const int wpr = q6k_warps_per_row(N, nb, sms);
+    const int rows_per_cta = q6::RPW * (q6::kWarps / wpr);
+    const int groups = (N + rows_per_cta - 1) / rows_per_cta;
+    // x staged in shared memory when it is small enough to leave room for six
+    // or more CTAs per SM (a larger x there cost more in latency hiding than
+    // it saved in loads: measured); persistent CTAs then load it once each
+    const size_t xbytes = static_cast<size_t>(batch) * static_cast<size_t>(nb) * 256 * 4;
+    const bool xs = xbytes <= 32 * 1024;
+    if (batch == 1)
+        return xs ? q6k_launch<1, true>(W, x, y, N, ldy, nb, batch, wpr, groups, sms, xbytes, s)
+                  : q6k_launch<1, false>(W, x, y, N, ldy, nb, batch, wpr, groups, sms, 0, s);
+    if (batch <= 4)
+        return xs ? q6k_launch<4, true>(W, x, y, N, ldy, nb, batch, wpr, groups, sms, xbytes, s)
+                  : q6k_launch<4, false>(W, x, y, N, ldy, nb, batch, wpr, groups, sms, 0, s);
+    return xs ? q6k_launch<16, true>(W, x, y, N, ldy, nb, batch, wpr, groups, sms, xbytes, s)
+              : q6k_launch<16, false>(W, x, y, N, ldy, nb, batch, wpr, groups, sms, 0, s);
+}
+
+unsigned int read_q6k_error()
+{
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, q6::g_q6k_error, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+    return v;
 }
 
 q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream)
@@ -198,28 +384,32 @@ q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int
     if (st != Q4K_OK) return st;
     if (N == 0) return Q4K_OK;
     const int nb = static_cast<int>(K / 256);
-    const int wpr = q6k_warps_per_row(N, nb, sms);
-    const int rows_per_cta = q6::RPW * (q6::kWarps / wpr);
-    const long long groups = (N + rows_per_cta - 1) / rows_per_cta;
-    // x staged in shared memory when it is small enough to leave room for six
-    // or more CTAs per SM (a larger x there cost more in latency hiding than
-    // it saved in loads: measured); persistent CTAs then load it once each
-    const size_t xbytes = static_cast<size_t>(batch) * static_cast<size_t>(K) * 4;
-    const bool xs = xbytes <= 32 * 1024;
-    if (groups > 0x7FFFFFFFll) return Q4K_ERR_INVALID_ARG;
+    const int n = static_cast<int>(N);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint8_t *Wb = static_cast<const uint8_t *>(W);
-    const int n = static_cast<int>(N), g = static_cast<int>(groups), gr = sms;
-    cudaError_t e;
-    if (batch == 1)
-        e = xs ? q6k_launch<1, true>(Wb, x, y, n, nb, batch, wpr, g, gr, xbytes, s)
-               : q6k_launch<1, false>(Wb, x, y, n, nb, batch, wpr, g, gr, 0, s);
-    else if (batch <= 4)
-        e = xs ? q6k_launch<4, true>(Wb, x, y, n, nb, batch, wpr, g, gr, xbytes, s)
-               : q6k_launch<4, false>(Wb, x, y, n, nb, batch, wpr, g, gr, 0, s);
-    else
-        e = xs ? q6k_launch<16, true>(Wb, x, y, n, nb, batch, wpr, g, gr, xbytes, s)
-               : q6k_launch<16, false>(Wb, x, y, n, nb, batch, wpr, g, gr, 0, s);
+    cudaError_t e = cudaSuccess;
+    // Staged path: whole tiles of 8 rows (8 x row bytes <= 32 KB, a multiple of
+    // 16 starting on a 16-byte boundary), x in shared memory beside the ring,
+    // when ring and x still leave room for two CTAs per SM (with one, the batch-5
+    // LM head ran 1.5x slower than the direct kernel: measured); the remaining
+    // N % 8 rows go to the direct kernel.
+    const long long stage_bytes = 8ll * nb * q6::kBytes;
+    const size_t smem_staged = static_cast<size_t>(q6::kStages * stage_bytes) +
+                               static_cast<size_t>(batch) * static_cast<size_t>(K) * 4;
+    const int tiles = n / 8;
+    if (stage_bytes <= q6::kStageMax && smem_staged <= 110 * 1024 && tiles > 0) {
+        if (batch == 1)
+            e = q6k_launch_staged<1>(Wb, x, y, n, nb, batch, tiles, sms, smem_staged, s);
+        else if (batch <= 4)
+            e = q6k_launch_staged<4>(Wb, x, y, n, nb, batch, tiles, sms, smem_staged, s);
+        else
+            e = q6k_launch_staged<16>(Wb, x, y, n, nb, batch, tiles, sms, smem_staged, s);
+        const int done = tiles * 8;
+        if (e == cudaSuccess && done < n)
+            e = q6k_direct(Wb + static_cast<size_t>(done) * nb * q6::kBytes, x, y + done, n - done, n, nb, batch, sms, s);
+    } else {
+        e = q6k_direct(Wb, x, y, n, n, nb, batch, sms, s);
+    }
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return Q4K_ERR_CUDA;

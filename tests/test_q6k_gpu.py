@@ -30,9 +30,11 @@ def _run(q4k, W, x):
     return y.cpu().numpy()
 
 
-# (N, K, B): ragged row counts, every warps-per-row choice (few rows -> up to 8 warps per row)
+# (N, K, B): ragged row counts, every warps-per-row choice (few rows -> up to 8 warps per row), the
+# staged path (whole 8-row tiles through shared memory) at batch bounds 1 / 4 / 16 with and without a
+# remainder of rows for the direct kernel, and shapes that only take the direct kernel
 SHAPES = [(1, 256, 1), (7, 512, 2), (129, 3584, 1), (300, 4096, 5), (512, 3584, 1), (1000, 2048, 16),
-          (65, 18944, 3), (3584, 3584, 1), (37, 768, 9)]
+          (65, 18944, 3), (3584, 3584, 1), (37, 768, 9), (64, 1024, 3), (29, 2560, 4)]
 
 
 @pytest.mark.parametrize("N,K,B", SHAPES)
