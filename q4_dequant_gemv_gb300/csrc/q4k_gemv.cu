@@ -12,28 +12,32 @@
 //
 // Design (GB300-first; the pages' own kernels were HLSL Wave32 shaders and
 // sm_75..sm_90 cubins):
-//   * Weights are streamed HBM -> shared memory with 1-D TMA bulk copies
-//     (cp.async.bulk) by one producer warp per CTA into a ring of stages
-//     guarded by mbarriers; the consumers never issue global loads for W.
-//   * The inner product runs on the tensor cores with mma.sync m16n8k16:
-//     A = the weights' q*sc_j as exact fp16 integers (<= 945), built in
-//     registers from the nibbles with one LOP3 (magic-exponent trick) and one
-//     HFMA2 per two weights; B = the activations split into fp16 hi + lo parts
-//     (x = hi + lo to ~2^-22 relative), one column each, so the fp32
-//     accumulation sees x at nearly full fp32 precision.  Column pairs hold
-//     batch rows (up to 4 per n8 tile).  The dmin*m_j term is one extra k16
-//     step per super-block whose A holds m_j and whose B holds the per
-//     sub-block sums of x (again hi + lo).  Per super-block the two fp32 tiles
-//     are combined as d*C - dmin*Cmin.
-//   * x is rescaled by a power of two per chunk and batch row before the fp16
-//     split (so any finite fp32 x works); the scale is undone in the fp32
-//     epilogue.
-//   * Row tiles of 64 rows (4 consumer warps x 16 rows).  When there are too
-//     few row tiles to fill the GPU the K range of a tile is split over the
-//     CTAs of a thread-block cluster, and the partial sums are added in rank
-//     order through distributed shared memory (deterministic, no atomics, no
-//     global scratch).  With a single K slice the grid is persistent and CTAs
-//     loop over row tiles, so the weight stream never drains between tiles.
+//   * Weights are streamed HBM -> shared memory with 2-D TMA tensor copies (one
+//     super-block of all 128 rows of a tile per stage) into a 4-stage ring
+//     guarded by mbarriers.  There is no producer warp: thread 0 issues the
+//     first stages before the dependency wait, and the last warp to finish a
+//     stage issues the one four ahead into it; the consumers never issue
+//     global loads for W.
+//   * Batch 1 (default): an integer inner product.  Each super-block of x is
+//     carried as two int8 parts per element against its own max|x|, the
+//     weight nibbles multiply them with dp4a, the sub-block sums are exact in
+//     int32, and the scales are applied once per super-block in fp32.
+//   * Batch >= 2 (and batch 1 on request): the tensor cores with mma.sync
+//     m16n8k16.  A = the weights' q*sc_j as exact fp16 integers (<= 945),
+//     built in registers from the nibbles with one LOP3 (magic-exponent trick)
+//     and one HFMA2 per two weights; B = the activations split into fp16 hi +
+//     lo parts (x = hi + lo to ~2^-22 relative after a power-of-two scale per
+//     super-block and batch row), one column each; column pairs hold batch
+//     rows (up to 4 per n8 tile).  The dmin*m_j term is one extra k16 step per
+//     super-block whose A holds m_j and whose B holds the per sub-block sums
+//     of x; per super-block the two fp32 tiles are combined as d*C - dmin*Cmin.
+//   * Row tiles of 128 rows (8 warps x 16 rows), two CTAs per SM.  When there
+//     are too few row tiles to fill the GPU the K range of a tile is split
+//     over the CTAs of a thread-block cluster (up to 16), and the partial sums
+//     are added in rank order through distributed shared memory
+//     (deterministic, no atomics, no global scratch).  With a single K slice
+//     the grid is persistent and CTAs loop over row tiles, so the weight
+//     stream never drains between tiles.
 //   * The argmax variant keeps per-CTA (max, lowest index) keys in shared
 //     memory and combines CTAs with one 64-bit atomicMax per batch row plus a
 //     last-CTA ticket (no spin-waits).
