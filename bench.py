@@ -550,6 +550,9 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms1, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "arithmetic": "batch 1: x as two int8 parts per super-block, dp4a with the 4-bit weights into int32 "
+                      "per sub-block, scales and accumulation in fp32; batch >= 2: fp16 hi+lo x and exact fp16 "
+                      "weights on mma.sync, fp32 accumulation",
         "config": {"workload": "qwen2.5-7b-shaped decode: 28 layers x 7 Q4_K GEMVs (q,k,v,o 3584x3584/512x3584, "
                                "gate/up 18944x3584, down 3584x18944), batch 1",
                    "batch": 1, "layers": LAYERS, "weight_bytes_per_step": LAYERS * sum(N * (K // 256) * 144 for _, N, K in shapes),
