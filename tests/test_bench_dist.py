@@ -59,3 +59,23 @@ def test_reference_arm_prints_json_line():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_traffic_record_follows_code_not_comments(tmp_path, monkeypatch):
+    """The recorded DRAM traffic is reported only while the GEMV kernel's code
+    matches the capture: comment or whitespace edits keep the hash, a code edit
+    changes it."""
+    import shutil
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = tmp_path / "q4_dequant_gemv_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for f in ("q4k_gemv.cu", "ptx.cuh"):
+        shutil.copy(os.path.join(ROOT, "q4_dequant_gemv_gb300", "csrc", f), csrc / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.kernel_source_hash()
+    src = (csrc / "q4k_gemv.cu").read_text()
+    (csrc / "q4k_gemv.cu").write_text("// a new comment line\n" + src.replace("namespace q4k {", "namespace  q4k  {  /* c */"))
+    assert bench.kernel_source_hash() == h0
+    (csrc / "q4k_gemv.cu").write_text(src.replace("constexpr int kStages = 4;", "constexpr int kStages = 5;"))
+    assert bench.kernel_source_hash() != h0
