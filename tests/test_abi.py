@@ -176,3 +176,32 @@ def test_split_receive_slots_fit():
             rows = (rank + 1) * k_rows // split - rank * k_rows // split
             top = max(top, (split - 1) * rows + rows - 1)
         assert top < buf_rows, (split, top)
+
+
+def test_q6k_host_validation(q4k):
+    """q6k_gemv argument errors come back before any device call."""
+    ok = 0x10000
+    q6 = lambda W, x, y, N, K, B: q4k.raw_call("q6k_gemv", P(W), P(x), P(y), N, K, B, P(0))
+    assert q6(0, ok, ok, 64, 256, 1) == 1
+    assert q6(ok, 0, ok, 64, 256, 1) == 1
+    assert q6(ok, ok, 0, 64, 256, 1) == 1
+    assert q6(ok, ok, ok, 64, 300, 1) == 1
+    assert q6(ok, ok, ok, -1, 256, 1) == 1
+    assert q6(ok, ok, ok, 64, 256, 0) == 1
+    assert q6(ok, ok, ok, 64, 256, 17) == 1
+    assert q6(ok + 2, ok, ok, 64, 256, 1) == 2
+    assert q6(ok, ok + 4, ok, 64, 256, 1) == 2
+    assert q6(0, ok, 0, 0, 256, 1) in (0, 3, 4)      # N == 0: no weight or output pointer needed
+
+
+def test_binding_refuses_host_tensors(q4k):
+    """The Python entry points take device tensors only: host tensors raise
+    before anything is computed (there is no CPU path)."""
+    import torch
+    W = torch.zeros((4, 144), dtype=torch.uint8)
+    x = torch.zeros((1, 256), dtype=torch.float32)
+    for call in (lambda: q4k.gemv(W, x), lambda: q4k.gemv_argmax(W, x),
+                 lambda: q4k.q6k_gemv(torch.zeros((4, 210), dtype=torch.uint8), x),
+                 lambda: q4k.gemm_prefill(W, torch.zeros((32, 256), dtype=torch.bfloat16))):
+        with pytest.raises((ValueError, TypeError, RuntimeError)):
+            call()
