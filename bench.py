@@ -162,6 +162,63 @@ def oracle_sample(seconds_target: float = 8.0):
                       f"single_thread_value: one pass on one thread ({dt1:.1f} s)"}
 
 
+def _best_and_cv(fn, min_reps=3, max_s=3.0):
+    """Best-of-N wall time of fn() with its coefficient of variation (the
+    dotLLM README's benchmark method: best of several runs, CV reported)."""
+    import numpy as np
+    ts, t_all = [], time.perf_counter()
+    while len(ts) < min_reps or (time.perf_counter() - t_all < max_s and len(ts) < 50):
+        t0 = time.perf_counter()
+        fn()
+        ts.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_all > 4 * max_s:
+            break
+    return min(ts), float(np.std(ts) / np.mean(ts)), len(ts)
+
+
+def oracle_configs():
+    """The CPU oracle (fp64, OpenMP over rows on all host cores) on the other
+    configurations: the single 4096 x 4096 GEMV and the LM head + argmax in
+    full, the batch-5 VerifyBatch pass over layer 0 (the 28-layer step time
+    extrapolated from it), and the four Llama-3-8B prefill shapes at T = 32
+    and T = 512 in full."""
+    import oracle
+    import synth
+    oracle.build()
+    th = oracle.max_threads()
+    out = {"cores": th}
+    W0 = synth.q4k_weights(4096, 4096, (0, 0))
+    x0 = synth.normal_f32((1, 4096), (0, 1))
+    best, cv, n = _best_and_cv(lambda: oracle.gemv(W0, x0, 4096, 4096, threads=th))
+    b0 = 4096 * 16 * 144 + 4 * 4096 * 2
+    out["single_gemv_4096x4096_b1"] = {"ms_best": best * 1e3, "cv": cv, "reps": n, "gbs": b0 / best / 1e9}
+    layer = synth.qwen_layer_weights(0)
+    xs5 = {K: synth.normal_f32((5, K), (0, 9, K, 5)) for K in {k for _, _, k, _ in layer}}
+    best, cv, n = _best_and_cv(lambda: [oracle.gemv(W, xs5[K], N, K, threads=th) for _, N, K, W in layer])
+    b5 = sum(N * (K // 256) * 144 + 4 * 5 * K + 4 * 5 * N for _, N, K, _ in layer)
+    out["verify_batch5_layer0"] = {"ms_best": best * 1e3, "cv": cv, "reps": n, "gbs": b5 / best / 1e9,
+                                   "ms_per_step_28_layers_extrapolated": best * 1e3 * LAYERS}
+    del layer, xs5
+    Nv, Kv = 152064, 3584
+    Wl = synth.q4k_weights(Nv, Kv, (3, 0))
+    xl = synth.normal_f32((1, Kv), (3, 2))
+    best, cv, n = _best_and_cv(lambda: oracle.argmax(oracle.gemv(Wl, xl, Nv, Kv, threads=th)[0]))
+    out["lm_head_argmax_b1"] = {"ms_best": best * 1e3, "cv": cv, "reps": n,
+                                "gbs": (Nv * (Kv // 256) * 144 + 4 * Kv + 4) / best / 1e9}
+    del Wl
+    pf = {}
+    for name, N, K in synth.llama3_8b_prefill_shapes():
+        Wp = synth.q4k_weights(N, K, (4, N, K))
+        for T in (32, 512):
+            X = synth.normal_bf16_bits((T, K), (4, T, K))
+            best, cv, n = _best_and_cv(lambda: oracle.prefill(Wp, X, N, K, threads=th),
+                                       min_reps=1 if T == 512 else 3, max_s=0.5 if T == 512 else 2.0)
+            pf[f"{name}_{N}x{K}_T{T}"] = {"ms_best": best * 1e3, "cv": cv, "reps": n,
+                                          "gflops": 2.0 * N * K * T / best / 1e9}
+    out["prefill"] = pf
+    return out
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -351,6 +408,48 @@ def run_ours(args):
     bytes1 = step_bytes(1)
     value = whole_job_rate(bytes1, world, ms1 * 1e-3) / 1e9
 
+    # ---- time per kind of launch: the 28 launches of one kind (q/k/v, o,
+    # gate/up, down) replayed alone in a graph with PDL, per launch, beside the
+    # time its bytes take at the peak of record
+    def kind_step(kind, B=1):
+        for layer in range(LAYERS):
+            W, y = Ws[layer], (lambda mi: y_view(B, layer, mi))
+            if kind == "qkv":
+                q4k.gemv_grouped(W[0:3], x_view(B, layer, "attn"), [y(0), y(1), y(2)], stream=stream, pdl=True)
+            elif kind == "o":
+                q4k.gemv(W[3], x_view(B, layer, "o"), y(3), stream=stream, pdl=True)
+            elif kind == "gate_up":
+                q4k.gemv_grouped(W[4:6], x_view(B, layer, "mlp"), [y(4), y(5)], stream=stream, pdl=True)
+            else:
+                q4k.gemv(W[6], x_view(B, layer, "down"), y(6), stream=stream, pdl=True)
+    kind_mats = {"qkv": (0, 1, 2), "o": (3,), "gate_up": (4, 5), "down": (6,)}
+    kinds_us = {}
+    for kind, mats in kind_mats.items():
+        gk = capture(lambda k=kind: kind_step(k))
+        msk = time_graph(gk, max(20, args.steps // 4), args.warmup)
+        del gk
+        kb = sum(shapes[m][1] * (shapes[m][2] // 256) * 144 + 4 * shapes[m][2] + 4 * shapes[m][1] for m in mats)
+        kinds_us[kind] = {"us_per_launch": msk * 1e3 / LAYERS, "bytes_per_launch": kb,
+                          "us_at_peak": kb / (pk["hbm_gbs"] * 1e9) * 1e6}
+
+    # ---- read-only streaming probe (the ceiling a weight stream can reach on
+    # this GPU; a copy's read+write rate, the peak of record, is lower)
+    probe_buf = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        pbest, pbytes = None, 0
+        for _ in range(6):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            pbytes = q4k.stream_read(probe_buf, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            t = e0.elapsed_time(e1)
+            pbest = t if pbest is None else min(pbest, t)
+    del probe_buf
+    read_probe = {"gbs": pbytes / (pbest * 1e-3) / 1e9, "bytes": pbytes, "best_of": 6,
+                  "kernel": "q4k_stream_read (one CTA per SM, 32 KB bulk copies, 4-deep ring)"}
+
     # ---- the same step with one launch per matrix (196 launches), for contrast
     g1u = capture(lambda: decode_step(1, fused=False))
     ms1u = time_graph(g1u, max(20, args.steps // 4), args.warmup)
@@ -371,25 +470,6 @@ def run_ours(args):
     q8k_b1 = {"gbs": bytes1 / (ms1q * 1e-3) / 1e9, "us_per_step": ms1q * 1e3,
               "kernel": "q4k_gemv_kernel<1,false,2> (dp4a, x as Q8_K int8 codes per 256-block)",
               "numerics": "W times the Q8_K-quantized x: differs from W x by <= sum|w| d/2 per row"}
-
-    # ---- the same step as one chain (one persistent launch for all 112 steps)
-    def chain_steps(B):
-        st = []
-        for layer in range(LAYERS):
-            W, y = Ws[layer], (lambda mi: y_view(B, layer, mi))
-            st += [(x_view(B, layer, "attn"), [(W[0], y(0)), (W[1], y(1)), (W[2], y(2))]),
-                   (x_view(B, layer, "o"), [(W[3], y(3))]),
-                   (x_view(B, layer, "mlp"), [(W[4], y(4)), (W[5], y(5))]),
-                   (x_view(B, layer, "down"), [(W[6], y(6))])]
-        return st
-    chain_res = {}
-    for B in (1, 5):
-        ch = q4k.Chain(chain_steps(B), B)
-        gc = capture(lambda: ch.run(stream=stream))
-        msc = time_graph(gc, max(10, args.steps // 4), args.warmup)
-        del gc
-        ch.close()
-        chain_res[f"batch{B}"] = {"gbs": step_bytes(B) / (msc * 1e-3) / 1e9, "us_per_step": msc * 1e3}
 
     # ---- VerifyBatch sweep (same weights)
     sweep = {}
@@ -549,7 +629,9 @@ def run_ours(args):
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms1, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None,
+        "dtype": "q4_k u4 weights x int8 hi+lo parts of x (dp4a, int32 per sub-block), fp32 scales and sums",
+        "data": "synthetic",
         "arithmetic": "batch 1: x as two int8 parts per super-block, dp4a with the 4-bit weights into int32 "
                       "per sub-block, scales and accumulation in fp32; batch >= 2: fp16 hi+lo x and exact fp16 "
                       "weights on mma.sync, fp32 accumulation",
@@ -562,14 +644,14 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}"},
         "frac_of_peak": value / world / pk["hbm_gbs"],
         "frac_of_spec_8tbs": value / world / SPEC_HBM_GBS,
+        "frac_of_read_probe": value / world / read_probe["gbs"],
+        "read_probe": read_probe,
         "us_per_layer": ms1 * 1e3 / LAYERS,
         "tok_per_s_equiv": 1e3 / ms1,
+        "per_kind_us": kinds_us,
         "unfused_one_launch_per_matrix": unfused,
         "batch1_tensor_core_path": tensor_core_b1,
         "batch1_q8k_activations": q8k_b1,
-        "chain_one_launch_per_step": chain_res,
-        "verify_batch": sweep,
-        "lm_head_argmax": lm,
         "single_gemv_4096": single,
         "q6k_gemv_batch1": q6,
         "prefill": prefill,
@@ -581,7 +663,20 @@ def run_ours(args):
         "peaks": pk,
     }
     if rank == 0:
-        out["cpu_baseline"] = oracle_sample(args.cpu_seconds) if world == 1 or rank == 0 else None
+        cb = oracle_sample(args.cpu_seconds)
+        if not args.skip_cpu_configs:
+            cb["configs"] = oracle_configs()
+        out["cpu_baseline"] = cb
+        # the metric's three figures, last in the line: batch-1 and batch-5
+        # decode GB/s with their fractions of the peak, and the LM head + argmax
+        b5 = sweep["batch5"]
+        out["verify_batch"] = sweep
+        out["lm_head_argmax"] = lm
+        out["metric_figures"] = {
+            "batch1_gbs": value / world, "batch1_frac_of_peak": value / world / pk["hbm_gbs"],
+            "batch1_ms_per_step": ms1,
+            "batch5_gbs": b5["gbs"], "batch5_frac_of_peak": b5["frac_of_peak"], "batch5_ms_per_step": b5["us_per_step"] / 1e3,
+            "lm_head_argmax_us_batch1": lm["batch1"]["us"], "lm_head_argmax_us_batch5": lm["batch5"]["us"]}
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -598,25 +693,6 @@ def run_profile_case(spec: str, iters: int):
     import q4_dequant_gemv_gb300 as q4k
     import synth
     __graft_entry__.build()
-    if spec.startswith("chain"):
-        # chain:L:B -- L Qwen2.5-7B-shaped layers as one chain (4 steps per layer)
-        _, L, B = spec.split(":")
-        L, B = int(L), int(B)
-        layers = [[torch.from_numpy(W).cuda() for _, _, _, W in synth.qwen_layer_weights(l)] for l in range(L)]
-        shapes = synth.qwen25_7b_shapes()
-        xs = {K: torch.from_numpy(synth.normal_f32((B, K), (9, K))).cuda() for K in (3584, 18944)}
-        ys = [[torch.empty((B, N), device="cuda") for _, N, _ in shapes] for _ in range(L)]
-        steps = []
-        for W, y in zip(layers, ys):
-            steps += [(xs[3584], [(W[0], y[0]), (W[1], y[1]), (W[2], y[2])]), (xs[3584], [(W[3], y[3])]),
-                      (xs[3584], [(W[4], y[4]), (W[5], y[5])]), (xs[18944], [(W[6], y[6])])]
-        ch = q4k.Chain(steps, B)
-        for _ in range(iters):
-            ch.run()
-        torch.cuda.synchronize()
-        ch.close()
-        print(f"profile case {spec} x{iters} done")
-        return
     if spec.startswith("decode"):
         # decode:L:B -- L Qwen2.5-7B-shaped layers (7 GEMVs each), eager launches
         _, L, B = spec.split(":")
@@ -670,7 +746,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
-    ap.add_argument("--profile-case", default=None, help="gemv:N:K:B | argmax:N:K:B | prefill:N:K:T | q6k:N:K:B | decode:L:B | chain:L:B (ncu helper)")
+    ap.add_argument("--skip-cpu-configs", action="store_true", help="time the oracle on the headline sample only")
+    ap.add_argument("--profile-case", default=None, help="gemv:N:K:B | argmax:N:K:B | prefill:N:K:T | q6k:N:K:B | decode:L:B (ncu helper)")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:

@@ -141,8 +141,11 @@ q4k_status q4k_gemv_argmax_debug(const void *W, const float *x, int32_t *idx, fl
  * keeps until the process exits.
  *   - batch must be <= 16 (the array's capacity); larger batches return
  *     Q4K_ERR_INVALID_ARG.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - The array's device address is looked up (cudaGetSymbolAddress) on the
+ *     first call on a device and on every call made outside stream capture;
+ *     a call made during capture reuses the last address looked up, so make a
+ *     first call on each device before any stream capture (and again after a
+ *     cudaDeviceReset, which may move the array).
  *   - Each call clears the array with cudaMemsetAsync on `stream` before its
  *     kernel.  All calls share the array: calls that overlap on the GPU
  *     (different streams, concurrently running graphs) race and may return
@@ -217,14 +220,24 @@ q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t
  *            sum_k |w_k| d/2 per row -- its own tolerance, not the one stated
  *            for q4k_gemv.  Returns Q4K_ERR_INVALID_ARG with batch > 1 or
  *            together with Q4K_FLAG_TENSOR_CORE.
+ *            Q4K_FLAG_TEST_STALL (failure-path tests only): the first weight
+ *            copy of every CTA is awaited for 16 bytes more than it brings, so
+ *            that every wait on it runs out.  The kernel then does what it does
+ *            after any timed-out wait: sets bit 0 of q4k_device_error_flags(),
+ *            stops waiting, writes no outputs, waits (bounded) for its own
+ *            copies in flight and returns; the context stays usable.
+ *   wait_limit_us  bound of each wait inside the kernel in microseconds;
+ *            0 = the default of 2 s.
  */
 #define Q4K_FLAG_PDL 1u
 #define Q4K_FLAG_TENSOR_CORE 2u
 #define Q4K_FLAG_Q8K_X 4u
+#define Q4K_FLAG_TEST_STALL 8u
 typedef struct {
     int split_k;
     unsigned flags;
-    int reserved[6];
+    unsigned wait_limit_us;
+    int reserved[5];
 } q4k_launch_opts;
 
 q4k_status q4k_gemv_ex(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch,
@@ -252,49 +265,18 @@ q4k_status q4k_gemv_grouped(const q4k_gemv_group *groups, int ngroups, const flo
                             int batch, void *stream, const q4k_launch_opts *opts);
 
 /*
- * Chains: a fixed sequence of GEMV steps run by ONE persistent kernel launch.
- * Each step is what one q4k_gemv_grouped call computes (1..4 matrices that
- * multiply the same x).  The semantics are those of issuing the steps one
- * after the other on a stream: step s+1 reads its x only after every output
- * of steps 0..s has been written, so a step may read an earlier step's
- * output, and an output may overwrite an earlier step's input.  The gain over
- * separate launches is that the weights of step s+1 already stream into the
- * GPU while step s finishes, and no CTA has to be launched or drained between
- * steps.  This extends the pages' fused decode dispatch (dotLLM README, News
- * 2026-03: fewer dispatches per decode step) to a whole decode step; the
- * pages have no chain API of their own, this is an interface choice of this
- * library.
- *
- * q4k_chain_create validates the steps, picks each step's split and encodes
- * its tensor maps into device memory allocated with cudaMalloc on the current
- * device (synchronous: call it outside stream capture).  The chain keeps the
- * pointers it was given: the weights, x and y buffers must stay allocated and
- * at the same addresses while the chain is used; their contents may change
- * between runs.  q4k_chain_run launches the whole sequence on `stream`
- * (capturable in a CUDA graph): two stream-ordered memsets of the chain's
- * small counters, then one cooperative kernel launch; runs of the same chain
- * must not overlap on the GPU.  q4k_chain_destroy frees the device memory
- * (synchronous; no run may still be pending).
- *   steps[s].x       fp32 [batch][K], 16-byte aligned
- *   steps[s].K       multiple of 256 (same for the step's matrices)
- *   steps[s].ngroups 1..4; groups as in q4k_gemv_grouped (N == 0 skipped)
- *   nsteps           1..4096 (the step table must also fit in shared memory:
- *                    Q4K_ERR_INVALID_ARG if it does not)
- *   batch            1..16
+ * Read-only streaming probe (a measurement aid; no counterpart on the pages):
+ * streams the first *bytes_read bytes of buf from device memory into shared
+ * memory the way the GEMV kernels stream their weights -- one CTA per SM,
+ * each reading a contiguous slice with 32 KB bulk asynchronous copies through
+ * a 4-deep ring -- and discards them.  Timing it gives the read-only HBM rate
+ * that bounds the GEMVs (a copy's read+write rate is lower).  *bytes_read is
+ * bytes rounded down to a whole number of 32 KB chunks per SM (0 when bytes
+ * is smaller).  buf: device pointer, 16-byte aligned; asynchronous on stream.
+ * Errors: INVALID_ARG (bytes < 0, null buf or bytes_read), MISALIGNED,
+ * UNSUPPORTED_DEVICE, CUDA.
  */
-#define Q4K_CHAIN_MAX_STEPS 4096
-typedef struct {
-    const float *x;
-    int64_t K;
-    int ngroups;
-    q4k_gemv_group groups[4];
-} q4k_chain_step;
-
-typedef struct q4k_chain q4k_chain;
-
-q4k_status q4k_chain_create(const q4k_chain_step *steps, int nsteps, int batch, q4k_chain **chain);
-q4k_status q4k_chain_run(const q4k_chain *chain, void *stream);
-q4k_status q4k_chain_destroy(q4k_chain *chain);
+q4k_status q4k_stream_read(const void *buf, int64_t bytes, int64_t *bytes_read, void *stream);
 
 /* Launch plan the automatic heuristics pick for a shape (for tests and
  * reports): out[0] = split_k, out[1] = number of CTAs, out[2] = rows per CTA
@@ -302,10 +284,16 @@ q4k_status q4k_chain_destroy(q4k_chain *chain);
 q4k_status q4k_gemv_plan(int64_t N, int64_t K, int batch, int out[4]);
 
 /* Sticky device-side error bits of the library's kernels, read synchronously
- * from the current device: bit 0 = a bounded wait inside a GEMV/argmax kernel
- * (Q4_K or Q6_K) timed out, bit 1 = the same in the prefill kernel; the kernel then wound down
- * early and its outputs are invalid.  0 = no error. */
+ * from the current device: bit 0 = a bounded wait inside a GEMV/argmax
+ * kernel (Q4_K or Q6_K) or the streaming probe timed out, bit 1 = the same in the prefill
+ * kernel; the kernel then wound down early and its outputs are invalid.
+ * 0 = no error.  The bits stay set until q4k_device_error_clear(). */
 unsigned int q4k_device_error_flags(void);
+
+/* Reset the sticky error bits on the current device (synchronous; call it
+ * when no kernel of the library is running).  Q4K_ERR_CUDA if a copy to the
+ * device failed. */
+q4k_status q4k_device_error_clear(void);
 
 #ifdef __cplusplus
 }

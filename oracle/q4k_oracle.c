@@ -422,10 +422,12 @@ void oracle_prefill(const uint8_t *W, const uint16_t *X, double *Y, int64_t N, i
     free(Xd);
 }
 
+/* Processors available to this process (not the current OpenMP thread
+ * count, which a call with threads > 0 changes). */
 int oracle_max_threads(void)
 {
 #ifdef _OPENMP
-    return omp_get_max_threads();
+    return omp_get_num_procs();
 #else
     return 1;
 #endif

@@ -18,6 +18,7 @@ Q4K_OK = 0
 Q4K_FLAG_PDL = 1
 Q4K_FLAG_TENSOR_CORE = 2
 Q4K_FLAG_Q8K_X = 4
+Q4K_FLAG_TEST_STALL = 8
 QK = 256
 QBYTES = 144
 MAX_BATCH = 16
@@ -33,22 +34,18 @@ class Q4KError(RuntimeError):
 
 
 class LaunchOpts(ctypes.Structure):
-    _fields_ = [("split_k", ctypes.c_int), ("flags", ctypes.c_uint), ("reserved", ctypes.c_int * 6)]
+    _fields_ = [("split_k", ctypes.c_int), ("flags", ctypes.c_uint), ("wait_limit_us", ctypes.c_uint),
+                ("reserved", ctypes.c_int * 5)]
 
 
 class GemvGroup(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("y", ctypes.c_void_p), ("N", ctypes.c_int64)]
 
 
-class ChainStep(ctypes.Structure):
-    _fields_ = [("x", ctypes.c_void_p), ("K", ctypes.c_int64), ("ngroups", ctypes.c_int),
-                ("groups", GemvGroup * 4)]
-
-
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("q4k_status_string", "q4k_abi_version", "q4k_gemv", "q4k_gemv_argmax", "q4k_gemv_argmax_debug",
            "q4k_gemv_argmax_noalloc", "q4k_gemm_prefill", "q4k_gemv_ex", "q4k_gemv_grouped", "q4k_gemv_plan",
-           "q4k_device_error_flags", "q4k_chain_create", "q4k_chain_run", "q4k_chain_destroy", "q6k_gemv")
+           "q4k_device_error_flags", "q4k_device_error_clear", "q4k_stream_read", "q6k_gemv")
 
 
 def lib():
@@ -83,12 +80,9 @@ def lib():
         L.q4k_gemv_plan.argtypes = [I64, I64, I, ctypes.POINTER(ctypes.c_int * 4)]
         L.q4k_gemv_plan.restype = I
         L.q4k_device_error_flags.restype = ctypes.c_uint
-        L.q4k_chain_create.argtypes = [ctypes.POINTER(ChainStep), I, I, ctypes.POINTER(ctypes.c_void_p)]
-        L.q4k_chain_create.restype = I
-        L.q4k_chain_run.argtypes = [P, P]
-        L.q4k_chain_run.restype = I
-        L.q4k_chain_destroy.argtypes = [P]
-        L.q4k_chain_destroy.restype = I
+        L.q4k_device_error_clear.restype = I
+        L.q4k_stream_read.argtypes = [P, I64, ctypes.POINTER(ctypes.c_int64), P]
+        L.q4k_stream_read.restype = I
         _lib = L
         return L
 
@@ -135,10 +129,11 @@ def _flags(pdl: bool, tensor_core: bool, q8k: bool = False) -> int:
 
 
 def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False, tensor_core: bool = False,
-         q8k: bool = False):
+         q8k: bool = False, wait_limit_us: int = 0, test_stall: bool = False):
     """y [B, N] (fp32) = W_q4k [N, K] . x [B, K] (fp32); x may also be [K].
     tensor_core: batch 1 on the tensor-core inner product instead of the integer one.
-    q8k: batch 1 with x quantized Q8_K style (int8 codes per 256-block), its own error bound."""
+    q8k: batch 1 with x quantized Q8_K style (int8 codes per 256-block), its own error bound.
+    wait_limit_us, test_stall: bound of the kernel's waits, and a wait made to run out (failure tests)."""
     import torch
     _dev(W, "W", torch.uint8)
     _dev(x, "x", torch.float32)
@@ -152,8 +147,9 @@ def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False, tens
     if y.numel() != B * N:
         raise ValueError("y has the wrong size")
     L = lib()
-    if split_k or pdl or tensor_core or q8k:
-        o = LaunchOpts(split_k, _flags(pdl, tensor_core, q8k))
+    if split_k or pdl or tensor_core or q8k or wait_limit_us or test_stall:
+        o = LaunchOpts(split_k, _flags(pdl, tensor_core, q8k) | (Q4K_FLAG_TEST_STALL if test_stall else 0),
+                       int(wait_limit_us))
         st = L.q4k_gemv_ex(W.data_ptr(), x2.data_ptr(), y.data_ptr(), N, K, B, _stream_ptr(stream), ctypes.byref(o))
         _check("q4k_gemv_ex", st)
     else:
@@ -246,70 +242,30 @@ def gemm_prefill(W, X, Y=None, *, stream=None):
     return Y
 
 
-class Chain:
-    """A fixed sequence of GEMV steps run by one persistent launch (q4k_chain_*).
-
-    steps: list of (x, [(W, y), ...]) with x fp32 [batch, K] and per matrix W
-    uint8 [N, K/256*144], y fp32 [batch, N] (1..4 matrices per step).  Step s+1
-    reads its x only after all outputs of the earlier steps are written, so x of
-    a later step may be the y of an earlier one.  The chain keeps the tensors'
-    addresses: they stay referenced by this object."""
-
-    def __init__(self, steps, batch: int):
-        import torch
-        L = lib()
-        self._keep = []
-        arr = (ChainStep * len(steps))()
-        for i, (x, groups) in enumerate(steps):
-            _dev(x, "x", torch.float32)
-            x2 = x.view(1, -1) if x.dim() == 1 else x
-            if x2.shape[0] != batch:
-                raise ValueError(f"step {i}: x has {x2.shape[0]} rows, batch is {batch}")
-            K = x2.shape[1]
-            if not 1 <= len(groups) <= 4:
-                raise ValueError(f"step {i}: 1 to 4 matrices")
-            arr[i].x = x2.data_ptr()
-            arr[i].K = K
-            arr[i].ngroups = len(groups)
-            for g, (W, y) in enumerate(groups):
-                _dev(W, "W", torch.uint8)
-                _dev(y, "y", torch.float32)
-                N = _shape_wk(W, K)
-                if y.numel() != batch * N:
-                    raise ValueError(f"step {i}: y has the wrong size")
-                arr[i].groups[g] = GemvGroup(W.data_ptr(), y.data_ptr(), N)
-                self._keep += [W, y]
-            self._keep.append(x)
-        h = ctypes.c_void_p()
-        _check("q4k_chain_create", L.q4k_chain_create(arr, len(steps), batch, ctypes.byref(h)))
-        self._h = h
-        self._lib = L
-
-    def run(self, stream=None):
-        if self._h is None:
-            raise RuntimeError("chain is closed")
-        _check("q4k_chain_run", self._lib.q4k_chain_run(self._h, _stream_ptr(stream)))
-
-    def close(self):
-        if getattr(self, "_h", None) is not None:
-            self._lib.q4k_chain_destroy(self._h)
-            self._h = None
-
-    def __del__(self):
-        try:
-            self.close()
-        except Exception:
-            pass
-
-
 def gemv_plan(N: int, K: int, batch: int):
     out = (ctypes.c_int * 4)()
     _check("q4k_gemv_plan", lib().q4k_gemv_plan(N, K, batch, ctypes.byref(out)))
     return {"split_k": out[0], "ctas": out[1], "rows_per_tile": out[2], "x_chunk_blocks": out[3]}
 
 
+def stream_read(buf, *, stream=None) -> int:
+    """Read-only streaming probe over a device buffer (any dtype, contiguous):
+    launches the probe kernel and returns the number of bytes it streams."""
+    import torch
+    if not isinstance(buf, torch.Tensor) or not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    n = ctypes.c_int64(0)
+    _check("q4k_stream_read", lib().q4k_stream_read(buf.data_ptr(), buf.numel() * buf.element_size(), ctypes.byref(n),
+                                                    _stream_ptr(stream)))
+    return int(n.value)
+
+
 def device_error_flags() -> int:
     return int(lib().q4k_device_error_flags())
+
+
+def device_error_clear():
+    _check("q4k_device_error_clear", lib().q4k_device_error_clear())
 
 
 def raw_call(name: str, *args):

@@ -67,14 +67,10 @@ q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t
     return q4k::prefill_impl(W, X_bf16, Y, N, K, T, stream);
 }
 
-q4k_status q4k_chain_create(const q4k_chain_step *steps, int nsteps, int batch, q4k_chain **chain)
+q4k_status q4k_stream_read(const void *buf, int64_t bytes, int64_t *bytes_read, void *stream)
 {
-    return q4k::chain_create_impl(steps, nsteps, batch, chain);
+    return q4k::stream_read_impl(buf, bytes, bytes_read, stream);
 }
-
-q4k_status q4k_chain_run(const q4k_chain *chain, void *stream) { return q4k::chain_run_impl(chain, stream); }
-
-q4k_status q4k_chain_destroy(q4k_chain *chain) { return q4k::chain_destroy_impl(chain); }
 
 q4k_status q4k_gemv_plan(int64_t N, int64_t K, int batch, int out[4])
 {
@@ -85,7 +81,14 @@ q4k_status q4k_gemv_plan(int64_t N, int64_t K, int batch, int out[4])
  * out and the kernel wound down early).  Synchronous; 0 means no error. */
 unsigned int q4k_device_error_flags(void)
 {
-    return q4k::read_device_error() | q4k::read_prefill_error() | q4k::read_q6k_error();
+    return q4k::read_device_error() | q4k::read_prefill_error() | q4k::read_q6k_error() | q4k::read_probe_error();
+}
+
+q4k_status q4k_device_error_clear(void)
+{
+    const bool ok = q4k::clear_device_error() & q4k::clear_prefill_error() & q4k::clear_q6k_error() &
+                    q4k::clear_probe_error();
+    return ok ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -59,13 +59,13 @@
 #include "ptx.cuh"
 #include "q4k_internal.h"
 
+#include "q4k_dev.cuh"
+
 namespace q4k {
 
-constexpr int kBlockBytes = 144;
 constexpr int kWarps = 8;                 // warps per CTA, 16 weight rows each
 constexpr int kRows = 16 * kWarps;        // rows per tile (128)
 constexpr int kThreads = 32 * kWarps;
-constexpr int kKsteps = 17;               // 16 k16 steps + 1 min-term step per super-block
 constexpr int kStages = 4;                // W ring depth
 constexpr int kStageBytes = kRows * kBlockBytes;   // one super-block of every tile row (18 KB)
 constexpr size_t kSmemPerCta2 = 110 * 1024;        // two CTAs per SM (batch <= 8)
@@ -89,27 +89,10 @@ struct GemvArgs {
     unsigned long long *keys;  // argmax: [B] 64-bit keys (zeroed), null otherwise
     unsigned int *ticket;      // argmax: CTA ticket (zeroed)
     int32_t *idx;              // argmax: output [B]
+    uint64_t wait_ns;          // bound of every wait (default 2 s)
+    int test_stall;            // tests: the first stage expects 16 bytes more than its copy brings
 };
 
-__host__ __device__ inline int frag_lanes(int NT, int B) { return NT == 1 ? 8 * B : 32; }
-
-// B fragments are stored lane-major: the 17*NT entries (uint2) of one lane for
-// one super-block are contiguous, so a consumer lane reads them at constant
-// offsets from one base.  The per-lane stride is odd in 8-byte units for even
-// NT so that the 16 lanes of a wavefront hit distinct bank pairs.
-__host__ __device__ constexpr int lane_stride(int NT)
-{
-    // even (16-byte aligned lanes: a k-step's even and odd fragments load as one
-    // 16-byte access; lane L starts at bank 4L mod 32 for NT = 1, 2, 4, so the
-    // eight lanes of a 16-byte wavefront hit distinct banks); NT = 3 loads
-    // 8-byte fragments and keeps an odd stride
-    return NT == 3 ? kKsteps * NT : kKsteps * NT + ((kKsteps * NT) & 1);
-}
-
-__host__ __device__ inline size_t xfrag_bytes_per_block(int NT, int B)
-{
-    return static_cast<size_t>(lane_stride(NT)) * frag_lanes(NT, B) * 8;
-}
 
 // Dynamic shared memory: [ring | x fragments | split-K receive buffer (split
 // slots of at most ceil(128/split) rows x B, only with a split)].
@@ -127,34 +110,15 @@ __host__ inline size_t gemv_smem_bytes(int NT, int B, int kc, int split)
 }
 
 // ---------------------------------------------------------------------------
-// x chunk -> fp16 hi/lo B fragments in shared memory.
-// Entry (bl, s, nt, L) is a uint2 {b01, b23} for lane L = 4*col8 + t of n-tile
-// nt at k-step s of local super-block bl.  Thread t of an A fragment handles
-// sub-block pair t of each super-block (sub-blocks 2t and 2t+1), so for k-step
-// s < 16 (word u = s/2, sub-block 2t + (s&1)) the four B values are the x
-// entries 4u..4u+3 of that sub-block ordered {4u, 4u+2 | 4u+1, 4u+3}.  Step 16
-// holds the sub-block sums of x for sub-blocks 2t, 2t+1 (the dmin*m term).
-// ---------------------------------------------------------------------------
-// Power-of-two scale 2^s with max|x| * 2^s in [2^9, 2^10) (s = 0 for an all
-// zero or non-finite chunk), clamped to the normal range.
-__device__ __forceinline__ int chunk_scale_exp(uint32_t amax_bits)
-{
-    const int E = static_cast<int>((amax_bits >> 23) & 255u);
-    int s = (amax_bits != 0u && E != 255) ? 136 - E : 0;
-    return max(-126, min(126, s));
-}
 
+// ---------------------------------------------------------------------------
 // A chunk of x (B rows x nblk super-blocks, B * nblk <= 32) -> B fragments in
-// shared memory.  One warp converts one (batch row, super-block) item per
-// round; lane l holds float4 l and l + 32 of the super-block (elements
-// 4i..4i+3, sub-block i/8, word i%8).  All loads of all rounds are issued
-// first.  Each item gets its own power-of-two scale from a warp-level max
-// (no shared-memory max, no barrier in between), stored as s_unscale[bl*B + b];
-// then the fp16 hi/lo fragments and the sub-block sums (8-lane shuffles).
-// Float4 i is sub-block j = i/8 (pair t = j/2, half h = j%2), word u = i%8 ->
-// k-step s = 2u + h of pair t.  Ends with a barrier over all nthr threads; the
-// caller must have finished reading the previous chunk's fragments and scales.
-template <int NT, bool L2ONLY = false>
+// shared memory (x_item_tc per item).  One warp converts one (batch row,
+// super-block) item per round; all loads of all rounds are issued first.  The
+// item scales go to s_unscale[bl*B + b].  Ends with a barrier over all nthr
+// threads; the caller must have finished reading the previous chunk's
+// fragments and scales.
+template <int NT>
 __device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int kb0, int nblk, uint2 *xf,
                                  float *s_unscale, int tid, int nthr)
 {
@@ -170,8 +134,8 @@ __device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int 
             const int b = it / nblk;
             const float4 *src = reinterpret_cast<const float4 *>(
                 x + static_cast<size_t>(b) * K + static_cast<size_t>(kb0 + (it - b * nblk)) * 256);
-            v[r][0] = L2ONLY ? __ldcg(src + lane) : __ldg(src + lane);
-            v[r][1] = L2ONLY ? __ldcg(src + 32 + lane) : __ldg(src + 32 + lane);
+            v[r][0] = __ldg(src + lane);
+            v[r][1] = __ldg(src + 32 + lane);
         }
     }
 #pragma unroll
@@ -180,74 +144,17 @@ __device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int 
         if (it >= items) continue;   // warp-uniform
         const int b = it / nblk;
         const int bl = it - b * nblk;
-        uint32_t m = 0u;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const float4 w = v[r][h2];
-            m = max(m, max(max(__float_as_uint(fabsf(w.x)), __float_as_uint(fabsf(w.y))),
-                           max(__float_as_uint(fabsf(w.z)), __float_as_uint(fabsf(w.w)))));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const int e = chunk_scale_exp(m);
-        const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
-        if (lane == 0) s_unscale[bl * B + b] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-        const int chi = 2 * b, clo = 2 * b + 1;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const int i = lane + 32 * h2;
-            float4 w = v[r][h2];
-            w.x *= sc; w.y *= sc; w.z *= sc; w.w *= sc;
-            const int sb = i >> 3, u = i & 7;
-            const int t = sb >> 1, s = 2 * u + (sb & 1);
-            const uint32_t h01 = pack_half2(w.x, w.z);
-            const uint32_t h23 = pack_half2(w.y, w.w);
-            const uint32_t l01 = pack_half2(w.x - half_lo_f32(h01), w.z - half_hi_f32(h01));
-            const uint32_t l23 = pack_half2(w.y - half_lo_f32(h23), w.w - half_hi_f32(h23));
-            xf[(bl * LW + 4 * (chi % 8) + t) * LS + s * NT + chi / 8] = make_uint2(h01, h23);
-            xf[(bl * LW + 4 * (clo % 8) + t) * LS + s * NT + clo / 8] = make_uint2(l01, l23);
-            // sub-block sum over the 8 lanes holding it, then pair it with the
-            // odd sub-block held by the next 8 lanes
-            float sum = (w.x + w.y) + (w.z + w.w);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            const float sum_odd = __shfl_down_sync(0xffffffffu, sum, 8);
-            if ((i & 15) == 0) {
-                const uint32_t hs = pack_half2(sum, sum_odd);
-                const uint32_t ls = pack_half2(sum - half_lo_f32(hs), sum_odd - half_hi_f32(hs));
-                xf[(bl * LW + 4 * (chi % 8) + t) * LS + 16 * NT + chi / 8] = make_uint2(hs, 0u);
-                xf[(bl * LW + 4 * (clo % 8) + t) * LS + 16 * NT + clo / 8] = make_uint2(ls, 0u);
-            }
-        }
+        const float us = x_item_tc<NT>(v[r][0], v[r][1], lane, b, LW, xf + static_cast<size_t>(bl) * LW * LS);
+        if (lane == 0) s_unscale[bl * B + b] = us;
     }
     named_bar_sync(1, nthr);
 }
 
-// ---------------------------------------------------------------------------
-// Batch 1, integer inner product: x of one super-block as two int8 parts per
-// element,  x ~= (dx / 254) * (254 * xh + xl)  with dx = max|x| / 127,
-// q = x * (127 / max|x|), xh = rint(q) and xl = rint((q - xh) * 254), all in
-// fp32 (x and max|x| first scaled by 2^64 when max|x| < 2^-64), so that
-// |x - (dx / 254)(254 xh + xl)| <= dx (1/508 + 2^-16).  Per local
-// super-block bl, at byte offset bl * blk_bytes of the fragment area:
-//   [0, 320)    xh: the 64 values of sub-block pair t at 80 t, in k order
-//   [320, 640)  xl: the same at 320 + 80 t
-//   [640, 672)  int32 per sub-block j: 254 * sum(xh) + sum(xl) over its 32 k
-// (the 16-byte pad per pair puts the four pairs' 16-byte loads of one
-// quarter-warp on distinct banks)
-// and s_unscale[bl] * s_pre[bl] = dx / 254, with s_unscale[bl] kept in the
-// normal range (s_pre = 2^-64 for the scaled blocks, else 1); s_unscale is 0
-// for an all-zero super-block and the non-finite max itself when x holds an
-// inf or NaN, so that the result is not finite.
-// One warp per super-block; lane l holds float4 l and l + 32 (k = 4l..4l+3 and
-// 128 + 4l..).  Ends with a barrier over all nthr threads.
-// ---------------------------------------------------------------------------
-constexpr int kI8Bytes = 672;
-constexpr int kI8Pair = 80;        // bytes per sub-block pair in each part
-static_assert(kI8Bytes <= lane_stride(1) * 8 * 8, "batch-1 fragment area holds the int8 parts");
-
-template <bool Q8, bool L2ONLY = false>
+// Batch 1: a chunk of x (nblk <= 32 super-blocks) -> the int8 parts of
+// x_item_i8, one super-block per warp and round, at xb + bl * blk_bytes; the
+// scales go to s_unscale[bl], s_pre[bl].  Ends with a barrier over all nthr
+// threads.
+template <bool Q8>
 __device__ void convert_x_i8_blocks(const float *__restrict__ x, int kb0, int nblk, uint8_t *xb, int blk_bytes,
                                     float *s_unscale, float *s_pre, int tid, int nthr)
 {
@@ -258,289 +165,23 @@ __device__ void convert_x_i8_blocks(const float *__restrict__ x, int kb0, int nb
         const int it = warp + r * nwarps;
         if (it < nblk) {   // warp-uniform
             const float4 *src = reinterpret_cast<const float4 *>(x + static_cast<size_t>(kb0 + it) * 256);
-            v[r][0] = L2ONLY ? __ldcg(src + lane) : __ldg(src + lane);
-            v[r][1] = L2ONLY ? __ldcg(src + 32 + lane) : __ldg(src + 32 + lane);
+            v[r][0] = __ldg(src + lane);
+            v[r][1] = __ldg(src + 32 + lane);
         }
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int it = warp + r * nwarps;
         if (it >= nblk) continue;   // warp-uniform
-        uint32_t m = 0u;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const float4 w = v[r][h2];
-            m = max(m, max(max(__float_as_uint(fabsf(w.x)), __float_as_uint(fabsf(w.y))),
-                           max(__float_as_uint(fabsf(w.z)), __float_as_uint(fabsf(w.w)))));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float amax = __uint_as_float(m);
-        const bool ok = m != 0u && m < 0x7F800000u;   // finite and not all zero
-        // below 2^-64 the reciprocal is taken of the max scaled by 2^64 (exact)
-        // and x is scaled alike, so that it stays finite
-        const float pre = (m < 0x1F800000u) ? 0x1p64f : 1.0f;
-        const float inv = ok ? 127.0f / (amax * pre) : 0.0f;
-        uint8_t *base = xb + static_cast<size_t>(it) * blk_bytes;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-            const float4 w = v[r][h2];
-            const float e[4] = {w.x, w.y, w.z, w.w};
-            uint32_t hw = 0u, lw = 0u;
-            int sum = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float q = (e[j] * pre) * inv;
-                const float hq = rintf(q);
-                const int hi = static_cast<int>(hq);
-                hw |= (static_cast<uint32_t>(hi) & 0xFFu) << (8 * j);
-                if constexpr (Q8) {
-                    sum += hi;
-                } else {
-                    const int lo = static_cast<int>(rintf((q - hq) * 254.0f));
-                    lw |= (static_cast<uint32_t>(lo) & 0xFFu) << (8 * j);
-                    sum += 254 * hi + lo;
-                }
-            }
-            const int i = lane + 32 * h2;   // float4 index: k = 4i..4i+3, sub-block i/8, pair i/16
-            const int off = kI8Pair * (i >> 4) + 4 * (i & 15);
-            *reinterpret_cast<uint32_t *>(base + off) = hw;
-            if constexpr (!Q8) *reinterpret_cast<uint32_t *>(base + 4 * kI8Pair + off) = lw;
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-            if ((i & 7) == 0) reinterpret_cast<int *>(base + 8 * kI8Pair)[i >> 3] = sum;
-        }
+        const float2 sp = x_item_i8<Q8>(v[r][0], v[r][1], lane, xb + static_cast<size_t>(it) * blk_bytes);
         if (lane == 0) {
-            s_unscale[it] = ok ? (Q8 ? (amax * pre) / 127.0f : (amax * pre) / 127.0f / 254.0f)
-                               : (m == 0u ? 0.0f : amax);
-            s_pre[it] = 1.0f / pre;
+            s_unscale[it] = sp.x;
+            s_pre[it] = sp.y;
         }
     }
     named_bar_sync(1, nthr);
 }
 
-// Warm L2 with x[b][kb0*256, kb1*256) for every batch row (one 128-byte line
-// per thread and round).  Safe before a dependency wait: L2 is where the
-// earlier writes land, so the loads after the wait still see them.
-__device__ __forceinline__ void prefetch_x_l2(const float *x, int K, int B, int kb0, int kb1, int tid, int nthr)
-{
-    const int lines = (kb1 - kb0) * 8;   // 1 KB of floats per super-block
-    for (int i = tid; i < B * lines; i += nthr) {
-        const int b = i / lines;
-        prefetch_l2(x + static_cast<size_t>(b) * K + static_cast<size_t>(kb0) * 256 + (i - b * lines) * 32);
-    }
-}
-
-// Scale/min constants of one row of a super-block for thread t (pair t).
-struct RowConsts {
-    uint32_t mulE, addE, mulO, addO;  // f16x2 (sc_2t), (-1024 sc_2t), (sc_2t+1 / 16), (-64 sc_2t+1)
-    uint32_t mpair;                   // f16x2 {m_2t, m_2t+1}
-    float d, dmin;
-};
-
-__device__ __forceinline__ RowConsts decode_header(uint4 h, int t)
-{
-    RowConsts rc;
-    rc.d = half_lo_f32(h.x);
-    rc.dmin = half_hi_f32(h.x);
-    const uint32_t sh = (t & 1) ? 16u : 0u;
-    const uint32_t a0 = (h.y >> sh) & 0xFFFFu;   // s[2(t&1)], s[2(t&1)+1]
-    const uint32_t a1 = (h.z >> sh) & 0xFFFFu;   // s[4+...]
-    const uint32_t a2 = (h.w >> sh) & 0xFFFFu;   // s[8+...]
-    uint32_t scp, mp;
-    if (t < 2) {
-        scp = a0 & 0x3F3Fu;
-        mp = a1 & 0x3F3Fu;
-    } else {
-        scp = (a2 & 0x0F0Fu) | ((a0 >> 2) & 0x3030u);
-        mp = ((a2 >> 4) & 0x0F0Fu) | ((a1 >> 2) & 0x3030u);
-    }
-    const uint32_t k1024 = 0x64006400u;          // f16x2 {1024, 1024}
-    uint32_t sch = hsub2_u32(__byte_perm(scp, 0u, 0x4140u) | k1024, k1024);   // {sc_2t, sc_2t+1}
-    rc.mpair = hsub2_u32(__byte_perm(mp, 0u, 0x4140u) | k1024, k1024);       // {m_2t, m_2t+1}
-    const uint32_t lo2 = __byte_perm(sch, 0u, 0x1010u);   // {sc_2t, sc_2t}
-    const uint32_t hi2 = __byte_perm(sch, 0u, 0x3232u);   // {sc_2t+1, sc_2t+1}
-    rc.mulE = lo2;
-    rc.addE = hmul2_u32(lo2, 0xE400E400u);        // * -1024
-    rc.mulO = hmul2_u32(hi2, 0x2C002C00u);        // * 1/16
-    rc.addO = hmul2_u32(hi2, 0xD400D400u);        // * -64
-    return rc;
-}
-
-// Integer scale/min constants of one row for thread t (sub-blocks 2t, 2t+1).
-struct RowConstsI {
-    int scE, scO, mE, mO;
-    float d, dmin;
-};
-__device__ __forceinline__ RowConstsI decode_header_i(uint4 h, int t)
-{
-    RowConstsI rc;
-    rc.d = half_lo_f32(h.x);
-    rc.dmin = half_hi_f32(h.x);
-    const uint32_t sh = (t & 1) ? 16u : 0u;
-    const uint32_t a0 = (h.y >> sh) & 0xFFFFu;   // s[2(t&1)], s[2(t&1)+1]
-    const uint32_t a1 = (h.z >> sh) & 0xFFFFu;   // s[4+...]
-    const uint32_t a2 = (h.w >> sh) & 0xFFFFu;   // s[8+...]
-    uint32_t scp, mp;
-    if (t < 2) {
-        scp = a0 & 0x3F3Fu;
-        mp = a1 & 0x3F3Fu;
-    } else {
-        scp = (a2 & 0x0F0Fu) | ((a0 >> 2) & 0x3030u);
-        mp = ((a2 >> 4) & 0x0F0Fu) | ((a1 >> 2) & 0x3030u);
-    }
-    rc.scE = static_cast<int>(scp & 0xFFu);
-    rc.scO = static_cast<int>(scp >> 8);
-    rc.mE = static_cast<int>(mp & 0xFFu);
-    rc.mO = static_cast<int>(mp >> 8);
-    return rc;
-}
-
-// Batch 1, integer inner product of one super-block for thread (g, t): rows g
-// (ra) and g + 8 (rb), sub-block pair t.  Byte i of the pair's 32 quant bytes
-// holds q of weight i of sub-block 2t (low nibble) and of 2t+1 (high nibble);
-// dp4a multiplies four of them with four int8 parts of x at a time.  Low
-// nibbles go in as q, high nibbles in place as 16 q (one exact shift per sum
-// afterwards).  Per row the sums are exact in int32:
-//   T = 254 (scE SEh + scO SOh) + (scE SEl + scO SOl)    (|T| < 1.96e9)
-//   M = mE BS_2t + mO BS_2t+1                            (|M| < 1.4e8)
-// and y += ((d T - dmin M) u) pre with u pre = dx / 254 for this super-block
-// (every intermediate in the normal range, whatever the size of x).
-template <bool Q8, typename Release>
-__device__ __forceinline__ void stage_compute_i8(const uint8_t *ra, const uint8_t *rb, const uint8_t *xb, int t,
-                                                 float u, float pre, float (&acc)[1][2], Release &&release)
-{
-    const RowConstsI r0 = decode_header_i(*reinterpret_cast<const uint4 *>(ra), t);
-    const RowConstsI r1 = decode_header_i(*reinterpret_cast<const uint4 *>(rb), t);
-    int eh0 = 0, el0 = 0, oh0 = 0, ol0 = 0, eh1 = 0, el1 = 0, oh1 = 0, ol1 = 0;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const uint4 qa = *reinterpret_cast<const uint4 *>(ra + 16 + 32 * t + 16 * half);
-        const uint4 qb = *reinterpret_cast<const uint4 *>(rb + 16 + 32 * t + 16 * half);
-        // x parts of k = 64t + 16 half + 0..15 (sub-block 2t) and + 32 (2t+1)
-        const uint8_t *xh = xb + kI8Pair * t + 16 * half;
-        const uint4 xhE = *reinterpret_cast<const uint4 *>(xh);
-        const uint4 xhO = *reinterpret_cast<const uint4 *>(xh + 32);
-        const uint4 xlE = Q8 ? make_uint4(0, 0, 0, 0) : *reinterpret_cast<const uint4 *>(xh + 4 * kI8Pair);
-        const uint4 xlO = Q8 ? make_uint4(0, 0, 0, 0) : *reinterpret_cast<const uint4 *>(xh + 4 * kI8Pair + 32);
-        const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
-        const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
-        const uint32_t he[4] = {xhE.x, xhE.y, xhE.z, xhE.w};
-        const uint32_t ho[4] = {xhO.x, xhO.y, xhO.z, xhO.w};
-        const uint32_t le[4] = {xlE.x, xlE.y, xlE.z, xlE.w};
-        const uint32_t lo[4] = {xlO.x, xlO.y, xlO.z, xlO.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t aE = wa[j] & 0x0F0F0F0Fu, aO = wa[j] & 0xF0F0F0F0u;
-            const uint32_t bE = wb[j] & 0x0F0F0F0Fu, bO = wb[j] & 0xF0F0F0F0u;
-            eh0 = dp4a_us(aE, he[j], eh0);
-            oh0 = dp4a_us(aO, ho[j], oh0);
-            eh1 = dp4a_us(bE, he[j], eh1);
-            oh1 = dp4a_us(bO, ho[j], oh1);
-            if constexpr (!Q8) {
-                el0 = dp4a_us(aE, le[j], el0);
-                ol0 = dp4a_us(aO, lo[j], ol0);
-                el1 = dp4a_us(bE, le[j], el1);
-                ol1 = dp4a_us(bO, lo[j], ol1);
-            }
-        }
-    }
-    release();
-    const int2 bs = *reinterpret_cast<const int2 *>(xb + 8 * kI8Pair + 8 * t);
-    // the high-nibble sums are multiples of 16: exact shifts
-    oh0 >>= 4; ol0 >>= 4; oh1 >>= 4; ol1 >>= 4;
-    const int T0 = Q8 ? r0.scE * eh0 + r0.scO * oh0 : 254 * (r0.scE * eh0 + r0.scO * oh0) + (r0.scE * el0 + r0.scO * ol0);
-    const int T1 = Q8 ? r1.scE * eh1 + r1.scO * oh1 : 254 * (r1.scE * eh1 + r1.scO * oh1) + (r1.scE * el1 + r1.scO * ol1);
-    const int M0 = r0.mE * bs.x + r0.mO * bs.y;
-    const int M1 = r1.mE * bs.x + r1.mO * bs.y;
-    const float v0 = fmaf(r0.d, static_cast<float>(T0), -r0.dmin * static_cast<float>(M0));
-    const float v1 = fmaf(r1.d, static_cast<float>(T1), -r1.dmin * static_cast<float>(M1));
-    acc[0][0] = fmaf(v0 * u, pre, acc[0][0]);
-    acc[0][1] = fmaf(v1 * u, pre, acc[0][1]);
-}
-
-// One super-block of this warp's 16 rows (rows g and g + 8 for thread (g, t)):
-// dequantize into A fragments, run the k16 steps against the x fragments at
-// xl, call release() once the slot's bytes have been read, then fold the
-// super-block into acc as d*C - dmin*Cmin.  NC accumulator chains per
-// sub-block parity (2: shorter dependency chains; 1: fewer registers).
-template <int NT, int NC, typename Release>
-__device__ __forceinline__ void stage_compute(const uint8_t *ra, const uint8_t *rb, const uint2 *xl, int t,
-                                              const float (&unscale)[NT], float (&acc)[NT][2], Release &&release)
-{
-    const RowConsts r0 = decode_header(*reinterpret_cast<const uint4 *>(ra), t);
-    const RowConsts r1 = decode_header(*reinterpret_cast<const uint4 *>(rb), t);
-    float cE[NC][NT][4], cO[NC][NT][4], cM[NT][4];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const uint4 qa = *reinterpret_cast<const uint4 *>(ra + 16 + 32 * t + 16 * half);
-        const uint4 qb = *reinterpret_cast<const uint4 *>(rb + 16 + 32 * t + 16 * half);
-        const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w};
-        const uint32_t wb[4] = {qb.x, qb.y, qb.z, qb.w};
-#pragma unroll
-        for (int uu = 0; uu < 4; ++uu) {
-            const int u = 4 * half + uu;
-            const uint32_t a = wa[uu], a8 = a >> 8;
-            const uint32_t c = wb[uu], c8 = c >> 8;
-            const uint32_t mlo = 0x000F000Fu, mhi = 0x00F000F0u, magic = 0x64006400u;
-            const uint32_t e0 = hfma2_u32(and_or(a, mlo, magic), r0.mulE, r0.addE);
-            const uint32_t e1 = hfma2_u32(and_or(a8, mlo, magic), r0.mulE, r0.addE);
-            const uint32_t o0 = hfma2_u32(and_or(a, mhi, magic), r0.mulO, r0.addO);
-            const uint32_t o1 = hfma2_u32(and_or(a8, mhi, magic), r0.mulO, r0.addO);
-            const uint32_t f0 = hfma2_u32(and_or(c, mlo, magic), r1.mulE, r1.addE);
-            const uint32_t f1 = hfma2_u32(and_or(c8, mlo, magic), r1.mulE, r1.addE);
-            const uint32_t p0 = hfma2_u32(and_or(c, mhi, magic), r1.mulO, r1.addO);
-            const uint32_t p1 = hfma2_u32(and_or(c8, mhi, magic), r1.mulO, r1.addO);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                uint2 be, bo;
-                if constexpr (NT == 1) {   // even and odd fragment of k-step pair u: one 16-byte load
-                    const uint4 q = *reinterpret_cast<const uint4 *>(&xl[2 * u]);
-                    be = make_uint2(q.x, q.y);
-                    bo = make_uint2(q.z, q.w);
-                } else if constexpr ((NT & 1) == 0) {   // two n-tiles per 16-byte load
-                    const uint4 qe = *reinterpret_cast<const uint4 *>(&xl[2 * u * NT + (nt & ~1)]);
-                    const uint4 qo = *reinterpret_cast<const uint4 *>(&xl[(2 * u + 1) * NT + (nt & ~1)]);
-                    be = (nt & 1) ? make_uint2(qe.z, qe.w) : make_uint2(qe.x, qe.y);
-                    bo = (nt & 1) ? make_uint2(qo.z, qo.w) : make_uint2(qo.x, qo.y);
-                } else {
-                    be = xl[2 * u * NT + nt];
-                    bo = xl[(2 * u + 1) * NT + nt];
-                }
-                if (u < NC) {   // first k-step of each accumulator chain
-                    mma_16816_z(cE[uu % NC][nt], e0, f0, e1, f1, be.x, be.y);
-                    mma_16816_z(cO[uu % NC][nt], o0, p0, o1, p1, bo.x, bo.y);
-                } else {
-                    mma_16816(cE[uu % NC][nt], e0, f0, e1, f1, be.x, be.y);
-                    mma_16816(cO[uu % NC][nt], o0, p0, o1, p1, bo.x, bo.y);
-                }
-            }
-        }
-    }
-    release();
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const uint2 bm = xl[16 * NT + nt];
-        mma_16816_z(cM[nt], r0.mpair, r1.mpair, 0u, 0u, bm.x, bm.y);
-        float s0, s1;
-        if constexpr (NC == 2) {
-            s0 = ((cE[0][nt][0] + cE[1][nt][0]) + (cO[0][nt][0] + cO[1][nt][0])) +
-                 ((cE[0][nt][1] + cE[1][nt][1]) + (cO[0][nt][1] + cO[1][nt][1]));
-            s1 = ((cE[0][nt][2] + cE[1][nt][2]) + (cO[0][nt][2] + cO[1][nt][2])) +
-                 ((cE[0][nt][3] + cE[1][nt][3]) + (cO[0][nt][3] + cO[1][nt][3]));
-        } else {
-            s0 = (cE[0][nt][0] + cO[0][nt][0]) + (cE[0][nt][1] + cO[0][nt][1]);
-            s1 = (cE[0][nt][2] + cO[0][nt][2]) + (cE[0][nt][3] + cO[0][nt][3]);
-        }
-        const float m0 = cM[nt][0] + cM[nt][1];
-        const float m1 = cM[nt][2] + cM[nt][3];
-        acc[nt][0] = fmaf(r0.d * unscale[nt], s0, acc[nt][0]);
-        acc[nt][0] = fmaf(-r0.dmin * unscale[nt], m0, acc[nt][0]);
-        acc[nt][1] = fmaf(r1.d * unscale[nt], s1, acc[nt][1]);
-        acc[nt][1] = fmaf(-r1.dmin * unscale[nt], m1, acc[nt][1]);
-    }
-}
 
 // ---------------------------------------------------------------------------
 // The kernel body.  All 8 warps consume (16 rows each); there is no producer
@@ -602,7 +243,9 @@ struct StageIssuer {
         for (int g = 1; g < kMaxGroups; ++g)
             if (g == ti.grp) map = &maps->m[g];
         const int slot = i % kStages;
-        mbar_arrive_expect_tx(smem_u32(&full[slot]), kStageBytes);
+        // (test_stall: the first stage waits for 16 bytes that never come, so
+        // that a test can make the bounded waits run out)
+        mbar_arrive_expect_tx(smem_u32(&full[slot]), kStageBytes + ((args->test_stall && i == 0) ? 16 : 0));
         tma_load_2d_hint(smem_u32(ring + slot * kStageBytes), map, kb * (kBlockBytes / 8), ti.row0,
                          smem_u32(&full[slot]), policy);
     }
@@ -629,7 +272,6 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     __shared__ int s_abort;
     __shared__ int s_issued;                 // stages issued so far (for the abort drain)
     __shared__ int s_slot_done[kStages];     // warp arrivals per ring slot (monotonic)
-    __shared__ int s_cons[kWarps];
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -662,7 +304,6 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
         s_issued = first;
     }
     if (ARGMAX && tid < 16) s_best[tid] = 0ull;
-    if (tid < kWarps) s_cons[tid] = 0;
     __syncthreads();
     iss.policy = l2_policy_evict_first();
     // every CTA of a cluster has started once this phase completes; it is
@@ -725,7 +366,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             const uint32_t phase = static_cast<uint32_t>((consumed / kStages) & 1);
             // After an abort the warps keep walking the same schedule (every
             // named barrier is still reached) but stop waiting.
-            if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), phase, kWaitLimitNs)) {
+            if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), phase, args.wait_ns)) {
                 atomicOr(&g_device_error, 1u);
                 s_abort = 1;
             }
@@ -803,17 +444,16 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             }
         }
     }
-    if (lane == 0) s_cons[warp] = consumed;
 
-    // After a timed-out wait, wait (bounded) for the copies this CTA issued but
-    // did not consume, so that none of them lands after the CTA has exited.
+    // After a timed-out wait, wait (bounded) for the copies this CTA may still
+    // have in flight, so that none of them lands after the CTA has exited.
+    // Stage i + kStages is issued only once every warp has waited for stage i,
+    // and nothing is issued after the abort, so only the last kStages stages
+    // issued can be outstanding.
     __syncthreads();
     if (*(volatile int *)&s_abort && tid == 0) {
-        int lo = s_cons[0];
-        for (int w = 1; w < kWarps; ++w) lo = min(lo, s_cons[w]);
-        for (int i = lo; i < s_issued; ++i)
-            if (!mbar_wait_bounded(smem_u32(&full[i % kStages]), static_cast<uint32_t>((i / kStages) & 1), kWaitLimitNs))
-                break;
+        for (int i = max(0, s_issued - kStages); i < s_issued; ++i)
+            (void)mbar_wait_bounded(smem_u32(&full[i % kStages]), static_cast<uint32_t>((i / kStages) & 1), args.wait_ns);
     }
 
     if (split > 1) {
@@ -875,337 +515,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel_wide(const __grid
     gemv_body<NT, ARGMAX, 0>(maps, args);
 }
 
-// ---------------------------------------------------------------------------
-// Chain: a sequence of GEMV steps (each one grouped GEMV: up to four matrices
-// sharing one x) in ONE persistent launch.
-//
-// The CTAs of a cooperative grid stay resident across steps.  Each CTA works
-// through a fixed share of every step (work unit = row tile x K slice; with
-// G CTAs, unit u goes to CTA u mod G) and streams its weight stages through
-// one ring for the whole chain, so the stages of step s+1 are already in
-// flight while step s finishes: the same last-arriver refill as above, with
-// the stage -> (step, unit, super-block) map looked up in a per-CTA table.
-// Step s+1 reads x only after every CTA has finished step s (a counter in
-// global memory, bounded spin), so a step may consume the output of an
-// earlier one.  A K split over CTAs (a power of two dividing G, so that a
-// CTA's K slice is the same for all its units of a step) is reduced without
-// clusters: each slice writes its partial rows to a scratch area and the last
-// slice of the tile (global ticket) adds them in slice order.
-// ---------------------------------------------------------------------------
-// One step as the kernel reads it from device memory (the tensor maps make it
-// 128-byte aligned).
-struct ChainStep {
-    CUtensorMap maps[kMaxGroups];
-    const float *x;
-    float *y[kMaxGroups];
-    int N[kMaxGroups];
-    int tile_start[kMaxGroups + 1];
-    int ngroups;
-    int nb;      // super-blocks per row
-    int tiles;   // row tiles of all matrices
-    int split;   // K slices per tile (power of two dividing the grid)
-    int kc;      // super-blocks per x chunk
-};
-
-// The copy each CTA keeps in shared memory, with its own K slice and unit count.
-struct ChainStepS {
-    float *y[kMaxGroups];
-    const float *x;
-    int N[kMaxGroups];
-    int tile_start[kMaxGroups + 1];
-    int ngroups, nb, split, kc;
-    int kb0, ks, mine;   // this CTA: first super-block and length of its K slice, units
-};
-
-struct ChainArgs {
-    const ChainStep *steps;
-    int nsteps;
-    int B;
-    int kc_max;                 // x chunk capacity of the shared-memory layout
-    float *partials;            // split-K partial rows [tile][slice][B][128]
-    unsigned int *tickets;      // per row tile, zero between uses
-    unsigned int *bar;          // arrivals of all CTAs, zeroed before the launch
-};
-
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p)
-{
-    unsigned int v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Wait until *bar >= target (bounded; gives up early once any kernel of the
-// library has flagged an error).
-__device__ __forceinline__ bool grid_wait(const unsigned int *bar, unsigned int target)
-{
-    if (ld_acquire_u32(bar) >= target) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        __nanosleep(64);
-        if (ld_acquire_u32(bar) >= target) return true;
-        if (*(volatile unsigned int *)&g_device_error) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-    }
-}
-
-__host__ __device__ inline size_t chain_xf_bytes(int NT, int B, int kc_max)
-{
-    return (xfrag_bytes_per_block(NT, B) * kc_max + 127) & ~size_t(127);
-}
-
-// Issue global stage i of this CTA's chain schedule into ring slot i % kStages.
-// The slot's next stage is always kStages further on, so its step is found by
-// walking forward from the step of the slot's previous stage (cursor[slot]).
-__device__ __forceinline__ void chain_issue(const ChainArgs &args, const ChainStepS *s_steps, const int *s_start,
-                                            int *cursor, uint8_t *ring, uint64_t *full, int i)
-{
-    const int slot = i % kStages;
-    int si = cursor[slot];
-    while (s_start[si + 1] <= i) ++si;
-    cursor[slot] = si;
-    const ChainStepS &st = s_steps[si];
-    const int local = i - s_start[si];
-    const int ul = local / st.ks;
-    const int kb = st.kb0 + (local - ul * st.ks);
-    const int tile = (static_cast<int>(blockIdx.x) + ul * static_cast<int>(gridDim.x)) / st.split;
-    const TileInfo ti = tile_info(st, tile);
-    mbar_arrive_expect_tx(smem_u32(&full[slot]), kStageBytes);
-    tma_load_2d_hint(smem_u32(ring + slot * kStageBytes), &args.steps[si].maps[ti.grp], kb * (kBlockBytes / 8),
-                     ti.row0, smem_u32(&full[slot]), l2_policy_evict_first());
-}
-
-template <int NT>
-__device__ __forceinline__ void chain_body(const ChainArgs &args)
-{
-    extern __shared__ __align__(128) uint8_t smem_raw[];
-    uint8_t *ring = smem_raw;
-    const int B = args.B;
-    const int LW = frag_lanes(NT, B);
-    uint2 *xf = reinterpret_cast<uint2 *>(smem_raw + xfrag_offset());
-    ChainStepS *s_steps = reinterpret_cast<ChainStepS *>(smem_raw + xfrag_offset() + chain_xf_bytes(NT, B, args.kc_max));
-    int *s_start = reinterpret_cast<int *>(s_steps + args.nsteps);   // [nsteps + 1]
-    __shared__ __align__(8) uint64_t full[kStages];
-    __shared__ float s_unscale[32];   // per (super-block of the chunk, batch row)
-    __shared__ int s_abort;
-    __shared__ int s_issued;
-    __shared__ int s_last;
-    __shared__ int s_slot_done[kStages];
-    __shared__ int s_cons[kWarps];
-    __shared__ int s_cursor[kStages];
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int G = gridDim.x;
-    const int c = blockIdx.x;
-    const int nsteps = args.nsteps;
-
-    // this CTA's copy of the steps and its number of stages per step
-    for (int si = tid; si < nsteps; si += kThreads) {
-        const ChainStep &st = args.steps[si];
-        ChainStepS &d = s_steps[si];
-#pragma unroll
-        for (int g = 0; g < kMaxGroups; ++g) {
-            d.y[g] = st.y[g];
-            d.N[g] = st.N[g];
-            d.tile_start[g] = st.tile_start[g];
-        }
-        d.tile_start[kMaxGroups] = st.tile_start[kMaxGroups];
-        d.x = st.x;
-        d.ngroups = st.ngroups;
-        d.nb = st.nb;
-        d.split = st.split;
-        d.kc = st.kc;
-        const int units = st.tiles * st.split;
-        const int rank = c & (st.split - 1);
-        d.mine = (c < units) ? (units - c + G - 1) / G : 0;
-        d.kb0 = (rank * st.nb) / st.split;
-        d.ks = ((rank + 1) * st.nb) / st.split - d.kb0;
-        s_start[si + 1] = d.mine * d.ks;
-    }
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(smem_u32(&full[i]), 1);
-            s_slot_done[i] = 0;
-            s_cursor[i] = 0;
-        }
-        s_abort = 0;
-        fence_barrier_init();
-    }
-    if (tid < kWarps) s_cons[tid] = 0;
-    __syncthreads();
-    if (tid == 0) {
-        s_start[0] = 0;
-        for (int si = 0; si < nsteps; ++si) s_start[si + 1] += s_start[si];
-    }
-    __syncthreads();
-    const int total = s_start[nsteps];
-    auto issue = [&](int i) { chain_issue(args, s_steps, s_start, s_cursor, ring, full, i); };
-
-    if (tid == 0) {
-        // the TMA unit reads the tensor maps from global memory: warm its
-        // descriptor cache for the first two steps before the first copies
-        for (int si = 0; si < min(nsteps, 2); ++si)
-            for (int g = 0; g < s_steps[si].ngroups; ++g) prefetch_tensormap(&args.steps[si].maps[g]);
-        const int first = min(kStages, total);
-        for (int i = 0; i < first; ++i) issue(i);
-        s_issued = first;
-    }
-
-    const int g = lane >> 2;
-    const int t = lane & 3;
-    const int blane = (g < 2 * B) ? lane : (lane % LW);
-    const int row_off = (warp * 16 + g) * kBlockBytes;
-    int consumed = 0;
-
-    for (int si = 0; si < nsteps; ++si) {
-        const ChainStepS &st = s_steps[si];
-        const int split = st.split;
-        const int rank = c & (split - 1);
-        const int kb_begin = st.kb0;
-        const int ks = st.ks;
-        const int mine = st.mine;
-        // x of this step may be an output of an earlier step: wait until
-        // every CTA has finished step si - 1
-        if (tid == 32 && si + 2 < nsteps)   // maps of the step after next (its copies start during step si + 1)
-            for (int gi = 0; gi < s_steps[si + 2].ngroups; ++gi) prefetch_tensormap(&args.steps[si + 2].maps[gi]);
-        if (mine > 0) prefetch_x_l2(st.x, st.nb * 256, B, kb_begin, kb_begin + ks, tid, kThreads);
-        if (si > 0) {
-            if (tid == 0 && !*(volatile int *)&s_abort && !grid_wait(args.bar, static_cast<unsigned>(si * G))) {
-                atomicOr(&g_device_error, 1u);
-                s_abort = 1;
-            }
-            __syncthreads();
-        }
-        if (mine > 0 && !*(volatile int *)&s_abort) {
-            const int kc = st.kc;
-            const bool single_chunk = ks <= kc;
-            if (single_chunk) convert_x_blocks<NT, true>(st.x, st.nb * 256, B, kb_begin, ks, xf, s_unscale, tid, kThreads);
-            for (int ul = 0; ul < mine; ++ul) {
-                float acc[NT][2];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
-                float unscale[NT];
-                int chunk_end = -1;
-                for (int kbl = 0; kbl < ks; ++kbl) {
-                    if (!single_chunk && kbl > chunk_end) {
-                        const int cn = min(kc, ks - kbl);
-                        named_bar_sync(1, kThreads);   // everyone done with the previous chunk
-                        convert_x_blocks<NT, true>(st.x, st.nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, tid,
-                                                   kThreads);
-                        chunk_end = kbl + cn - 1;
-                    }
-                    const int blk = single_chunk ? kbl : (kbl % kc);
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int b = t + 4 * nt;
-                        unscale[nt] = (b < B) ? s_unscale[blk * B + b] : 0.f;
-                    }
-                    const int slot = consumed % kStages;
-                    const uint32_t phase = static_cast<uint32_t>((consumed / kStages) & 1);
-                    if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), phase, kWaitLimitNs)) {
-                        atomicOr(&g_device_error, 1u);
-                        s_abort = 1;
-                    }
-                    const uint8_t *ra = ring + slot * kStageBytes + row_off;
-                    const uint8_t *rb = ra + 8 * kBlockBytes;
-                    const uint2 *xl =
-                        xf + static_cast<size_t>((single_chunk ? kbl : (kbl % kc)) * LW + blane) * lane_stride(NT);
-                    // the refill runs after the stage (fewer live registers than
-                    // inside it: the stage-to-step lookup is longer here)
-                    stage_compute<NT, 1>(ra, rb, xl, t, unscale, acc, []() {});
-                    __syncwarp();
-                    if (lane == 0) {
-                        __threadfence_block();
-                        const int prev = atomicAdd(&s_slot_done[slot], 1);
-                        if (prev % kWarps == kWarps - 1) {
-                            const int next = consumed + kStages;
-                            if (next < total && !*(volatile int *)&s_abort) {
-                                issue(next);
-                                atomicAdd(&s_issued, 1);
-                            }
-                        }
-                    }
-                    ++consumed;
-                }
-                // ---------------- unit epilogue
-                const int tile = (c + ul * G) / split;
-                const TileInfo ti = tile_info(st, tile);
-                if (split == 1) {
-                    if (!*(volatile int *)&s_abort) {
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            const int b = t + 4 * nt;
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const int row = ti.row0 + warp * 16 + g + 8 * h;
-                                if (b < B && row < ti.N) ti.y[static_cast<size_t>(b) * ti.N + row] = acc[nt][h];
-                            }
-                        }
-                    }
-                } else {
-                    float *part = args.partials + static_cast<size_t>(tile * split + rank) * B * kRows;
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int b = t + 4 * nt;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            if (b < B) part[b * kRows + warp * 16 + g + 8 * h] = acc[nt][h];
-                    }
-                    __syncthreads();
-                    if (tid == 0) {
-                        __threadfence();
-                        const unsigned prev = atomicAdd(&args.tickets[tile], 1u);
-                        s_last = (prev == static_cast<unsigned>(split - 1));
-                    }
-                    __syncthreads();
-                    if (s_last) {
-                        // every slice of the tile is in: add them in slice order
-                        __threadfence();
-                        const float *p0 = args.partials + static_cast<size_t>(tile * split) * B * kRows;
-                        for (int idx = tid; idx < B * kRows; idx += kThreads) {
-                            float sum = __ldcg(p0 + idx);
-                            for (int q = 1; q < split; ++q) sum += __ldcg(p0 + static_cast<size_t>(q) * B * kRows + idx);
-                            const int b = idx / kRows;
-                            const int row = ti.row0 + (idx - b * kRows);
-                            if (row < ti.N && !*(volatile int *)&s_abort) ti.y[static_cast<size_t>(b) * ti.N + row] = sum;
-                        }
-                        if (tid == 0) args.tickets[tile] = 0u;
-                    }
-                }
-            }
-        }
-        // this CTA's share of step si is done: its outputs are written and its x is read
-        __syncthreads();
-        if (tid == 0) {
-            __threadfence();
-            atomicAdd(args.bar, 1u);
-        }
-    }
-    if (lane == 0) s_cons[warp] = consumed;
-
-    // After a timed-out wait: wait (bounded) for the copies issued but not consumed.
-    __syncthreads();
-    if (*(volatile int *)&s_abort && tid == 0) {
-        int lo = s_cons[0];
-        for (int w = 1; w < kWarps; ++w) lo = min(lo, s_cons[w]);
-        for (int i = lo; i < s_issued; ++i)
-            if (!mbar_wait_bounded(smem_u32(&full[i % kStages]), static_cast<uint32_t>((i / kStages) & 1), kWaitLimitNs))
-                break;
-    }
-}
-
-template <int NT>
-__global__ void __maxnreg__(128) q4k_chain_kernel(const __grid_constant__ ChainArgs args)
-{
-    chain_body<NT>(args);
-}
-
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) q4k_chain_kernel_wide(const __grid_constant__ ChainArgs args)
-{
-    chain_body<NT>(args);
-}
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -1458,6 +767,13 @@ static cudaError_t launch_gemv(const GemvPlan &p, const void *const *Ws, int64_t
 
 static int row_tiles(int64_t N) { return static_cast<int>((N + kRows - 1) / kRows); }
 
+// Wait bound and the test-only stall of the launch options.
+static void set_wait_opts(GemvArgs &a, const q4k_launch_opts *opts)
+{
+    a.wait_ns = (opts && opts->wait_limit_us > 0) ? static_cast<uint64_t>(opts->wait_limit_us) * 1000ull : kWaitLimitNs;
+    a.test_stall = (opts && (opts->flags & Q4K_FLAG_TEST_STALL)) ? 1 : 0;
+}
+
 static q4k_status validate(const void *W, const void *x, const void *out, int64_t N, int64_t K, int batch,
                            bool argmax)
 {
@@ -1495,6 +811,7 @@ q4k_status gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t
     a.tiles = p.tiles;
     a.kc = p.kc;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
+    set_wait_opts(a, opts);
     if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.xm = 0;
     if (opts && (opts->flags & Q4K_FLAG_Q8K_X)) {
         if (batch != 1 || (opts->flags & Q4K_FLAG_TENSOR_CORE)) return Q4K_ERR_INVALID_ARG;
@@ -1541,6 +858,7 @@ q4k_status gemv_grouped_impl(const q4k_gemv_group *groups, int ngroups, const fl
     a.tiles = p.tiles;
     a.kc = p.kc;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
+    set_wait_opts(a, opts);
     if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.xm = 0;
     if (opts && (opts->flags & Q4K_FLAG_Q8K_X)) {
         if (batch != 1 || (opts->flags & Q4K_FLAG_TENSOR_CORE)) return Q4K_ERR_INVALID_ARG;
@@ -1576,6 +894,7 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
     a.kc = p.kc;
     a.idx = idx;
     const bool pdl = opts && (opts->flags & Q4K_FLAG_PDL);
+    set_wait_opts(a, opts);
     if (opts && (opts->flags & Q4K_FLAG_TENSOR_CORE)) p.xm = 0;
     if (opts && (opts->flags & Q4K_FLAG_Q8K_X)) {
         if (batch != 1 || (opts->flags & Q4K_FLAG_TENSOR_CORE)) return Q4K_ERR_INVALID_ARG;
@@ -1613,19 +932,20 @@ q4k_status gemv_argmax_impl(const void *W, const float *x, int32_t *idx, float *
 // a CTA ticket) lives in this file-scope device array instead of coming from
 // cudaMallocAsync.  Every GPU that loads the library holds these bytes until
 // the process exits.  Host code cannot use the array's name as a device
-// address, so the address is looked up with cudaGetSymbolAddress once per
-// device (with that device current) on the first call there; make that first
-// call before any stream capture.  All calls share the array: it is cleared
-// with cudaMemsetAsync on the caller's stream before every launch, and calls
-// whose executions overlap on the GPU (different streams, concurrent graphs)
-// race on it.
+// address, so the address is looked up with cudaGetSymbolAddress with the
+// device current: on the first call on each device, and again on every call
+// made outside stream capture (a device reset reloads the module and may move
+// the array); a call made during capture uses the address of the last call
+// made outside it, so make a first call before any stream capture.  All calls
+// share the array: it is cleared with cudaMemsetAsync on the caller's stream
+// before every launch, and calls whose executions overlap on the GPU
+// (different streams, concurrent graphs) race on it.
 // ---------------------------------------------------------------------------
 constexpr int kNoAllocMaxBatch = 16;   // keys held by the static scratch
 __device__ __align__(256) static unsigned long long g_argmax_scratch[kNoAllocMaxBatch + 2];
 
-static unsigned long long *g_scratch_addr[64];
-static std::once_flag g_scratch_once[64];
-static cudaError_t g_scratch_err[64];
+static unsigned long long *g_scratch_addr[64];   // per device: address from the last lookup
+static std::mutex g_scratch_mu;
 
 q4k_status gemv_argmax_noalloc_impl(const void *W, const float *x, int32_t *idx, int64_t N, int64_t K, int batch,
                                     void *stream)
@@ -1637,15 +957,23 @@ q4k_status gemv_argmax_noalloc_impl(const void *W, const float *x, int32_t *idx,
     if (st != Q4K_OK) return st;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return Q4K_ERR_CUDA;
-    std::call_once(g_scratch_once[dev], [dev]() {
-        void *p = nullptr;
-        g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_argmax_scratch);
-        g_scratch_addr[dev] = static_cast<unsigned long long *>(p);
-    });
-    if (g_scratch_err[dev] != cudaSuccess || g_scratch_addr[dev] == nullptr) return Q4K_ERR_CUDA;
-    unsigned long long *keys = g_scratch_addr[dev];
-    unsigned int *ticket = reinterpret_cast<unsigned int *>(keys + kNoAllocMaxBatch);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return Q4K_ERR_CUDA;
+    unsigned long long *keys = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_scratch_mu);
+        if (cap == cudaStreamCaptureStatusNone || g_scratch_addr[dev] == nullptr) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_argmax_scratch) != cudaSuccess || p == nullptr) {
+                (void)cudaGetLastError();
+                return Q4K_ERR_CUDA;
+            }
+            g_scratch_addr[dev] = static_cast<unsigned long long *>(p);
+        }
+        keys = g_scratch_addr[dev];
+    }
+    unsigned int *ticket = reinterpret_cast<unsigned int *>(keys + kNoAllocMaxBatch);
     if (cudaMemsetAsync(keys, 0, sizeof(g_argmax_scratch), s) != cudaSuccess) return Q4K_ERR_CUDA;
     return gemv_argmax_impl(W, x, idx, nullptr, N, K, batch, stream, keys, ticket, nullptr);
 }
@@ -1664,224 +992,17 @@ q4k_status gemv_plan_impl(int64_t N, int64_t K, int batch, int out[4])
     return Q4K_OK;
 }
 
-// ---------------------------------------------------------------------------
-// Chains (host side)
-// ---------------------------------------------------------------------------
-// K split of one chain step: a power of two dividing the grid (so that a CTA's
-// K slice is the same for all its units), chosen to minimise (units on the
-// busiest CTA) x (super-blocks per unit + per-unit overhead), with a small
-// charge for the partial-sum fix-up.
-static int chain_split(int tiles, int nb, int G)
-{
-    int best = 1;
-    double best_cost = 1e30;
-    for (int s = 1; s <= 16 && s <= nb; s *= 2) {
-        if (G % s) break;
-        const long long units = static_cast<long long>(tiles) * s;
-        const long long per_cta = (units + G - 1) / G;
-        const int per_unit = (nb + s - 1) / s;
-        const double cost = static_cast<double>(per_cta) * (per_unit + 0.75) + (s > 1 ? 0.25 : 0.0);
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = s;
-        }
-    }
-    return best;
-}
-
-template <int NT>
-static void (*chain_kernel())(const ChainArgs)
-{
-    if constexpr (NT <= 2)
-        return q4k_chain_kernel<NT>;
-    else
-        return q4k_chain_kernel_wide<NT>;
-}
-
-static void (*chain_kernel_for(int NT))(const ChainArgs)
-{
-    switch (NT) {
-        case 1: return chain_kernel<1>();
-        case 2: return chain_kernel<2>();
-        case 3: return chain_kernel<3>();
-        default: return chain_kernel<4>();
-    }
-}
-
-}  // namespace q4k
-
-struct q4k_chain {
-    int dev;
-    int NT;
-    int grid;
-    size_t smem;
-    size_t counter_bytes;   // tickets + barrier counter, cleared before every run
-    void *dmem;
-    q4k::ChainArgs args;
-};
-
-namespace q4k {
-
-q4k_status chain_create_impl(const q4k_chain_step *steps, int nsteps, int batch, q4k_chain **chain)
-{
-    if (!chain) return Q4K_ERR_INVALID_ARG;
-    *chain = nullptr;
-    if (!steps || nsteps < 1 || nsteps > Q4K_CHAIN_MAX_STEPS || batch < 1 || batch > Q4K_MAX_BATCH)
-        return Q4K_ERR_INVALID_ARG;
-    for (int si = 0; si < nsteps; ++si) {
-        const q4k_chain_step &st = steps[si];
-        if (!st.x || st.ngroups < 1 || st.ngroups > kMaxGroups) return Q4K_ERR_INVALID_ARG;
-        if (st.K <= 0 || (st.K % 256) != 0 || st.K / 256 >= (1ll << 24)) return Q4K_ERR_INVALID_ARG;
-        if (reinterpret_cast<uintptr_t>(st.x) & 15u) return Q4K_ERR_MISALIGNED;
-        for (int g = 0; g < st.ngroups; ++g) {
-            const q4k_gemv_group &gr = st.groups[g];
-            if (gr.N < 0 || gr.N > 0x7FFFFFFFll) return Q4K_ERR_INVALID_ARG;
-            if (gr.N == 0) continue;
-            if (!gr.W || !gr.y) return Q4K_ERR_INVALID_ARG;
-            if (reinterpret_cast<uintptr_t>(gr.W) & 15u) return Q4K_ERR_MISALIGNED;
-        }
-    }
-    int sms = 0;
-    q4k_status st = check_device(&sms);
-    if (st != Q4K_OK) return st;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return Q4K_ERR_CUDA;
-
-    const int NT = batch_ntiles(batch);
-    const int cps = (NT <= 2) ? 2 : 1;
-    // shared memory: W ring | x chunk | step table
-    const size_t table = static_cast<size_t>(nsteps) * sizeof(ChainStepS) + static_cast<size_t>(nsteps + 1) * 4;
-    const size_t budget = (NT <= 2) ? kSmemPerCta2 : kSmemPerCta1;
-    const size_t per_blk = xfrag_bytes_per_block(NT, batch);
-    if (xfrag_offset() + table + chain_xf_bytes(NT, batch, 1) > budget) return Q4K_ERR_INVALID_ARG;
-    int kc_need = 1;
-    for (int si = 0; si < nsteps; ++si) kc_need = std::max(kc_need, static_cast<int>(steps[si].K / 256));
-    int kc_max = static_cast<int>((budget - xfrag_offset() - table) / per_blk);
-    while (kc_max > 1 && xfrag_offset() + table + chain_xf_bytes(NT, batch, kc_max) > budget) --kc_max;
-    kc_max = std::max(1, std::min(std::min(kc_max, 32 / batch), kc_need));
-    const size_t smem = xfrag_offset() + chain_xf_bytes(NT, batch, kc_max) + table;
-
-    void (*kern)(const ChainArgs) = chain_kernel_for(NT);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return Q4K_ERR_CUDA;
-    }
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess || occ < 1) {
-        (void)cudaGetLastError();
-        return Q4K_ERR_CUDA;
-    }
-    const int G = sms * std::min(occ, cps);
-
-    // the device-side step table
-    std::vector<ChainStep> hs(nsteps);
-    size_t partial_floats = 0;
-    int max_tiles = 1;
-    for (int si = 0; si < nsteps; ++si) {
-        const q4k_chain_step &in = steps[si];
-        ChainStep &d = hs[si];
-        memset(&d, 0, sizeof(d));
-        d.x = in.x;
-        d.nb = static_cast<int>(in.K / 256);
-        int tiles = 0;
-        for (int g = 0; g < in.ngroups; ++g) {
-            const q4k_gemv_group &gr = in.groups[g];
-            if (gr.N == 0) continue;
-            const int i = d.ngroups++;
-            d.y[i] = gr.y;
-            d.N[i] = static_cast<int>(gr.N);
-            d.tile_start[i] = tiles;
-            tiles += row_tiles(gr.N);
-            if (!encode_w_map(&d.maps[i], gr.W, gr.N, in.K)) return Q4K_ERR_CUDA;
-        }
-        for (int g = d.ngroups; g <= kMaxGroups; ++g) d.tile_start[g] = tiles;
-        d.tiles = tiles;
-        d.split = tiles > 0 ? chain_split(tiles, d.nb, G) : 1;
-        const int ks_max = (d.nb + d.split - 1) / d.split;
-        d.kc = std::min(kc_max, ks_max);
-        if (d.split > 1) {
-            partial_floats = std::max(partial_floats, static_cast<size_t>(tiles) * d.split * batch * kRows);
-            max_tiles = std::max(max_tiles, tiles);
-        }
-    }
-    // one allocation: steps | partial rows | tickets | barrier counter
-    const size_t steps_bytes = (static_cast<size_t>(nsteps) * sizeof(ChainStep) + 255) & ~size_t(255);
-    const size_t part_bytes = (partial_floats * 4 + 255) & ~size_t(255);
-    const size_t counter_bytes = static_cast<size_t>(max_tiles + 1) * 4;
-    void *dmem = nullptr;
-    if (cudaMalloc(&dmem, steps_bytes + part_bytes + counter_bytes) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return Q4K_ERR_CUDA;
-    }
-    uint8_t *base = static_cast<uint8_t *>(dmem);
-    if (cudaMemcpy(base, hs.data(), static_cast<size_t>(nsteps) * sizeof(ChainStep), cudaMemcpyHostToDevice) !=
-        cudaSuccess) {
-        cudaFree(dmem);
-        return Q4K_ERR_CUDA;
-    }
-    q4k_chain *ch = new (std::nothrow) q4k_chain;
-    if (!ch) {
-        cudaFree(dmem);
-        return Q4K_ERR_CUDA;
-    }
-    ch->dev = dev;
-    ch->NT = NT;
-    ch->grid = G;
-    ch->smem = smem;
-    ch->counter_bytes = counter_bytes;
-    ch->dmem = dmem;
-    ch->args.steps = reinterpret_cast<const ChainStep *>(base);
-    ch->args.nsteps = nsteps;
-    ch->args.B = batch;
-    ch->args.kc_max = kc_max;
-    ch->args.partials = reinterpret_cast<float *>(base + steps_bytes);
-    ch->args.tickets = reinterpret_cast<unsigned int *>(base + steps_bytes + part_bytes);
-    ch->args.bar = ch->args.tickets + max_tiles;
-    *chain = ch;
-    return Q4K_OK;
-}
-
-q4k_status chain_run_impl(const q4k_chain *ch, void *stream)
-{
-    if (!ch) return Q4K_ERR_INVALID_ARG;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return Q4K_ERR_CUDA;
-    if (dev != ch->dev) return Q4K_ERR_INVALID_ARG;   // the chain's memory lives on another device
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ch->args.tickets, 0, ch->counter_bytes, s) != cudaSuccess) return Q4K_ERR_CUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(ch->grid, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = ch->smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: they wait for one another between steps
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, chain_kernel_for(ch->NT), ch->args);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        return Q4K_ERR_CUDA;
-    }
-    return Q4K_OK;
-}
-
-q4k_status chain_destroy_impl(q4k_chain *ch)
-{
-    if (!ch) return Q4K_OK;
-    const cudaError_t e = cudaFree(ch->dmem);
-    delete ch;
-    return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
-}
-
 unsigned int read_device_error()
 {
     unsigned int v = 0;
     if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
     return v;
+}
+
+bool clear_device_error()
+{
+    const unsigned int z = 0;
+    return cudaMemcpyToSymbol(g_device_error, &z, sizeof(z)) == cudaSuccess;
 }
 
 }  // namespace q4k

@@ -43,6 +43,12 @@ unsigned int read_prefill_error()
     return v;
 }
 
+bool clear_prefill_error()
+{
+    const unsigned int z = 0;
+    return cudaMemcpyToSymbol(g_prefill_error, &z, sizeof(z)) == cudaSuccess;
+}
+
 namespace pf {
 
 constexpr int kRowsM = 128;          // MMA M
@@ -453,12 +459,17 @@ static cudaError_t launch_prefill(const uint8_t *W, const void *X, float *Y, int
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     auto kern = pf::q4k_prefill_kernel<TN, NTT>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [&]() {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+    // the shared-memory limit is a per-device attribute: set it once per device
+    int dev = 0;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return de;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    std::call_once(once[dev], [&]() {
+        attr_err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
     });
-    if (attr_err != cudaSuccess) return attr_err;
+    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((N + pf::kRowsM - 1) / pf::kRowsM, (T + TN * NTT - 1) / (TN * NTT), split);
     cfg.blockDim = dim3(pf::kThreads, 1, 1);

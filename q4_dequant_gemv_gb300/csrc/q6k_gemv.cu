@@ -372,6 +372,12 @@ unsigned int read_q6k_error()
     return v;
 }
 
+bool clear_q6k_error()
+{
+    const unsigned int z = 0;
+    return cudaMemcpyToSymbol(q6::g_q6k_error, &z, sizeof(z)) == cudaSuccess;
+}
+
 q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream)
 {
     if (!x) return Q4K_ERR_INVALID_ARG;

@@ -112,49 +112,16 @@ def test_product_does_not_touch_oracle():
     assert "oracle" not in text.lower()
 
 
-def test_chain_host_validation(q4k):
-    """The chain entry points reject bad arguments before any device call."""
+def test_stream_read_host_validation(q4k):
+    """The streaming probe rejects bad arguments before any device call."""
     L = q4k.lib()
+    n = ctypes.c_int64(-1)
     ok = 0x10000
-    h = ctypes.c_void_p()
-
-    def steps(**kw):
-        arr = (q4k.ChainStep * 2)()
-        for i in range(2):
-            arr[i].x = ok
-            arr[i].K = 256
-            arr[i].ngroups = 1
-            arr[i].groups[0] = q4k.GemvGroup(ok, ok, 64)
-        for k, v in kw.items():
-            if k in ("W", "y", "N"):
-                g = arr[1].groups[0]
-                setattr(g, k, v)
-                arr[1].groups[0] = g
-            else:
-                setattr(arr[1], k, v)
-        return arr
-
-    create = lambda arr, n=2, b=1: L.q4k_chain_create(arr, n, b, ctypes.byref(h))
-    assert L.q4k_chain_create(None, 1, 1, ctypes.byref(h)) == 1
-    assert L.q4k_chain_create(steps(), 2, 1, None) == 1
-    assert create(steps(), 0) == 1
-    assert create(steps(), 4097) == 1
-    assert create(steps(), 2, 0) == 1
-    assert create(steps(), 2, 17) == 1
-    assert create(steps(K=255)) == 1
-    assert create(steps(K=0)) == 1
-    assert create(steps(ngroups=0)) == 1
-    assert create(steps(ngroups=5)) == 1
-    assert create(steps(x=0)) == 1
-    assert create(steps(x=ok + 4)) == 2
-    assert create(steps(W=ok + 8)) == 2
-    assert create(steps(W=0)) == 1
-    assert create(steps(y=0)) == 1
-    assert create(steps(N=-1)) == 1
-    assert create(steps(N=2 ** 31)) == 1
-    assert create(steps(W=0, y=0, N=0)) in (0, 3, 4)   # empty matrices need no pointers
-    assert L.q4k_chain_run(None, None) == 1
-    assert L.q4k_chain_destroy(None) == 0
+    assert L.q4k_stream_read(P(ok), 1 << 20, None, P(0)) == 1
+    assert L.q4k_stream_read(P(ok), -1, ctypes.byref(n), P(0)) == 1
+    assert n.value == 0
+    assert L.q4k_stream_read(P(0), 1 << 20, ctypes.byref(n), P(0)) == 1
+    assert L.q4k_stream_read(P(ok + 4), 1 << 20, ctypes.byref(n), P(0)) == 2
 
 
 def test_split_receive_slots_fit():
