@@ -16,7 +16,7 @@
  *                      Warp-Shuffle Argmax")
  *   - q4k_gemm_prefill the prefill product with bf16 activations ("cuBLAS HGEMM
  *                      for prefill", dotLLM README, News 2026-03), here on the
- *                      tcgen05 tensor cores after a dequantize-to-bf16 step.
+ *                      tcgen05 tensor cores after a dequantize-to-fp16 step.
  *   - q6k_gemv         y = W x for a Q6_K matrix, the other block format of
  *                      Q4_K_M files ("custom quantized GEMV for decode (Q8_0,
  *                      Q4_K, Q6_K)", same page and item).
@@ -186,11 +186,20 @@ q4k_status q6k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t 
  *   W  Q4_K rows as above (16-byte aligned)
  *   X  bf16 [T][K] row-major (16-byte aligned)
  *   Y  fp32 [T][N] row-major
- * The weights are dequantized to bf16 (round to nearest even) in shared memory
- * and multiplied on the tcgen05 tensor cores with fp32 accumulation in tensor
- * memory.  Any T >= 0 is accepted (T == 0 or N == 0 is a no-op, and the
- * pointers may then be NULL); the tensor path is built for T >= 32.
- * Errors: INVALID_ARG, MISALIGNED (W or X), UNSUPPORTED_DEVICE, CUDA.
+ * Each weight is dequantized in fp32, multiplied by a power of two chosen per
+ * row from the row's largest possible |w|, and rounded once to fp16 (nearest
+ * even) in shared memory; each token's activations are converted to fp16
+ * under a power of two chosen per token from its largest |x| (exact for every
+ * value of at least 2^-31 times that largest).  The tcgen05 tensor cores
+ * multiply them with fp32 accumulation in tensor memory and the epilogue
+ * removes both scales.  Result: |Y - exact| <= ~2^-11 sum_k |w||x| for any
+ * finite inputs, no overflow from large d, dmin or x.
+ * Scratch: the converted X (2*T*K bytes) and T scale exponents come from
+ * cudaMallocAsync on `stream` and are freed on it after the product.
+ * Any T >= 0 is accepted (T == 0 or N == 0 is a no-op, and the pointers may
+ * then be NULL); the tensor path is built for T >= 32.
+ * Errors: INVALID_ARG, MISALIGNED (W or X), UNSUPPORTED_DEVICE, CUDA
+ * (including a failed scratch allocation).
  */
 q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t N, int64_t K,
                             int64_t T, void *stream);

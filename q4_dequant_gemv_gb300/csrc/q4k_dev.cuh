@@ -211,23 +211,44 @@ struct RowConsts {
     float d, dmin;
 };
 
-__device__ __forceinline__ RowConsts decode_header(uint4 h, int t)
+// Scale/min bytes of pair t: scp = {sc_2t, sc_2t+1}, mp = {m_2t, m_2t+1} as
+// two bytes each, branch-free for a lane with fixed t (see PairSel).
+struct PairSel {
+    uint32_t sh;    // 16 for odd t
+    uint32_t hi;    // t >= 2: sub-blocks 4..7
+    uint32_t mA;    // 0x3F3F (t < 2) or 0x0F0F
+    uint32_t mB;    // 0 (t < 2) or 0x3030
+};
+__device__ __forceinline__ PairSel pair_sel(int t)
+{
+    PairSel p;
+    p.sh = (t & 1) ? 16u : 0u;
+    p.hi = (t >= 2) ? 1u : 0u;
+    p.mA = p.hi ? 0x0F0Fu : 0x3F3Fu;
+    p.mB = p.hi ? 0x3030u : 0u;
+    return p;
+}
+
+__device__ __forceinline__ void pair_scales(uint4 h, const PairSel &p, uint32_t &scp, uint32_t &mp)
+{
+    const uint32_t a0 = h.y >> p.sh;   // s[2(t&1)], s[2(t&1)+1] in the low 16 bits
+    const uint32_t a1 = h.z >> p.sh;   // s[4+...]
+    const uint32_t a2 = h.w >> p.sh;   // s[8+...]
+    // t < 2:  sc = a0 & 63,                       m = a1 & 63
+    // t >= 2: sc = (a2 & 15) | (a0 >> 6) << 4,     m = (a2 >> 4 & 15) | (a1 >> 6) << 4
+    const uint32_t lsc = p.hi ? a2 : a0;
+    const uint32_t lm = p.hi ? (a2 >> 4) : a1;
+    scp = (lsc & p.mA) | ((a0 >> 2) & p.mB);
+    mp = (lm & p.mA) | ((a1 >> 2) & p.mB);
+}
+
+__device__ __forceinline__ RowConsts decode_header(uint4 h, const PairSel &ps)
 {
     RowConsts rc;
     rc.d = half_lo_f32(h.x);
     rc.dmin = half_hi_f32(h.x);
-    const uint32_t sh = (t & 1) ? 16u : 0u;
-    const uint32_t a0 = (h.y >> sh) & 0xFFFFu;   // s[2(t&1)], s[2(t&1)+1]
-    const uint32_t a1 = (h.z >> sh) & 0xFFFFu;   // s[4+...]
-    const uint32_t a2 = (h.w >> sh) & 0xFFFFu;   // s[8+...]
     uint32_t scp, mp;
-    if (t < 2) {
-        scp = a0 & 0x3F3Fu;
-        mp = a1 & 0x3F3Fu;
-    } else {
-        scp = (a2 & 0x0F0Fu) | ((a0 >> 2) & 0x3030u);
-        mp = ((a2 >> 4) & 0x0F0Fu) | ((a1 >> 2) & 0x3030u);
-    }
+    pair_scales(h, ps, scp, mp);
     const uint32_t k1024 = 0x64006400u;          // f16x2 {1024, 1024}
     uint32_t sch = hsub2_u32(__byte_perm(scp, 0u, 0x4140u) | k1024, k1024);   // {sc_2t, sc_2t+1}
     rc.mpair = hsub2_u32(__byte_perm(mp, 0u, 0x4140u) | k1024, k1024);       // {m_2t, m_2t+1}
@@ -245,27 +266,17 @@ struct RowConstsI {
     int scE, scO, mE, mO;
     float d, dmin;
 };
-__device__ __forceinline__ RowConstsI decode_header_i(uint4 h, int t)
+__device__ __forceinline__ RowConstsI decode_header_i(uint4 h, const PairSel &p)
 {
     RowConstsI rc;
     rc.d = half_lo_f32(h.x);
     rc.dmin = half_hi_f32(h.x);
-    const uint32_t sh = (t & 1) ? 16u : 0u;
-    const uint32_t a0 = (h.y >> sh) & 0xFFFFu;   // s[2(t&1)], s[2(t&1)+1]
-    const uint32_t a1 = (h.z >> sh) & 0xFFFFu;   // s[4+...]
-    const uint32_t a2 = (h.w >> sh) & 0xFFFFu;   // s[8+...]
     uint32_t scp, mp;
-    if (t < 2) {
-        scp = a0 & 0x3F3Fu;
-        mp = a1 & 0x3F3Fu;
-    } else {
-        scp = (a2 & 0x0F0Fu) | ((a0 >> 2) & 0x3030u);
-        mp = ((a2 >> 4) & 0x0F0Fu) | ((a1 >> 2) & 0x3030u);
-    }
+    pair_scales(h, p, scp, mp);
     rc.scE = static_cast<int>(scp & 0xFFu);
-    rc.scO = static_cast<int>(scp >> 8);
+    rc.scO = static_cast<int>((scp >> 8) & 0xFFu);
     rc.mE = static_cast<int>(mp & 0xFFu);
-    rc.mO = static_cast<int>(mp >> 8);
+    rc.mO = static_cast<int>((mp >> 8) & 0xFFu);
     return rc;
 }
 
@@ -281,10 +292,11 @@ __device__ __forceinline__ RowConstsI decode_header_i(uint4 h, int t)
 // (every intermediate in the normal range, whatever the size of x).
 template <bool Q8, typename Release>
 __device__ __forceinline__ void stage_compute_i8(const uint8_t *ra, const uint8_t *rb, const uint8_t *xb, int t,
-                                                 float u, float pre, float (&acc)[1][2], Release &&release)
+                                                 const PairSel &ps, float u, float pre, float (&acc)[1][2],
+                                                 Release &&release)
 {
-    const RowConstsI r0 = decode_header_i(*reinterpret_cast<const uint4 *>(ra), t);
-    const RowConstsI r1 = decode_header_i(*reinterpret_cast<const uint4 *>(rb), t);
+    const RowConstsI r0 = decode_header_i(*reinterpret_cast<const uint4 *>(ra), ps);
+    const RowConstsI r1 = decode_header_i(*reinterpret_cast<const uint4 *>(rb), ps);
     int eh0 = 0, el0 = 0, oh0 = 0, ol0 = 0, eh1 = 0, el1 = 0, oh1 = 0, ol1 = 0;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -339,10 +351,11 @@ __device__ __forceinline__ void stage_compute_i8(const uint8_t *ra, const uint8_
 // sub-block parity (2: shorter dependency chains; 1: fewer registers).
 template <int NT, int NC, typename Release>
 __device__ __forceinline__ void stage_compute(const uint8_t *ra, const uint8_t *rb, const uint2 *xl, int t,
-                                              const float (&unscale)[NT], float (&acc)[NT][2], Release &&release)
+                                              const PairSel &ps, const float (&unscale)[NT], float (&acc)[NT][2],
+                                              Release &&release)
 {
-    const RowConsts r0 = decode_header(*reinterpret_cast<const uint4 *>(ra), t);
-    const RowConsts r1 = decode_header(*reinterpret_cast<const uint4 *>(rb), t);
+    const RowConsts r0 = decode_header(*reinterpret_cast<const uint4 *>(ra), ps);
+    const RowConsts r1 = decode_header(*reinterpret_cast<const uint4 *>(rb), ps);
     float cE[NC][NT][4], cO[NC][NT][4], cM[NT][4];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {

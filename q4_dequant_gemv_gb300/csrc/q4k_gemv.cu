@@ -315,6 +315,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
 
     const int g = lane >> 2;
     const int t = lane & 3;
+    const PairSel psel = pair_sel(t);
     const int nchunks = (ks + args.kc - 1) / args.kc;
     const bool single_chunk = (nchunks == 1);
     // batch 1 on the integer path: int8 x parts, one block of the fragment area per super-block
@@ -344,7 +345,9 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
         for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = 0.f;
         float unscale[NT];
         int chunk_end = -1;
+        int blk = -1;   // this super-block's place in the x chunk (counted, not divided)
         for (int kbl = 0; kbl < ks; ++kbl) {
+            ++blk;
             if (!single_chunk && kbl > chunk_end) {
                 const int cn = min(args.kc, ks - kbl);
                 named_bar_sync(1, kThreads);     // everyone done with the previous chunk
@@ -353,9 +356,9 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
                 else
                     convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, tid, kThreads);
                 chunk_end = kbl + cn - 1;
+                blk = 0;
             }
             // this super-block's x scale per batch row
-            const int blk = single_chunk ? kbl : (kbl % args.kc);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const int b = t + 4 * nt;
@@ -373,8 +376,7 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             const uint8_t *ra = ring + slot * kStageBytes + row_off;   // row g of this warp
             const uint8_t *rb = ra + 8 * kBlockBytes;                   // row g + 8
             // this lane's B fragments of this super-block (lane-major layout)
-            const uint2 *xl = xf + static_cast<size_t>((single_chunk ? kbl : (kbl % args.kc)) * LW + blane) *
-                                       lane_stride(NT);
+            const uint2 *xl = xf + static_cast<size_t>(blk * LW + blane) * lane_stride(NT);
             // two accumulator chains per parity at batch <= 4 (shorter chains), one above (fewer registers)
             auto release = [&]() {
                 // This warp is done with the slot: the last warp to finish refills it.
@@ -394,9 +396,9 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
                 ++consumed;
             };
             if constexpr (I8)
-                stage_compute_i8<Q8>(ra, rb, xb + blk * blk_bytes, t, unscale[0], s_pre[blk], acc, release);
+                stage_compute_i8<Q8>(ra, rb, xb + blk * blk_bytes, t, psel, unscale[0], s_pre[blk], acc, release);
             else
-                stage_compute<NT, NT == 1 ? 2 : 1>(ra, rb, xl, t, unscale, acc, release);
+                stage_compute<NT, NT == 1 ? 2 : 1>(ra, rb, xl, t, psel, unscale, acc, release);
         }
         // ---------------- tile epilogue
         if constexpr (I8) {   // sum the four sub-block-pair lanes of each row

@@ -3,21 +3,30 @@
 // Y[t][n] = sum_k w[n][k] X[t][k] for a block of T prompt tokens: the dense
 // contraction that the dotLLM README's CUDA backend sends to "cuBLAS HGEMM for
 // prefill" after "on-the-fly weight dequantization" (News 2026-03).  Here the
-// weights are dequantized straight into shared memory as bf16 and multiplied
-// by hand-issued tcgen05.mma instructions, fp32 accumulation in tensor memory.
+// weights are dequantized straight into shared memory as 16-bit floats and
+// multiplied by hand-issued tcgen05.mma instructions, fp32 accumulation in
+// tensor memory.
+//
+// Precision: kind::f16 takes A and B of one type, and X arrives as bf16.  Both
+// sides go to fp16 (11 significant bits, 3 more than bf16: one fp16 rounding
+// of w keeps the product well inside the decode path's error budget, one bf16
+// rounding does not), each under a power-of-two scale that keeps it in fp16's
+// range whatever the data: a small kernel first converts X per token (max|x|
+// brought to [2^14, 2^15), so every bf16 value of at least 2^-31 times the
+// token's max converts exactly), and each dequantizing thread scales its weight
+// row by 2^r chosen from the row's largest possible |w| (|d|*945 + |dmin|*63
+// over its super-blocks).  The epilogue multiplies by 2^-r and the token's
+// inverse scale.
 //
 // CTA tile: 128 weight rows (the MMA M side) x TN*NTT tokens (the N side),
 // full K.  Per 64-wide K chunk (a quarter of a super-block):
 //   * warps 0-3 (one thread per weight row) read the row's sub-block pair from
-//     global memory, compute w = d*sc*q - dmin*m in fp32 and split it into two
-//     bf16 values, hi = bf16(w) and lo = bf16(w - hi) (|w - hi - lo| <=
-//     2^-17 |w|), stored as two 128-byte-swizzled K-major tiles.  A single
-//     bf16 rounding of w (8 significant bits) would put the product outside
-//     the decode path's error budget; the split keeps it at fp32 quality;
-//   * warp 4 loads the X tile [TN x 64] with a TMA tensor copy (128B swizzle);
-//   * warp 5 (one elected thread) issues 2 x 4 x NTT tcgen05.mma (K = 16
-//     each: hi tile, then lo tile, same accumulator) into TMEM and commits to
-//     the stage's "empty" barrier.
+//     global memory, compute w = d*sc*q - dmin*m in fp32, scale it by 2^r and
+//     round it to fp16 into a 128-byte-swizzled K-major tile;
+//   * warp 4 loads the X tile [TN x 64] (fp16) with a TMA tensor copy (128B
+//     swizzle);
+//   * warp 5 (one elected thread) issues 4 x NTT tcgen05.mma (K = 16 each)
+//     into TMEM and commits to the stage's "empty" barrier.
 // A ring of NS stages overlaps the three.  The epilogue reads TMEM with
 // tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = weight rows) and writes Y
 // with coalesced stores.  Every mbarrier wait is bounded in time.
@@ -54,8 +63,8 @@ namespace pf {
 constexpr int kRowsM = 128;          // MMA M
 constexpr int kChunk = 64;           // K elements per stage (one 128-byte swizzle row)
 constexpr int kThreads = 192;        // 4 dequant/epilogue warps + TMA warp + MMA warp
-constexpr int kATileBytes = kRowsM * kChunk * 2;    // 16 KB: one bf16 weight tile
-constexpr int kAStageBytes = 2 * kATileBytes;       // hi + lo tiles
+constexpr int kATileBytes = kRowsM * kChunk * 2;    // 16 KB: one fp16 weight tile
+constexpr int kAStageBytes = kATileBytes;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kPrefetch = 3;        // chunks of weight loads in flight per dequant thread
 
@@ -75,8 +84,8 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                          uint32_t accumulate)
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -128,25 +137,90 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
     return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+// Instruction descriptor, kind::f16: fp16 A and B (format 0), fp32 D, both
+// K-major.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N)
 {
     return (1u << 4)                                   // D format f32
-           | (1u << 7)                                 // A format bf16
-           | (1u << 10)                                // B format bf16
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-__device__ __forceinline__ float bf16_lo_f32(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi_f32(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+// Power-of-two exponent e with v * 2^e in [2^14, 2^15) for a positive finite
+// v (0 for 0, inf or NaN), clamped so that 2^e and 2^-e stay normal.
+__device__ __forceinline__ int f16_range_exp(float v)
 {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
+    const uint32_t b = __float_as_uint(v);
+    const int E = static_cast<int>((b >> 23) & 255u);
+    if (b == 0u || E == 255) return 0;
+    return max(-126, min(126, 141 - E));
 }
+
+// X (bf16 [T][K]) -> fp16 [T][K] times 2^e_t per token, and xexp[t] = e_t.
+// One CTA per token: the max |x|, then the exact conversion.  A token of up
+// to kXv * 8 * 256 elements is read once and held in registers; longer rows
+// are read twice.  The prefill kernel that follows is launched as its
+// programmatic dependent: it starts streaming and dequantizing W while this
+// runs.
+constexpr int kXv = 8;
+__global__ void __launch_bounds__(256) x_to_f16_kernel(const uint16_t *__restrict__ X, uint16_t *__restrict__ Xh,
+                                                       int *__restrict__ xexp, int K)
+{
+    __shared__ uint32_t s_max[8];
+    pdl_launch_dependents();
+    const size_t t = blockIdx.x;
+    const uint4 *src = reinterpret_cast<const uint4 *>(X + t * K);
+    uint4 *dst = reinterpret_cast<uint4 *>(Xh + t * K);
+    const int nv = K / 8;
+    const bool in_regs = nv <= kXv * static_cast<int>(blockDim.x);
+    uint4 v[kXv];
+    uint32_t m = 0u;   // max |x| as fp32 bits
+    auto absmax = [](uint32_t m, const uint4 &q) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m = max(m, max((w[j] << 16) & 0x7FFFFFFFu, w[j] & 0x7FFF0000u));
+        return m;
+    };
+    if (in_regs) {
+#pragma unroll
+        for (int r = 0; r < kXv; ++r) {
+            const int i = threadIdx.x + r * blockDim.x;
+            v[r] = (i < nv) ? src[i] : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int r = 0; r < kXv; ++r) m = absmax(m, v[r]);
+    } else {
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) m = absmax(m, src[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = s_max[0];
+    for (int i = 1; i < static_cast<int>(blockDim.x >> 5); ++i) m = max(m, s_max[i]);
+    const int e = f16_range_exp(__uint_as_float(m));
+    const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
+    if (threadIdx.x == 0) xexp[t] = e;
+    auto convert = [sc](const uint4 &q) {
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[j] = pack_half2(__uint_as_float(w[j] << 16) * sc, __uint_as_float(w[j] & 0xFFFF0000u) * sc);
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    if (in_regs) {
+#pragma unroll
+        for (int r = 0; r < kXv; ++r) {
+            const int i = threadIdx.x + r * blockDim.x;
+            if (i < nv) dst[i] = convert(v[r]);
+        }
+    } else {
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = convert(src[i]);
+    }
+}
+
+
 
 template <int TN, int NTT>
 struct Cfg {
@@ -161,8 +235,8 @@ struct Cfg {
 
 template <int TN, int NTT>
 __global__ void __launch_bounds__(kThreads, 1)
-    q4k_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t *__restrict__ W, float *__restrict__ Y,
-                       int N, int K, int T)
+    q4k_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t *__restrict__ W,
+                       const int *__restrict__ xexp, float *__restrict__ Y, int N, int K, int T)
 {
     using C = Cfg<TN, NTT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -176,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = tid & 31;
     const int row0 = blockIdx.x * kRowsM;
     const int t0 = blockIdx.y * TN * NTT;
+    int rexp = 0;   // dequant/epilogue threads: r of the tile row they own (w scaled by 2^r)
     const int nsub = min(NTT, (T - t0 + TN - 1) / TN);
     // K split over the CTAs of a cluster along z (split == 1: whole K)
     const int split = gridDim.z;
@@ -212,6 +287,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint8_t *wrow = W + static_cast<size_t>(live ? n : 0) * row_bytes;
         int stage = 0;
         uint32_t phase = 0;
+        // Row scale 2^rs: the largest |w| this CTA's super-blocks of the row
+        // can hold, |d|*945 + |dmin|*63, brought to [2^14, 2^15).
+        float wmax = 0.f;
+        if (live) {
+            const int b0 = c_begin >> 2, b1 = (c_end + 3) >> 2;
+            for (int b = b0; b < b1; b += 8) {
+                uint32_t hb[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    hb[i] = (b + i < b1) ? __ldg(reinterpret_cast<const uint32_t *>(wrow + static_cast<size_t>(b + i) * 144)) : 0u;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    wmax = fmaxf(wmax, fmaf(fabsf(half_lo_f32(hb[i])), 945.0f, fabsf(half_hi_f32(hb[i])) * 63.0f));
+            }
+        }
+        rexp = f16_range_exp(wmax);
+        const float rscale = __uint_as_float(static_cast<uint32_t>(rexp + 127) << 23);
         // The row's global loads run kPrefetch chunks ahead of the dequant, so
         // the memory latency overlaps the work on the chunks in between.
         uint4 nh[kPrefetch], na[kPrefetch], nb[kPrefetch];
@@ -254,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 };
                 scE = sc_of(j0); mE = m_of(j0); scO = sc_of(j1); mO = m_of(j1);
             }
-            const float dsE = d * static_cast<float>(scE), dmE = dmin * static_cast<float>(mE);
-            const float dsO16 = d * static_cast<float>(scO) * 0.0625f, dmO = dmin * static_cast<float>(mO);
+            const float dsE = d * static_cast<float>(scE) * rscale, dmE = dmin * static_cast<float>(mE) * rscale;
+            const float dsO16 = d * static_cast<float>(scO) * 0.0625f * rscale, dmO = dmin * static_cast<float>(mO) * rscale;
             const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
             uint8_t *arow = smem + stage * C::kStageBytes + r * 128;
             const uint32_t k1024 = 0x64006400u;
@@ -263,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int half = 0; half < 2; ++half) {           // 0: low nibbles (k 0..31), 1: high (k 32..63)
 #pragma unroll
                 for (int c8 = 0; c8 < 4; ++c8) {             // 16-byte chunk: k = 32*half + 8*c8 .. +7
-                    uint32_t out[4], outl[4];
+                    uint32_t out[4];
 #pragma unroll
                     for (int uu = 0; uu < 2; ++uu) {         // word u = 2*c8 + uu -> k offset 4u..4u+3
                         const uint32_t w = words[2 * c8 + uu];
@@ -277,17 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float w2 = fmaf(half_hi_f32(h02), ds, -dm);
                         const float w1 = fmaf(half_lo_f32(h13), ds, -dm);
                         const float w3 = fmaf(half_hi_f32(h13), ds, -dm);
-                        const uint32_t h01 = pack_bf16x2(w0, w1), h23 = pack_bf16x2(w2, w3);
-                        out[2 * uu] = h01;
-                        out[2 * uu + 1] = h23;
-                        outl[2 * uu] = pack_bf16x2(w0 - bf16_lo_f32(h01), w1 - bf16_hi_f32(h01));
-                        outl[2 * uu + 1] = pack_bf16x2(w2 - bf16_lo_f32(h23), w3 - bf16_hi_f32(h23));
+                        out[2 * uu] = pack_half2(w0, w1);
+                        out[2 * uu + 1] = pack_half2(w2, w3);
                     }
                     const int chunk = 4 * half + c8;
-                    uint4 v = live ? make_uint4(out[0], out[1], out[2], out[3]) : make_uint4(0, 0, 0, 0);
-                    uint4 vl = live ? make_uint4(outl[0], outl[1], outl[2], outl[3]) : make_uint4(0, 0, 0, 0);
+                    const uint4 v = live ? make_uint4(out[0], out[1], out[2], out[3]) : make_uint4(0, 0, 0, 0);
                     *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) = v;
-                    *reinterpret_cast<uint4 *>(arow + kATileBytes + ((chunk ^ (r & 7)) << 4)) = vl;
                 }
             }
             fence_proxy_async_smem();
@@ -297,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 4) {
         // ------------------------------------------------ X tiles by TMA
         if (lane == 0) {
+            pdl_wait();   // X (fp16) is written by the conversion kernel launched just before
             int stage = 0;
             uint32_t phase = 0;
             int issued = 0;
@@ -331,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
-            constexpr uint32_t idesc = idesc_bf16(kRowsM, TN);
+            constexpr uint32_t idesc = idesc_f16(kRowsM, TN);
             for (int c = c_begin; c < c_end; ++c) {
                 bool ok = !*(volatile int *)&s_abort;
                 if (ok && !mbar_wait_bounded(smem_u32(&full_a[stage]), phase, kWaitLimitNs)) ok = false;
@@ -350,9 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int kk = 0; kk < kChunk / 16; ++kk) {
                                 const uint64_t bd = sw128_desc(b_addr + j * C::kBBytes + kk * 32);
-                                umma_bf16(tmem + j * TN, sw128_desc(a_addr + kk * 32), bd, idesc,
-                                          (c > c_begin || kk > 0) ? 1u : 0u);
-                                umma_bf16(tmem + j * TN, sw128_desc(a_addr + kATileBytes + kk * 32), bd, idesc, 1u);
+                                umma_f16(tmem + j * TN, sw128_desc(a_addr + kk * 32), bd, idesc,
+                                         (c > c_begin || kk > 0) ? 1u : 0u);
                             }
                         }
                     }
@@ -371,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // [z*128/split, (z+1)*128/split) over ranks 0..split-1 in order and writes Y.
     float *part = reinterpret_cast<float *>(smem);   // pipeline buffers are idle by now
     if (warp < 4) {
+        pdl_wait();   // the token exponents come from the conversion kernel
         const bool ok = mbar_wait_bounded(smem_u32(&done_bar), 0u, kWaitLimitNs);
         if (!ok) {
             atomicOr(&g_prefill_error, 2u);
@@ -386,14 +474,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[16];
                 tmem_ld16(lane_addr + j * TN + c0, v);
                 tmem_wait_ld();
+                // undo the row's and the tokens' power-of-two scales (one
+                // exact scaling by 2^-(r + e_t))
+                float o[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int t = min(t0 + j * TN + c0 + i, T - 1);
+                    o[i] = ldexpf(__uint_as_float(v[i]), -(rexp + __ldg(xexp + t)));
+                }
                 if (split > 1) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) part[(j * TN + c0 + i) * kRowsM + r] = __uint_as_float(v[i]);
+                    for (int i = 0; i < 16; ++i) part[(j * TN + c0 + i) * kRowsM + r] = o[i];
                 } else if (ok && n < N) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int t = t0 + j * TN + c0 + i;
-                        if (t < T) Y[static_cast<size_t>(t) * N + n] = __uint_as_float(v[i]);
+                        if (t < T) Y[static_cast<size_t>(t) * N + n] = o[i];
                     }
                 }
             }
@@ -441,8 +537,8 @@ static q4k_status validate_prefill(const void *W, const void *X, const float *Y,
 }
 
 template <int TN, int NTT>
-static cudaError_t launch_prefill(const uint8_t *W, const void *X, float *Y, int N, int K, int T, int split,
-                                  cudaStream_t s)
+static cudaError_t launch_prefill(const uint8_t *W, const void *Xh, const int *xexp, float *Y, int N, int K, int T,
+                                  int split, cudaStream_t s)
 {
     using C = pf::Cfg<TN, NTT>;
     // the split-K partial tile (128 x TN*NTT fp32) reuses the pipeline buffers
@@ -454,7 +550,7 @@ static cudaError_t launch_prefill(const uint8_t *W, const void *X, float *Y, int
     cuuint64_t gstride[1] = {static_cast<cuuint64_t>(K) * 2};
     cuuint32_t box[2] = {static_cast<cuuint32_t>(pf::kChunk), static_cast<cuuint32_t>(TN)};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(X), gdim, gstride, box, estr,
+    CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(Xh), gdim, gstride, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
@@ -480,9 +576,17 @@ static cudaError_t launch_prefill(const uint8_t *W, const void *X, float *Y, int
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = split;
-    cfg.attrs = attr;
-    cfg.numAttrs = split > 1 ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, W, Y, N, K, T);
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (split > 1) attrs[na++] = attr[0];
+    // W streams and dequantizes while the X conversion before it finishes;
+    // the kernel waits for it (griddepcontrol.wait) before reading X
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, W, xexp, Y, N, K, T);
     if (e != cudaSuccess) (void)cudaGetLastError();
     return e;
 }
@@ -518,12 +622,27 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     int split = 1;
     while (ntt == 1 && split < 8 && ctas * split * 2 <= static_cast<long long>(sms) + sms / 2 && (k / 64) / (split * 2) >= 8)
         split *= 2;
-    cudaError_t e;
-    if (tn == 32) e = launch_prefill<32, 1>(Wb, X, Y, n, k, t, split, s);
-    else if (tn == 64) e = launch_prefill<64, 1>(Wb, X, Y, n, k, t, split, s);
-    else if (tn == 128) e = launch_prefill<128, 1>(Wb, X, Y, n, k, t, split, s);
-    else if (ntt == 1) e = launch_prefill<256, 1>(Wb, X, Y, n, k, t, split, s);
-    else e = launch_prefill<256, 2>(Wb, X, Y, n, k, t, split, s);
+    // X in fp16 under a power-of-two scale per token: T*K*2 bytes plus the
+    // exponents, from the stream-ordered allocator on the caller's stream
+    const size_t xh_bytes = (static_cast<size_t>(T) * static_cast<size_t>(K) * 2 + 255) & ~size_t(255);
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, xh_bytes + static_cast<size_t>(T) * 4, s) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return Q4K_ERR_CUDA;
+    }
+    uint16_t *Xh = static_cast<uint16_t *>(scratch);
+    int *xexp = reinterpret_cast<int *>(static_cast<uint8_t *>(scratch) + xh_bytes);
+    pf::x_to_f16_kernel<<<t, 256, 0, s>>>(static_cast<const uint16_t *>(X), Xh, xexp, k);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) {
+        if (tn == 32) e = launch_prefill<32, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
+        else if (tn == 64) e = launch_prefill<64, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
+        else if (tn == 128) e = launch_prefill<128, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
+        else if (ntt == 1) e = launch_prefill<256, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
+        else e = launch_prefill<256, 2>(Wb, Xh, xexp, Y, n, k, t, split, s);
+    }
+    const cudaError_t ef = cudaFreeAsync(scratch, s);
+    if (e == cudaSuccess) e = ef;
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
 
