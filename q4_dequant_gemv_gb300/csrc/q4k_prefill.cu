@@ -39,6 +39,7 @@
 #include <mutex>
 
 #include "ptx.cuh"
+#include "q4k_dev.cuh"
 #include "q4k_internal.h"
 
 namespace q4k {
@@ -66,7 +67,6 @@ constexpr int kThreads = 192;        // 4 dequant/epilogue warps + TMA warp + MM
 constexpr int kATileBytes = kRowsM * kChunk * 2;    // 16 KB: one fp16 weight tile
 constexpr int kAStageBytes = kATileBytes;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int kPrefetch = 3;        // chunks of weight loads in flight per dequant thread
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
@@ -84,20 +84,30 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// tcgen05.mma and tcgen05.commit issued by one elected lane of a warp that
+// runs the issue loop as a whole: the loop's descriptor arithmetic then stays
+// warp-uniform.  (Measured on this GPU: an M128 K16 MMA every ~40 cycles at
+// N <= 32 this way, against ~108 cycles from a loop that only lane 0 runs.)
+// The caller keeps the warp converged at every call.
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate)
 {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t"
+        "{\n\t.reg .pred p, e;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
@@ -162,9 +172,17 @@ __device__ __forceinline__ int f16_range_exp(float v)
 // are read twice.  The prefill kernel that follows is launched as its
 // programmatic dependent: it starts streaming and dequantizing W while this
 // runs.
+//
+// EXACT (the small-T kernel's layout): within every aligned group of four k
+// the middle two are swapped (k order 0, 2, 1, 3), the order in which that
+// kernel's weight tiles come out of its nibble arithmetic, and XS[t][sb][0..15]
+// receives the sums of the scaled x over the eight 32-wide sub-blocks of
+// super-block sb, times 2^-6, as fp16 hi (0..7) and lo (8..15) parts; entries
+// 16..63 of each super-block are zero.
 constexpr int kXv = 8;
+template <bool EXACT>
 __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint16_t *__restrict__ X, uint16_t *__restrict__ Xh,
-                                                       int *__restrict__ xexp, int K)
+                                                       int *__restrict__ xexp, uint16_t *__restrict__ XS, int K)
 {
     __shared__ uint32_t s_max[8];
     pdl_launch_dependents();
@@ -201,25 +219,53 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint16_t *__restric
     const int e = f16_range_exp(__uint_as_float(m));
     const float sc = __uint_as_float(static_cast<uint32_t>(e + 127) << 23);
     if (threadIdx.x == 0) xexp[t] = e;
-    auto convert = [sc](const uint4 &q) {
+    // converts one 8-element group; i = its index in the row
+    auto convert = [&](const uint4 &q, int i) {
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-        uint32_t o[4];
+        float f[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            o[j] = pack_half2(__uint_as_float(w[j] << 16) * sc, __uint_as_float(w[j] & 0xFFFF0000u) * sc);
-        return make_uint4(o[0], o[1], o[2], o[3]);
+        for (int j = 0; j < 4; ++j) {
+            f[2 * j] = __uint_as_float(w[j] << 16) * sc;
+            f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u) * sc;
+        }
+        if (EXACT) {
+            dst[i] = make_uint4(pack_half2(f[0], f[2]), pack_half2(f[1], f[3]), pack_half2(f[4], f[6]),
+                                pack_half2(f[5], f[7]));
+            // sub-block j = i / 4 is held by the four lanes 4(i/4) .. +3 of
+            // this warp (the row stride of the loop is a multiple of 4)
+            float sum = ((f[0] + f[1]) + (f[2] + f[3])) + ((f[4] + f[5]) + (f[6] + f[7]));
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            if ((i & 3) == 0) {
+                const int j = i >> 2;
+                uint16_t *xs = XS + (t * (K / 256) + (j >> 3)) * 64;
+                const float s6 = sum * 0.015625f;
+                const __half hi = __float2half_rn(s6);
+                const __half lo = __float2half_rn(s6 - __half2float(hi));
+                xs[j & 7] = __half_as_ushort(hi);
+                xs[8 + (j & 7)] = __half_as_ushort(lo);
+                if ((j & 7) == 0) {
+                    uint4 *z = reinterpret_cast<uint4 *>(xs + 16);
+#pragma unroll
+                    for (int u = 0; u < 6; ++u) z[u] = make_uint4(0, 0, 0, 0);
+                }
+            }
+        } else {
+            dst[i] = make_uint4(pack_half2(f[0], f[1]), pack_half2(f[2], f[3]), pack_half2(f[4], f[5]),
+                                pack_half2(f[6], f[7]));
+        }
     };
     if (in_regs) {
 #pragma unroll
         for (int r = 0; r < kXv; ++r) {
             const int i = threadIdx.x + r * blockDim.x;
-            if (i < nv) dst[i] = convert(v[r]);
+            // (whole warps take the same branch: nv is a multiple of 32)
+            if (i < nv) convert(v[r], i);
         }
     } else {
-        for (int i = threadIdx.x; i < nv; i += blockDim.x) dst[i] = convert(src[i]);
+        for (int i = threadIdx.x; i < nv; i += blockDim.x) convert(src[i], i);
     }
 }
-
 
 
 template <int TN, int NTT>
@@ -234,7 +280,7 @@ struct Cfg {
 };
 
 template <int TN, int NTT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, (TN * NTT <= 32) ? 2 : 1)
     q4k_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t *__restrict__ W,
                        const int *__restrict__ xexp, float *__restrict__ Y, int N, int K, int T)
 {
@@ -244,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) uint64_t full_a[C::kStages], full_b[C::kStages], empty[C::kStages], done_bar;
     __shared__ uint32_t tmem_base_s;
     __shared__ int s_abort;
+    __shared__ __align__(16) int s_xexp[TN * NTT];   // token scale exponents of this CTA's tokens
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -255,9 +302,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // K split over the CTAs of a cluster along z (split == 1: whole K)
     const int split = gridDim.z;
     const int kz = blockIdx.z;
-    const int c_begin = static_cast<int>((static_cast<long long>(kz) * (K / kChunk)) / split);
-    const int c_end = static_cast<int>((static_cast<long long>(kz + 1) * (K / kChunk)) / split);
+    // (whole super-blocks per CTA: four chunks each)
+    const int c_begin = 4 * static_cast<int>((static_cast<long long>(kz) * (K / 256)) / split);
+    const int c_end = 4 * static_cast<int>((static_cast<long long>(kz + 1) * (K / 256)) / split);
     const size_t row_bytes = static_cast<size_t>(K / 256) * 144;
+    // Super-blocks of this CTA's K range in a per-row-tile rotated order (so
+    // that the CTAs' X tile requests spread over L2).
+    const int sb_begin = c_begin >> 2, sb_end = c_end >> 2, nloc = sb_end - sb_begin;
+    const int rot = static_cast<int>(blockIdx.x % static_cast<unsigned>(nloc));
+    auto sb_of = [&](int i) {
+        const int j = i + rot;
+        return sb_begin + (j >= nloc ? j - nloc : j);
+    };
 
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -291,12 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // can hold, |d|*945 + |dmin|*63, brought to [2^14, 2^15).
         float wmax = 0.f;
         if (live) {
-            const int b0 = c_begin >> 2, b1 = (c_end + 3) >> 2;
-            for (int b = b0; b < b1; b += 8) {
+            for (int b = sb_begin; b < sb_end; b += 8) {
                 uint32_t hb[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    hb[i] = (b + i < b1) ? __ldg(reinterpret_cast<const uint32_t *>(wrow + static_cast<size_t>(b + i) * 144)) : 0u;
+                    hb[i] = (b + i < sb_end) ? __ldg(reinterpret_cast<const uint32_t *>(wrow + static_cast<size_t>(b + i) * 144)) : 0u;
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     wmax = fmaxf(wmax, fmaf(fabsf(half_lo_f32(hb[i])), 945.0f, fabsf(half_hi_f32(hb[i])) * 63.0f));
@@ -304,82 +359,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         rexp = f16_range_exp(wmax);
         const float rscale = __uint_as_float(static_cast<uint32_t>(rexp + 127) << 23);
-        // The row's global loads run kPrefetch chunks ahead of the dequant, so
-        // the memory latency overlaps the work on the chunks in between.
-        uint4 nh[kPrefetch], na[kPrefetch], nb[kPrefetch];
-        auto load_chunk = [&](int c, uint4 &h, uint4 &a, uint4 &b) {
-            h = a = b = make_uint4(0, 0, 0, 0);
-            if (live && c < c_end) {
-                const uint8_t *bp = wrow + static_cast<size_t>(c >> 2) * 144;
-                const int p = c & 3;
-                h = __ldg(reinterpret_cast<const uint4 *>(bp));
-                a = __ldg(reinterpret_cast<const uint4 *>(bp + 16 + 32 * p));
-                b = __ldg(reinterpret_cast<const uint4 *>(bp + 32 + 32 * p));
+        // A super-block of the row as nine 16-byte words (header, then the
+        // 128 quant bytes), loaded one super-block ahead of its dequant.  Rows
+        // past N and super-blocks past the CTA's range read as zeros: d = dmin
+        // = 0 makes every weight of them zero.
+        auto load_sb = [&](int i, uint4 (&q)[9]) {
+            const bool ok = live && i < nloc;
+            const uint4 *bp = reinterpret_cast<const uint4 *>(wrow + static_cast<size_t>(sb_of(ok ? i : 0)) * 144);
+#pragma unroll
+            for (int u = 0; u < 9; ++u) q[u] = ok ? __ldg(bp + u) : make_uint4(0, 0, 0, 0);
+            if (live && i + 1 < nloc) {   // the super-block after it, into L2
+                const uint8_t *nb = wrow + static_cast<size_t>(sb_of(i + 1)) * 144;
+                prefetch_l2(nb);
+                prefetch_l2(nb + 128);
+                prefetch_l2(nb + 143);
             }
         };
+        // One super-block = four K chunks; chunk p holds sub-blocks 2p (low
+        // nibbles of quant bytes 32p..32p+31) and 2p+1 (their high nibbles).
+        auto dequant_sb = [&](const uint4 (&q)[9]) {
+            const float d = half_lo_f32(q[0].x) * rscale, dmin = half_hi_f32(q[0].x) * rscale;
 #pragma unroll
-        for (int i = 0; i < kPrefetch; ++i) load_chunk(c_begin + i, nh[i], na[i], nb[i]);
-        for (int c = c_begin; c < c_end; ++c) {
-            const int p = c & 3;
-            const uint4 hdr = nh[0], qa = na[0], qb = nb[0];
-#pragma unroll
-            for (int i = 0; i + 1 < kPrefetch; ++i) { nh[i] = nh[i + 1]; na[i] = na[i + 1]; nb[i] = nb[i + 1]; }
-            load_chunk(c + kPrefetch, nh[kPrefetch - 1], na[kPrefetch - 1], nb[kPrefetch - 1]);
-            if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
-                atomicOr(&g_prefill_error, 2u);
-                s_abort = 1;
-            }
-            // scales of sub-blocks 2p (low nibbles) and 2p+1 (high nibbles)
-            const float d = half_lo_f32(hdr.x), dmin = half_hi_f32(hdr.x);
-            const uint32_t s0 = hdr.y, s1 = hdr.z, s2 = hdr.w;
-            auto byte_of = [](uint32_t w, int i) { return (w >> (8 * i)) & 0xFFu; };
-            int scE, mE, scO, mO;
-            {
-                const int j0 = 2 * p, j1 = 2 * p + 1;
-                auto sc_of = [&](int j) {
-                    return j < 4 ? static_cast<int>(byte_of(s0, j) & 63u)
-                                 : static_cast<int>((byte_of(s2, j - 4) & 15u) | ((byte_of(s0, j - 4) >> 6) << 4));
-                };
-                auto m_of = [&](int j) {
-                    return j < 4 ? static_cast<int>(byte_of(s1, j) & 63u)
-                                 : static_cast<int>((byte_of(s2, j - 4) >> 4) | ((byte_of(s1, j - 4) >> 6) << 4));
-                };
-                scE = sc_of(j0); mE = m_of(j0); scO = sc_of(j1); mO = m_of(j1);
-            }
-            const float dsE = d * static_cast<float>(scE) * rscale, dmE = dmin * static_cast<float>(mE) * rscale;
-            const float dsO16 = d * static_cast<float>(scO) * 0.0625f * rscale, dmO = dmin * static_cast<float>(mO) * rscale;
-            const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-            uint8_t *arow = smem + stage * C::kStageBytes + r * 128;
-            const uint32_t k1024 = 0x64006400u;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {           // 0: low nibbles (k 0..31), 1: high (k 32..63)
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {             // 16-byte chunk: k = 32*half + 8*c8 .. +7
-                    uint32_t out[4];
-#pragma unroll
-                    for (int uu = 0; uu < 2; ++uu) {         // word u = 2*c8 + uu -> k offset 4u..4u+3
-                        const uint32_t w = words[2 * c8 + uu];
-                        const uint32_t mask = half ? 0x00F000F0u : 0x000F000Fu;
-                        // {q(4u), q(4u+2)} and {q(4u+1), q(4u+3)} (x16 for the high nibbles)
-                        const uint32_t h02 = hsub2_u32(and_or(w, mask, k1024), k1024);
-                        const uint32_t h13 = hsub2_u32(and_or(w >> 8, mask, k1024), k1024);
-                        const float ds = half ? dsO16 : dsE;
-                        const float dm = half ? dmO : dmE;
-                        const float w0 = fmaf(half_lo_f32(h02), ds, -dm);
-                        const float w2 = fmaf(half_hi_f32(h02), ds, -dm);
-                        const float w1 = fmaf(half_lo_f32(h13), ds, -dm);
-                        const float w3 = fmaf(half_hi_f32(h13), ds, -dm);
-                        out[2 * uu] = pack_half2(w0, w1);
-                        out[2 * uu + 1] = pack_half2(w2, w3);
-                    }
-                    const int chunk = 4 * half + c8;
-                    const uint4 v = live ? make_uint4(out[0], out[1], out[2], out[3]) : make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) = v;
+            for (int p = 0; p < 4; ++p) {
+                uint32_t scp, mp;
+                pair_scales(q[0], pair_sel(p), scp, mp);
+                const float dsE = d * static_cast<float>(scp & 0xFFu), dmE = dmin * static_cast<float>(mp & 0xFFu);
+                const float dsO16 = d * static_cast<float>((scp >> 8) & 0xFFu) * 0.0625f;
+                const float dmO = dmin * static_cast<float>((mp >> 8) & 0xFFu);
+                if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
+                    atomicOr(&g_prefill_error, 2u);
+                    s_abort = 1;
                 }
+                const uint32_t words[8] = {q[1 + 2 * p].x, q[1 + 2 * p].y, q[1 + 2 * p].z, q[1 + 2 * p].w,
+                                           q[2 + 2 * p].x, q[2 + 2 * p].y, q[2 + 2 * p].z, q[2 + 2 * p].w};
+                uint8_t *arow = smem + stage * C::kStageBytes + r * 128;
+                const uint32_t k1024 = 0x64006400u;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {           // 0: low nibbles (k 0..31), 1: high (k 32..63)
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {             // 16-byte chunk: k = 32*half + 8*c8 .. +7
+                        uint32_t out[4];
+#pragma unroll
+                        for (int uu = 0; uu < 2; ++uu) {         // word u = 2*c8 + uu -> k offset 4u..4u+3
+                            const uint32_t w = words[2 * c8 + uu];
+                            const uint32_t mask = half ? 0x00F000F0u : 0x000F000Fu;
+                            // {q(4u), q(4u+2)} and {q(4u+1), q(4u+3)} (x16 for the high nibbles)
+                            const uint32_t h02 = hsub2_u32(and_or(w, mask, k1024), k1024);
+                            const uint32_t h13 = hsub2_u32(and_or(w >> 8, mask, k1024), k1024);
+                            const float ds = half ? dsO16 : dsE;
+                            const float dm = half ? dmO : dmE;
+                            const float w0 = fmaf(half_lo_f32(h02), ds, -dm);
+                            const float w2 = fmaf(half_hi_f32(h02), ds, -dm);
+                            const float w1 = fmaf(half_lo_f32(h13), ds, -dm);
+                            const float w3 = fmaf(half_hi_f32(h13), ds, -dm);
+                            out[2 * uu] = pack_half2(w0, w1);
+                            out[2 * uu + 1] = pack_half2(w2, w3);
+                        }
+                        const int chunk = 4 * half + c8;
+                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) =
+                            make_uint4(out[0], out[1], out[2], out[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&full_a[stage]));
+                if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
             }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&full_a[stage]));
-            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        };
+        // Two register sets alternate so that no loaded word is ever moved.
+        uint4 qa[9], qb[9];
+        load_sb(0, qa);
+        for (int i = 0; i < nloc; i += 2) {
+            load_sb(i + 1, qb);
+            dequant_sb(qa);
+            if (i + 1 < nloc) {
+                load_sb(i + 2, qa);
+                dequant_sb(qb);
+            }
         }
     } else if (warp == 4) {
         // ------------------------------------------------ X tiles by TMA
@@ -398,8 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!*(volatile int *)&s_abort) {
                     mbar_arrive_expect_tx(smem_u32(&full_b[stage]), bytes);
                     uint8_t *bbase = smem + stage * C::kStageBytes + kAStageBytes;
+                    const int kc = 4 * sb_of((c - c_begin) >> 2) + (c & 3);
                     for (int j = 0; j < nsub; ++j)
-                        tma_load_2d(smem_u32(bbase + j * C::kBBytes), &tmX, c * kChunk, t0 + j * TN,
+                        tma_load_2d(smem_u32(bbase + j * C::kBBytes), &tmX, kc * kChunk, t0 + j * TN,
                                     smem_u32(&full_b[stage]));
                     ++issued;
                 }
@@ -415,8 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // ------------------------------------------------ MMA issuer (whole warp, one elected lane issues)
+        {
             int stage = 0;
             uint32_t phase = 0;
             constexpr uint32_t idesc = idesc_f16(kRowsM, TN);
@@ -424,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = !*(volatile int *)&s_abort;
                 if (ok && !mbar_wait_bounded(smem_u32(&full_a[stage]), phase, kWaitLimitNs)) ok = false;
                 if (ok && !mbar_wait_bounded(smem_u32(&full_b[stage]), phase, kWaitLimitNs)) ok = false;
-                if (!ok && !*(volatile int *)&s_abort) {
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok && lane == 0 && !*(volatile int *)&s_abort) {
                     atomicOr(&g_prefill_error, 2u);
                     s_abort = 1;
                 }
@@ -459,6 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *part = reinterpret_cast<float *>(smem);   // pipeline buffers are idle by now
     if (warp < 4) {
         pdl_wait();   // the token exponents come from the conversion kernel
+        for (int i = tid; i < TN * NTT; i += 128) s_xexp[i] = (t0 + i < T) ? __ldg(xexp + t0 + i) : 0;
+        named_bar_sync(1, 128);
         const bool ok = mbar_wait_bounded(smem_u32(&done_bar), 0u, kWaitLimitNs);
         if (!ok) {
             atomicOr(&g_prefill_error, 2u);
@@ -474,13 +533,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[16];
                 tmem_ld16(lane_addr + j * TN + c0, v);
                 tmem_wait_ld();
-                // undo the row's and the tokens' power-of-two scales (one
-                // exact scaling by 2^-(r + e_t))
+                // undo the row's and the tokens' power-of-two scales: times
+                // 2^-(r + e_t), as two factors that are normal floats (the
+                // second is 1 unless |r + e_t| > 126), so the result is the
+                // correctly rounded scaled value
                 float o[16];
+                const int4 *ex = reinterpret_cast<const int4 *>(s_xexp + j * TN + c0);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int t = min(t0 + j * TN + c0 + i, T - 1);
-                    o[i] = ldexpf(__uint_as_float(v[i]), -(rexp + __ldg(xexp + t)));
+                for (int i4 = 0; i4 < 4; ++i4) {
+                    const int4 e4 = ex[i4];
+                    const int es[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int tot = -rexp - es[u];
+                        const int a = max(-126, min(126, tot));
+                        const float f1 = __uint_as_float(static_cast<uint32_t>(a + 127) << 23);
+                        const float f2 = __uint_as_float(static_cast<uint32_t>(tot - a + 127) << 23);
+                        o[4 * i4 + u] = __uint_as_float(v[4 * i4 + u]) * f1 * f2;
+                    }
                 }
                 if (split > 1) {
 #pragma unroll
@@ -523,9 +593,345 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Small token counts: exact integer weight tiles, scales applied per super-block.
+//
+// For T up to a few dozen tokens the fp32 dequant above costs far more than
+// the weight stream.  This kernel never forms w: the weight tile holds
+// q * sc_j, an integer of at most 945 that fp16 represents exactly (two
+// instructions per two weights: the nibbles under the exponent of 1024, one
+// f16x2 fma with sc and -1024 sc), the MMAs of one super-block accumulate
+// D = sum_k (q sc)_k x_k in tensor memory, one more MMA per super-block forms
+// M = sum_j m_j S_j from the sub-block sums S_j of x, and the epilogue warps
+// add d * D - dmin * M into fp32 registers before tensor memory is reused.
+// D and M are double-buffered so that the next super-block's MMAs run while
+// the epilogue reads the last one.  Every product is exact; the only
+// roundings are fp32 accumulation and the split of S_j into fp16 hi + lo.
+//
+// Per super-block the stage ring carries five stages: its four 64-wide K
+// chunks (weight tile + X tile) and a "min" stage whose weight tile holds
+// {m_0..m_7, m_0..m_7} in its first 16 columns and whose X tile holds
+// {S_hi 0..7, S_lo 0..7} (one K16 MMA).  X arrives in the converted layout
+// with the middle two of every four k swapped, which is the order in which
+// the nibble arithmetic emits the weights.
+template <int TN>
+struct ECfg {
+    static constexpr int kBBytes = TN * kChunk * 2;
+    static constexpr int kStageBytes = kATileBytes + kBBytes;
+    // TN = 32: two CTAs per SM, five 20 KB stages each; TN = 64: one CTA per
+    // SM with eight 24 KB stages (measured best of the two layouts for each)
+    static constexpr int kStages = (TN <= 32) ? 5 : (200 * 1024) / kStageBytes;
+    static constexpr int kTmemCols = 4 * TN;      // {D, M} x 2 buffers
+    static constexpr size_t kSmem = static_cast<size_t>(kStages) * kStageBytes;
+    static_assert(static_cast<size_t>(TN) * kRowsM * 4 <= kSmem, "split-K partial tile must fit the ring");
+};
+
+template <int TN>
+__global__ void __launch_bounds__(kThreads, (TN <= 32) ? 2 : 1)
+    q4k_prefill_exact_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
+                             const uint8_t *__restrict__ W, const int *__restrict__ xexp, float *__restrict__ Y,
+                             int N, int K, int T)
+{
+    using C = ECfg<TN>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full_a[C::kStages], full_b[C::kStages], empty[C::kStages];
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int s_abort;
+    __shared__ __align__(16) int s_xexp[TN];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int row0 = blockIdx.x * kRowsM;
+    const int t0 = blockIdx.y * TN;
+    const int split = gridDim.z;
+    const int kz = blockIdx.z;
+    const int nsb = K / 256;
+    const int sb_begin = static_cast<int>((static_cast<long long>(kz) * nsb) / split);
+    const int sb_end = static_cast<int>((static_cast<long long>(kz + 1) * nsb) / split);
+    const int nloc = sb_end - sb_begin;    // >= 1 (the planner keeps split <= nsb / 2)
+    // Every row tile walks its super-blocks from a different start (wrapping
+    // around), so that the CTAs do not all ask L2 for the same X tile at the
+    // same moment.
+    const int rot = static_cast<int>(blockIdx.x % static_cast<unsigned>(nloc));
+    auto sb_of = [&](int i) {
+        const int j = i + rot;
+        return sb_begin + (j >= nloc ? j - nloc : j);
+    };
+    const size_t row_bytes = static_cast<size_t>(nsb) * 144;
+
+    if (tid == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(smem_u32(&full_a[s]), 128);
+            mbar_init(smem_u32(&full_b[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), 128);
+        }
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(smem_u32(&tmem_base_s), C::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmS);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    auto fail = [&]() {
+        atomicOr(&g_prefill_error, 2u);
+        s_abort = 1;
+    };
+    auto aborted = [&]() { return *(volatile int *)&s_abort != 0; };
+
+    float acc[TN];
+#pragma unroll
+    for (int i = 0; i < TN; ++i) acc[i] = 0.f;
+
+    if (warp < 4) {
+        // ------------------------------------------------ weight tiles + epilogue
+        const int r = tid;
+        const int n = row0 + r;
+        const bool live = n < N;
+        const uint8_t *wrow = W + static_cast<size_t>(live ? n : 0) * row_bytes;
+        int stage = 0;
+        uint32_t phase = 0;
+        auto load_sb = [&](int i, uint4 (&q)[9]) {
+            const bool ok = live && i < nloc;
+            const uint4 *bp = reinterpret_cast<const uint4 *>(wrow + static_cast<size_t>(sb_of(ok ? i : 0)) * 144);
+#pragma unroll
+            for (int u = 0; u < 9; ++u) q[u] = ok ? __ldg(bp + u) : make_uint4(0, 0, 0, 0);
+            // and ask L2 for the super-block after it, so that its loads,
+            // issued one super-block from now, find it there
+            if (live && i + 1 < nloc) {
+                const uint8_t *nb = wrow + static_cast<size_t>(sb_of(i + 1)) * 144;
+                prefetch_l2(nb);
+                prefetch_l2(nb + 128);
+                prefetch_l2(nb + 143);
+            }
+        };
+        auto next_stage = [&]() {
+            if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+        };
+        auto wait_empty = [&]() {
+            if (!aborted() && !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) fail();
+        };
+        // the five stages of one super-block; returns its {d, 64 dmin}
+        auto produce_sb = [&](const uint4 (&q)[9]) {
+            uint32_t mpairs[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const RowConsts rc = decode_header(q[0], pair_sel(p));
+                mpairs[p] = rc.mpair;
+                wait_empty();
+                uint8_t *arow = smem + stage * C::kStageBytes + r * 128;
+                const uint32_t words[8] = {q[1 + 2 * p].x, q[1 + 2 * p].y, q[1 + 2 * p].z, q[1 + 2 * p].w,
+                                           q[2 + 2 * p].x, q[2 + 2 * p].y, q[2 + 2 * p].z, q[2 + 2 * p].w};
+                const uint32_t k1024 = 0x64006400u;
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {       // 0: sub-block 2p (low nibbles), 1: 2p+1
+                    const uint32_t mask = half ? 0x00F000F0u : 0x000F000Fu;
+                    const uint32_t mul = half ? rc.mulO : rc.mulE;
+                    const uint32_t add = half ? rc.addO : rc.addE;
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        uint32_t out[4];
+#pragma unroll
+                        for (int uu = 0; uu < 2; ++uu) {
+                            const uint32_t w = words[2 * c8 + uu];
+                            // {q sc (4u), q sc (4u+2)}, {q sc (4u+1), q sc (4u+3)}
+                            out[2 * uu] = hfma2_u32(and_or(w, mask, k1024), mul, add);
+                            out[2 * uu + 1] = hfma2_u32(and_or(w >> 8, mask, k1024), mul, add);
+                        }
+                        const int chunk = 4 * half + c8;
+                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) =
+                            make_uint4(out[0], out[1], out[2], out[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&full_a[stage]));
+                next_stage();
+            }
+            // min stage: {m_0..m_7} in k 0..7 and again in k 8..15
+            wait_empty();
+            {
+                uint8_t *arow = smem + stage * C::kStageBytes + r * 128;
+                const uint4 mv = make_uint4(mpairs[0], mpairs[1], mpairs[2], mpairs[3]);
+                *reinterpret_cast<uint4 *>(arow + ((0 ^ (r & 7)) << 4)) = mv;
+                *reinterpret_cast<uint4 *>(arow + ((1 ^ (r & 7)) << 4)) = mv;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&full_a[stage]));
+            next_stage();
+            return make_float2(half_lo_f32(q[0].x), 64.0f * half_hi_f32(q[0].x));
+        };
+        // acc += d D - 64 dmin M for local super-block i, then free its buffer
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        auto epilogue_sb = [&](int i, float2 dd) {
+            const int buf = i & 1;
+            if (!aborted() && !mbar_wait_bounded(smem_u32(&acc_full[buf]), static_cast<uint32_t>((i >> 1) & 1), kWaitLimitNs))
+                fail();
+            tc_fence_after();
+            const uint32_t col = lane_addr + static_cast<uint32_t>(buf * 2 * TN);
+#pragma unroll
+            for (int c0 = 0; c0 < TN; c0 += 16) {
+                uint32_t vd[16], vm[16];
+                tmem_ld16(col + c0, vd);
+                tmem_ld16(col + TN + c0, vm);
+                tmem_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    acc[c0 + u] = fmaf(dd.x, __uint_as_float(vd[u]), fmaf(-dd.y, __uint_as_float(vm[u]), acc[c0 + u]));
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&acc_empty[buf]));
+        };
+        uint4 qa[9], qb[9];
+        float2 dprev = make_float2(0.f, 0.f);
+        load_sb(0, qa);
+        for (int i = 0; i < nloc; i += 2) {
+            load_sb(i + 1, qb);
+            const float2 da = produce_sb(qa);
+            if (i > 0) epilogue_sb(i - 1, dprev);
+            dprev = da;
+            if (i + 1 < nloc) {
+                load_sb(i + 2, qa);
+                const float2 db = produce_sb(qb);
+                epilogue_sb(i, dprev);
+                dprev = db;
+            }
+        }
+        epilogue_sb(nloc - 1, dprev);
+    } else if (warp == 4) {
+        // ------------------------------------------------ X tiles and sub-block sums by TMA
+        if (lane == 0) {
+            pdl_wait();   // X and the sums are written by the conversion kernel launched just before
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            for (int i = 0; i < nloc; ++i) {
+                const int sb = sb_of(i);
+                for (int p = 0; p < 5; ++p) {
+                    if (!aborted() && !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) fail();
+                    if (!aborted()) {
+                        const uint32_t bar = smem_u32(&full_b[stage]);
+                        mbar_arrive_expect_tx(bar, C::kBBytes);
+                        const uint32_t dst = smem_u32(smem + stage * C::kStageBytes + kATileBytes);
+                        if (p < 4) tma_load_2d(dst, &tmX, (4 * sb + p) * kChunk, t0, bar);
+                        else tma_load_2d(dst, &tmS, sb * kChunk, t0, bar);
+                        ++issued;
+                    }
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (aborted()) {
+                for (int j = max(0, issued - C::kStages); j < issued; ++j)
+                    if (!mbar_wait_bounded(smem_u32(&full_b[j % C::kStages]), static_cast<uint32_t>((j / C::kStages) & 1),
+                                           kWaitLimitNs))
+                        break;
+            }
+        }
+    } else {
+        // ------------------------------------------------ MMA issuer (whole warp, one elected lane issues)
+        {
+            int stage = 0;
+            uint32_t phase = 0;
+            constexpr uint32_t idesc = idesc_f16(kRowsM, TN);
+            for (int i = 0; i < nloc; ++i) {
+                const int buf = i & 1;
+                bool bok = i < 2 || aborted() ||
+                           mbar_wait_bounded(smem_u32(&acc_empty[buf]), static_cast<uint32_t>(((i >> 1) - 1) & 1), kWaitLimitNs);
+                bok = __all_sync(0xffffffffu, bok);
+                if (!bok && lane == 0) fail();
+                tc_fence_after();
+                const uint32_t dcol = tmem + static_cast<uint32_t>(buf * 2 * TN);
+                for (int p = 0; p < 5; ++p) {
+                    bool ok = !aborted();
+                    if (ok && !mbar_wait_bounded(smem_u32(&full_a[stage]), phase, kWaitLimitNs)) ok = false;
+                    if (ok && !mbar_wait_bounded(smem_u32(&full_b[stage]), phase, kWaitLimitNs)) ok = false;
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok && lane == 0 && !aborted()) fail();
+                    tc_fence_after();
+                    if (ok) {
+                        const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
+                        const uint32_t b_addr = a_addr + kATileBytes;
+                        if (p < 4) {
+#pragma unroll
+                            for (int kk = 0; kk < kChunk / 16; ++kk)
+                                umma_f16(dcol, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), idesc,
+                                         (p > 0 || kk > 0) ? 1u : 0u);
+                        } else {
+                            umma_f16(dcol + TN, sw128_desc(a_addr), sw128_desc(b_addr), idesc, 0u);
+                        }
+                    }
+                    umma_commit(smem_u32(&empty[stage]));
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                }
+                umma_commit(smem_u32(&acc_full[buf]));
+            }
+        }
+    }
+
+    // ---------------------------------------------------- output (warps 0-3)
+    // y = acc * 2^-e_t.  With a K split the scaled partial rows go to shared
+    // memory and CTA rank z of the cluster sums its share of rows over the
+    // ranks in order (as in the kernel above).
+    float *part = reinterpret_cast<float *>(smem);
+    if (warp < 4) {
+        pdl_wait();
+        if (tid < TN) s_xexp[tid] = (t0 + tid < T) ? __ldg(xexp + t0 + tid) : 0;
+        named_bar_sync(1, 128);
+        const int r = tid;
+        const int n = row0 + r;
+        const bool ok = !aborted();
+#pragma unroll
+        for (int i = 0; i < TN; ++i) {
+            const float o = acc[i] * __uint_as_float(static_cast<uint32_t>(127 - s_xexp[i]) << 23);
+            if (split > 1) part[i * kRowsM + r] = o;
+            else if (ok && n < N && t0 + i < T) Y[static_cast<size_t>(t0 + i) * N + n] = o;
+        }
+    }
+    if (split > 1) {
+        __syncthreads();
+        cluster_sync_all();
+        if (!aborted()) {
+            const int r0 = (kz * kRowsM) / split, r1 = ((kz + 1) * kRowsM) / split;
+            const int rows = r1 - r0;
+            const uint32_t part_addr = smem_u32(part);
+            for (int it = tid; it < rows * TN; it += kThreads) {
+                const int c = it / rows;
+                const int rr = r0 + it % rows;
+                const uint32_t off = static_cast<uint32_t>((c * kRowsM + rr) * 4);
+                float sum = 0.f;
+                for (int q = 0; q < split; ++q) sum += ld_shared_cluster_f32(map_shared_rank(part_addr + off, q));
+                const int n = row0 + rr, t = t0 + c;
+                if (n < N && t < T) Y[static_cast<size_t>(t) * N + n] = sum;
+            }
+        }
+        cluster_sync_all();
+    }
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
 }  // namespace pf
 
 // ------------------------------------------------------------------ host
+// Token counts up to this go to the exact kernel.
+constexpr int kExactMaxT = 64;
+
 static q4k_status validate_prefill(const void *W, const void *X, const float *Y, int64_t N, int64_t K, int64_t T)
 {
     const bool empty = (N == 0 || T == 0);       // nothing is read or written
@@ -591,6 +997,62 @@ static cudaError_t launch_prefill(const uint8_t *W, const void *Xh, const int *x
     return e;
 }
 
+static bool encode_f16_map(CUtensorMap *map, const void *base, int cols, int rows, int box_rows)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(pf::kChunk), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), gdim, gstride, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int TN>
+static cudaError_t launch_prefill_exact(const uint8_t *W, const void *Xh, const void *XS, const int *xexp, float *Y,
+                                        int N, int K, int T, int split, cudaStream_t s)
+{
+    using C = pf::ECfg<TN>;
+    CUtensorMap mx, ms;
+    if (!encode_f16_map(&mx, Xh, K, T, TN) || !encode_f16_map(&ms, XS, (K / 256) * pf::kChunk, T, TN))
+        return cudaErrorInvalidValue;
+    auto kern = pf::q4k_prefill_exact_kernel<TN>;
+    int dev = 0;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de != cudaSuccess) return de;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static std::once_flag once[64];
+    static cudaError_t attr_err[64];
+    std::call_once(once[dev], [&]() {
+        attr_err[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::kSmem));
+    });
+    if (attr_err[dev] != cudaSuccess) return attr_err[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + pf::kRowsM - 1) / pf::kRowsM, (T + TN - 1) / TN, split);
+    cfg.blockDim = dim3(pf::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (split > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 1;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = split;
+        ++na;
+    }
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mx, ms, W, xexp, Y, N, K, T);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return e;
+}
+
 q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream)
 {
     q4k_status st = validate_prefill(W, X, Y, N, K, T);
@@ -616,26 +1078,42 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     // tiles)
     else if (static_cast<long long>(mtiles) * ((t + 511) / 512) * 10 >= static_cast<long long>(sms) * 7) { tn = 256; ntt = 2; }
     else { tn = 256; ntt = 1; }
+    // Up to kExactMaxT tokens: the exact kernel (integer weight tiles), in
+    // 32- or 64-token tiles.
+    const bool exact = t <= kExactMaxT;
+    if (exact) {
+        tn = (t <= 32) ? 32 : 64;
+        ntt = 1;
+    }
     const long long ctas = static_cast<long long>(mtiles) * ((t + tn * ntt - 1) / (tn * ntt));
     // K split over a cluster until the GPU is covered (at most 8, at least
-    // 8 chunks of 64 per CTA).
+    // two super-blocks per CTA).
+    // (the exact kernel fits two CTAs per SM with 32-token tiles, one with 64)
+    const long long slots = !exact ? static_cast<long long>(sms) + sms / 2 : (tn == 32 ? 2LL * sms : static_cast<long long>(sms));
     int split = 1;
-    while (ntt == 1 && split < 8 && ctas * split * 2 <= static_cast<long long>(sms) + sms / 2 && (k / 64) / (split * 2) >= 8)
+    while (ntt == 1 && split < 8 && ctas * split * 2 <= slots && (k / 256) / (split * 2) >= 2)
         split *= 2;
-    // X in fp16 under a power-of-two scale per token: T*K*2 bytes plus the
-    // exponents, from the stream-ordered allocator on the caller's stream
+    // X in fp16 under a power-of-two scale per token: T*K*2 bytes, the
+    // exponents, and for the exact kernel the sub-block sums (T*K/2 bytes),
+    // from the stream-ordered allocator on the caller's stream
     const size_t xh_bytes = (static_cast<size_t>(T) * static_cast<size_t>(K) * 2 + 255) & ~size_t(255);
+    const size_t xe_bytes = (static_cast<size_t>(T) * 4 + 255) & ~size_t(255);
+    const size_t xs_bytes = exact ? static_cast<size_t>(T) * static_cast<size_t>(K) / 2 : 0;
     void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, xh_bytes + static_cast<size_t>(T) * 4, s) != cudaSuccess) {
+    if (cudaMallocAsync(&scratch, xh_bytes + xe_bytes + xs_bytes, s) != cudaSuccess) {
         (void)cudaGetLastError();
         return Q4K_ERR_CUDA;
     }
     uint16_t *Xh = static_cast<uint16_t *>(scratch);
     int *xexp = reinterpret_cast<int *>(static_cast<uint8_t *>(scratch) + xh_bytes);
-    pf::x_to_f16_kernel<<<t, 256, 0, s>>>(static_cast<const uint16_t *>(X), Xh, xexp, k);
+    uint16_t *XS = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(scratch) + xh_bytes + xe_bytes);
+    if (exact) pf::x_to_f16_kernel<true><<<t, 256, 0, s>>>(static_cast<const uint16_t *>(X), Xh, xexp, XS, k);
+    else pf::x_to_f16_kernel<false><<<t, 256, 0, s>>>(static_cast<const uint16_t *>(X), Xh, xexp, nullptr, k);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) {
-        if (tn == 32) e = launch_prefill<32, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
+        if (exact && tn == 32) e = launch_prefill_exact<32>(Wb, Xh, XS, xexp, Y, n, k, t, split, s);
+        else if (exact) e = launch_prefill_exact<64>(Wb, Xh, XS, xexp, Y, n, k, t, split, s);
+        else if (tn == 32) e = launch_prefill<32, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else if (tn == 64) e = launch_prefill<64, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else if (tn == 128) e = launch_prefill<128, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else if (ntt == 1) e = launch_prefill<256, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);

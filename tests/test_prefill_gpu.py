@@ -81,6 +81,22 @@ def test_llama_shapes_full_t512(env, name, N, K):
     _check(q4k, oracle, N, K, 512, N + K, f"{name} T=512 (all rows)")
 
 
+@pytest.mark.parametrize("N,K,T", [(256, 1024, 1), (300, 4096, 32), (128, 14336, 64), (1000, 2048, 40)])
+def test_exact_path_precision(env, N, K, T):
+    """Up to 64 tokens the product uses integer weight tiles (q * sc, exact
+    in fp16) with the scales applied in fp32 per super-block: no weight is
+    rounded, so the error stays near fp32 accumulation error, far below one
+    fp16 rounding of w."""
+    q4k, oracle = env
+    W = synth.q4k_weights(N, K, (N, K, T, 3))
+    X = synth.normal_bf16_bits((T, K), (N, K, T, 4))
+    Y = _run(q4k, W, X)
+    Xf = synth.bf16_bits_to_f32(X).astype(np.float64)
+    ref = oracle.prefill(W, X, N, K)
+    bound = 2.0 ** -14 * (np.abs(Xf) @ np.abs(oracle.dequant_matrix(W, N, K)).T) + 1e-6
+    assert np.all(np.abs(Y - ref) <= bound), f"N={N} K={K} T={T}: error beyond fp32 accumulation"
+
+
 def test_prefill_matches_gemv_within_tolerance(env):
     """Prefill with T rows equals T decode GEMVs of the same (bf16-valued) activations."""
     q4k, oracle = env
