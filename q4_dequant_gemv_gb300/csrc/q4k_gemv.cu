@@ -67,6 +67,7 @@ constexpr int kWarps = 8;                 // warps per CTA, 16 weight rows each
 constexpr int kRows = 16 * kWarps;        // rows per tile (128)
 constexpr int kThreads = 32 * kWarps;
 constexpr int kStages = 4;                // W ring depth
+constexpr int kPreWait = 1;               // stages issued before the dependency wait
 constexpr int kStageBytes = kRows * kBlockBytes;   // one super-block of every tile row (18 KB)
 constexpr size_t kSmemPerCta2 = 110 * 1024;        // two CTAs per SM (batch <= 8)
 constexpr size_t kSmemPerCta1 = 200 * 1024;        // one CTA per SM (batch > 8)
@@ -114,13 +115,15 @@ __host__ inline size_t gemv_smem_bytes(int NT, int B, int kc, int split)
 // ---------------------------------------------------------------------------
 // A chunk of x (B rows x nblk super-blocks, B * nblk <= 32) -> B fragments in
 // shared memory (x_item_tc per item).  One warp converts one (batch row,
-// super-block) item per round; all loads of all rounds are issued first.  The
+// super-block) item per round; all loads of all rounds are issued first, then
+// after_loads() runs (the kernel issues its remaining weight stages there, so
+// that they queue behind x, not ahead of it).  The
 // item scales go to s_unscale[bl*B + b].  Ends with a barrier over all nthr
 // threads; the caller must have finished reading the previous chunk's
 // fragments and scales.
-template <int NT>
+template <int NT, typename AfterLoads>
 __device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int kb0, int nblk, uint2 *xf,
-                                 float *s_unscale, int tid, int nthr)
+                                 float *s_unscale, int tid, int nthr, AfterLoads after_loads)
 {
     const int LW = frag_lanes(NT, B);
     constexpr int LS = lane_stride(NT);
@@ -138,6 +141,7 @@ __device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int 
             v[r][1] = __ldg(src + 32 + lane);
         }
     }
+    after_loads();
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int it = warp + r * nwarps;
@@ -154,9 +158,9 @@ __device__ void convert_x_blocks(const float *__restrict__ x, int K, int B, int 
 // x_item_i8, one super-block per warp and round, at xb + bl * blk_bytes; the
 // scales go to s_unscale[bl], s_pre[bl].  Ends with a barrier over all nthr
 // threads.
-template <bool Q8>
+template <bool Q8, typename AfterLoads>
 __device__ void convert_x_i8_blocks(const float *__restrict__ x, int kb0, int nblk, uint8_t *xb, int blk_bytes,
-                                    float *s_unscale, float *s_pre, int tid, int nthr)
+                                    float *s_unscale, float *s_pre, int tid, int nthr, AfterLoads after_loads)
 {
     const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
     float4 v[4][2];
@@ -169,6 +173,7 @@ __device__ void convert_x_i8_blocks(const float *__restrict__ x, int kb0, int nb
             v[r][1] = __ldg(src + 32 + lane);
         }
     }
+    after_loads();
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int it = warp + r * nwarps;
@@ -298,8 +303,12 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             if (g < args.ngroups) prefetch_tensormap(&maps.m[g]);
         // The first stages stream in while the CTA sets up and, under PDL,
         // while the previous kernel finishes (weights never depend on it).
+        // Only kPreWait of them: the x loads after the wait queue behind every
+        // weight byte already requested by this SM, and a CTA that starts only
+        // when the previous kernel ends would otherwise wait for its whole
+        // ring before it sees x.  The rest follow the x loads.
         iss.policy = l2_policy_evict_first();
-        const int first = min(kStages, iss.total);
+        const int first = min(kPreWait, iss.total);
         for (int i = 0; i < first; ++i) iss.issue(i);
         s_issued = first;
     }
@@ -313,6 +322,14 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     pdl_launch_dependents();
     pdl_wait();                             // x may come from the previous kernel
 
+    // the rest of the first kStages stages, once this thread's x loads are out
+    auto issue_rest = [&]() {
+        if (tid == 0) {
+            const int first = min(kStages, iss.total);
+            for (int i = s_issued; i < first; ++i) iss.issue(i);
+            s_issued = first;
+        }
+    };
     const int g = lane >> 2;
     const int t = lane & 3;
     const PairSel psel = pair_sel(t);
@@ -324,9 +341,9 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
     const int blk_bytes = static_cast<int>(xfrag_bytes_per_block(1, 1));
     if (single_chunk) {
         if constexpr (I8)
-            convert_x_i8_blocks<Q8>(args.x, kb_begin, ks, xb, blk_bytes, s_unscale, s_pre, tid, kThreads);
+            convert_x_i8_blocks<Q8>(args.x, kb_begin, ks, xb, blk_bytes, s_unscale, s_pre, tid, kThreads, issue_rest);
         else
-            convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_unscale, tid, kThreads);
+            convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin, ks, xf, s_unscale, tid, kThreads, issue_rest);
     }
     // B-fragment lane.  Lanes whose column holds no batch row read some other
     // valid entry: MMA columns are independent, and those output columns are
@@ -351,10 +368,15 @@ __device__ __forceinline__ void gemv_body(const WMaps &maps, const GemvArgs &arg
             if (!single_chunk && kbl > chunk_end) {
                 const int cn = min(args.kc, ks - kbl);
                 named_bar_sync(1, kThreads);     // everyone done with the previous chunk
+                const bool first_chunk = ti_idx == 0 && kbl == 0;
+                auto maybe_rest = [&]() {
+                    if (first_chunk) issue_rest();
+                };
                 if constexpr (I8)
-                    convert_x_i8_blocks<Q8>(args.x, kb_begin + kbl, cn, xb, blk_bytes, s_unscale, s_pre, tid, kThreads);
+                    convert_x_i8_blocks<Q8>(args.x, kb_begin + kbl, cn, xb, blk_bytes, s_unscale, s_pre, tid, kThreads,
+                                            maybe_rest);
                 else
-                    convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, tid, kThreads);
+                    convert_x_blocks<NT>(args.x, nb * 256, B, kb_begin + kbl, cn, xf, s_unscale, tid, kThreads, maybe_rest);
                 chunk_end = kbl + cn - 1;
                 blk = 0;
             }
