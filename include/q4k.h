@@ -175,8 +175,13 @@ q4k_status q4k_gemv_argmax_noalloc(const void *W, const float *x, int32_t *idx, 
  * y[b][n] = sum_k w[n][k] * x[b][k] for a Q6_K matrix W, b < batch, n < N.
  *   W uint8 [N][K/256*210] (16-byte aligned), x fp32 [batch][K] (16-byte
  *   aligned), y fp32 [batch][N]; N >= 0 (0: no-op), K a positive multiple of
- *   256, 1 <= batch <= 16.  fp32 accumulation; each block is read once for all
- *   batch rows; deterministic.
+ *   256, 1 <= batch <= 16.  Each block is read once for all batch rows;
+ *   deterministic.  For batch <= 4 and K <= 4096, whole 8-row tiles take an
+ *   integer inner product: x enters per 256-block as two int8 parts
+ *   (x ~ (a/32258)(254 xh + xl), a = the block's max |x|, error <=
+ *   a (1/64516 + 2^-16) per element), the weight codes meet them in exact
+ *   int32 dot products and the scales in fp32; the other rows and shapes
+ *   multiply in fp32.  Both stay far inside the stated tolerance.
  * Errors: INVALID_ARG, MISALIGNED (W or x), UNSUPPORTED_DEVICE, CUDA.
  */
 q4k_status q6k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream);

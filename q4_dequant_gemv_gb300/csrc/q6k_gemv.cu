@@ -157,47 +157,137 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_kernel(const uint8_t *__res
 
 
 // ---------------------------------------------------------------------------
-// Staged variant for rows of up to kStageMax / 8 bytes: 8 consecutive rows are
-// one contiguous byte range starting on a 16-byte boundary (8 x an even row
-// length), so one bulk async copy fills a ring stage with a whole tile of 8
-// rows; warp w decodes row w of the tile from shared memory (16-bit loads at
-// low latency instead of global ones).  Persistent CTAs over the full tiles;
-// the last warp to finish a stage issues the tile kStages ahead into it.  Every
-// wait is bounded: on a timeout the CTA flags g_q6k_error, keeps walking its
-// schedule without waiting, and waits (bounded) for its copies in flight
-// before it exits.
+// Staged variant, integer inner product (batch <= 4).
+//
+// Tiles of 8 rows, each streamed through shared memory in K-slices of up to
+// kSliceBlocks blocks (one bulk async copy per row and slice, its range
+// rounded out to 16-byte boundaries, so the row's first block starts at an
+// even offset inside the stage); warp w works on row w of the tile.  x is
+// converted once per CTA, block by block, into two int8 parts
+// (x ~ (a/32258)(254 xh + xl), a = the block's max |x|, rounding to nearest
+// even), laid out so that lane L finds the parts of its eight x values in one
+// 16-byte word, with the exact int32 sums of each four of them beside.  Each
+// lane then forms q (0..63) of its four low and four high weights as packed
+// bytes and takes the dot products with dp4a: per scale group
+// T = 254 (q . xh) + (q . xl) - 32 X4 is the exact integer sum of (q - 32) x
+// in units of the block's step, and sc_lo T_lo + sc_hi T_hi stays exact in
+// int32 (|.| < 1.1e9); y += (d u) p (that sum), with u p the block's step.
+// (The float path, one fp32 FMA per weight, was instruction-bound.)
+// Persistent CTAs over the tiles; the last warp to finish a stage issues the
+// stage kStages ahead into it.  Every wait is bounded: on a timeout the CTA
+// flags g_q6k_error, keeps walking its schedule without waiting, and waits
+// (bounded) for its copies in flight before it exits.
 // ---------------------------------------------------------------------------
-constexpr int kStages = 4;
-constexpr int kStageMax = 32 * 1024;
+constexpr int kStages = 3;
+constexpr int kRowsPerWarp = 1;    // x parts loaded once serve this many rows
+constexpr int kStageKB = 28;       // stage size target
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr int kXItemBytes = 32 * 16 + 32 * 8;      // int8 parts + four-value sums of one (batch row, block)
 
 __device__ unsigned int g_q6k_error = 0;   // bit 0: a bounded wait of the staged kernel timed out
 
 __device__ __forceinline__ uint32_t lds_u16(const uint8_t *p) { return *reinterpret_cast<const unsigned short *>(p); }
 
-template <int BMAX>
-__global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__restrict__ W, const float *__restrict__ x,
-                                                           float *__restrict__ y, int N, int nb, int B, int tiles)
+// Row pitch of a stage for slices of sb blocks: the slice plus up to 15 bytes
+// of rounding on each side, a multiple of 16.
+__host__ __device__ inline int q6_pitch(int sb) { return ((sb * kBytes + 30 + 15) / 16) * 16; }
+
+// One (batch row, block) of x for the integer path, by one warp: lane L holds
+// x[k_lo .. k_lo + 3] (v0) and x[k_lo + 64 .. + 67] (v1) of the block.
+// Writes {xh(v0), xh(v1), xl(v0), xl(v1)} as packed int8 to xq[L], -32 times
+// the exact sums 254 xh + xl of each four to x4[L] (the q - 32 offset of the
+// weights), and returns {u, p}: x ~ u p (254 xh + xl).  Below 2^-64 the max is scaled by 2^64 first (exact), so that u
+// stays normal; p = 2^-64 then.  A block whose max is zero or not finite gets
+// zero parts and u = 0 (zero) or u = max (inf/NaN propagate).
+__device__ __forceinline__ float2 q6_x_item(float4 v0, float4 v1, int lane, uint4 *xq, int2 *x4)
 {
+    uint32_t m = 0u;
+    m = max(m, max(max(__float_as_uint(fabsf(v0.x)), __float_as_uint(fabsf(v0.y))),
+                   max(__float_as_uint(fabsf(v0.z)), __float_as_uint(fabsf(v0.w)))));
+    m = max(m, max(max(__float_as_uint(fabsf(v1.x)), __float_as_uint(fabsf(v1.y))),
+                   max(__float_as_uint(fabsf(v1.z)), __float_as_uint(fabsf(v1.w)))));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float amax = __uint_as_float(m);
+    const bool ok = m != 0u && m < 0x7F800000u;
+    const float pre = (m < 0x1F800000u) ? 0x1p64f : 1.0f;
+    const float inv = ok ? 127.0f / (amax * pre) : 0.0f;
+    constexpr float kMagic = 12582912.0f;          // 1.5 * 2^23: adding it rounds to an integer
+    constexpr uint32_t kMagicBits = 0x4B400000u;
+    uint32_t hw[2], lw[2];
+    int sums[2];
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+        const float4 w = h2 ? v1 : v0;
+        const float e[4] = {w.x * pre, w.y * pre, w.z * pre, w.w * pre};
+        uint32_t th[4], tl[4];
+        uint32_t sum = 0u;   // mod 2^32: the constant offsets cancel below
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float q = e[j] * inv;
+            const float t1 = __fadd_rn(q, kMagic);
+            const float hq = __fsub_rn(t1, kMagic);
+            const float r = __fmul_rn(__fsub_rn(q, hq), 254.0f);
+            th[j] = __float_as_uint(t1);
+            tl[j] = __float_as_uint(__fadd_rn(r, kMagic));
+            sum += 254u * th[j] + tl[j];
+        }
+        hw[h2] = __byte_perm(__byte_perm(th[0], th[1], 0x0040), __byte_perm(th[2], th[3], 0x0040), 0x5410);
+        lw[h2] = __byte_perm(__byte_perm(tl[0], tl[1], 0x0040), __byte_perm(tl[2], tl[3], 0x0040), 0x5410);
+        sums[h2] = static_cast<int>(sum - 4u * 255u * kMagicBits);
+    }
+    if (!ok) hw[0] = hw[1] = lw[0] = lw[1] = 0u, sums[0] = sums[1] = 0;
+    xq[lane] = make_uint4(hw[0], hw[1], lw[0], lw[1]);
+    x4[lane] = make_int2(-32 * sums[0], -32 * sums[1]);
+    const float u = ok ? (amax * pre) / 127.0f / 254.0f : (m == 0u ? 0.0f : amax);
+    return make_float2(u, 1.0f / pre);
+}
+
+template <int BMAX, int RW>
+__global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__restrict__ W, const float *__restrict__ x,
+                                                           float *__restrict__ y, int N, int nb, int B, int tiles,
+                                                           int sb)
+{
+    constexpr int TR = 8 * RW;                            // rows per tile: warp w takes rows w, w + 8, ...
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full[kStages];
     __shared__ int s_done[kStages];
     __shared__ int s_abort;
     __shared__ int s_issued;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int K = nb * 256;
-    const int RB = nb * kBytes;                 // row bytes
-    const int stage_bytes = 8 * RB;             // a multiple of 16
-    float *xs = reinterpret_cast<float *>(smem + kStages * stage_bytes);
+    const size_t RB = static_cast<size_t>(nb) * kBytes;   // row bytes
+    const int pitch = q6_pitch(sb);
+    const int stage_bytes = TR * pitch;
+    const int nslices = (nb + sb - 1) / sb;
+    // x area: per (batch row, block) 32 x 16 bytes of parts and 32 x 8 of sums, then the steps
+    uint8_t *xa = smem + kStages * stage_bytes;
+    float2 *xup = reinterpret_cast<float2 *>(xa + static_cast<size_t>(B) * nb * kXItemBytes);
     const int my_tiles = (tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                          static_cast<int>(gridDim.x);
+    const int total = my_tiles * nslices;
     const uint64_t policy = l2_policy_evict_first();
-    auto issue = [&](int i) {   // tile i of this CTA's schedule into slot i % kStages
+    // stage i of this CTA's schedule: tile blockIdx.x + (i / nslices) * gridDim.x, slice i % nslices
+    auto issue = [&](int i) {
         const int slot = i % kStages;
-        const size_t tile = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(i) * gridDim.x;
-        mbar_arrive_expect_tx(smem_u32(&full[slot]), static_cast<uint32_t>(stage_bytes));
-        bulk_g2s(smem_u32(smem + slot * stage_bytes), W + tile * stage_bytes, static_cast<uint32_t>(stage_bytes),
-                 smem_u32(&full[slot]), policy);
+        const size_t tile = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(i / nslices) * gridDim.x;
+        const int sl = i % nslices;
+        const int j0 = sl * sb, j1 = min(nb, j0 + sb);
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int r = 0; r < TR; ++r) {
+            const size_t start = (tile * TR + r) * RB + static_cast<size_t>(j0) * kBytes;
+            const size_t end = start + static_cast<size_t>(j1 - j0) * kBytes;
+            bytes += static_cast<uint32_t>(((end + 15) & ~static_cast<size_t>(15)) - (start & ~static_cast<size_t>(15)));
+        }
+        mbar_arrive_expect_tx(smem_u32(&full[slot]), bytes);
+#pragma unroll
+        for (int r = 0; r < TR; ++r) {
+            const size_t start = (tile * TR + r) * RB + static_cast<size_t>(j0) * kBytes;
+            const size_t end = start + static_cast<size_t>(j1 - j0) * kBytes;
+            const size_t a0 = start & ~static_cast<size_t>(15);
+            bulk_g2s(smem_u32(smem + slot * stage_bytes + r * pitch), W + a0,
+                     static_cast<uint32_t>(((end + 15) & ~static_cast<size_t>(15)) - a0), smem_u32(&full[slot]), policy);
+        }
     };
     if (tid == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -206,63 +296,85 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__res
         }
         s_abort = 0;
         fence_barrier_init();
-        const int first = min(kStages, my_tiles);
+        const int first = min(kStages, total);
         for (int i = 0; i < first; ++i) issue(i);
         s_issued = first;
     }
-    {
-        const float4 *src = reinterpret_cast<const float4 *>(x);
-        float4 *dst = reinterpret_cast<float4 *>(xs);
-        for (int i = tid; i < B * K / 4; i += kThreads) dst[i] = __ldg(src + i);
+    const int h = lane >> 4, c1 = (lane >> 3) & 1, l0 = 4 * (lane & 7);
+    const int k_lo = 128 * h + 32 * c1 + l0;   // this lane's first low weight; +64 for the high ones
+    // x -> int8 parts, one (batch row, block) per warp and round
+    for (int it = warp; it < B * nb; it += kWarps) {
+        const float *xb = x + static_cast<size_t>(it) * 256 + k_lo;   // row b = it / nb, block it % nb
+        const float4 v0 = __ldg(reinterpret_cast<const float4 *>(xb));
+        const float4 v1 = __ldg(reinterpret_cast<const float4 *>(xb + 64));
+        uint8_t *item = xa + static_cast<size_t>(it) * kXItemBytes;
+        const float2 up = q6_x_item(v0, v1, lane, reinterpret_cast<uint4 *>(item), reinterpret_cast<int2 *>(item + 512));
+        if (lane == 0) xup[it] = up;
     }
     __syncthreads();
-    const int h = lane >> 4, c1 = (lane >> 3) & 1, l0 = 4 * (lane & 7);
     const int ql_off = 4 * lane;
     const int qh_off = 128 + 32 * h + l0;
-    const int sc_off = 192 + 8 * h + 2 * c1 + (l0 >> 4);
-    const int k_lo = 128 * h + 32 * c1 + l0;
-    for (int i = 0; i < my_tiles; ++i) {
-        const int tile = static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x);
+    const int sc_off = 192 + 8 * h + 2 * c1 + (l0 >> 4);   // scale of the low weights; +4 for the high ones
+    const int qsh = 2 * c1;                                 // qh bits of the low weights; +4 for the high ones
+    float acc[RW][BMAX];
+    for (int i = 0; i < total; ++i) {
+        const int ti = i / nslices, sl = i % nslices;
+        const int tile = static_cast<int>(blockIdx.x) + ti * static_cast<int>(gridDim.x);
+        if (sl == 0) {
+#pragma unroll
+            for (int r = 0; r < RW; ++r)
+#pragma unroll
+                for (int b = 0; b < BMAX; ++b) acc[r][b] = 0.f;
+        }
         const int slot = i % kStages;
         const uint32_t phase = static_cast<uint32_t>((i / kStages) & 1);
         if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), phase, kWaitLimitNs)) {
             atomicOr(&g_q6k_error, 1u);
             s_abort = 1;
         }
-        const uint8_t *rowp = smem + slot * stage_bytes + warp * RB;
-        float acc[BMAX];
+        const int j0 = sl * sb, nj = min(nb, j0 + sb) - j0;
+        const uint8_t *rowp[RW];
 #pragma unroll
-        for (int b = 0; b < BMAX; ++b) acc[b] = 0.f;
-        for (int blk = 0; blk < nb; ++blk) {
-            const uint8_t *A = rowp + blk * kBytes;
-            const uint32_t ql = lds_u16(A + ql_off) | (lds_u16(A + ql_off + 2) << 16);
-            const uint32_t qh = lds_u16(A + qh_off) | (lds_u16(A + qh_off + 2) << 16);
-            const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(lds_u16(A + 208))));
-            const float s_lo = d * static_cast<float>(static_cast<int8_t>(A[sc_off]));
-            const float s_hi = d * static_cast<float>(static_cast<int8_t>(A[sc_off + 4]));
-            const uint32_t q_lo = (ql & 0x0F0F0F0Fu) | (((qh >> (2 * c1)) & 0x03030303u) << 4);
-            const uint32_t q_hi = ((ql >> 4) & 0x0F0F0F0Fu) | (((qh >> (2 * c1 + 4)) & 0x03030303u) << 4);
-            float w_lo[4], w_hi[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {   // 2^23 + q - (2^23 + 32) = q - 32, exact
-                w_lo[j] = __uint_as_float(__byte_perm(q_lo, 0x4B000000u, 0x7440u | j)) - 8388640.0f;
-                w_hi[j] = __uint_as_float(__byte_perm(q_hi, 0x4B000000u, 0x7440u | j)) - 8388640.0f;
-            }
-            const float *xb = xs + blk * 256 + k_lo;
+        for (int r = 0; r < RW; ++r) {
+            const int tr = warp + 8 * r;
+            const size_t start = (static_cast<size_t>(tile) * TR + tr) * RB + static_cast<size_t>(j0) * kBytes;
+            rowp[r] = smem + slot * stage_bytes + tr * pitch + static_cast<int>(start & 15);
+        }
+#pragma unroll 2
+        for (int j = 0; j < nj; ++j) {
+            // this lane's x parts of block j0 + j, shared by the warp's RW rows
+            uint4 xv[BMAX];
+            int2 x4[BMAX];
+            float xs[BMAX];
 #pragma unroll
             for (int b = 0; b < BMAX; ++b) {
-                if (b >= B) break;
-                const float4 xa = *reinterpret_cast<const float4 *>(xb + b * K);
-                const float4 xc = *reinterpret_cast<const float4 *>(xb + b * K + 64);
-                float t_lo = w_lo[0] * xa.x;
-                t_lo = fmaf(w_lo[1], xa.y, t_lo);
-                t_lo = fmaf(w_lo[2], xa.z, t_lo);
-                t_lo = fmaf(w_lo[3], xa.w, t_lo);
-                float t_hi = w_hi[0] * xc.x;
-                t_hi = fmaf(w_hi[1], xc.y, t_hi);
-                t_hi = fmaf(w_hi[2], xc.z, t_hi);
-                t_hi = fmaf(w_hi[3], xc.w, t_hi);
-                acc[b] = fmaf(s_lo, t_lo, fmaf(s_hi, t_hi, acc[b]));
+                // rows past B read row 0's parts (never used for an output)
+                const int item = (b < B ? b : 0) * nb + j0 + j;
+                const uint8_t *xi = xa + static_cast<size_t>(item) * kXItemBytes;
+                xv[b] = reinterpret_cast<const uint4 *>(xi)[lane];
+                x4[b] = reinterpret_cast<const int2 *>(xi + 512)[lane];
+                const float2 up = xup[item];
+                xs[b] = up.x * up.y;
+            }
+#pragma unroll
+            for (int r = 0; r < RW; ++r) {
+                const uint8_t *A = rowp[r] + j * kBytes;
+                const uint32_t ql = lds_u16(A + ql_off) | (lds_u16(A + ql_off + 2) << 16);
+                const uint32_t qh = lds_u16(A + qh_off) | (lds_u16(A + qh_off + 2) << 16);
+                const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(lds_u16(A + 208))));
+                const int sc_lo = static_cast<int8_t>(A[sc_off]);
+                const int sc_hi = static_cast<int8_t>(A[sc_off + 4]);
+                // q (0..63) of the four low and the four high weights, one per
+                // byte: low nibble from ql, bits 4-5 from the lane's qh pair
+                const uint32_t q_lo = and_or(ql, 0x0F0F0F0Fu, (qh << (4 - qsh)) & 0x30303030u);
+                const uint32_t q_hi = and_or(ql >> 4, 0x0F0F0F0Fu, (qh >> qsh) & 0x30303030u);
+#pragma unroll
+                for (int b = 0; b < BMAX; ++b) {
+                    const int t_lo = 254 * dp4a_us(q_lo, xv[b].x, 0) + dp4a_us(q_lo, xv[b].z, x4[b].x);
+                    const int t_hi = 254 * dp4a_us(q_hi, xv[b].y, 0) + dp4a_us(q_hi, xv[b].w, x4[b].y);
+                    const int ts = sc_lo * t_lo + sc_hi * t_hi;
+                    acc[r][b] = fmaf(static_cast<float>(ts), d * xs[b], acc[r][b]);
+                }
             }
         }
         // this warp is done with the slot: the last warp to finish refills it
@@ -272,18 +384,24 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__res
             const int prev = atomicAdd(&s_done[slot], 1);
             if (prev % kWarps == kWarps - 1) {
                 const int next = i + kStages;
-                if (next < my_tiles && !*(volatile int *)&s_abort) {
+                if (next < total && !*(volatile int *)&s_abort) {
                     issue(next);
                     atomicAdd(&s_issued, 1);
                 }
             }
         }
+        if (sl == nslices - 1) {
 #pragma unroll
-        for (int b = 0; b < BMAX; ++b) {
-            if (b >= B) break;
+            for (int r = 0; r < RW; ++r)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc[b] += __shfl_xor_sync(0xffffffffu, acc[b], o);
-            if (lane == 0 && !*(volatile int *)&s_abort) y[static_cast<size_t>(b) * N + tile * 8 + warp] = acc[b];
+                for (int b = 0; b < BMAX; ++b) {
+                    if (b >= B) break;
+                    float v = acc[r][b];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0 && !*(volatile int *)&s_abort)
+                        y[static_cast<size_t>(b) * N + tile * TR + warp + 8 * r] = v;
+                }
         }
     }
     // After a timed-out wait, wait (bounded) for the copies issued but not
@@ -328,18 +446,18 @@ static cudaError_t q6k_launch(const uint8_t *W, const float *x, float *y, int N,
     return cudaGetLastError();
 }
 
-template <int BMAX>
+template <int BMAX, int RW>
 static cudaError_t q6k_launch_staged(const uint8_t *W, const float *x, float *y, int N, int nb, int B, int tiles,
-                                     int sms, size_t smem, cudaStream_t s)
+                                     int sb, int sms, size_t smem, cudaStream_t s)
 {
-    auto kern = q6::q6k_gemv_staged<BMAX>;
+    auto kern = q6::q6k_gemv_staged<BMAX, RW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, q6::kThreads, smem);
     if (e != cudaSuccess) return e;
     const int grid = static_cast<int>(std::min<long long>(tiles, static_cast<long long>(sms) * std::max(occ, 1)));
-    kern<<<grid, q6::kThreads, smem, s>>>(W, x, y, N, nb, B, tiles);
+    kern<<<grid, q6::kThreads, smem, s>>>(W, x, y, N, nb, B, tiles, sb);
     return cudaGetLastError();
 }
 
@@ -394,23 +512,23 @@ q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const uint8_t *Wb = static_cast<const uint8_t *>(W);
     cudaError_t e = cudaSuccess;
-    // Staged path: whole tiles of 8 rows (8 x row bytes <= 32 KB, a multiple of
-    // 16 starting on a 16-byte boundary), x in shared memory beside the ring,
-    // when ring and x still leave room for two CTAs per SM (with one, the batch-5
-    // LM head ran 1.5x slower than the direct kernel: measured); the remaining
-    // N % 8 rows go to the direct kernel.
-    const long long stage_bytes = 8ll * nb * q6::kBytes;
-    const size_t smem_staged = static_cast<size_t>(q6::kStages * stage_bytes) +
-                               static_cast<size_t>(batch) * static_cast<size_t>(K) * 4;
-    const int tiles = n / 8;
-    if (stage_bytes <= q6::kStageMax && smem_staged <= 110 * 1024 && tiles > 0) {
+    // Staged integer path (batch <= 4): whole tiles of 8 rows in K-slices of
+    // up to 16 blocks, x converted into shared memory beside the ring (when
+    // that takes at most 64 KB); the remaining N % 8 rows go to the direct
+    // kernel.
+    constexpr int RW = q6::kRowsPerWarp;
+    const int tiles = n / (8 * RW);
+    const size_t xbytes = static_cast<size_t>(batch) * nb * (q6::kXItemBytes + 8);
+    // (rows longer than one slice, e.g. K = 18944, measured faster on the
+    // direct kernel: 27 against 31 us)
+    const int sb = std::max(1, std::min(nb, ((q6::kStageKB * 1024) / (8 * RW) - 30) / q6::kBytes));
+    if (batch <= 4 && tiles > 0 && xbytes <= 64 * 1024 && sb == nb) {
+        const size_t smem = static_cast<size_t>(q6::kStages) * 8 * RW * q6::q6_pitch(sb) + xbytes;
         if (batch == 1)
-            e = q6k_launch_staged<1>(Wb, x, y, n, nb, batch, tiles, sms, smem_staged, s);
-        else if (batch <= 4)
-            e = q6k_launch_staged<4>(Wb, x, y, n, nb, batch, tiles, sms, smem_staged, s);
+            e = q6k_launch_staged<1, RW>(Wb, x, y, n, nb, batch, tiles, sb, sms, smem, s);
         else
-            e = q6k_launch_staged<16>(Wb, x, y, n, nb, batch, tiles, sms, smem_staged, s);
-        const int done = tiles * 8;
+            e = q6k_launch_staged<4, RW>(Wb, x, y, n, nb, batch, tiles, sb, sms, smem, s);
+        const int done = tiles * 8 * RW;
         if (e == cudaSuccess && done < n)
             e = q6k_direct(Wb + static_cast<size_t>(done) * nb * q6::kBytes, x, y + done, n - done, n, nb, batch, sms, s);
     } else {

@@ -30,11 +30,14 @@ def _run(q4k, W, x):
     return y.cpu().numpy()
 
 
-# (N, K, B): ragged row counts, every warps-per-row choice (few rows -> up to 8 warps per row), the
-# staged path (whole 8-row tiles through shared memory) at batch bounds 1 / 4 / 16 with and without a
-# remainder of rows for the direct kernel, and shapes that only take the direct kernel
+# (N, K, B): ragged row counts, every warps-per-row choice of the direct kernel (few rows -> up to 8
+# warps per row), the staged path (8-row tiles through shared memory in K-slices of up to 16 blocks,
+# batch <= 4) with and without a remainder of rows for the direct kernel, and shapes that only take
+# the direct kernel (batch > 4, fewer than 8 rows)
 SHAPES = [(1, 256, 1), (7, 512, 2), (129, 3584, 1), (300, 4096, 5), (512, 3584, 1), (1000, 2048, 16),
-          (65, 18944, 3), (3584, 3584, 1), (37, 768, 9), (64, 1024, 3), (29, 2560, 4)]
+          (65, 18944, 3), (3584, 3584, 1), (37, 768, 9), (64, 1024, 3), (29, 2560, 4),
+          # K-sliced stages: several slices per tile, a short last slice, batch 1 and 4
+          (3584, 18944, 1), (40, 4608, 4), (16, 4352, 1)]
 
 
 @pytest.mark.parametrize("N,K,B", SHAPES)
