@@ -261,7 +261,7 @@ def kernel_source_hash():
     dropped as soon as any code changes."""
     import re
     h = hashlib.sha256()
-    for f in ("q4k_gemv.cu", "ptx.cuh"):
+    for f in ("q4k_gemv.cu", "q4k_dev.cuh", "ptx.cuh"):
         src = open(os.path.join(ROOT, "q4_dequant_gemv_gb300", "csrc", f)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         src = re.sub(r"//[^\n]*", "", src)
