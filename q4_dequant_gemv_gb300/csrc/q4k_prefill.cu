@@ -279,8 +279,23 @@ struct Cfg {
     static constexpr size_t kSmem = static_cast<size_t>(kStages) * kStageBytes;
 };
 
+// Named barrier 1 over the 128 epilogue threads, returning the AND of p over them.
+__device__ __forceinline__ bool bar_and_128(bool p)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred a, b;\n\t"
+        "setp.ne.u32 a, %1, 0;\n\t"
+        "bar.red.and.pred b, 1, 128, a;\n\t"
+        "selp.u32 %0, 1, 0, b;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(p))
+        : "memory");
+    return r != 0;
+}
+
 template <int TN, int NTT>
-__global__ void __launch_bounds__(kThreads, (TN * NTT <= 32) ? 2 : 1)
+__global__ void __launch_bounds__(kThreads, 1)
     q4k_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t *__restrict__ W,
                        const int *__restrict__ xexp, float *__restrict__ Y, int N, int K, int T)
 {
@@ -291,6 +306,7 @@ __global__ void __launch_bounds__(kThreads, (TN * NTT <= 32) ? 2 : 1)
     __shared__ uint32_t tmem_base_s;
     __shared__ int s_abort;
     __shared__ __align__(16) int s_xexp[TN * NTT];   // token scale exponents of this CTA's tokens
+    __shared__ __align__(16) float s_xinv[TN * NTT]; // 2^-e_t
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -346,14 +362,14 @@ __global__ void __launch_bounds__(kThreads, (TN * NTT <= 32) ? 2 : 1)
         // Row scale 2^rs: the largest |w| this CTA's super-blocks of the row
         // can hold, |d|*945 + |dmin|*63, brought to [2^14, 2^15).
         float wmax = 0.f;
-        if (live) {
-            for (int b = sb_begin; b < sb_end; b += 8) {
-                uint32_t hb[8];
+        if (live) {   // sixteen headers in flight per round (the prescan is pure load latency)
+            for (int b = sb_begin; b < sb_end; b += 16) {
+                uint32_t hb[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < 16; ++i)
                     hb[i] = (b + i < sb_end) ? __ldg(reinterpret_cast<const uint32_t *>(wrow + static_cast<size_t>(b + i) * 144)) : 0u;
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
+                for (int i = 0; i < 16; ++i)
                     wmax = fmaxf(wmax, fmaf(fabsf(half_lo_f32(hb[i])), 945.0f, fabsf(half_hi_f32(hb[i])) * 63.0f));
             }
         }
@@ -516,8 +532,17 @@ __global__ void __launch_bounds__(kThreads, (TN * NTT <= 32) ? 2 : 1)
     float *part = reinterpret_cast<float *>(smem);   // pipeline buffers are idle by now
     if (warp < 4) {
         pdl_wait();   // the token exponents come from the conversion kernel
-        for (int i = tid; i < TN * NTT; i += 128) s_xexp[i] = (t0 + i < T) ? __ldg(xexp + t0 + i) : 0;
-        named_bar_sync(1, 128);
+        // token factors 2^-e_t; moderate = every |e_t| <= 63 (then, for rows
+        // with |r| <= 63 too, 2^-r 2^-e_t is an exact normal float and one
+        // multiply scales a value)
+        bool mod = true;
+        for (int i = tid; i < TN * NTT; i += 128) {
+            const int e = (t0 + i < T) ? __ldg(xexp + t0 + i) : 0;
+            s_xexp[i] = e;
+            s_xinv[i] = __uint_as_float(static_cast<uint32_t>(127 - max(-126, min(126, e))) << 23);
+            mod = mod && e >= -63 && e <= 63;
+        }
+        const bool all_mod = bar_and_128(mod);
         const bool ok = mbar_wait_bounded(smem_u32(&done_bar), 0u, kWaitLimitNs);
         if (!ok) {
             atomicOr(&g_prefill_error, 2u);
@@ -527,39 +552,68 @@ __global__ void __launch_bounds__(kThreads, (TN * NTT <= 32) ? 2 : 1)
         const int r = warp * 32 + lane;
         const int n = row0 + r;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const bool fast = all_mod && rexp >= -63 && rexp <= 63;
+        const float rinv = __uint_as_float(static_cast<uint32_t>(127 - max(-126, min(126, rexp))) << 23);
+        // 64 columns per round: four tensor-memory loads in flight, one wait
+        // (a wait per 16 columns left the 512-token epilogue at ~14 us)
         for (int j = 0; j < nsub; ++j) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < TN; c0 += 16) {
-                uint32_t v[16];
-                tmem_ld16(lane_addr + j * TN + c0, v);
+            for (int c64 = 0; c64 < TN; c64 += 64) {
+                uint32_t v[4][16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    if (c64 + 16 * q < TN) tmem_ld16(lane_addr + j * TN + c64 + 16 * q, v[q]);
                 tmem_wait_ld();
-                // undo the row's and the tokens' power-of-two scales: times
-                // 2^-(r + e_t), as two factors that are normal floats (the
-                // second is 1 unless |r + e_t| > 126), so the result is the
-                // correctly rounded scaled value
-                float o[16];
-                const int4 *ex = reinterpret_cast<const int4 *>(s_xexp + j * TN + c0);
 #pragma unroll
-                for (int i4 = 0; i4 < 4; ++i4) {
-                    const int4 e4 = ex[i4];
-                    const int es[4] = {e4.x, e4.y, e4.z, e4.w};
+                for (int q = 0; q < 4; ++q) {
+                    const int c0 = c64 + 16 * q;
+                    if (c0 >= TN) break;
+                    // undo the row's and the tokens' power-of-two scales: times
+                    // 2^-(r + e_t), one correctly rounded multiply by an exact
+                    // power of two when both are moderate, else as two factors
+                    // that are normal floats (the second is 1 unless
+                    // |r + e_t| > 126)
+                    float o[16];
+                    if (fast) {
+                        const float4 *gx = reinterpret_cast<const float4 *>(s_xinv + j * TN + c0);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int tot = -rexp - es[u];
-                        const int a = max(-126, min(126, tot));
-                        const float f1 = __uint_as_float(static_cast<uint32_t>(a + 127) << 23);
-                        const float f2 = __uint_as_float(static_cast<uint32_t>(tot - a + 127) << 23);
-                        o[4 * i4 + u] = __uint_as_float(v[4 * i4 + u]) * f1 * f2;
+                        for (int i4 = 0; i4 < 4; ++i4) {
+                            const float4 g = gx[i4];
+                            o[4 * i4 + 0] = __uint_as_float(v[q][4 * i4 + 0]) * (rinv * g.x);
+                            o[4 * i4 + 1] = __uint_as_float(v[q][4 * i4 + 1]) * (rinv * g.y);
+                            o[4 * i4 + 2] = __uint_as_float(v[q][4 * i4 + 2]) * (rinv * g.z);
+                            o[4 * i4 + 3] = __uint_as_float(v[q][4 * i4 + 3]) * (rinv * g.w);
+                        }
+                    } else {
+                        const int4 *ex = reinterpret_cast<const int4 *>(s_xexp + j * TN + c0);
+#pragma unroll
+                        for (int i4 = 0; i4 < 4; ++i4) {
+                            const int4 e4 = ex[i4];
+                            const int es[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int tot = -rexp - es[u];
+                                const int a = max(-126, min(126, tot));
+                                const float f1 = __uint_as_float(static_cast<uint32_t>(a + 127) << 23);
+                                const float f2 = __uint_as_float(static_cast<uint32_t>(tot - a + 127) << 23);
+                                o[4 * i4 + u] = __uint_as_float(v[q][4 * i4 + u]) * f1 * f2;
+                            }
+                        }
                     }
-                }
-                if (split > 1) {
+                    const int tb = t0 + j * TN + c0;
+                    if (split > 1) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) part[(j * TN + c0 + i) * kRowsM + r] = o[i];
-                } else if (ok && n < N) {
+                        for (int i = 0; i < 16; ++i) part[(j * TN + c0 + i) * kRowsM + r] = o[i];
+                    } else if (ok && n < N) {
+                        float *yp = Y + static_cast<size_t>(tb) * N + n;
+                        if (tb + 16 <= T) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int t = t0 + j * TN + c0 + i;
-                        if (t < T) Y[static_cast<size_t>(t) * N + n] = o[i];
+                            for (int i = 0; i < 16; ++i) yp[static_cast<size_t>(i) * N] = o[i];
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (tb + i < T) yp[static_cast<size_t>(i) * N] = o[i];
+                        }
                     }
                 }
             }
@@ -1113,8 +1167,6 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     if (e == cudaSuccess) {
         if (exact && tn == 32) e = launch_prefill_exact<32>(Wb, Xh, XS, xexp, Y, n, k, t, split, s);
         else if (exact) e = launch_prefill_exact<64>(Wb, Xh, XS, xexp, Y, n, k, t, split, s);
-        else if (tn == 32) e = launch_prefill<32, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
-        else if (tn == 64) e = launch_prefill<64, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else if (tn == 128) e = launch_prefill<128, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else if (ntt == 1) e = launch_prefill<256, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else e = launch_prefill<256, 2>(Wb, Xh, xexp, Y, n, k, t, split, s);

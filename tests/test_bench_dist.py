@@ -70,7 +70,7 @@ def test_traffic_record_follows_code_not_comments(tmp_path, monkeypatch):
     import bench
     csrc = tmp_path / "q4_dequant_gemv_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    for f in ("q4k_gemv.cu", "ptx.cuh"):
+    for f in ("q4k_gemv.cu", "q4k_dev.cuh", "ptx.cuh"):
         shutil.copy(os.path.join(ROOT, "q4_dequant_gemv_gb300", "csrc", f), csrc / f)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h0 = bench.kernel_source_hash()
@@ -78,4 +78,9 @@ def test_traffic_record_follows_code_not_comments(tmp_path, monkeypatch):
     (csrc / "q4k_gemv.cu").write_text("// a new comment line\n" + src.replace("namespace q4k {", "namespace  q4k  {  /* c */"))
     assert bench.kernel_source_hash() == h0
     (csrc / "q4k_gemv.cu").write_text(src.replace("constexpr int kStages = 4;", "constexpr int kStages = 5;"))
+    assert bench.kernel_source_hash() != h0
+    # the device helpers shared by the kernel count as its code too
+    (csrc / "q4k_gemv.cu").write_text(src)
+    dev = (csrc / "q4k_dev.cuh").read_text()
+    (csrc / "q4k_dev.cuh").write_text(dev.replace("constexpr int kI8Pair = 80;", "constexpr int kI8Pair = 96;"))
     assert bench.kernel_source_hash() != h0

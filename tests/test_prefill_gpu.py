@@ -110,15 +110,16 @@ def test_prefill_matches_gemv_within_tolerance(env):
     assert_close(Y[:16], yg.astype(np.float64), Xf[:16], K, "prefill vs gemv")
 
 
-def test_prefill_extreme_scales(env):
+@pytest.mark.parametrize("T", [40, 200])
+def test_prefill_extreme_scales(env, T):
     """Weights and activations far outside fp16's range (|w| up to ~6e7 and
-    ~1e-3, |x| up to ~4e12 and ~4e-12): the power-of-two scales per row and
+    ~1e-3, |x| up to ~4e12 and down to ~3e-24): the power-of-two scales per row and
     per token keep every output finite and within one fp16 rounding of w of
     the exact product.  (The stated decode tolerance's absolute clause,
     1e-3 sqrt(K) max|x|, assumes weights of order one, so it is not the
     measure here.)"""
     q4k, oracle = env
-    N, K, T = 256, 1024, 40
+    N, K = 256, 1024
     W = synth.q4k_weights(N, K, 67).copy()
     blocks = W.reshape(N, K // 256, 144)
     # rows 0..63: d = 60000, dmin = 1000 (|w| up to ~6e7); rows 64..127: d = dmin = 2^-20
@@ -126,10 +127,13 @@ def test_prefill_extreme_scales(env):
     blocks[:64, :, 2:4] = np.frombuffer(np.float16(1000.0).tobytes(), np.uint8)
     blocks[64:128, :, 0:4] = np.frombuffer((np.float16(2.0 ** -20).tobytes()) * 2, np.uint8)
     X = synth.normal_bf16_bits((T, K), 68).copy()
-    # tokens 0..9 scaled by 2^40, tokens 10..19 by 2^-40 (exact in bf16)
+    # tokens 0..9 scaled by 2^40, 10..19 by 2^-40, 20..29 by 2^-80 (exact in
+    # bf16; the last ones need a token scale beyond 2^63, the slow path of the
+    # epilogue's unscaling)
     Xf = synth.bf16_bits_to_f32(X)
     Xf[:10] *= np.float32(2.0 ** 40)
     Xf[10:20] *= np.float32(2.0 ** -40)
+    Xf[20:30] *= np.float32(2.0 ** -80)
     X = (Xf.view(np.uint32) >> 16).astype(np.uint16)
     Y = _run(q4k, W, X)
     ref = oracle.prefill(W, X, N, K)
