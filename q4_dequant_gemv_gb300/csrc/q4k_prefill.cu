@@ -663,31 +663,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the epilogue reads the last one.  Every product is exact; the only
 // roundings are fp32 accumulation and the split of S_j into fp16 hi + lo.
 //
-// Per super-block the stage ring carries five stages: its four 64-wide K
-// chunks (weight tile + X tile) and a "min" stage whose weight tile holds
+// Per super-block five parts go through the stage ring: its four 64-wide K
+// chunks (weight tile + X tile) and a "min" part whose weight tile holds
 // {m_0..m_7, m_0..m_7} in its first 16 columns and whose X tile holds
-// {S_hi 0..7, S_lo 0..7} (one K16 MMA).  X arrives in the converted layout
-// with the middle two of every four k swapped, which is the order in which
-// the nibble arithmetic emits the weights.
-template <int TN>
+// {S_hi 0..7, S_lo 0..7} (one K16 MMA).  PS parts share one stage (one
+// barrier hand-off): PS = 5 puts a whole super-block in a stage.  X arrives
+// in the converted layout with the middle two of every four k swapped, which
+// is the order in which the nibble arithmetic emits the weights.
+template <int TN, int PS>
 struct ECfg {
-    static constexpr int kBBytes = TN * kChunk * 2;
-    static constexpr int kStageBytes = kATileBytes + kBBytes;
-    // TN = 32: two CTAs per SM, five 20 KB stages each; TN = 64: one CTA per
-    // SM with eight 24 KB stages (measured best of the two layouts for each)
-    static constexpr int kStages = (TN <= 32) ? 5 : (200 * 1024) / kStageBytes;
+    static constexpr int kBBytes = TN * kChunk * 2;                 // X tile of a part
+    static constexpr int kStageBytes = PS * (kATileBytes + kBBytes);  // PS weight tiles, then PS X tiles
+    static constexpr int kStages = (PS == 1) ? ((TN <= 32) ? 5 : (200 * 1024) / kStageBytes) : (200 * 1024) / kStageBytes;
     static constexpr int kTmemCols = 4 * TN;      // {D, M} x 2 buffers
     static constexpr size_t kSmem = static_cast<size_t>(kStages) * kStageBytes;
+    static constexpr bool kTwoPerSm = PS == 1 && TN <= 32;
+    static_assert(kStages >= 2, "at least two stages");
     static_assert(static_cast<size_t>(TN) * kRowsM * 4 <= kSmem, "split-K partial tile must fit the ring");
 };
 
-template <int TN>
-__global__ void __launch_bounds__(kThreads, (TN <= 32) ? 2 : 1)
+template <int TN, int PS>
+__global__ void __launch_bounds__(kThreads, (PS == 1 && TN <= 32) ? 2 : 1)
     q4k_prefill_exact_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmS,
                              const uint8_t *__restrict__ W, const int *__restrict__ xexp, float *__restrict__ Y,
                              int N, int K, int T)
 {
-    using C = ECfg<TN>;
+    using C = ECfg<TN, PS>;
     extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ __align__(8) uint64_t full_a[C::kStages], full_b[C::kStages], empty[C::kStages];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2];
@@ -779,15 +780,27 @@ __global__ void __launch_bounds__(kThreads, (TN <= 32) ? 2 : 1)
         auto wait_empty = [&]() {
             if (!aborted() && !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) fail();
         };
-        // the five stages of one super-block; returns its {d, 64 dmin}
+        // part g of a super-block: the stage it goes to is entered at its
+        // first part and handed over after its last
+        auto part_begin = [&](int g) {
+            if (g % PS == 0) wait_empty();
+            return smem + stage * C::kStageBytes + (g % PS) * kATileBytes + r * 128;
+        };
+        auto part_end = [&](int g) {
+            if (g % PS == PS - 1) {
+                fence_proxy_async_smem();
+                mbar_arrive(smem_u32(&full_a[stage]));
+                next_stage();
+            }
+        };
+        // the five parts of one super-block; returns its {d, 64 dmin}
         auto produce_sb = [&](const uint4 (&q)[9]) {
             uint32_t mpairs[4];
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 const RowConsts rc = decode_header(q[0], pair_sel(p));
                 mpairs[p] = rc.mpair;
-                wait_empty();
-                uint8_t *arow = smem + stage * C::kStageBytes + r * 128;
+                uint8_t *arow = part_begin(p);
                 const uint32_t words[8] = {q[1 + 2 * p].x, q[1 + 2 * p].y, q[1 + 2 * p].z, q[1 + 2 * p].w,
                                            q[2 + 2 * p].x, q[2 + 2 * p].y, q[2 + 2 * p].z, q[2 + 2 * p].w};
                 const uint32_t k1024 = 0x64006400u;
@@ -811,21 +824,16 @@ __global__ void __launch_bounds__(kThreads, (TN <= 32) ? 2 : 1)
                             make_uint4(out[0], out[1], out[2], out[3]);
                     }
                 }
-                fence_proxy_async_smem();
-                mbar_arrive(smem_u32(&full_a[stage]));
-                next_stage();
+                part_end(p);
             }
-            // min stage: {m_0..m_7} in k 0..7 and again in k 8..15
-            wait_empty();
+            // min part: {m_0..m_7} in k 0..7 and again in k 8..15
             {
-                uint8_t *arow = smem + stage * C::kStageBytes + r * 128;
+                uint8_t *arow = part_begin(4);
                 const uint4 mv = make_uint4(mpairs[0], mpairs[1], mpairs[2], mpairs[3]);
                 *reinterpret_cast<uint4 *>(arow + ((0 ^ (r & 7)) << 4)) = mv;
                 *reinterpret_cast<uint4 *>(arow + ((1 ^ (r & 7)) << 4)) = mv;
             }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&full_a[stage]));
-            next_stage();
+            part_end(4);
             return make_float2(half_lo_f32(q[0].x), 64.0f * half_hi_f32(q[0].x));
         };
         // acc += d D - 64 dmin M for local super-block i, then free its buffer
@@ -875,16 +883,21 @@ __global__ void __launch_bounds__(kThreads, (TN <= 32) ? 2 : 1)
             for (int i = 0; i < nloc; ++i) {
                 const int sb = sb_of(i);
                 for (int p = 0; p < 5; ++p) {
-                    if (!aborted() && !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) fail();
+                    const uint32_t bar = smem_u32(&full_b[stage]);
+                    if (p % PS == 0) {
+                        if (!aborted() && !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) fail();
+                        if (!aborted()) {
+                            mbar_arrive_expect_tx(bar, PS * C::kBBytes);
+                            ++issued;
+                        }
+                    }
                     if (!aborted()) {
-                        const uint32_t bar = smem_u32(&full_b[stage]);
-                        mbar_arrive_expect_tx(bar, C::kBBytes);
-                        const uint32_t dst = smem_u32(smem + stage * C::kStageBytes + kATileBytes);
+                        const uint32_t dst =
+                            smem_u32(smem + stage * C::kStageBytes + PS * kATileBytes + (p % PS) * C::kBBytes);
                         if (p < 4) tma_load_2d(dst, &tmX, (4 * sb + p) * kChunk, t0, bar);
                         else tma_load_2d(dst, &tmS, sb * kChunk, t0, bar);
-                        ++issued;
                     }
-                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                    if (p % PS == PS - 1 && ++stage == C::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
             if (aborted()) {
@@ -908,16 +921,19 @@ __global__ void __launch_bounds__(kThreads, (TN <= 32) ? 2 : 1)
                 if (!bok && lane == 0) fail();
                 tc_fence_after();
                 const uint32_t dcol = tmem + static_cast<uint32_t>(buf * 2 * TN);
+                bool ok = true;
                 for (int p = 0; p < 5; ++p) {
-                    bool ok = !aborted();
-                    if (ok && !mbar_wait_bounded(smem_u32(&full_a[stage]), phase, kWaitLimitNs)) ok = false;
-                    if (ok && !mbar_wait_bounded(smem_u32(&full_b[stage]), phase, kWaitLimitNs)) ok = false;
-                    ok = __all_sync(0xffffffffu, ok);
-                    if (!ok && lane == 0 && !aborted()) fail();
-                    tc_fence_after();
+                    if (p % PS == 0) {
+                        ok = !aborted();
+                        if (ok && !mbar_wait_bounded(smem_u32(&full_a[stage]), phase, kWaitLimitNs)) ok = false;
+                        if (ok && !mbar_wait_bounded(smem_u32(&full_b[stage]), phase, kWaitLimitNs)) ok = false;
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok && lane == 0 && !aborted()) fail();
+                        tc_fence_after();
+                    }
                     if (ok) {
-                        const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
-                        const uint32_t b_addr = a_addr + kATileBytes;
+                        const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes + (p % PS) * kATileBytes);
+                        const uint32_t b_addr = smem_u32(smem + stage * C::kStageBytes + PS * kATileBytes + (p % PS) * C::kBBytes);
                         if (p < 4) {
 #pragma unroll
                             for (int kk = 0; kk < kChunk / 16; ++kk)
@@ -927,8 +943,10 @@ __global__ void __launch_bounds__(kThreads, (TN <= 32) ? 2 : 1)
                             umma_f16(dcol + TN, sw128_desc(a_addr), sw128_desc(b_addr), idesc, 0u);
                         }
                     }
-                    umma_commit(smem_u32(&empty[stage]));
-                    if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                    if (p % PS == PS - 1) {
+                        umma_commit(smem_u32(&empty[stage]));
+                        if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                    }
                 }
                 umma_commit(smem_u32(&acc_full[buf]));
             }
@@ -985,6 +1003,9 @@ __global__ void __launch_bounds__(kThreads, (TN <= 32) ? 2 : 1)
 // ------------------------------------------------------------------ host
 // Token counts up to this go to the exact kernel.
 constexpr int kExactMaxT = 64;
+// Parts of a super-block per stage of the exact kernel at 32-token tiles (5:
+// the whole super-block in one stage, one barrier hand-off per super-block).
+constexpr int kExactParts32 = 5;
 
 static q4k_status validate_prefill(const void *W, const void *X, const float *Y, int64_t N, int64_t K, int64_t T)
 {
@@ -1064,15 +1085,15 @@ static bool encode_f16_map(CUtensorMap *map, const void *base, int cols, int row
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int TN>
+template <int TN, int PS>
 static cudaError_t launch_prefill_exact(const uint8_t *W, const void *Xh, const void *XS, const int *xexp, float *Y,
                                         int N, int K, int T, int split, cudaStream_t s)
 {
-    using C = pf::ECfg<TN>;
+    using C = pf::ECfg<TN, PS>;
     CUtensorMap mx, ms;
     if (!encode_f16_map(&mx, Xh, K, T, TN) || !encode_f16_map(&ms, XS, (K / 256) * pf::kChunk, T, TN))
         return cudaErrorInvalidValue;
-    auto kern = pf::q4k_prefill_exact_kernel<TN>;
+    auto kern = pf::q4k_prefill_exact_kernel<TN, PS>;
     int dev = 0;
     cudaError_t de = cudaGetDevice(&dev);
     if (de != cudaSuccess) return de;
@@ -1142,8 +1163,9 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     const long long ctas = static_cast<long long>(mtiles) * ((t + tn * ntt - 1) / (tn * ntt));
     // K split over a cluster until the GPU is covered (at most 8, at least
     // two super-blocks per CTA).
-    // (the exact kernel fits two CTAs per SM with 32-token tiles, one with 64)
-    const long long slots = !exact ? static_cast<long long>(sms) + sms / 2 : (tn == 32 ? 2LL * sms : static_cast<long long>(sms));
+    // (the exact kernel fits two CTAs per SM only with 32-token tiles of one part per stage)
+    const long long slots = !exact ? static_cast<long long>(sms) + sms / 2
+                                   : (tn == 32 && pf::ECfg<32, kExactParts32>::kTwoPerSm ? 2LL * sms : static_cast<long long>(sms));
     int split = 1;
     while (ntt == 1 && split < 8 && ctas * split * 2 <= slots && (k / 256) / (split * 2) >= 2)
         split *= 2;
@@ -1165,8 +1187,8 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     else pf::x_to_f16_kernel<false><<<t, 256, 0, s>>>(static_cast<const uint16_t *>(X), Xh, xexp, nullptr, k);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess) {
-        if (exact && tn == 32) e = launch_prefill_exact<32>(Wb, Xh, XS, xexp, Y, n, k, t, split, s);
-        else if (exact) e = launch_prefill_exact<64>(Wb, Xh, XS, xexp, Y, n, k, t, split, s);
+        if (exact && tn == 32) e = launch_prefill_exact<32, kExactParts32>(Wb, Xh, XS, xexp, Y, n, k, t, split, s);
+        else if (exact) e = launch_prefill_exact<64, 1>(Wb, Xh, XS, xexp, Y, n, k, t, split, s);
         else if (tn == 128) e = launch_prefill<128, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else if (ntt == 1) e = launch_prefill<256, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else e = launch_prefill<256, 2>(Wb, Xh, xexp, Y, n, k, t, split, s);
