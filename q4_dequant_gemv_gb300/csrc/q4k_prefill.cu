@@ -268,15 +268,22 @@ __global__ void __launch_bounds__(256) x_to_f16_kernel(const uint16_t *__restric
 }
 
 
+// The raw weight super-blocks of the tile (128 rows x 144 bytes) come by TMA
+// into a ring of their own, kWSlots super-blocks ahead of the dequant: loaded
+// by each producer thread from global memory one super-block ahead, they kept
+// the producers waiting on memory (long-scoreboard stalls on top in ncu).
+constexpr int kWSlots = 3;
+constexpr int kWSlotBytes = kRowsM * 144;
 template <int TN, int NTT>
 struct Cfg {
     static constexpr int kBBytes = TN * kChunk * 2;                       // one token subtile
     static constexpr int kStageBytes = kAStageBytes + NTT * kBBytes;
-    // 32-token tiles: three stages (two CTAs per SM); otherwise up to four.
-    static constexpr int kStages =
-        (TN * NTT <= 32) ? 3 : ((200 * 1024 / kStageBytes) < 4 ? (200 * 1024 / kStageBytes) : 4);
-    static constexpr int kTmemCols = TN * NTT;                            // 32..512, power of two
-    static constexpr size_t kSmem = static_cast<size_t>(kStages) * kStageBytes;
+    static constexpr int kRoom = 224 * 1024 - kWSlots * kWSlotBytes;      // for the stage ring
+    static constexpr int kStages = (kRoom / kStageBytes) < 4 ? (kRoom / kStageBytes) : 4;
+    static constexpr int kTmemCols = TN * NTT;                            // 128..512, power of two
+    static constexpr size_t kWOffset = static_cast<size_t>(kStages) * kStageBytes;
+    static constexpr size_t kSmem = kWOffset + static_cast<size_t>(kWSlots) * kWSlotBytes;
+    static_assert(kStages >= 2, "at least two stages");
 };
 
 // Named barrier 1 over the 128 epilogue threads, returning the AND of p over them.
@@ -296,13 +303,15 @@ __device__ __forceinline__ bool bar_and_128(bool p)
 
 template <int TN, int NTT>
 __global__ void __launch_bounds__(kThreads, 1)
-    q4k_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const uint8_t *__restrict__ W,
-                       const int *__restrict__ xexp, float *__restrict__ Y, int N, int K, int T)
+    q4k_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                       const uint8_t *__restrict__ W, const int *__restrict__ xexp, float *__restrict__ Y, int N,
+                       int K, int T)
 {
     using C = Cfg<TN, NTT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;   // 1024-byte aligned: the 128B-swizzle atoms need it
     __shared__ __align__(8) uint64_t full_a[C::kStages], full_b[C::kStages], empty[C::kStages], done_bar;
+    __shared__ __align__(8) uint64_t wfull[kWSlots], wempty[kWSlots];
     __shared__ uint32_t tmem_base_s;
     __shared__ int s_abort;
     __shared__ __align__(16) int s_xexp[TN * NTT];   // token scale exponents of this CTA's tokens
@@ -338,6 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&empty[s]), 1);
         }
         mbar_init(smem_u32(&done_bar), 1);
+        for (int s = 0; s < kWSlots; ++s) {
+            mbar_init(smem_u32(&wfull[s]), 1);
+            mbar_init(smem_u32(&wempty[s]), 128);
+        }
         s_abort = 0;
         fence_barrier_init();
     }
@@ -345,7 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(&tmem_base_s), C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) prefetch_tmap(&tmX);
+    if (warp == 4 && lane == 0) {
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -376,19 +392,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         rexp = f16_range_exp(wmax);
         const float rscale = __uint_as_float(static_cast<uint32_t>(rexp + 127) << 23);
         // A super-block of the row as nine 16-byte words (header, then the
-        // 128 quant bytes), loaded one super-block ahead of its dequant.  Rows
-        // past N and super-blocks past the CTA's range read as zeros: d = dmin
-        // = 0 makes every weight of them zero.
+        // 128 quant bytes), read from the weight ring one super-block ahead of
+        // its dequant.  Rows past N arrive as zeros from the TMA unit (d =
+        // dmin = 0 makes every weight of them zero); super-blocks past the
+        // CTA's range read as zeros.
+        const uint8_t *wring = smem + C::kWOffset;
         auto load_sb = [&](int i, uint4 (&q)[9]) {
-            const bool ok = live && i < nloc;
-            const uint4 *bp = reinterpret_cast<const uint4 *>(wrow + static_cast<size_t>(sb_of(ok ? i : 0)) * 144);
+            if (i < nloc) {
+                const int slot = i % kWSlots;
+                if (!*(volatile int *)&s_abort &&
+                    !mbar_wait_bounded(smem_u32(&wfull[slot]), static_cast<uint32_t>((i / kWSlots) & 1), kWaitLimitNs)) {
+                    atomicOr(&g_prefill_error, 2u);
+                    s_abort = 1;
+                }
+                const uint4 *bp = reinterpret_cast<const uint4 *>(wring + slot * kWSlotBytes + r * 144);
 #pragma unroll
-            for (int u = 0; u < 9; ++u) q[u] = ok ? __ldg(bp + u) : make_uint4(0, 0, 0, 0);
-            if (live && i + 1 < nloc) {   // the super-block after it, into L2
-                const uint8_t *nb = wrow + static_cast<size_t>(sb_of(i + 1)) * 144;
-                prefetch_l2(nb);
-                prefetch_l2(nb + 128);
-                prefetch_l2(nb + 143);
+                for (int u = 0; u < 9; ++u) q[u] = bp[u];
+                mbar_arrive(smem_u32(&wempty[slot]));   // (release: orders the reads before the refill)
+            } else {
+#pragma unroll
+                for (int u = 0; u < 9; ++u) q[u] = make_uint4(0, 0, 0, 0);
             }
         };
         // One super-block = four K chunks; chunk p holds sub-blocks 2p (low
@@ -453,7 +476,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 4) {
-        // ------------------------------------------------ X tiles by TMA
+        // ------------------------------------------------ weight super-blocks by TMA (lane 1)
+        if (lane == 1) {
+            const uint64_t pol = l2_policy_evict_first();
+            int issued = 0;
+            for (int i = 0; i < nloc; ++i) {
+                const int slot = i % kWSlots;
+                if (i >= kWSlots && !*(volatile int *)&s_abort &&
+                    !mbar_wait_bounded(smem_u32(&wempty[slot]), static_cast<uint32_t>(((i / kWSlots) - 1) & 1),
+                                       kWaitLimitNs)) {
+                    atomicOr(&g_prefill_error, 2u);
+                    s_abort = 1;
+                }
+                if (*(volatile int *)&s_abort) break;
+                mbar_arrive_expect_tx(smem_u32(&wfull[slot]), kWSlotBytes);
+                tma_load_2d_hint(smem_u32(smem + C::kWOffset + slot * kWSlotBytes), &tmW, sb_of(i) * 18, row0,
+                                 smem_u32(&wfull[slot]), pol);
+                ++issued;
+            }
+            if (*(volatile int *)&s_abort) {   // let the copies in flight land before the CTA exits
+                for (int j = max(0, issued - kWSlots); j < issued; ++j)
+                    if (!mbar_wait_bounded(smem_u32(&wfull[j % kWSlots]), static_cast<uint32_t>((j / kWSlots) & 1),
+                                           kWaitLimitNs))
+                        break;
+            }
+        }
+        // ------------------------------------------------ X tiles by TMA (lane 0)
         if (lane == 0) {
             pdl_wait();   // X (fp16) is written by the conversion kernel launched just before
             int stage = 0;
@@ -1035,6 +1083,19 @@ static cudaError_t launch_prefill(const uint8_t *W, const void *Xh, const int *x
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    // W as a 2-D tensor of 8-byte words: [N rows] x [K/256 * 18 words], box =
+    // one super-block of 128 rows (rows past N read as zeros)
+    CUtensorMap wmap;
+    {
+        const int64_t nb = K / 256;
+        cuuint64_t wdim[2] = {static_cast<cuuint64_t>(nb * 18), static_cast<cuuint64_t>(N)};
+        cuuint64_t wstride[1] = {static_cast<cuuint64_t>(nb * 144)};
+        cuuint32_t wbox[2] = {18, static_cast<cuuint32_t>(pf::kRowsM)};
+        if (enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<uint8_t *>(W), wdim, wstride, wbox, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     auto kern = pf::q4k_prefill_kernel<TN, NTT>;
     // the shared-memory limit is a per-device attribute: set it once per device
     int dev = 0;
@@ -1067,7 +1128,7 @@ static cudaError_t launch_prefill(const uint8_t *W, const void *Xh, const int *x
     ++na;
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, W, xexp, Y, N, K, T);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, wmap, W, xexp, Y, N, K, T);
     if (e != cudaSuccess) (void)cudaGetLastError();
     return e;
 }
@@ -1163,9 +1224,9 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     const long long ctas = static_cast<long long>(mtiles) * ((t + tn * ntt - 1) / (tn * ntt));
     // K split over a cluster until the GPU is covered (at most 8, at least
     // two super-blocks per CTA).
-    // (the exact kernel fits two CTAs per SM only with 32-token tiles of one part per stage)
-    const long long slots = !exact ? static_cast<long long>(sms) + sms / 2
-                                   : (tn == 32 && pf::ECfg<32, kExactParts32>::kTwoPerSm ? 2LL * sms : static_cast<long long>(sms));
+    // (one CTA per SM, except the exact kernel's 32-token tiles with one part per stage)
+    const long long slots = exact && tn == 32 && pf::ECfg<32, kExactParts32>::kTwoPerSm ? 2LL * sms
+                                                                                         : static_cast<long long>(sms);
     int split = 1;
     while (ntt == 1 && split < 8 && ctas * split * 2 <= slots && (k / 256) / (split * 2) >= 2)
         split *= 2;
