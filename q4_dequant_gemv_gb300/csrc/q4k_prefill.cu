@@ -301,6 +301,95 @@ __device__ __forceinline__ bool bar_and_128(bool p)
     return r != 0;
 }
 
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// K-split reduction over a cluster of S CTAs.  Every rank holds its scaled
+// partial tile as fp32 [col][128 rows] at part_addr; rank kz sums rows
+// [kz*128/S, (kz+1)*128/S) over the ranks in rank order (0 + p_0 + p_1 + ...,
+// the same order for every element) and stores them to Y [T][N].  An item is
+// four consecutive rows of one column (16-byte loads); 8/S items per round put
+// eight remote loads in flight per thread (one at a time left a 128 x 256
+// tile's reduction at tens of microseconds).
+template <int S>
+__device__ __forceinline__ void reduce_split_tile(uint32_t part_addr, int kz, int cols, int row0, int t0, float *Y,
+                                                  int N, int T, int tid, int nthreads)
+{
+    constexpr int kU = 8 / S;
+    constexpr int kQuads = kRowsM / S / 4;
+    static_assert(S >= 2 && S <= 8 && kRowsM % (4 * S) == 0, "split of 2, 4 or 8");
+    const int r0 = kz * (kRowsM / S);
+    const int items = kQuads * cols;
+    const bool vec = (N % 4) == 0 && (reinterpret_cast<uintptr_t>(Y) & 15u) == 0;
+    for (int base = tid; base < items; base += kU * nthreads) {
+        float4 v[kU][S];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int it = min(base + u * nthreads, items - 1);
+            const int c = it / kQuads, r = r0 + 4 * (it % kQuads);
+            const uint32_t off = static_cast<uint32_t>((c * kRowsM + r) * 4);
+#pragma unroll
+            for (int q = 0; q < S; ++q) v[u][q] = ld_cluster_v4(map_shared_rank(part_addr + off, q));
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int it = base + u * nthreads;
+            if (it < items) {
+                const int c = it / kQuads, r = r0 + 4 * (it % kQuads);
+                float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int q = 0; q < S; ++q) {
+                    s.x += v[u][q].x;
+                    s.y += v[u][q].y;
+                    s.z += v[u][q].z;
+                    s.w += v[u][q].w;
+                }
+                const int n = row0 + r, t = t0 + c;
+                if (t < T) {
+                    float *yp = Y + static_cast<size_t>(t) * N + n;
+                    if (vec && n + 3 < N) {
+                        *reinterpret_cast<float4 *>(yp) = s;
+                    } else {
+                        const float sv[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            if (n + i < N) yp[i] = sv[i];
+                    }
+                }
+            }
+        }
+    }
+}
+
+// Rank-order sum of any split (the host launches 2, 4 or 8).
+__device__ __forceinline__ void reduce_split(uint32_t part_addr, int split, int kz, int cols, int row0, int t0,
+                                             float *Y, int N, int T, int tid, int nthreads)
+{
+    switch (split) {
+    case 2: reduce_split_tile<2>(part_addr, kz, cols, row0, t0, Y, N, T, tid, nthreads); break;
+    case 4: reduce_split_tile<4>(part_addr, kz, cols, row0, t0, Y, N, T, tid, nthreads); break;
+    case 8: reduce_split_tile<8>(part_addr, kz, cols, row0, t0, Y, N, T, tid, nthreads); break;
+    default: {
+        const int r0 = (kz * kRowsM) / split, rows = ((kz + 1) * kRowsM) / split - r0;
+        for (int it = tid; it < rows * cols; it += nthreads) {
+            const int c = it / rows, r = r0 + it % rows;
+            const uint32_t off = static_cast<uint32_t>((c * kRowsM + r) * 4);
+            float sum = 0.f;
+            for (int q = 0; q < split; ++q) sum += ld_shared_cluster_f32(map_shared_rank(part_addr + off, q));
+            const int n = row0 + r, t = t0 + c;
+            if (n < N && t < T) Y[static_cast<size_t>(t) * N + n] = sum;
+        }
+    }
+    }
+}
+
 template <int TN, int NTT>
 __global__ void __launch_bounds__(kThreads, 1)
     q4k_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -310,7 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     using C = Cfg<TN, NTT>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;   // 1024-byte aligned: the 128B-swizzle atoms need it
-    __shared__ __align__(8) uint64_t full_a[C::kStages], full_b[C::kStages], empty[C::kStages], done_bar;
+    // full_a/empty: the stage's weight tile; full_x/empty_x: each token
+    // tile's X tile of the stage (freed as soon as its own MMAs finish)
+    __shared__ __align__(8) uint64_t full_a[C::kStages], empty[C::kStages], done_bar;
+    __shared__ __align__(8) uint64_t full_x[C::kStages * NTT], empty_x[C::kStages * NTT];
     __shared__ __align__(8) uint64_t wfull[kWSlots], wempty[kWSlots];
     __shared__ uint32_t tmem_base_s;
     __shared__ int s_abort;
@@ -343,8 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(smem_u32(&full_a[s]), 128);
-            mbar_init(smem_u32(&full_b[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int s = 0; s < C::kStages * NTT; ++s) {
+            mbar_init(smem_u32(&full_x[s]), 1);
+            mbar_init(smem_u32(&empty_x[s]), 1);
         }
         mbar_init(smem_u32(&done_bar), 1);
         for (int s = 0; s < kWSlots; ++s) {
@@ -506,21 +601,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             pdl_wait();   // X (fp16) is written by the conversion kernel launched just before
             int stage = 0;
             uint32_t phase = 0;
-            int issued = 0;
-            const uint32_t bytes = static_cast<uint32_t>(nsub * C::kBBytes);
+            int issued = 0;   // X tiles issued (nsub per stage use)
             for (int c = c_begin; c < c_end; ++c) {
-                if (!*(volatile int *)&s_abort &&
-                    !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
-                    atomicOr(&g_prefill_error, 2u);
-                    s_abort = 1;
-                }
-                if (!*(volatile int *)&s_abort) {
-                    mbar_arrive_expect_tx(smem_u32(&full_b[stage]), bytes);
-                    uint8_t *bbase = smem + stage * C::kStageBytes + kAStageBytes;
-                    const int kc = 4 * sb_of((c - c_begin) >> 2) + (c & 3);
-                    for (int j = 0; j < nsub; ++j)
-                        tma_load_2d(smem_u32(bbase + j * C::kBBytes), &tmX, kc * kChunk, t0 + j * TN,
-                                    smem_u32(&full_b[stage]));
+                uint8_t *bbase = smem + stage * C::kStageBytes + kAStageBytes;
+                const int kc = 4 * sb_of((c - c_begin) >> 2) + (c & 3);
+                for (int j = 0; j < nsub; ++j) {
+                    const uint32_t bx = smem_u32(&empty_x[stage * NTT + j]);
+                    if (!*(volatile int *)&s_abort && !mbar_wait_bounded(bx, phase ^ 1u, kWaitLimitNs)) {
+                        atomicOr(&g_prefill_error, 2u);
+                        s_abort = 1;
+                    }
+                    if (*(volatile int *)&s_abort) break;
+                    mbar_arrive_expect_tx(smem_u32(&full_x[stage * NTT + j]), static_cast<uint32_t>(C::kBBytes));
+                    tma_load_2d(smem_u32(bbase + j * C::kBBytes), &tmX, kc * kChunk, t0 + j * TN,
+                                smem_u32(&full_x[stage * NTT + j]));
                     ++issued;
                 }
                 if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
@@ -528,10 +622,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // After an abort, wait (bounded) for the copies still in flight so
             // none lands after the CTA has exited.
             if (*(volatile int *)&s_abort) {
-                for (int i = max(0, issued - C::kStages); i < issued; ++i)
-                    if (!mbar_wait_bounded(smem_u32(&full_b[i % C::kStages]), static_cast<uint32_t>((i / C::kStages) & 1),
-                                           kWaitLimitNs))
+                for (int i = max(0, issued - C::kStages * nsub); i < issued; ++i) {
+                    const int use = i / nsub, j = i % nsub;
+                    if (!mbar_wait_bounded(smem_u32(&full_x[(use % C::kStages) * NTT + j]),
+                                           static_cast<uint32_t>((use / C::kStages) & 1), kWaitLimitNs))
                         break;
+                }
             }
         }
     } else {
@@ -543,19 +639,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = c_begin; c < c_end; ++c) {
                 bool ok = !*(volatile int *)&s_abort;
                 if (ok && !mbar_wait_bounded(smem_u32(&full_a[stage]), phase, kWaitLimitNs)) ok = false;
-                if (ok && !mbar_wait_bounded(smem_u32(&full_b[stage]), phase, kWaitLimitNs)) ok = false;
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok && lane == 0 && !*(volatile int *)&s_abort) {
-                    atomicOr(&g_prefill_error, 2u);
-                    s_abort = 1;
-                }
-                tc_fence_after();
-                if (ok) {
-                    const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
-                    const uint32_t b_addr = a_addr + kAStageBytes;
+                const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
+                const uint32_t b_addr = a_addr + kAStageBytes;
+                // token tile j's MMAs start as soon as its own X tile has landed
 #pragma unroll
-                    for (int j = 0; j < NTT; ++j) {
-                        if (j < nsub) {
+                for (int j = 0; j < NTT; ++j) {
+                    if (j < nsub) {
+                        if (ok && !mbar_wait_bounded(smem_u32(&full_x[stage * NTT + j]), phase, kWaitLimitNs))
+                            ok = false;
+                        ok = __all_sync(0xffffffffu, ok);
+                        tc_fence_after();
+                        if (ok) {
 #pragma unroll
                             for (int kk = 0; kk < kChunk / 16; ++kk) {
                                 const uint64_t bd = sw128_desc(b_addr + j * C::kBBytes + kk * 32);
@@ -563,9 +657,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          (c > c_begin || kk > 0) ? 1u : 0u);
                             }
                         }
+                        umma_commit(smem_u32(&empty_x[stage * NTT + j]));   // frees this X tile
                     }
                 }
-                umma_commit(smem_u32(&empty[stage]));   // frees the stage once these MMAs finish
+                if (!ok && lane == 0 && !*(volatile int *)&s_abort) {
+                    atomicOr(&g_prefill_error, 2u);
+                    s_abort = 1;
+                }
+                umma_commit(smem_u32(&empty[stage]));   // frees the weight tile once all its MMAs finish
                 if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
             }
             umma_commit(smem_u32(&done_bar));
@@ -671,21 +770,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (split > 1) {
         __syncthreads();
         cluster_sync_all();
-        if (!*(volatile int *)&s_abort) {
-            const int r0 = (kz * kRowsM) / split, r1 = ((kz + 1) * kRowsM) / split;
-            const int rows = r1 - r0;
-            const int cols = nsub * TN;
-            const uint32_t part_addr = smem_u32(part);
-            for (int it = tid; it < rows * cols; it += kThreads) {
-                const int c = it / rows;
-                const int r = r0 + it % rows;
-                const uint32_t off = static_cast<uint32_t>((c * kRowsM + r) * 4);
-                float sum = 0.f;
-                for (int q = 0; q < split; ++q) sum += ld_shared_cluster_f32(map_shared_rank(part_addr + off, q));
-                const int n = row0 + r, t = t0 + c;
-                if (n < N && t < T) Y[static_cast<size_t>(t) * N + n] = sum;
-            }
-        }
+        if (!*(volatile int *)&s_abort)
+            reduce_split(smem_u32(part), split, kz, nsub * TN, row0, t0, Y, N, T, tid, kThreads);
         cluster_sync_all();
     }
     __syncthreads();
@@ -1023,20 +1109,7 @@ __global__ void __launch_bounds__(kThreads, (PS == 1 && TN <= 32) ? 2 : 1)
     if (split > 1) {
         __syncthreads();
         cluster_sync_all();
-        if (!aborted()) {
-            const int r0 = (kz * kRowsM) / split, r1 = ((kz + 1) * kRowsM) / split;
-            const int rows = r1 - r0;
-            const uint32_t part_addr = smem_u32(part);
-            for (int it = tid; it < rows * TN; it += kThreads) {
-                const int c = it / rows;
-                const int rr = r0 + it % rows;
-                const uint32_t off = static_cast<uint32_t>((c * kRowsM + rr) * 4);
-                float sum = 0.f;
-                for (int q = 0; q < split; ++q) sum += ld_shared_cluster_f32(map_shared_rank(part_addr + off, q));
-                const int n = row0 + rr, t = t0 + c;
-                if (n < N && t < T) Y[static_cast<size_t>(t) * N + n] = sum;
-            }
-        }
+        if (!aborted()) reduce_split(smem_u32(part), split, kz, TN, row0, t0, Y, N, T, tid, kThreads);
         cluster_sync_all();
     }
     __syncthreads();
