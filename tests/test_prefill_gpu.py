@@ -53,7 +53,9 @@ def _check(q4k, oracle, N, K, T, seed, what):
                                    (128, 1024, 256), (256, 512, 300), (128, 768, 512), (100, 256, 600),
                                    (128, 4096, 32), (256, 4096, 512), (1000, 2048, 40), (128, 8192, 300),
                                    # enough row tiles for 512-token tiles; ragged last token tile
-                                   (13696, 256, 520), (14336, 512, 1030)])
+                                   (13696, 256, 520), (14336, 512, 1030),
+                                   # odd row-tile counts, with and without a K split
+                                   (384, 2048, 300), (640, 1024, 200), (1152, 4096, 512)])
 def test_prefill_shapes(env, N, K, T):
     q4k, oracle = env
     _check(q4k, oracle, N, K, T, N * 7 + K + T, f"N={N} K={K} T={T}")
