@@ -20,16 +20,23 @@
 //
 // CTA tile: 128 weight rows (the MMA M side) x TN*NTT tokens (the N side),
 // full K.  Per 64-wide K chunk (a quarter of a super-block):
-//   * warps 0-3 (one thread per weight row) read the row's sub-block pair from
-//     global memory, compute w = d*sc*q - dmin*m in fp32, scale it by 2^r and
-//     round it to fp16 into a 128-byte-swizzled K-major tile;
-//   * warp 4 loads the X tile [TN x 64] (fp16) with a TMA tensor copy (128B
-//     swizzle);
-//   * warp 5 (one elected thread) issues 4 x NTT tcgen05.mma (K = 16 each)
-//     into TMEM and commits to the stage's "empty" barrier.
+//   * warps 0-7 (two threads per weight row, one per nibble half) read the
+//     row's sub-block pair from the raw weight ring, compute
+//     w = d*sc*q - dmin*m in fp32, scale it by 2^r and round it to fp16 into
+//     a 128-byte-swizzled K-major tile (with one thread per row the dequant
+//     took ~900 cycles a chunk against 512 for the MMAs at 256 tokens);
+//   * warp 8 loads the X tile [TN x 64] (fp16) with a TMA tensor copy (128B
+//     swizzle), and the raw weight super-blocks;
+//   * warps 9 and 10 (one elected thread each) issue the tcgen05.mma (K = 16
+//     each) into TMEM and commit to the stage's "empty" barriers: with two
+//     token tiles (NTT = 2) warp 5 + j takes tile j, otherwise warp 5 takes the
+//     even chunks and warp 6 the odd ones, into an accumulator of its own that
+//     the epilogue adds.  One issuing warp spent ~500 cycles a chunk on its
+//     barrier waits, fences and commits on top of ~100 per MMA issued, so the
+//     tensor pipe sat idle about half the time.
 // A ring of NS stages overlaps the three.  The epilogue reads TMEM with
-// tcgen05.ld (warp w owns TMEM lanes 32w..32w+31 = weight rows) and writes Y
-// with coalesced stores.  Every mbarrier wait is bounded in time.
+// tcgen05.ld (warps w and w + 4 own TMEM lanes 32w..32w+31 = weight rows) and
+// writes Y with coalesced stores.  Every mbarrier wait is bounded in time.
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -64,6 +71,11 @@ namespace pf {
 constexpr int kRowsM = 128;          // MMA M
 constexpr int kChunk = 64;           // K elements per stage (one 128-byte swizzle row)
 constexpr int kThreads = 192;        // 4 dequant/epilogue warps + TMA warp + MMA warp
+// fp16 kernel: 8 dequant/epilogue warps (two threads per weight row, one per
+// nibble half), a TMA warp and two MMA warps
+constexpr int kProdF16 = 256;
+constexpr int kThreadsF16 = kProdF16 + 96;
+constexpr int kTmaWarpF16 = kProdF16 / 32;
 constexpr int kATileBytes = kRowsM * kChunk * 2;    // 16 KB: one fp16 weight tile
 constexpr int kAStageBytes = kATileBytes;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -280,23 +292,24 @@ struct Cfg {
     static constexpr int kStageBytes = kAStageBytes + NTT * kBBytes;
     static constexpr int kRoom = 224 * 1024 - kWSlots * kWSlotBytes;      // for the stage ring
     static constexpr int kStages = (kRoom / kStageBytes) < 4 ? (kRoom / kStageBytes) : 4;
-    static constexpr int kTmemCols = TN * NTT;                            // 128..512, power of two
+    static constexpr int kTmemCols = TN * 2;   // NTT = 2: one accumulator per tile; NTT = 1: one per MMA warp
     static constexpr size_t kWOffset = static_cast<size_t>(kStages) * kStageBytes;
     static constexpr size_t kSmem = kWOffset + static_cast<size_t>(kWSlots) * kWSlotBytes;
     static_assert(kStages >= 2, "at least two stages");
 };
 
-// Named barrier 1 over the 128 epilogue threads, returning the AND of p over them.
-__device__ __forceinline__ bool bar_and_128(bool p)
+// Named barrier 1 over the first `count` threads (the epilogue warps),
+// returning the AND of p over them.
+__device__ __forceinline__ bool bar_and_n(bool p, uint32_t count)
 {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred a, b;\n\t"
         "setp.ne.u32 a, %1, 0;\n\t"
-        "bar.red.and.pred b, 1, 128, a;\n\t"
+        "bar.red.and.pred b, 1, %2, a;\n\t"
         "selp.u32 %0, 1, 0, b;\n\t}"
         : "=r"(r)
-        : "r"(static_cast<uint32_t>(p))
+        : "r"(static_cast<uint32_t>(p)), "r"(count)
         : "memory");
     return r != 0;
 }
@@ -391,7 +404,7 @@ __device__ __forceinline__ void reduce_split(uint32_t part_addr, int split, int 
 }
 
 template <int TN, int NTT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsF16, 1)
     q4k_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                        const uint8_t *__restrict__ W, const int *__restrict__ xexp, float *__restrict__ Y, int N,
                        int K, int T)
@@ -434,26 +447,26 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(smem_u32(&full_a[s]), 128);
-            mbar_init(smem_u32(&empty[s]), 1);
+            mbar_init(smem_u32(&full_a[s]), kProdF16);
+            mbar_init(smem_u32(&empty[s]), NTT == 2 ? 2 : 1);   // both tiles' warps read the weight tile
         }
         for (int s = 0; s < C::kStages * NTT; ++s) {
             mbar_init(smem_u32(&full_x[s]), 1);
             mbar_init(smem_u32(&empty_x[s]), 1);
         }
-        mbar_init(smem_u32(&done_bar), 1);
+        mbar_init(smem_u32(&done_bar), 2);   // a final commit from each MMA warp
         for (int s = 0; s < kWSlots; ++s) {
             mbar_init(smem_u32(&wfull[s]), 1);
-            mbar_init(smem_u32(&wempty[s]), 128);
+            mbar_init(smem_u32(&wempty[s]), kProdF16);
         }
         s_abort = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kTmaWarpF16 + 1) {
         tmem_alloc(smem_u32(&tmem_base_s), C::kTmemCols);
         tmem_relinquish();
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == kTmaWarpF16 && lane == 0) {
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
     }
@@ -462,9 +475,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
-    if (warp < 4) {
+    if (warp < kTmaWarpF16) {
         // ------------------------------------------------ dequant producers
-        const int r = tid;                    // tile row 0..127
+        const int r = tid & (kRowsM - 1);     // tile row 0..127
+        const int hsel = tid >> 7;            // 0: low nibbles (k 0..31 of a chunk), 1: high nibbles (k 32..63)
         const int n = row0 + r;
         const bool live = n < N;
         const uint8_t *wrow = W + static_cast<size_t>(live ? n : 0) * row_bytes;
@@ -510,16 +524,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         // One super-block = four K chunks; chunk p holds sub-blocks 2p (low
-        // nibbles of quant bytes 32p..32p+31) and 2p+1 (their high nibbles).
+        // nibbles of quant bytes 32p..32p+31) and 2p+1 (their high nibbles):
+        // this thread's sub-block is 2p + hsel.
         auto dequant_sb = [&](const uint4 (&q)[9]) {
             const float d = half_lo_f32(q[0].x) * rscale, dmin = half_hi_f32(q[0].x) * rscale;
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 uint32_t scp, mp;
                 pair_scales(q[0], pair_sel(p), scp, mp);
-                const float dsE = d * static_cast<float>(scp & 0xFFu), dmE = dmin * static_cast<float>(mp & 0xFFu);
-                const float dsO16 = d * static_cast<float>((scp >> 8) & 0xFFu) * 0.0625f;
-                const float dmO = dmin * static_cast<float>((mp >> 8) & 0xFFu);
+                // (the high nibbles come out as 16 q: their scale carries 1/16)
+                const float ds = hsel ? d * static_cast<float>((scp >> 8) & 0xFFu) * 0.0625f
+                                      : d * static_cast<float>(scp & 0xFFu);
+                const float dm = dmin * static_cast<float>(hsel ? ((mp >> 8) & 0xFFu) : (mp & 0xFFu));
                 if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, kWaitLimitNs)) {
                     atomicOr(&g_prefill_error, 2u);
                     s_abort = 1;
@@ -528,31 +544,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            q[2 + 2 * p].x, q[2 + 2 * p].y, q[2 + 2 * p].z, q[2 + 2 * p].w};
                 uint8_t *arow = smem + stage * C::kStageBytes + r * 128;
                 const uint32_t k1024 = 0x64006400u;
+                const uint32_t mask = hsel ? 0x00F000F0u : 0x000F000Fu;
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {           // 0: low nibbles (k 0..31), 1: high (k 32..63)
+                for (int c8 = 0; c8 < 4; ++c8) {                 // 16-byte chunk: k = 32*hsel + 8*c8 .. +7
+                    uint32_t out[4];
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8) {             // 16-byte chunk: k = 32*half + 8*c8 .. +7
-                        uint32_t out[4];
-#pragma unroll
-                        for (int uu = 0; uu < 2; ++uu) {         // word u = 2*c8 + uu -> k offset 4u..4u+3
-                            const uint32_t w = words[2 * c8 + uu];
-                            const uint32_t mask = half ? 0x00F000F0u : 0x000F000Fu;
-                            // {q(4u), q(4u+2)} and {q(4u+1), q(4u+3)} (x16 for the high nibbles)
-                            const uint32_t h02 = hsub2_u32(and_or(w, mask, k1024), k1024);
-                            const uint32_t h13 = hsub2_u32(and_or(w >> 8, mask, k1024), k1024);
-                            const float ds = half ? dsO16 : dsE;
-                            const float dm = half ? dmO : dmE;
-                            const float w0 = fmaf(half_lo_f32(h02), ds, -dm);
-                            const float w2 = fmaf(half_hi_f32(h02), ds, -dm);
-                            const float w1 = fmaf(half_lo_f32(h13), ds, -dm);
-                            const float w3 = fmaf(half_hi_f32(h13), ds, -dm);
-                            out[2 * uu] = pack_half2(w0, w1);
-                            out[2 * uu + 1] = pack_half2(w2, w3);
-                        }
-                        const int chunk = 4 * half + c8;
-                        *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) =
-                            make_uint4(out[0], out[1], out[2], out[3]);
+                    for (int uu = 0; uu < 2; ++uu) {             // word u = 2*c8 + uu -> k offset 4u..4u+3
+                        const uint32_t w = words[2 * c8 + uu];
+                        // {q(4u), q(4u+2)} and {q(4u+1), q(4u+3)} (x16 for the high nibbles)
+                        const uint32_t h02 = hsub2_u32(and_or(w, mask, k1024), k1024);
+                        const uint32_t h13 = hsub2_u32(and_or(w >> 8, mask, k1024), k1024);
+                        const float w0 = fmaf(half_lo_f32(h02), ds, -dm);
+                        const float w2 = fmaf(half_hi_f32(h02), ds, -dm);
+                        const float w1 = fmaf(half_lo_f32(h13), ds, -dm);
+                        const float w3 = fmaf(half_hi_f32(h13), ds, -dm);
+                        out[2 * uu] = pack_half2(w0, w1);
+                        out[2 * uu + 1] = pack_half2(w2, w3);
                     }
+                    const int chunk = 4 * hsel + c8;
+                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) =
+                        make_uint4(out[0], out[1], out[2], out[3]);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(smem_u32(&full_a[stage]));
@@ -570,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dequant_sb(qb);
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == kTmaWarpF16) {
         // ------------------------------------------------ weight super-blocks by TMA (lane 1)
         if (lane == 1) {
             const uint64_t pol = l2_policy_evict_first();
@@ -631,90 +642,111 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------ MMA issuer (whole warp, one elected lane issues)
+        // ------------------------------------------------ MMA issuers (two whole warps, one elected lane issues)
         {
-            int stage = 0;
-            uint32_t phase = 0;
+            const int w = warp - (kTmaWarpF16 + 1);
             constexpr uint32_t idesc = idesc_f16(kRowsM, TN);
-            for (int c = c_begin; c < c_end; ++c) {
+            // NTT == 2: every chunk, token tile w.  NTT == 1: chunks c_begin + w,
+            // c_begin + w + 2, ...  Either way into accumulator columns w*TN.
+            constexpr int kStep = (NTT == 2) ? 1 : 2;
+            const int first = (NTT == 2) ? c_begin : c_begin + w;
+            const int j = (NTT == 2) ? w : 0;
+            const bool active = j < nsub;   // (a second tile past T has no X and no MMAs)
+            for (int c = first; c < c_end; c += kStep) {
+                const int u = c - c_begin;
+                const int stage = u % C::kStages;
+                const uint32_t phase = static_cast<uint32_t>((u / C::kStages) & 1);
                 bool ok = !*(volatile int *)&s_abort;
                 if (ok && !mbar_wait_bounded(smem_u32(&full_a[stage]), phase, kWaitLimitNs)) ok = false;
-                const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
-                const uint32_t b_addr = a_addr + kAStageBytes;
-                // token tile j's MMAs start as soon as its own X tile has landed
-#pragma unroll
-                for (int j = 0; j < NTT; ++j) {
-                    if (j < nsub) {
-                        if (ok && !mbar_wait_bounded(smem_u32(&full_x[stage * NTT + j]), phase, kWaitLimitNs))
-                            ok = false;
-                        ok = __all_sync(0xffffffffu, ok);
-                        tc_fence_after();
-                        if (ok) {
-#pragma unroll
-                            for (int kk = 0; kk < kChunk / 16; ++kk) {
-                                const uint64_t bd = sw128_desc(b_addr + j * C::kBBytes + kk * 32);
-                                umma_f16(tmem + j * TN, sw128_desc(a_addr + kk * 32), bd, idesc,
-                                         (c > c_begin || kk > 0) ? 1u : 0u);
-                            }
-                        }
-                        umma_commit(smem_u32(&empty_x[stage * NTT + j]));   // frees this X tile
-                    }
-                }
+                if (active && ok && !mbar_wait_bounded(smem_u32(&full_x[stage * NTT + j]), phase, kWaitLimitNs))
+                    ok = false;
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok && lane == 0 && !*(volatile int *)&s_abort) {
                     atomicOr(&g_prefill_error, 2u);
                     s_abort = 1;
                 }
-                umma_commit(smem_u32(&empty[stage]));   // frees the weight tile once all its MMAs finish
-                if (++stage == C::kStages) { stage = 0; phase ^= 1u; }
+                tc_fence_after();
+                if (active) {
+                    if (ok) {
+                        const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
+                        const uint32_t b_addr = a_addr + kAStageBytes + j * C::kBBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kChunk / 16; ++kk)
+                            umma_f16(tmem + w * TN, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), idesc,
+                                     (c > first || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(smem_u32(&empty_x[stage * NTT + j]));   // frees this X tile
+                }
+                umma_commit(smem_u32(&empty[stage]));   // this warp is done with the weight tile
             }
             umma_commit(smem_u32(&done_bar));
         }
     }
 
-    // ---------------------------------------------------- epilogue (warps 0-3)
-    // Warp w reads TMEM lanes 32w..32w+31 (= tile rows).  With a K split the
-    // partial tile goes to this CTA's shared memory (column-major, so a warp's
-    // stores are consecutive); after a cluster barrier CTA rank z sums rows
-    // [z*128/split, (z+1)*128/split) over ranks 0..split-1 in order and writes Y.
+    // ---------------------------------------------------- epilogue (warps 0-7)
+    // Warps w and w + 4 read TMEM lanes 32w..32w+31 (= tile rows); thread group
+    // g = tid / 128 takes token tile g (NTT == 2) or column half g (NTT == 1).
+    // With a K split the partial tile goes to this CTA's shared memory
+    // (column-major, so a warp's stores are consecutive); after a cluster
+    // barrier CTA rank z sums rows [z*128/split, (z+1)*128/split) over ranks
+    // 0..split-1 in order and writes Y.
     float *part = reinterpret_cast<float *>(smem);   // pipeline buffers are idle by now
-    if (warp < 4) {
+    if (warp < kTmaWarpF16) {
         pdl_wait();   // the token exponents come from the conversion kernel
         // token factors 2^-e_t; moderate = every |e_t| <= 63 (then, for rows
         // with |r| <= 63 too, 2^-r 2^-e_t is an exact normal float and one
         // multiply scales a value)
         bool mod = true;
-        for (int i = tid; i < TN * NTT; i += 128) {
+        for (int i = tid; i < TN * NTT; i += kProdF16) {
             const int e = (t0 + i < T) ? __ldg(xexp + t0 + i) : 0;
             s_xexp[i] = e;
             s_xinv[i] = __uint_as_float(static_cast<uint32_t>(127 - max(-126, min(126, e))) << 23);
             mod = mod && e >= -63 && e <= 63;
         }
-        const bool all_mod = bar_and_128(mod);
+        const bool all_mod = bar_and_n(mod, kProdF16);
         const bool ok = mbar_wait_bounded(smem_u32(&done_bar), 0u, kWaitLimitNs);
         if (!ok) {
             atomicOr(&g_prefill_error, 2u);
             s_abort = 1;
         }
         tc_fence_after();
-        const int r = warp * 32 + lane;
+        const int r = tid & (kRowsM - 1);
         const int n = row0 + r;
-        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const bool fast = all_mod && rexp >= -63 && rexp <= 63;
         const float rinv = __uint_as_float(static_cast<uint32_t>(127 - max(-126, min(126, rexp))) << 23);
-        // 64 columns per round: four tensor-memory loads in flight, one wait
-        // (a wait per 16 columns left the 512-token epilogue at ~14 us)
-        for (int j = 0; j < nsub; ++j) {
+        // Four tensor-memory loads in flight per wait (a wait per 16 columns
+        // left the 512-token epilogue at ~14 us): 64 columns of a tile per
+        // round, or with NTT == 1 32 columns of each MMA warp's accumulator,
+        // added (D0 + D1).
+        constexpr int kRound = (NTT == 1) ? 32 : 64;
+        const int g = tid >> 7;
+        const int j_lo = (NTT == 2) ? g : 0, j_hi = (NTT == 2) ? min(g + 1, nsub) : nsub;
+        const int c_lo = (NTT == 1) ? g * (TN / 2) : 0, c_hi = (NTT == 1) ? c_lo + TN / 2 : TN;
+        for (int j = j_lo; j < j_hi; ++j) {
 #pragma unroll 1
-            for (int c64 = 0; c64 < TN; c64 += 64) {
+            for (int c64 = c_lo; c64 < c_hi; c64 += kRound) {
                 uint32_t v[4][16];
+                if (NTT == 1) {
+                    tmem_ld16(lane_addr + c64, v[0]);
+                    tmem_ld16(lane_addr + c64 + 16, v[1]);
+                    tmem_ld16(lane_addr + TN + c64, v[2]);
+                    tmem_ld16(lane_addr + TN + c64 + 16, v[3]);
+                } else {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    if (c64 + 16 * q < TN) tmem_ld16(lane_addr + j * TN + c64 + 16 * q, v[q]);
+                    for (int q = 0; q < 4; ++q) tmem_ld16(lane_addr + j * TN + c64 + 16 * q, v[q]);
+                }
                 tmem_wait_ld();
+                if (NTT == 1) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                    for (int q = 0; q < 2; ++q)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            v[q][i] = __float_as_uint(__uint_as_float(v[q][i]) + __uint_as_float(v[q + 2][i]));
+                }
+#pragma unroll
+                for (int q = 0; q < kRound / 16; ++q) {
                     const int c0 = c64 + 16 * q;
-                    if (c0 >= TN) break;
                     // undo the row's and the tokens' power-of-two scales: times
                     // 2^-(r + e_t), one correctly rounded multiply by an exact
                     // power of two when both are moderate, else as two factors
@@ -771,11 +803,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
         cluster_sync_all();
         if (!*(volatile int *)&s_abort)
-            reduce_split(smem_u32(part), split, kz, nsub * TN, row0, t0, Y, N, T, tid, kThreads);
+            reduce_split(smem_u32(part), split, kz, nsub * TN, row0, t0, Y, N, T, tid, kThreadsF16);
         cluster_sync_all();
     }
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kTmaWarpF16 + 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
@@ -1183,7 +1215,7 @@ static cudaError_t launch_prefill(const uint8_t *W, const void *Xh, const int *x
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((N + pf::kRowsM - 1) / pf::kRowsM, (T + TN * NTT - 1) / (TN * NTT), split);
-    cfg.blockDim = dim3(pf::kThreads, 1, 1);
+    cfg.blockDim = dim3(pf::kThreadsF16, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
