@@ -26,8 +26,8 @@
 //     a 128-byte-swizzled K-major tile (with one thread per row the dequant
 //     took ~900 cycles a chunk against 512 for the MMAs at 256 tokens);
 //   * warp 8 loads the X tile [TN x 64] (fp16) with a TMA tensor copy (128B
-//     swizzle), and the raw weight super-blocks;
-//   * warps 9 and 10 (one elected thread each) issue the tcgen05.mma (K = 16
+//     swizzle), warp 9 the raw weight super-blocks;
+//   * warps 10 and 11 (one elected thread each) issue the tcgen05.mma (K = 16
 //     each) into TMEM and commit to the stage's "empty" barriers: with two
 //     token tiles (NTT = 2) warp 5 + j takes tile j, otherwise warp 5 takes the
 //     even chunks and warp 6 the odd ones, into an accumulator of its own that
@@ -72,10 +72,11 @@ constexpr int kRowsM = 128;          // MMA M
 constexpr int kChunk = 64;           // K elements per stage (one 128-byte swizzle row)
 constexpr int kThreads = 192;        // 4 dequant/epilogue warps + TMA warp + MMA warp
 // fp16 kernel: 8 dequant/epilogue warps (two threads per weight row, one per
-// nibble half), a TMA warp and two MMA warps
+// nibble half), an X-tile TMA warp, a weight TMA warp and two MMA warps
 constexpr int kProdF16 = 256;
-constexpr int kThreadsF16 = kProdF16 + 96;
-constexpr int kTmaWarpF16 = kProdF16 / 32;
+constexpr int kThreadsF16 = kProdF16 + 128;
+constexpr int kTmaWarpF16 = kProdF16 / 32;      // X tiles; the next warp: raw weights
+constexpr int kMmaWarpF16 = kTmaWarpF16 + 2;    // and the one after it
 constexpr int kATileBytes = kRowsM * kChunk * 2;    // 16 KB: one fp16 weight tile
 constexpr int kAStageBytes = kATileBytes;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -462,7 +463,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
         s_abort = 0;
         fence_barrier_init();
     }
-    if (warp == kTmaWarpF16 + 1) {
+    if (warp == kMmaWarpF16) {
         tmem_alloc(smem_u32(&tmem_base_s), C::kTmemCols);
         tmem_relinquish();
     }
@@ -581,9 +582,11 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
                 dequant_sb(qb);
             }
         }
-    } else if (warp == kTmaWarpF16) {
-        // ------------------------------------------------ weight super-blocks by TMA (lane 1)
-        if (lane == 1) {
+    } else if (warp == kTmaWarpF16 + 1) {
+        // ------------------------------------------------ weight super-blocks by TMA (lane 0)
+        // (a warp of its own: as a second lane of the X warp, its bounded
+        // waits held up the X copies of the diverged lane)
+        if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
             int issued = 0;
             for (int i = 0; i < nloc; ++i) {
@@ -607,6 +610,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
                         break;
             }
         }
+    } else if (warp == kTmaWarpF16) {
         // ------------------------------------------------ X tiles by TMA (lane 0)
         if (lane == 0) {
             pdl_wait();   // X (fp16) is written by the conversion kernel launched just before
@@ -644,7 +648,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
     } else {
         // ------------------------------------------------ MMA issuers (two whole warps, one elected lane issues)
         {
-            const int w = warp - (kTmaWarpF16 + 1);
+            const int w = warp - kMmaWarpF16;
             constexpr uint32_t idesc = idesc_f16(kRowsM, TN);
             // NTT == 2: every chunk, token tile w.  NTT == 1: chunks c_begin + w,
             // c_begin + w + 2, ...  Either way into accumulator columns w*TN.
@@ -807,7 +811,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
         cluster_sync_all();
     }
     __syncthreads();
-    if (warp == kTmaWarpF16 + 1) {
+    if (warp == kMmaWarpF16) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
