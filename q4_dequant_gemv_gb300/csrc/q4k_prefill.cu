@@ -1298,6 +1298,57 @@ static cudaError_t launch_prefill_exact(const uint8_t *W, const void *Xh, const 
     return e;
 }
 
+// Clusters of csize CTAs (2, 4 or 8) of kernel `kid` (0: exact 32-token,
+// 1: exact 64-token, 2: fp16 128-token, 3: fp16 256-token tiles) that the GPU
+// holds at once, queried once per device; -1 when the query fails (the caller
+// then does not limit the split on it).
+static int max_active_clusters(int kid, int csize)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    const int ci = (csize == 2) ? 0 : (csize == 4) ? 1 : 2;
+    static std::mutex mu;
+    static int cache[64][4][3];
+    static bool have[64][4][3];
+    std::lock_guard<std::mutex> lock(mu);
+    if (have[dev][kid][ci]) return cache[dev][kid][ci];
+    const void *kern = nullptr;
+    size_t smem = 0;
+    int threads = pf::kThreads;
+    switch (kid) {
+    case 0: kern = reinterpret_cast<const void *>(pf::q4k_prefill_exact_kernel<32, kExactParts32>);
+            smem = pf::ECfg<32, kExactParts32>::kSmem; break;
+    case 1: kern = reinterpret_cast<const void *>(pf::q4k_prefill_exact_kernel<64, 1>); smem = pf::ECfg<64, 1>::kSmem; break;
+    case 2: kern = reinterpret_cast<const void *>(pf::q4k_prefill_kernel<128, 1>); smem = pf::Cfg<128, 1>::kSmem;
+            threads = pf::kThreadsF16; break;
+    default: kern = reinterpret_cast<const void *>(pf::q4k_prefill_kernel<256, 1>); smem = pf::Cfg<256, 1>::kSmem;
+             threads = pf::kThreadsF16; break;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, csize);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = 1;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = csize;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        n = -1;
+    }
+    cache[dev][kid][ci] = n;
+    have[dev][kid][ci] = true;
+    return n;
+}
+
 q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream)
 {
     q4k_status st = validate_prefill(W, X, Y, N, K, T);
@@ -1336,9 +1387,17 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     // (one CTA per SM, except the exact kernel's 32-token tiles with one part per stage)
     const long long slots = exact && tn == 32 && pf::ECfg<32, kExactParts32>::kTwoPerSm ? 2LL * sms
                                                                                          : static_cast<long long>(sms);
+    // ... and only while every cluster of the split fits on the GPU at once
+    // (clusters of eight CTAs that take a whole SM each stop fitting well
+    // before 152 CTAs: at 1024 x 4096 and 512 tokens, sixteen of them ran
+    // in two waves, 30 us, against 19 us for sixteen clusters of four)
+    const int kid = exact ? (tn == 32 ? 0 : 1) : (tn == 128 ? 2 : 3);
     int split = 1;
-    while (ntt == 1 && split < 8 && ctas * split * 2 <= slots && (k / 256) / (split * 2) >= 2)
+    while (ntt == 1 && split < 8 && ctas * split * 2 <= slots && (k / 256) / (split * 2) >= 2) {
+        const int fit = max_active_clusters(kid, split * 2);
+        if (fit > 0 && ctas > fit) break;
         split *= 2;
+    }
     // X in fp16 under a power-of-two scale per token: T*K*2 bytes, the
     // exponents, and for the exact kernel the sub-block sums (T*K/2 bytes),
     // from the stream-ordered allocator on the caller's stream
