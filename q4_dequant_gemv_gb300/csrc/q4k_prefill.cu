@@ -422,6 +422,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
     __shared__ int s_abort;
     __shared__ __align__(16) int s_xexp[TN * NTT];   // token scale exponents of this CTA's tokens
     __shared__ __align__(16) float s_xinv[TN * NTT]; // 2^-e_t
+    __shared__ int s_rexp[kRowsM];                   // row scale exponents (from the prescan)
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -445,6 +446,22 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
         const int j = i + rot;
         return sb_begin + (j >= nloc ? j - nloc : j);
     };
+
+    // Row-scale prescan, first round of header loads issued before the setup
+    // barrier by the low-nibble thread of each row (the other thread of the
+    // row reads the result from shared memory): the prescan is pure load
+    // latency at the start of the launch.
+    const bool pre_thread = tid < kRowsM;
+    const bool pre_live = pre_thread && row0 + tid < N;
+    uint32_t hb0[16];
+    {
+        const uint8_t *wr = W + static_cast<size_t>(pre_live ? row0 + tid : 0) * row_bytes;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            hb0[i] = (pre_live && sb_begin + i < sb_end)
+                         ? __ldg(reinterpret_cast<const uint32_t *>(wr + static_cast<size_t>(sb_begin + i) * 144))
+                         : 0u;
+    }
 
     if (tid == 0) {
         for (int s = 0; s < C::kStages; ++s) {
@@ -487,19 +504,26 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
         uint32_t phase = 0;
         // Row scale 2^rs: the largest |w| this CTA's super-blocks of the row
         // can hold, |d|*945 + |dmin|*63, brought to [2^14, 2^15).
-        float wmax = 0.f;
-        if (live) {   // sixteen headers in flight per round (the prescan is pure load latency)
-            for (int b = sb_begin; b < sb_end; b += 16) {
-                uint32_t hb[16];
+        if (hsel == 0) {
+            float wmax = 0.f;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    hb[i] = (b + i < sb_end) ? __ldg(reinterpret_cast<const uint32_t *>(wrow + static_cast<size_t>(b + i) * 144)) : 0u;
+            for (int i = 0; i < 16; ++i)
+                wmax = fmaxf(wmax, fmaf(fabsf(half_lo_f32(hb0[i])), 945.0f, fabsf(half_hi_f32(hb0[i])) * 63.0f));
+            if (live) {   // sixteen headers in flight per further round
+                for (int b = sb_begin + 16; b < sb_end; b += 16) {
+                    uint32_t hb[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    wmax = fmaxf(wmax, fmaf(fabsf(half_lo_f32(hb[i])), 945.0f, fabsf(half_hi_f32(hb[i])) * 63.0f));
+                    for (int i = 0; i < 16; ++i)
+                        hb[i] = (b + i < sb_end) ? __ldg(reinterpret_cast<const uint32_t *>(wrow + static_cast<size_t>(b + i) * 144)) : 0u;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        wmax = fmaxf(wmax, fmaf(fabsf(half_lo_f32(hb[i])), 945.0f, fabsf(half_hi_f32(hb[i])) * 63.0f));
+                }
             }
+            s_rexp[r] = f16_range_exp(wmax);
         }
-        rexp = f16_range_exp(wmax);
+        named_bar_sync(2, kProdF16);
+        rexp = s_rexp[r];
         const float rscale = __uint_as_float(static_cast<uint32_t>(rexp + 127) << 23);
         // A super-block of the row as nine 16-byte words (header, then the
         // 128 quant bytes), read from the weight ring one super-block ahead of
