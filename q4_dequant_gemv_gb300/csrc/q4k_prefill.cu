@@ -473,12 +473,25 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
             mbar_init(smem_u32(&empty_x[s]), 1);
         }
         mbar_init(smem_u32(&done_bar), 2);   // a final commit from each MMA warp
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    // The weight warp sets up its own ring and issues the first super-blocks
+    // before the setup barrier (the weight stream is the first thing the
+    // dequant needs, with the prescan).
+    const int w_first = min(kWSlots, nloc);
+    if (warp == kTmaWarpF16 + 1 && lane == 0) {
         for (int s = 0; s < kWSlots; ++s) {
             mbar_init(smem_u32(&wfull[s]), 1);
             mbar_init(smem_u32(&wempty[s]), kProdF16);
         }
-        s_abort = 0;
         fence_barrier_init();
+        const uint64_t pol = l2_policy_evict_first();
+        for (int i = 0; i < w_first; ++i) {
+            mbar_arrive_expect_tx(smem_u32(&wfull[i]), kWSlotBytes);
+            tma_load_2d_hint(smem_u32(smem + C::kWOffset + i * kWSlotBytes), &tmW, sb_of(i) * 18, row0,
+                             smem_u32(&wfull[i]), pol);
+        }
     }
     if (warp == kMmaWarpF16) {
         tmem_alloc(smem_u32(&tmem_base_s), C::kTmemCols);
@@ -612,8 +625,8 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
         // waits held up the X copies of the diverged lane)
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            int issued = 0;
-            for (int i = 0; i < nloc; ++i) {
+            int issued = w_first;   // (the first ones went out before the setup barrier)
+            for (int i = w_first; i < nloc; ++i) {
                 const int slot = i % kWSlots;
                 if (i >= kWSlots && !*(volatile int *)&s_abort &&
                     !mbar_wait_bounded(smem_u32(&wempty[slot]), static_cast<uint32_t>(((i / kWSlots) - 1) & 1),
