@@ -29,11 +29,10 @@
 //     swizzle), warp 9 the raw weight super-blocks;
 //   * warps 10 and 11 (one elected thread each) issue the tcgen05.mma (K = 16
 //     each) into TMEM and commit to the stage's "empty" barriers: with two
-//     token tiles (NTT = 2) warp 5 + j takes tile j, otherwise warp 5 takes the
-//     even chunks and warp 6 the odd ones, into an accumulator of its own that
-//     the epilogue adds.  One issuing warp spent ~500 cycles a chunk on its
-//     barrier waits, fences and commits on top of ~100 per MMA issued, so the
-//     tensor pipe sat idle about half the time.
+//     token tiles (NTT = 2) warp 10 + j takes tile j, otherwise warp 10 takes
+//     the even chunks and warp 11 the odd ones, into an accumulator of its own
+//     that the epilogue adds (one issuing warp spent ~500 cycles a chunk on
+//     its barrier waits, fences and commits on top of ~100 per MMA issued).
 // A ring of NS stages overlaps the three.  The epilogue reads TMEM with
 // tcgen05.ld (warps w and w + 4 own TMEM lanes 32w..32w+31 = weight rows) and
 // writes Y with coalesced stores.  Every mbarrier wait is bounded in time.
