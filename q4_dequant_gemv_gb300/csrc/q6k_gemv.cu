@@ -159,10 +159,14 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_kernel(const uint8_t *__res
 // ---------------------------------------------------------------------------
 // Staged variant, integer inner product (batch <= 4).
 //
-// Tiles of 8 rows, each streamed through shared memory in K-slices of up to
-// kSliceBlocks blocks (one bulk async copy per row and slice, its range
-// rounded out to 16-byte boundaries, so the row's first block starts at an
-// even offset inside the stage); warp w works on row w of the tile.  x is
+// Tiles of 8 RW rows, each streamed through shared memory in K-slices (one
+// bulk async copy per row and slice, its range rounded out to 16-byte
+// boundaries, so the row's first block starts at an even offset inside the
+// stage); warp w works on rows w, w + 8, ... of the tile and loads its x
+// parts once per block for all of them.  Batch 1 takes RW = 2 in two 48 KB
+// stages (two CTAs per SM): the shared-memory load pipe bounds this kernel,
+// and the x loads, shared by two rows, are half of its wavefronts (LM head
+// 150 -> 125 us against RW = 1 in three 28 KB stages, which batch 2-4 keep).  x is
 // converted once per CTA, block by block, into two int8 parts
 // (x ~ (a/32258)(254 xh + xl), a = the block's max |x|, rounding to nearest
 // even), laid out so that lane L finds the parts of its eight x values in one
@@ -174,13 +178,14 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_kernel(const uint8_t *__res
 // int32 (|.| < 1.1e9); y += (d u) p (that sum), with u p the block's step.
 // (The float path, one fp32 FMA per weight, was instruction-bound.)
 // Persistent CTAs over the tiles; the last warp to finish a stage issues the
-// stage kStages ahead into it.  Every wait is bounded: on a timeout the CTA
+// stage ST ahead into it.  Every wait is bounded: on a timeout the CTA
 // flags g_q6k_error, keeps walking its schedule without waiting, and waits
 // (bounded) for its copies in flight before it exits.
 // ---------------------------------------------------------------------------
-constexpr int kStages = 3;
-constexpr int kRowsPerWarp = 1;    // x parts loaded once serve this many rows
-constexpr int kStageKB = 28;       // stage size target
+// staging of the batch-1 and the batch-2..4 kernels: rows per warp, stages,
+// stage size target
+constexpr int kRW1 = 2, kStages1 = 2, kStageKB1 = 48;
+constexpr int kRW4 = 1, kStages4 = 3, kStageKB4 = 28;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 constexpr int kXItemBytes = 32 * 16 + 32 * 8;      // int8 parts + four-value sums of one (batch row, block)
 
@@ -243,15 +248,15 @@ __device__ __forceinline__ float2 q6_x_item(float4 v0, float4 v1, int lane, uint
     return make_float2(u, 1.0f / pre);
 }
 
-template <int BMAX, int RW>
+template <int BMAX, int RW, int ST>
 __global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__restrict__ W, const float *__restrict__ x,
                                                            float *__restrict__ y, int N, int nb, int B, int tiles,
                                                            int sb)
 {
     constexpr int TR = 8 * RW;                            // rows per tile: warp w takes rows w, w + 8, ...
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ __align__(8) uint64_t full[kStages];
-    __shared__ int s_done[kStages];
+    __shared__ __align__(8) uint64_t full[ST];
+    __shared__ int s_done[ST];
     __shared__ int s_abort;
     __shared__ int s_issued;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__res
     const int stage_bytes = TR * pitch;
     const int nslices = (nb + sb - 1) / sb;
     // x area: per (batch row, block) 32 x 16 bytes of parts and 32 x 8 of sums, then the steps
-    uint8_t *xa = smem + kStages * stage_bytes;
+    uint8_t *xa = smem + ST * stage_bytes;
     float2 *xup = reinterpret_cast<float2 *>(xa + static_cast<size_t>(B) * nb * kXItemBytes);
     const int my_tiles = (tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
                          static_cast<int>(gridDim.x);
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__res
     const uint64_t policy = l2_policy_evict_first();
     // stage i of this CTA's schedule: tile blockIdx.x + (i / nslices) * gridDim.x, slice i % nslices
     auto issue = [&](int i) {
-        const int slot = i % kStages;
+        const int slot = i % ST;
         const size_t tile = static_cast<size_t>(blockIdx.x) + static_cast<size_t>(i / nslices) * gridDim.x;
         const int sl = i % nslices;
         const int j0 = sl * sb, j1 = min(nb, j0 + sb);
@@ -290,13 +295,13 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__res
         }
     };
     if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < ST; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
             s_done[i] = 0;
         }
         s_abort = 0;
         fence_barrier_init();
-        const int first = min(kStages, total);
+        const int first = min(ST, total);
         for (int i = 0; i < first; ++i) issue(i);
         s_issued = first;
     }
@@ -326,8 +331,8 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__res
 #pragma unroll
                 for (int b = 0; b < BMAX; ++b) acc[r][b] = 0.f;
         }
-        const int slot = i % kStages;
-        const uint32_t phase = static_cast<uint32_t>((i / kStages) & 1);
+        const int slot = i % ST;
+        const uint32_t phase = static_cast<uint32_t>((i / ST) & 1);
         if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), phase, kWaitLimitNs)) {
             atomicOr(&g_q6k_error, 1u);
             s_abort = 1;
@@ -383,7 +388,7 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__res
             __threadfence_block();
             const int prev = atomicAdd(&s_done[slot], 1);
             if (prev % kWarps == kWarps - 1) {
-                const int next = i + kStages;
+                const int next = i + ST;
                 if (next < total && !*(volatile int *)&s_abort) {
                     issue(next);
                     atomicAdd(&s_issued, 1);
@@ -408,8 +413,8 @@ __global__ void __launch_bounds__(kThreads) q6k_gemv_staged(const uint8_t *__res
     // consumed, so that none lands after the CTA has exited.
     __syncthreads();
     if (*(volatile int *)&s_abort && tid == 0) {
-        for (int i = max(0, s_issued - kStages); i < s_issued; ++i)
-            if (!mbar_wait_bounded(smem_u32(&full[i % kStages]), static_cast<uint32_t>((i / kStages) & 1), kWaitLimitNs))
+        for (int i = max(0, s_issued - ST); i < s_issued; ++i)
+            if (!mbar_wait_bounded(smem_u32(&full[i % ST]), static_cast<uint32_t>((i / ST) & 1), kWaitLimitNs))
                 break;
     }
 }
@@ -446,11 +451,11 @@ static cudaError_t q6k_launch(const uint8_t *W, const float *x, float *y, int N,
     return cudaGetLastError();
 }
 
-template <int BMAX, int RW>
+template <int BMAX, int RW, int ST>
 static cudaError_t q6k_launch_staged(const uint8_t *W, const float *x, float *y, int N, int nb, int B, int tiles,
                                      int sb, int sms, size_t smem, cudaStream_t s)
 {
-    auto kern = q6::q6k_gemv_staged<BMAX, RW>;
+    auto kern = q6::q6k_gemv_staged<BMAX, RW, ST>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int occ = 0;
@@ -516,18 +521,21 @@ q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int
     // up to 16 blocks, x converted into shared memory beside the ring (when
     // that takes at most 64 KB); the remaining N % 8 rows go to the direct
     // kernel.
-    constexpr int RW = q6::kRowsPerWarp;
+    const bool b1 = batch == 1;
+    const int RW = b1 ? q6::kRW1 : q6::kRW4;
+    const int ST = b1 ? q6::kStages1 : q6::kStages4;
+    const int SKB = b1 ? q6::kStageKB1 : q6::kStageKB4;
     const int tiles = n / (8 * RW);
     const size_t xbytes = static_cast<size_t>(batch) * nb * (q6::kXItemBytes + 8);
     // (rows longer than one slice, e.g. K = 18944, measured faster on the
     // direct kernel: 27 against 31 us)
-    const int sb = std::max(1, std::min(nb, ((q6::kStageKB * 1024) / (8 * RW) - 30) / q6::kBytes));
+    const int sb = std::max(1, std::min(nb, ((SKB * 1024) / (8 * RW) - 30) / q6::kBytes));
     if (batch <= 4 && tiles > 0 && xbytes <= 64 * 1024 && sb == nb) {
-        const size_t smem = static_cast<size_t>(q6::kStages) * 8 * RW * q6::q6_pitch(sb) + xbytes;
-        if (batch == 1)
-            e = q6k_launch_staged<1, RW>(Wb, x, y, n, nb, batch, tiles, sb, sms, smem, s);
+        const size_t smem = static_cast<size_t>(ST) * 8 * RW * q6::q6_pitch(sb) + xbytes;
+        if (b1)
+            e = q6k_launch_staged<1, q6::kRW1, q6::kStages1>(Wb, x, y, n, nb, batch, tiles, sb, sms, smem, s);
         else
-            e = q6k_launch_staged<4, RW>(Wb, x, y, n, nb, batch, tiles, sb, sms, smem, s);
+            e = q6k_launch_staged<4, q6::kRW4, q6::kStages4>(Wb, x, y, n, nb, batch, tiles, sb, sms, smem, s);
         const int done = tiles * 8 * RW;
         if (e == cudaSuccess && done < n)
             e = q6k_direct(Wb + static_cast<size_t>(done) * nb * q6::kBytes, x, y + done, n - done, n, nb, batch, sms, s);
