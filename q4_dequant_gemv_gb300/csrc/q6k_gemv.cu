@@ -521,19 +521,26 @@ q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int
     // up to 16 blocks, x converted into shared memory beside the ring (when
     // that takes at most 64 KB); the remaining N % 8 rows go to the direct
     // kernel.
-    const bool b1 = batch == 1;
-    const int RW = b1 ? q6::kRW1 : q6::kRW4;
-    const int ST = b1 ? q6::kStages1 : q6::kStages4;
-    const int SKB = b1 ? q6::kStageKB1 : q6::kStageKB4;
+    // Batch 1 takes two rows per warp when a row fits one 48 KB stage slice
+    // (K up to 3584) and there is a whole 16-row tile; otherwise, like batch
+    // 2-4, one row per warp in 28 KB stages (K up to 4096).
+    auto slice = [&](int rw, int skb) {
+        return std::max(1, std::min(nb, ((skb * 1024) / (8 * rw) - 30) / q6::kBytes));
+    };
+    const bool pair = batch == 1 && slice(q6::kRW1, q6::kStageKB1) == nb && n >= 8 * q6::kRW1;
+    const int RW = pair ? q6::kRW1 : q6::kRW4;
+    const int ST = pair ? q6::kStages1 : q6::kStages4;
     const int tiles = n / (8 * RW);
     const size_t xbytes = static_cast<size_t>(batch) * nb * (q6::kXItemBytes + 8);
     // (rows longer than one slice, e.g. K = 18944, measured faster on the
     // direct kernel: 27 against 31 us)
-    const int sb = std::max(1, std::min(nb, ((SKB * 1024) / (8 * RW) - 30) / q6::kBytes));
+    const int sb = slice(RW, pair ? q6::kStageKB1 : q6::kStageKB4);
     if (batch <= 4 && tiles > 0 && xbytes <= 64 * 1024 && sb == nb) {
         const size_t smem = static_cast<size_t>(ST) * 8 * RW * q6::q6_pitch(sb) + xbytes;
-        if (b1)
+        if (pair)
             e = q6k_launch_staged<1, q6::kRW1, q6::kStages1>(Wb, x, y, n, nb, batch, tiles, sb, sms, smem, s);
+        else if (batch == 1)
+            e = q6k_launch_staged<1, q6::kRW4, q6::kStages4>(Wb, x, y, n, nb, batch, tiles, sb, sms, smem, s);
         else
             e = q6k_launch_staged<4, q6::kRW4, q6::kStages4>(Wb, x, y, n, nb, batch, tiles, sb, sms, smem, s);
         const int done = tiles * 8 * RW;

@@ -38,8 +38,9 @@ SHAPES = [(1, 256, 1), (7, 512, 2), (129, 3584, 1), (300, 4096, 5), (512, 3584, 
           (65, 18944, 3), (3584, 3584, 1), (37, 768, 9), (64, 1024, 3), (29, 2560, 4),
           # K-sliced stages: several slices per tile, a short last slice, batch 1 and 4
           (3584, 18944, 1), (40, 4608, 4), (16, 4352, 1),
-          # batch 1 in 16-row tiles: a tail of 8 rows after whole tiles, one tile plus a tail
-          (1000, 3584, 1), (24, 3584, 1)]
+          # batch 1 in 16-row tiles: a tail of 8 rows after whole tiles, one tile plus a tail;
+          # batch 1 back on 8-row tiles: rows longer than a 48 KB slice, fewer than 16 rows
+          (1000, 3584, 1), (24, 3584, 1), (136, 4096, 1), (12, 3584, 1)]
 
 
 @pytest.mark.parametrize("N,K,B", SHAPES)
