@@ -605,15 +605,16 @@ def run_ours(args):
             # every launch reads them from HBM
             ncopy = max(1, -(-4 * l2 // Wp.numel())) if Wp.numel() < l2 else 1
             Wps = [Wp] + [Wp.clone() for _ in range(ncopy - 1)]
-            for T in (32, 512):
+            # (T = 32 also through q4k_gemm_prefill_exact, the no-weight-rounding entry point)
+            for T, exact in ((32, False), (32, True), (512, False)):
                 Xb = torch.from_numpy(synth.normal_bf16_bits((T, K), (4, T, K)).view(np.int16)).to(dev).view(torch.bfloat16)
                 Yp = torch.empty((T, N), dtype=torch.float32, device=dev)
-                g = capture(lambda: [q4k.gemm_prefill(Wq, Xb, Yp, stream=stream) for Wq in Wps])
+                g = capture(lambda: [q4k.gemm_prefill(Wq, Xb, Yp, stream=stream, exact=exact) for Wq in Wps])
                 ms = time_graph(g, max(4, args.steps // (4 * ncopy)), args.warmup) / ncopy
                 flops = 2.0 * N * K * T
                 byts = N * (K // 256) * 144 + 2 * T * K + 4 * T * N
                 ideal_s = max(byts / (pk["hbm_gbs"] * 1e9), flops / (pk["bf16_tflops"] * 1e12))
-                prefill[f"{name}_{N}x{K}_T{T}"] = {
+                prefill[f"{name}_{N}x{K}_T{T}" + ("_exact" if exact else "")] = {
                     "us": ms * 1e3, "tflops": flops / (ms * 1e-3) / 1e12, "gbs": byts / (ms * 1e-3) / 1e9,
                     "frac_tensor": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"],
                     "frac_hbm": byts / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],

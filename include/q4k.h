@@ -16,7 +16,9 @@
  *                      Warp-Shuffle Argmax")
  *   - q4k_gemm_prefill the prefill product with bf16 activations ("cuBLAS HGEMM
  *                      for prefill", dotLLM README, News 2026-03), here on the
- *                      tcgen05 tensor cores after a dequantize-to-fp16 step.
+ *                      tcgen05 tensor cores after a dequantize-to-fp16 step
+ *                      (q4k_gemm_prefill_exact: the same with exact integer
+ *                      weight tiles).
  *   - q6k_gemv         y = W x for a Q6_K matrix, the other block format of
  *                      Q4_K_M files ("custom quantized GEMV for decode (Q8_0,
  *                      Q4_K, Q6_K)", same page and item).
@@ -191,9 +193,10 @@ q4k_status q6k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t 
  *   W  Q4_K rows as above (16-byte aligned)
  *   X  bf16 [T][K] row-major (16-byte aligned)
  *   Y  fp32 [T][N] row-major
- * Each weight is dequantized in fp32, multiplied by a power of two chosen per
- * row from the row's largest possible |w|, and rounded once to fp16 (nearest
- * even) in shared memory; each token's activations are converted to fp16
+ * Up to 32 tokens this is q4k_gemm_prefill_exact (below: no weight is
+ * rounded).  Above that each weight is dequantized in fp32, multiplied by a
+ * power of two chosen per row from the row's largest possible |w|, and rounded
+ * once to fp16 (nearest even) in shared memory; each token's activations are converted to fp16
  * under a power of two chosen per token from its largest |x| (exact for every
  * value of at least 2^-31 times that largest).  The tcgen05 tensor cores
  * multiply them with fp32 accumulation in tensor memory and the epilogue
@@ -202,12 +205,29 @@ q4k_status q6k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t 
  * Scratch: the converted X (2*T*K bytes) and T scale exponents come from
  * cudaMallocAsync on `stream` and are freed on it after the product.
  * Any T >= 0 is accepted (T == 0 or N == 0 is a no-op, and the pointers may
- * then be NULL); the tensor path is built for T >= 32.
+ * then be NULL); tokens go in tiles of 64 (T <= 64), 128, 256 or 512.
  * Errors: INVALID_ARG, MISALIGNED (W or X), UNSUPPORTED_DEVICE, CUDA
  * (including a failed scratch allocation).
  */
 q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t N, int64_t K,
                             int64_t T, void *stream);
+
+/*
+ * The same product with no weight rounding at all (arguments, layouts, errors
+ * and scratch as q4k_gemm_prefill, plus T*K/2 bytes of scratch for the
+ * sub-block sums of X).  The weight tiles hold q * sc_j, an integer of at most
+ * 945 that fp16 represents exactly; the tensor cores accumulate
+ * D = sum (q sc) x per super-block in tensor memory, one more MMA forms
+ * M = sum_j m_j S_j from the sub-block sums S_j of the fp16 X (split into fp16
+ * hi + lo), and y += d D - dmin M in fp32.  The only roundings are the fp32
+ * accumulations and the hi + lo split of S_j.  Tiles of 32 (T <= 32) or 64
+ * tokens; any T >= 0.  q4k_gemm_prefill takes this path up to 32 tokens;
+ * from 33 tokens on the fp16 path is faster (14336 x 4096 at 64 tokens: 36.7
+ * against 44.2 us), so this entry point is for callers that want the weights
+ * exact there too.
+ */
+q4k_status q4k_gemm_prefill_exact(const void *W, const void *X_bf16, float *Y, int64_t N, int64_t K,
+                                  int64_t T, void *stream);
 
 /*
  * Extended launch control (tests and benchmarks).  Zero-initialised options

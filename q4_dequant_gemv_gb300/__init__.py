@@ -44,7 +44,8 @@ class GemvGroup(ctypes.Structure):
 
 # Every symbol the header declares (checked by the CPU tests).
 EXPORTS = ("q4k_status_string", "q4k_abi_version", "q4k_gemv", "q4k_gemv_argmax", "q4k_gemv_argmax_debug",
-           "q4k_gemv_argmax_noalloc", "q4k_gemm_prefill", "q4k_gemv_ex", "q4k_gemv_grouped", "q4k_gemv_plan",
+           "q4k_gemv_argmax_noalloc", "q4k_gemm_prefill", "q4k_gemm_prefill_exact", "q4k_gemv_ex",
+           "q4k_gemv_grouped", "q4k_gemv_plan",
            "q4k_device_error_flags", "q4k_device_error_clear", "q4k_stream_read", "q6k_gemv")
 
 
@@ -74,6 +75,8 @@ def lib():
         L.q4k_gemv_argmax_noalloc.argtypes = [P, P, P, I64, I64, I, P]
         L.q4k_gemv_argmax_noalloc.restype = I
         L.q4k_gemm_prefill.argtypes = [P, P, P, I64, I64, I64, P]
+        L.q4k_gemm_prefill_exact.argtypes = [P, P, P, I64, I64, I64, P]
+        L.q4k_gemm_prefill_exact.restype = I
         L.q6k_gemv.argtypes = [P, P, P, I64, I64, I, P]
         L.q6k_gemv.restype = I
         L.q4k_gemm_prefill.restype = I
@@ -227,8 +230,8 @@ def gemv_argmax(W, x, idx=None, *, logits=None, stream=None):
     return idx
 
 
-def gemm_prefill(W, X, Y=None, *, stream=None):
-    """Y [T, N] (fp32) = X [T, K] (bf16) . W_q4k^T."""
+def gemm_prefill(W, X, Y=None, *, stream=None, exact=False):
+    """Y [T, N] (fp32) = X [T, K] (bf16) . W_q4k^T; exact=True: q4k_gemm_prefill_exact (no weight rounding)."""
     import torch
     _dev(W, "W", torch.uint8)
     _dev(X, "X", torch.bfloat16)
@@ -237,8 +240,9 @@ def gemm_prefill(W, X, Y=None, *, stream=None):
     if Y is None:
         Y = torch.empty((T, N), dtype=torch.float32, device=X.device)
     _dev(Y, "Y", torch.float32)
-    st = lib().q4k_gemm_prefill(W.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, _stream_ptr(stream))
-    _check("q4k_gemm_prefill", st)
+    fn = "q4k_gemm_prefill_exact" if exact else "q4k_gemm_prefill"
+    st = getattr(lib(), fn)(W.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, _stream_ptr(stream))
+    _check(fn, st)
     return Y
 
 

@@ -64,7 +64,13 @@ q4k_status q4k_gemv_argmax_noalloc(const void *W, const float *x, int32_t *idx, 
 q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t N, int64_t K, int64_t T,
                             void *stream)
 {
-    return q4k::prefill_impl(W, X_bf16, Y, N, K, T, stream);
+    return q4k::prefill_impl(W, X_bf16, Y, N, K, T, stream, false);
+}
+
+q4k_status q4k_gemm_prefill_exact(const void *W, const void *X_bf16, float *Y, int64_t N, int64_t K, int64_t T,
+                                  void *stream)
+{
+    return q4k::prefill_impl(W, X_bf16, Y, N, K, T, stream, true);
 }
 
 q4k_status q4k_stream_read(const void *buf, int64_t bytes, int64_t *bytes_read, void *stream)

@@ -22,7 +22,8 @@ q4k_status gemv_grouped_impl(const q4k_gemv_group *groups, int ngroups, const fl
 q4k_status gemv_argmax_noalloc_impl(const void *W, const float *x, int32_t *idx, int64_t N, int64_t K, int batch,
                                     void *stream);
 q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream);
-q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream);
+q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream,
+                        bool exact);
 unsigned int read_device_error();
 unsigned int read_prefill_error();
 unsigned int read_q6k_error();

@@ -1194,8 +1194,6 @@ __global__ void __launch_bounds__(kThreads, (PS == 1 && TN <= 32) ? 2 : 1)
 }  // namespace pf
 
 // ------------------------------------------------------------------ host
-// Token counts up to this go to the exact kernel.
-constexpr int kExactMaxT = 64;
 // Parts of a super-block per stage of the exact kernel at 32-token tiles (5:
 // the whole super-block in one stage, one barrier hand-off per super-block).
 constexpr int kExactParts32 = 5;
@@ -1335,7 +1333,8 @@ static cudaError_t launch_prefill_exact(const uint8_t *W, const void *Xh, const 
 }
 
 // Clusters of csize CTAs (2, 4 or 8) of kernel `kid` (0: exact 32-token,
-// 1: exact 64-token, 2: fp16 128-token, 3: fp16 256-token tiles) that the GPU
+// 1: exact 64-token, 2: fp16 128-token, 3: fp16 256-token, 4: fp16 64-token
+// tiles) that the GPU
 // holds at once, queried once per device; -1 when the query fails (the caller
 // then does not limit the split on it).
 static int max_active_clusters(int kid, int csize)
@@ -1347,8 +1346,8 @@ static int max_active_clusters(int kid, int csize)
     }
     const int ci = (csize == 2) ? 0 : (csize == 4) ? 1 : 2;
     static std::mutex mu;
-    static int cache[64][4][3];
-    static bool have[64][4][3];
+    static int cache[64][5][3];
+    static bool have[64][5][3];
     std::lock_guard<std::mutex> lock(mu);
     if (have[dev][kid][ci]) return cache[dev][kid][ci];
     const void *kern = nullptr;
@@ -1359,6 +1358,8 @@ static int max_active_clusters(int kid, int csize)
             smem = pf::ECfg<32, kExactParts32>::kSmem; break;
     case 1: kern = reinterpret_cast<const void *>(pf::q4k_prefill_exact_kernel<64, 1>); smem = pf::ECfg<64, 1>::kSmem; break;
     case 2: kern = reinterpret_cast<const void *>(pf::q4k_prefill_kernel<128, 1>); smem = pf::Cfg<128, 1>::kSmem;
+            threads = pf::kThreadsF16; break;
+    case 4: kern = reinterpret_cast<const void *>(pf::q4k_prefill_kernel<64, 1>); smem = pf::Cfg<64, 1>::kSmem;
             threads = pf::kThreadsF16; break;
     default: kern = reinterpret_cast<const void *>(pf::q4k_prefill_kernel<256, 1>); smem = pf::Cfg<256, 1>::kSmem;
              threads = pf::kThreadsF16; break;
@@ -1385,7 +1386,13 @@ static int max_active_clusters(int kid, int csize)
     return n;
 }
 
-q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream)
+// Up to this many tokens the plain entry point takes the exact kernel too:
+// with the weights streamed from HBM it is as fast there or a little faster
+// (14336 x 4096 at 32 tokens: 35.3 against 36.2 us), and no weight is rounded.
+constexpr int kExactDefaultMaxT = 32;
+
+q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream,
+                        bool exact_requested)
 {
     q4k_status st = validate_prefill(W, X, Y, N, K, T);
     if (st != Q4K_OK) return st;
@@ -1410,12 +1417,16 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     // tiles)
     else if (static_cast<long long>(mtiles) * ((t + 511) / 512) * 10 >= static_cast<long long>(sms) * 7) { tn = 256; ntt = 2; }
     else { tn = 256; ntt = 1; }
-    // Up to kExactMaxT tokens: the exact kernel (integer weight tiles), in
-    // 32- or 64-token tiles.
-    const bool exact = t <= kExactMaxT;
+    // The exact kernel (integer weight tiles, no weight rounding) on request or
+    // up to kExactDefaultMaxT tokens, in 32- or 64-token tiles; the fp16
+    // kernel otherwise, whose 64-token tiles beat the exact kernel from 33 to
+    // 64 tokens (14336 x 4096 at 64 tokens: 36.7 against 44.2 us).
+    const bool exact = exact_requested || t <= kExactDefaultMaxT;
     if (exact) {
         tn = (t <= 32) ? 32 : 64;
         ntt = 1;
+    } else if (tn < 64) {
+        tn = 64;   // the fp16 kernel's smallest token tile
     }
     const long long ctas = static_cast<long long>(mtiles) * ((t + tn * ntt - 1) / (tn * ntt));
     // K split over a cluster until the GPU is covered (at most 8, at least
@@ -1427,7 +1438,7 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     // (clusters of eight CTAs that take a whole SM each stop fitting well
     // before 152 CTAs: at 1024 x 4096 and 512 tokens, sixteen of them ran
     // in two waves, 30 us, against 19 us for sixteen clusters of four)
-    const int kid = exact ? (tn == 32 ? 0 : 1) : (tn == 128 ? 2 : 3);
+    const int kid = exact ? (tn == 32 ? 0 : 1) : (tn == 64 ? 4 : tn == 128 ? 2 : 3);
     int split = 1;
     while (ntt == 1 && split < 8 && ctas * split * 2 <= slots && (k / 256) / (split * 2) >= 2) {
         const int fit = max_active_clusters(kid, split * 2);
@@ -1454,6 +1465,7 @@ q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64
     if (e == cudaSuccess) {
         if (exact && tn == 32) e = launch_prefill_exact<32, kExactParts32>(Wb, Xh, XS, xexp, Y, n, k, t, split, s);
         else if (exact) e = launch_prefill_exact<64, 1>(Wb, Xh, XS, xexp, Y, n, k, t, split, s);
+        else if (tn == 64) e = launch_prefill<64, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else if (tn == 128) e = launch_prefill<128, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else if (ntt == 1) e = launch_prefill<256, 1>(Wb, Xh, xexp, Y, n, k, t, split, s);
         else e = launch_prefill<256, 2>(Wb, Xh, xexp, Y, n, k, t, split, s);

@@ -70,13 +70,14 @@ def test_host_validation(q4k):
     assert am(ok, ok, ok, 8, 256, 17) == 1
     dbg = q4k.raw_call("q4k_gemv_argmax_debug", P(ok), P(ok), P(ok), P(0), 8, 256, 1, P(0))
     assert dbg == 1
-    pf = lambda W, X, Y, N, K, T: q4k.raw_call("q4k_gemm_prefill", P(W), P(X), P(Y), N, K, T, P(0))
-    assert pf(0, ok, ok, 64, 256, 32) == 1
-    assert pf(0, 0, 0, 0, 256, 32) in (0, 3, 4)      # N == 0: no pointer is needed
     assert _gemv(q4k, 0, ok, 0, 0, 256, 1) in (0, 3, 4)
-    assert pf(ok, ok, ok, 64, 100, 32) == 1
-    assert pf(ok, ok, ok, 64, 256, -1) == 1
-    assert pf(ok, ok + 2, ok, 64, 256, 32) == 2
+    for fn in ("q4k_gemm_prefill", "q4k_gemm_prefill_exact"):
+        pf = lambda W, X, Y, N, K, T: q4k.raw_call(fn, P(W), P(X), P(Y), N, K, T, P(0))
+        assert pf(0, ok, ok, 64, 256, 32) == 1
+        assert pf(0, 0, 0, 0, 256, 32) in (0, 3, 4)      # N == 0: no pointer is needed
+        assert pf(ok, ok, ok, 64, 100, 32) == 1
+        assert pf(ok, ok, ok, 64, 256, -1) == 1
+        assert pf(ok, ok + 2, ok, 64, 256, 32) == 2
 
 
 def test_no_device_reports_status(q4k):

@@ -27,18 +27,18 @@ def env():
     return q4k, oracle
 
 
-def _run(q4k, W, X_bits):
+def _run(q4k, W, X_bits, exact=False):
     Wd = torch.from_numpy(np.ascontiguousarray(W)).cuda()
     Xd = torch.from_numpy(np.ascontiguousarray(X_bits).view(np.int16)).cuda().view(torch.bfloat16)
-    Y = q4k.gemm_prefill(Wd, Xd)
+    Y = q4k.gemm_prefill(Wd, Xd, exact=exact)
     torch.cuda.synchronize()
     return Y.cpu().numpy()
 
 
-def _check(q4k, oracle, N, K, T, seed, what):
+def _check(q4k, oracle, N, K, T, seed, what, exact=False):
     W = synth.q4k_weights(N, K, (seed, 1))
     X = synth.normal_bf16_bits((T, K), (seed, 2))
-    Y = _run(q4k, W, X)
+    Y = _run(q4k, W, X, exact)
     Xf = synth.bf16_bits_to_f32(X)
     ref = oracle.prefill(W, X, N, K)
     assert_close(Y, ref, Xf, K, what)
@@ -83,20 +83,30 @@ def test_llama_shapes_full_t512(env, name, N, K):
     _check(q4k, oracle, N, K, 512, N + K, f"{name} T=512 (all rows)")
 
 
-@pytest.mark.parametrize("N,K,T", [(256, 1024, 1), (300, 4096, 32), (128, 14336, 64), (1000, 2048, 40)])
+@pytest.mark.parametrize("N,K,T", [(256, 1024, 1), (300, 4096, 32), (128, 14336, 64), (1000, 2048, 40),
+                                   (256, 1024, 100)])
 def test_exact_path_precision(env, N, K, T):
-    """Up to 64 tokens the product uses integer weight tiles (q * sc, exact
-    in fp16) with the scales applied in fp32 per super-block: no weight is
+    """q4k_gemm_prefill_exact uses integer weight tiles (q * sc, exact in
+    fp16) with the scales applied in fp32 per super-block: no weight is
     rounded, so the error stays near fp32 accumulation error, far below one
     fp16 rounding of w."""
     q4k, oracle = env
     W = synth.q4k_weights(N, K, (N, K, T, 3))
     X = synth.normal_bf16_bits((T, K), (N, K, T, 4))
-    Y = _run(q4k, W, X)
+    Y = _run(q4k, W, X, exact=True)
     Xf = synth.bf16_bits_to_f32(X).astype(np.float64)
     ref = oracle.prefill(W, X, N, K)
     bound = 2.0 ** -14 * (np.abs(Xf) @ np.abs(oracle.dequant_matrix(W, N, K)).T) + 1e-6
     assert np.all(np.abs(Y - ref) <= bound), f"N={N} K={K} T={T}: error beyond fp32 accumulation"
+
+
+@pytest.mark.parametrize("N,K,T", [(128, 256, 32), (200, 768, 33), (130, 512, 1), (64, 256, 7), (384, 1024, 64),
+                                   (1000, 2048, 40), (384, 2048, 130)])
+def test_prefill_exact_shapes(env, N, K, T):
+    """q4k_gemm_prefill_exact against the oracle: ragged rows and tokens, one
+    and several token tiles, K splits."""
+    q4k, oracle = env
+    _check(q4k, oracle, N, K, T, N * 5 + K + T, f"exact N={N} K={K} T={T}", exact=True)
 
 
 def test_prefill_matches_gemv_within_tolerance(env):
@@ -112,8 +122,8 @@ def test_prefill_matches_gemv_within_tolerance(env):
     assert_close(Y[:16], yg.astype(np.float64), Xf[:16], K, "prefill vs gemv")
 
 
-@pytest.mark.parametrize("T", [40, 200])
-def test_prefill_extreme_scales(env, T):
+@pytest.mark.parametrize("T,exact", [(40, False), (200, False), (40, True)])
+def test_prefill_extreme_scales(env, T, exact):
     """Weights and activations far outside fp16's range (|w| up to ~6e7 and
     ~1e-3, |x| up to ~4e12 and down to ~3e-24): the power-of-two scales per row and
     per token keep every output finite and within one fp16 rounding of w of
@@ -137,7 +147,7 @@ def test_prefill_extreme_scales(env, T):
     Xf[10:20] *= np.float32(2.0 ** -40)
     Xf[20:30] *= np.float32(2.0 ** -80)
     X = (Xf.view(np.uint32) >> 16).astype(np.uint16)
-    Y = _run(q4k, W, X)
+    Y = _run(q4k, W, X, exact)
     ref = oracle.prefill(W, X, N, K)
     assert np.all(np.isfinite(Y))
     Xf = synth.bf16_bits_to_f32(X).astype(np.float64)
