@@ -155,14 +155,21 @@ def test_prefill_extreme_scales(env, T, exact):
     assert np.all(np.abs(Y - ref) <= bound), "extreme scales: beyond one fp16 rounding of w"
 
 
-def test_prefill_guards_and_errors(env):
+@pytest.mark.parametrize("T,exact", [(40, False), (20, False), (40, True)])
+def test_prefill_guards_and_errors(env, T, exact):
+    """Nothing outside Y [T][N] is written (ragged rows and tokens), and T = 0 is a no-op."""
     q4k, _ = env
-    N, K, T = 130, 512, 40
+    N, K = 130, 512
     W = torch.from_numpy(synth.q4k_weights(N, K, 63)).cuda()
     X = torch.from_numpy(synth.normal_bf16_bits((T, K), 64).view(np.int16)).cuda().view(torch.bfloat16)
     buf = torch.full((T * N + 4096,), -777.0, device="cuda")
     Y = buf[2048:2048 + T * N].view(T, N)
-    q4k.gemm_prefill(W, X, Y)
+    q4k.gemm_prefill(W, X, Y, exact=exact)
     torch.cuda.synchronize()
     assert torch.all(buf[:2048] == -777.0) and torch.all(buf[2048 + T * N:] == -777.0)
+    assert torch.all(Y != -777.0)
+    X0 = X[:0]
+    Y0 = torch.empty((0, N), device="cuda")
+    q4k.gemm_prefill(W, X0, Y0, exact=exact)
+    torch.cuda.synchronize()
     assert q4k.device_error_flags() == 0
