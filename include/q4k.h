@@ -194,18 +194,21 @@ q4k_status q6k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t 
  *   X  bf16 [T][K] row-major (16-byte aligned)
  *   Y  fp32 [T][N] row-major
  * Up to 32 tokens this is q4k_gemm_prefill_exact (below: no weight is
- * rounded).  Above that each weight is dequantized in fp32, multiplied by a
- * power of two chosen per row from the row's largest possible |w|, and rounded
- * once to fp16 (nearest even) in shared memory; each token's activations are converted to fp16
+ * rounded).  Above that each weight is dequantized in fp32 (one fma),
+ * multiplied by a power of two chosen per row from the row's largest possible
+ * |w|, and rounded to fp16 (nearest even) in shared memory; each token's
+ * activations are converted to fp16
  * under a power of two chosen per token from its largest |x| (exact for every
  * value of at least 2^-31 times that largest).  The tcgen05 tensor cores
  * multiply them with fp32 accumulation in tensor memory and the epilogue
  * removes both scales.  Result: |Y - exact| <= ~2^-11 sum_k |w||x| for any
  * finite inputs, no overflow from large d, dmin or x.
- * Scratch: the converted X (2*T*K bytes) and T scale exponents come from
- * cudaMallocAsync on `stream` and are freed on it after the product.
+ * Scratch: the converted X (2*T*K bytes), T scale exponents and, up to 32
+ * tokens, T*K/2 bytes of sub-block sums come from cudaMallocAsync on `stream`
+ * and are freed on it after the product.
  * Any T >= 0 is accepted (T == 0 or N == 0 is a no-op, and the pointers may
- * then be NULL); tokens go in tiles of 64 (T <= 64), 128, 256 or 512.
+ * then be NULL); tokens go in tiles of 32 (T <= 32), 64 (T <= 64), 128, 256
+ * or 512.
  * Errors: INVALID_ARG, MISALIGNED (W or X), UNSUPPORTED_DEVICE, CUDA
  * (including a failed scratch allocation).
  */
@@ -222,7 +225,7 @@ q4k_status q4k_gemm_prefill(const void *W, const void *X_bf16, float *Y, int64_t
  * hi + lo), and y += d D - dmin M in fp32.  The only roundings are the fp32
  * accumulations and the hi + lo split of S_j.  Tiles of 32 (T <= 32) or 64
  * tokens; any T >= 0.  q4k_gemm_prefill takes this path up to 32 tokens;
- * from 33 tokens on the fp16 path is faster (14336 x 4096 at 64 tokens: 36.7
+ * from 33 tokens on the fp16 path is faster (14336 x 4096 at 64 tokens: 35.2
  * against 44.2 us), so this entry point is for callers that want the weights
  * exact there too.
  */
