@@ -72,10 +72,18 @@ constexpr int kChunk = 64;           // K elements per stage (one 128-byte swizz
 constexpr int kThreads = 192;        // 4 dequant/epilogue warps + TMA warp + MMA warp
 // fp16 kernel: 8 dequant/epilogue warps (two threads per weight row, one per
 // nibble half), an X-tile TMA warp, a weight TMA warp and two MMA warps
-constexpr int kProdF16 = 256;
-constexpr int kThreadsF16 = kProdF16 + 128;
-constexpr int kTmaWarpF16 = kProdF16 / 32;      // X tiles; the next warp: raw weights
-constexpr int kMmaWarpF16 = kTmaWarpF16 + 2;    // and the one after it
+// Thread layout of the fp16 kernel for token tiles of TN: P dequant threads
+// per weight row (P = 4 for the small tiles, where the dequant bounds the
+// kernel: each thread one nibble half of half of every chunk), then the X
+// warp, the weight warp and the two MMA warps.
+template <int TN>
+struct FLay {
+    static constexpr int P = (TN <= 64) ? 4 : 2;
+    static constexpr int kProd = 128 * P;
+    static constexpr int kThreads = kProd + 128;
+    static constexpr int kTmaWarp = kProd / 32;      // X tiles; the next warp: raw weights
+    static constexpr int kMmaWarp = kTmaWarp + 2;    // and the one after it
+};
 constexpr int kATileBytes = kRowsM * kChunk * 2;    // 16 KB: one fp16 weight tile
 constexpr int kAStageBytes = kATileBytes;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -438,12 +446,19 @@ __device__ __forceinline__ void reduce_split(uint32_t part_addr, int split, int 
 }
 
 template <int TN, int NTT>
-__global__ void __launch_bounds__(kThreadsF16, 1)
+__global__ void __launch_bounds__(FLay<TN>::kThreads, 1)
     q4k_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                        const uint8_t *__restrict__ W, const int *__restrict__ xexp, float *__restrict__ Y, int N,
                        int K, int T)
 {
     using C = Cfg<TN, NTT>;
+    using L = FLay<TN>;
+    constexpr int P = L::P;
+    constexpr int kProdF16 = L::kProd;
+    constexpr int kThreadsF16 = L::kThreads;
+    constexpr int kTmaWarpF16 = L::kTmaWarp;
+    constexpr int kMmaWarpF16 = L::kMmaWarp;
+    static_assert(P == 2 || NTT == 1, "four dequant threads per row only with one token tile");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw;   // 1024-byte aligned: the 128B-swizzle atoms need it
     // full_a/empty: the stage's weight tile; full_x/empty_x: each token
@@ -542,7 +557,12 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
     if (warp < kTmaWarpF16) {
         // ------------------------------------------------ dequant producers
         const int r = tid & (kRowsM - 1);     // tile row 0..127
-        const int hsel = tid >> 7;            // 0: low nibbles (k 0..31 of a chunk), 1: high nibbles (k 32..63)
+        const int hsel = (tid >> 7) & 1;      // 0: low nibbles (k 0..31 of a chunk), 1: high nibbles (k 32..63)
+        // P = 4: which half of the chunk's four 16-byte output chunks (and of
+        // its 32 quant bytes) this thread takes
+        const int quarter = (P == 4) ? (tid >> 8) : 0;
+        constexpr int NQ = (P == 4) ? 5 : 9;  // 16-byte words of a super-block a thread reads
+        constexpr int NC8 = 8 / P;            // 16-byte output chunks per chunk and thread
         const int n = row0 + r;
         const bool live = n < N;
         const uint8_t *wrow = W + static_cast<size_t>(live ? n : 0) * row_bytes;
@@ -550,7 +570,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
         uint32_t phase = 0;
         // Row scale 2^rs: the largest |w| this CTA's super-blocks of the row
         // can hold, |d|*945 + |dmin|*63, brought to [2^14, 2^15).
-        if (hsel == 0) {
+        if (tid < kRowsM) {   // one thread per row
             float wmax = 0.f;
 #pragma unroll
             for (int i = 0; i < 16; ++i)
@@ -577,7 +597,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
         // dmin = 0 makes every weight of them zero); super-blocks past the
         // CTA's range read as zeros.
         const uint8_t *wring = smem + C::kWOffset;
-        auto load_sb = [&](int i, uint4 (&q)[9]) {
+        auto load_sb = [&](int i, uint4 (&q)[NQ]) {
             if (i < nloc) {
                 const int slot = i % kWSlots;
                 if (!*(volatile int *)&s_abort &&
@@ -586,18 +606,24 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
                     s_abort = 1;
                 }
                 const uint4 *bp = reinterpret_cast<const uint4 *>(wring + slot * kWSlotBytes + r * 144);
+                if constexpr (P == 4) {   // the header and this thread's half of each part's quant bytes
+                    q[0] = bp[0];
 #pragma unroll
-                for (int u = 0; u < 9; ++u) q[u] = bp[u];
+                    for (int p = 0; p < 4; ++p) q[1 + p] = bp[1 + 2 * p + quarter];
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 9; ++u) q[u] = bp[u];
+                }
                 mbar_arrive(smem_u32(&wempty[slot]));   // (release: orders the reads before the refill)
             } else {
 #pragma unroll
-                for (int u = 0; u < 9; ++u) q[u] = make_uint4(0, 0, 0, 0);
+                for (int u = 0; u < NQ; ++u) q[u] = make_uint4(0, 0, 0, 0);
             }
         };
         // One super-block = four K chunks; chunk p holds sub-blocks 2p (low
         // nibbles of quant bytes 32p..32p+31) and 2p+1 (their high nibbles):
         // this thread's sub-block is 2p + hsel.
-        auto dequant_sb = [&](const uint4 (&q)[9]) {
+        auto dequant_sb = [&](const uint4 (&q)[NQ]) {
             const float d = half_lo_f32(q[0].x) * rscale, dmin = half_hi_f32(q[0].x) * rscale;
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
@@ -611,8 +637,15 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
                     atomicOr(&g_prefill_error, 2u);
                     s_abort = 1;
                 }
-                const uint32_t words[8] = {q[1 + 2 * p].x, q[1 + 2 * p].y, q[1 + 2 * p].z, q[1 + 2 * p].w,
-                                           q[2 + 2 * p].x, q[2 + 2 * p].y, q[2 + 2 * p].z, q[2 + 2 * p].w};
+                uint32_t words[2 * NC8];
+                if constexpr (P == 4) {
+                    words[0] = q[1 + p].x; words[1] = q[1 + p].y; words[2] = q[1 + p].z; words[3] = q[1 + p].w;
+                } else {
+                    const uint32_t w8[8] = {q[1 + 2 * p].x, q[1 + 2 * p].y, q[1 + 2 * p].z, q[1 + 2 * p].w,
+                                            q[2 + 2 * p].x, q[2 + 2 * p].y, q[2 + 2 * p].z, q[2 + 2 * p].w};
+#pragma unroll
+                    for (int u = 0; u < 2 * NC8; ++u) words[u] = w8[u];
+                }
                 uint8_t *arow = smem + stage * C::kStageBytes + r * 128;
                 // Each nibble goes straight under the fp32 exponent of 2^23 (one
                 // LOP3 on the word shifted by 0, 8, 16 or 24 bits: 2^23 + q 2^s,
@@ -627,7 +660,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
                 const uint64_t ds2 = f2_pack(ds, ds);
                 const uint64_t ndm2 = f2_pack(-dm, -dm);
 #pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {                 // 16-byte chunk: k = 32*hsel + 8*c8 .. +7
+                for (int c8 = 0; c8 < NC8; ++c8) {               // 16-byte chunk: k = 32*hsel + 8*(c8 + c8 base) .. +7
                     uint32_t out[4];
 #pragma unroll
                     for (int uu = 0; uu < 2; ++uu) {             // word u = 2*c8 + uu -> k offset 4u..4u+3
@@ -638,7 +671,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
                         out[2 * uu] = f2_to_half2(f2_fma(f2_add(A, nmag2), ds2, ndm2));
                         out[2 * uu + 1] = f2_to_half2(f2_fma(f2_add(B, nmag2), ds2, ndm2));
                     }
-                    const int chunk = 4 * hsel + c8;
+                    const int chunk = 4 * hsel + 2 * quarter + c8;
                     *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) =
                         make_uint4(out[0], out[1], out[2], out[3]);
                 }
@@ -648,7 +681,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
             }
         };
         // Two register sets alternate so that no loaded word is ever moved.
-        uint4 qa[9], qb[9];
+        uint4 qa[NQ], qb[NQ];
         load_sb(0, qa);
         for (int i = 0; i < nloc; i += 2) {
             load_sb(i + 1, qb);
@@ -799,19 +832,21 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
         // left the 512-token epilogue at ~14 us): 64 columns of a tile per
         // round, or with NTT == 1 32 columns of each MMA warp's accumulator,
         // added (D0 + D1).
-        constexpr int kRound = (NTT == 1) ? 32 : 64;
+        constexpr int kGroupCols = TN / P;   // NTT == 1: columns per thread group
+        constexpr int kRound = (NTT == 1) ? (kGroupCols < 32 ? kGroupCols : 32) : 64;
         const int g = tid >> 7;
         const int j_lo = (NTT == 2) ? g : 0, j_hi = (NTT == 2) ? min(g + 1, nsub) : nsub;
-        const int c_lo = (NTT == 1) ? g * (TN / 2) : 0, c_hi = (NTT == 1) ? c_lo + TN / 2 : TN;
+        const int c_lo = (NTT == 1) ? g * kGroupCols : 0, c_hi = (NTT == 1) ? c_lo + kGroupCols : TN;
         for (int j = j_lo; j < j_hi; ++j) {
 #pragma unroll 1
             for (int c64 = c_lo; c64 < c_hi; c64 += kRound) {
                 uint32_t v[4][16];
                 if (NTT == 1) {
-                    tmem_ld16(lane_addr + c64, v[0]);
-                    tmem_ld16(lane_addr + c64 + 16, v[1]);
-                    tmem_ld16(lane_addr + TN + c64, v[2]);
-                    tmem_ld16(lane_addr + TN + c64 + 16, v[3]);
+#pragma unroll
+                    for (int q = 0; q < kRound / 16; ++q) {
+                        tmem_ld16(lane_addr + c64 + 16 * q, v[q]);
+                        tmem_ld16(lane_addr + TN + c64 + 16 * q, v[q + 2]);
+                    }
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) tmem_ld16(lane_addr + j * TN + c64 + 16 * q, v[q]);
@@ -819,7 +854,7 @@ __global__ void __launch_bounds__(kThreadsF16, 1)
                 tmem_wait_ld();
                 if (NTT == 1) {
 #pragma unroll
-                    for (int q = 0; q < 2; ++q)
+                    for (int q = 0; q < kRound / 16; ++q)
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             v[q][i] = __float_as_uint(__uint_as_float(v[q][i]) + __uint_as_float(v[q + 2][i]));
@@ -1293,7 +1328,7 @@ static cudaError_t launch_prefill(const uint8_t *W, const void *Xh, const int *x
     if (attr_err[dev] != cudaSuccess) return attr_err[dev];
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((N + pf::kRowsM - 1) / pf::kRowsM, (T + TN * NTT - 1) / (TN * NTT), split);
-    cfg.blockDim = dim3(pf::kThreadsF16, 1, 1);
+    cfg.blockDim = dim3(pf::FLay<TN>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1398,11 +1433,11 @@ static int max_active_clusters(int kid, int csize)
             smem = pf::ECfg<32, kExactParts32>::kSmem; break;
     case 1: kern = reinterpret_cast<const void *>(pf::q4k_prefill_exact_kernel<64, 1>); smem = pf::ECfg<64, 1>::kSmem; break;
     case 2: kern = reinterpret_cast<const void *>(pf::q4k_prefill_kernel<128, 1>); smem = pf::Cfg<128, 1>::kSmem;
-            threads = pf::kThreadsF16; break;
+            threads = pf::FLay<128>::kThreads; break;
     case 4: kern = reinterpret_cast<const void *>(pf::q4k_prefill_kernel<64, 1>); smem = pf::Cfg<64, 1>::kSmem;
-            threads = pf::kThreadsF16; break;
+            threads = pf::FLay<64>::kThreads; break;
     default: kern = reinterpret_cast<const void *>(pf::q4k_prefill_kernel<256, 1>); smem = pf::Cfg<256, 1>::kSmem;
-             threads = pf::kThreadsF16; break;
+             threads = pf::FLay<256>::kThreads; break;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, csize);
