@@ -263,6 +263,14 @@ q4k_status q4k_gemm_prefill_exact(const void *W, const void *X_bf16, float *Y, i
  *            after any timed-out wait: sets bit 0 of q4k_device_error_flags(),
  *            stops waiting, writes no outputs, waits (bounded) for its own
  *            copies in flight and returns; the context stays usable.
+ *            Q4K_FLAG_ROWS16: batch 1 on the 16-row-tile kernel (a CTA owns 16
+ *            rows over the whole K; its warps split K and add their partial
+ *            rows in shared memory, in warp order).  Without the flag the
+ *            library takes it by itself for batch 1 when 128-row tiles would
+ *            need a K split over CTAs and K <= 8192 (the q/k/v and o
+ *            projections of a 7B-class layer); a forced split_k keeps the
+ *            128-row kernel.  INVALID_ARG with batch > 1, with
+ *            Q4K_FLAG_TENSOR_CORE or with K > 8192.
  *   wait_limit_us  bound of each wait inside the kernel in microseconds;
  *            0 = the default of 2 s.
  */
@@ -270,6 +278,7 @@ q4k_status q4k_gemm_prefill_exact(const void *W, const void *X_bf16, float *Y, i
 #define Q4K_FLAG_TENSOR_CORE 2u
 #define Q4K_FLAG_Q8K_X 4u
 #define Q4K_FLAG_TEST_STALL 8u
+#define Q4K_FLAG_ROWS16 16u
 typedef struct {
     int split_k;
     unsigned flags;

@@ -19,6 +19,7 @@ Q4K_FLAG_PDL = 1
 Q4K_FLAG_TENSOR_CORE = 2
 Q4K_FLAG_Q8K_X = 4
 Q4K_FLAG_TEST_STALL = 8
+Q4K_FLAG_ROWS16 = 16
 QK = 256
 QBYTES = 144
 MAX_BATCH = 16
@@ -126,16 +127,17 @@ def _shape_wk(W, K):
     return N
 
 
-def _flags(pdl: bool, tensor_core: bool, q8k: bool = False) -> int:
+def _flags(pdl: bool, tensor_core: bool, q8k: bool = False, rows16: bool = False) -> int:
     return ((Q4K_FLAG_PDL if pdl else 0) | (Q4K_FLAG_TENSOR_CORE if tensor_core else 0)
-            | (Q4K_FLAG_Q8K_X if q8k else 0))
+            | (Q4K_FLAG_Q8K_X if q8k else 0) | (Q4K_FLAG_ROWS16 if rows16 else 0))
 
 
 def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False, tensor_core: bool = False,
-         q8k: bool = False, wait_limit_us: int = 0, test_stall: bool = False):
+         q8k: bool = False, wait_limit_us: int = 0, test_stall: bool = False, rows16: bool = False):
     """y [B, N] (fp32) = W_q4k [N, K] . x [B, K] (fp32); x may also be [K].
     tensor_core: batch 1 on the tensor-core inner product instead of the integer one.
     q8k: batch 1 with x quantized Q8_K style (int8 codes per 256-block), its own error bound.
+    rows16: batch 1 on the 16-row-tile kernel (chosen automatically where it applies).
     wait_limit_us, test_stall: bound of the kernel's waits, and a wait made to run out (failure tests)."""
     import torch
     _dev(W, "W", torch.uint8)
@@ -150,8 +152,8 @@ def gemv(W, x, y=None, *, stream=None, split_k: int = 0, pdl: bool = False, tens
     if y.numel() != B * N:
         raise ValueError("y has the wrong size")
     L = lib()
-    if split_k or pdl or tensor_core or q8k or wait_limit_us or test_stall:
-        o = LaunchOpts(split_k, _flags(pdl, tensor_core, q8k) | (Q4K_FLAG_TEST_STALL if test_stall else 0),
+    if split_k or pdl or tensor_core or q8k or wait_limit_us or test_stall or rows16:
+        o = LaunchOpts(split_k, _flags(pdl, tensor_core, q8k, rows16) | (Q4K_FLAG_TEST_STALL if test_stall else 0),
                        int(wait_limit_us))
         st = L.q4k_gemv_ex(W.data_ptr(), x2.data_ptr(), y.data_ptr(), N, K, B, _stream_ptr(stream), ctypes.byref(o))
         _check("q4k_gemv_ex", st)
@@ -183,7 +185,7 @@ def q6k_gemv(W, x, y=None, *, stream=None):
 
 
 def gemv_grouped(Ws, x, ys=None, *, stream=None, split_k: int = 0, pdl: bool = False, tensor_core: bool = False,
-                 q8k: bool = False):
+                 q8k: bool = False, rows16: bool = False):
     """Several Q4_K matrices times the same x in one launch: returns [y_g [B, N_g]]."""
     import torch
     if not 1 <= len(Ws) <= 4:
@@ -201,7 +203,7 @@ def gemv_grouped(Ws, x, ys=None, *, stream=None, split_k: int = 0, pdl: bool = F
         if y.numel() != B * N:
             raise ValueError("y has the wrong size")
         arr[i] = GemvGroup(W.data_ptr(), y.data_ptr(), N)
-    o = LaunchOpts(split_k, _flags(pdl, tensor_core, q8k))
+    o = LaunchOpts(split_k, _flags(pdl, tensor_core, q8k, rows16))
     st = lib().q4k_gemv_grouped(arr, len(Ws), x2.data_ptr(), K, B, _stream_ptr(stream), ctypes.byref(o))
     _check("q4k_gemv_grouped", st)
     return ys

@@ -38,6 +38,9 @@
 //     (deterministic, no atomics, no global scratch).  With a single K slice
 //     the grid is persistent and CTAs loop over row tiles, so the weight
 //     stream never drains between tiles.
+//   * Batch 1 with too few 128-row tiles and K <= 8192 (q/k/v, o): 16-row
+//     tiles instead, one CTA per tile over the whole K, the K split between
+//     its warps and their partial rows added in shared memory (no cluster).
 //   * The argmax variant keeps per-CTA (max, lowest index) keys in shared
 //     memory and combines CTAs with one 64-bit atomicMax per batch row plus a
 //     last-CTA ticket (no spin-waits).
@@ -213,15 +216,15 @@ struct TileInfo {
     float *y;
 };
 
-template <typename Desc>
+template <int R = kRows, typename Desc>
 __device__ __forceinline__ TileInfo tile_info(const Desc &a, int tile)
 {
-    TileInfo ti{0, tile * kRows, a.N[0], a.y[0]};
+    TileInfo ti{0, tile * R, a.N[0], a.y[0]};
 #pragma unroll
     for (int i = 1; i < kMaxGroups; ++i) {
         if (i < a.ngroups && tile >= a.tile_start[i]) {
             ti.grp = i;
-            ti.row0 = (tile - a.tile_start[i]) * kRows;
+            ti.row0 = (tile - a.tile_start[i]) * R;
             ti.N = a.N[i];
             ti.y = a.y[i];
         }
@@ -539,6 +542,202 @@ __global__ void __launch_bounds__(kThreads, 1) q4k_gemv_kernel_wide(const __grid
     gemv_body<NT, ARGMAX, 0>(maps, args);
 }
 
+// ---------------------------------------------------------------------------
+// Batch 1, 16-row tiles (q4k_gemv_rows16_kernel).  For matrices with too few
+// 128-row tiles to fill the GPU (the q/k/v and o projections of a decoder
+// layer), the 128-row kernel splits K over the CTAs of a cluster, and its
+// epilogue (distributed shared-memory stores, a cluster barrier that waits
+// for the slowest CTA, the rank-ordered sum) is most of such a launch.  Here
+// a CTA of 8 warps owns 16 rows over the whole K instead: the K split is
+// between its warps, and their partial rows meet in shared memory.
+//   * Stage = the tile's 16 rows x kT16Sb super-blocks (one 2-D TMA box; the
+//     row stride kT16Sb*144 bytes, kT16Sb odd, keeps the fragment loads free
+//     of bank conflicts).  Super-block j of the row goes to warp j % 8.
+//   * Warp w converts the x of its own super-blocks (w, w + 8, ...) into the
+//     integer parts of the 128-row kernel, once per CTA (all tiles of a CTA
+//     share x), into shared memory of its own: no barrier comes before the
+//     first inner product.
+//   * The ring and its refill are those of the 128-row kernel: every warp
+//     waits for every stage, and the last warp to leave a slot issues the
+//     stage kT16Stages ahead into it.
+// ---------------------------------------------------------------------------
+constexpr int kT16Rows = 16;
+constexpr int kT16Sb = 7;                                          // super-blocks per stage
+constexpr int kT16Stages = 4;                                      // ring depth
+constexpr int kT16StageBytes = kT16Rows * kT16Sb * kBlockBytes;    // 16,128
+constexpr int kT16XPerWarp = 4;                                    // x super-blocks per warp
+constexpr int kT16MaxNb = kWarps * kT16XPerWarp;                   // K <= 8192
+constexpr int kT16PreWait = 1;                                     // stages issued before the dependency wait
+__host__ __device__ constexpr size_t t16_smem_bytes()
+{
+    return static_cast<size_t>(kT16Stages) * kT16StageBytes + static_cast<size_t>(kWarps) * kT16XPerWarp * kI8Bytes;
+}
+
+template <int XM>
+__global__ void __launch_bounds__(kThreads, 2) q4k_gemv_rows16_kernel(const __grid_constant__ WMaps maps,
+                                                                     const GemvArgs args)
+{
+    constexpr bool Q8 = XM == 2;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    uint8_t *ring = smem_raw;
+    uint8_t *xarea = smem_raw + static_cast<size_t>(kT16Stages) * kT16StageBytes;
+    __shared__ __align__(8) uint64_t full[kT16Stages];
+    __shared__ int s_slot_done[kT16Stages];
+    __shared__ int s_abort;
+    __shared__ int s_issued;
+    __shared__ float2 s_sc[kT16MaxNb];         // per super-block: (unscale, pre) of its x
+    __shared__ float s_red[2][kWarps][kT16Rows];
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int nb = args.nb;
+    const int spt = (nb + kT16Sb - 1) / kT16Sb;   // stages per tile
+    const int my_tiles = (args.tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                         static_cast<int>(gridDim.x);
+    const int total = my_tiles * spt;
+    uint64_t policy = 0;
+
+    // stage i of this CTA's schedule -> ring slot i % kT16Stages
+    auto issue = [&](int i) {
+        const int tile = static_cast<int>(blockIdx.x) + (i / spt) * static_cast<int>(gridDim.x);
+        const TileInfo ti = tile_info<kT16Rows>(args, tile);
+        const CUtensorMap *map = &maps.m[0];
+#pragma unroll
+        for (int gi = 1; gi < kMaxGroups; ++gi)
+            if (gi == ti.grp) map = &maps.m[gi];
+        const int slot = i % kT16Stages;
+        mbar_arrive_expect_tx(smem_u32(&full[slot]), kT16StageBytes + ((args.test_stall && i == 0) ? 16 : 0));
+        tma_load_2d_hint(smem_u32(ring + static_cast<size_t>(slot) * kT16StageBytes), map,
+                         (i % spt) * kT16Sb * (kBlockBytes / 8), ti.row0, smem_u32(&full[slot]), policy);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < kT16Stages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            s_slot_done[i] = 0;
+        }
+        s_abort = 0;
+        fence_barrier_init();
+#pragma unroll
+        for (int gi = 0; gi < kMaxGroups; ++gi)
+            if (gi < args.ngroups) prefetch_tensormap(&maps.m[gi]);
+        policy = l2_policy_evict_first();
+        const int first = min(kT16PreWait, total);
+        for (int i = 0; i < first; ++i) issue(i);
+        s_issued = first;
+    }
+    __syncthreads();
+    policy = l2_policy_evict_first();
+
+    pdl_launch_dependents();
+    pdl_wait();   // x may come from the previous kernel
+
+    // x of this warp's super-blocks, four at a time: loads first (the rest of
+    // the ring is issued behind the first four), then the conversion
+    uint8_t *xw = xarea + static_cast<size_t>(warp) * kT16XPerWarp * kI8Bytes;
+#pragma unroll 1
+    for (int r0 = 0; r0 < kT16XPerWarp && warp + kWarps * r0 < nb; r0 += 4) {
+        float4 v[4][2];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int j = warp + kWarps * (r0 + r);
+            if (r0 + r < kT16XPerWarp && j < nb) {   // warp-uniform
+                const float4 *src = reinterpret_cast<const float4 *>(args.x + static_cast<size_t>(j) * 256);
+                v[r][0] = __ldg(src + lane);
+                v[r][1] = __ldg(src + 32 + lane);
+            }
+        }
+        if (r0 == 0 && tid == 0) {
+            const int first = min(kT16Stages, total);
+            for (int i = s_issued; i < first; ++i) issue(i);
+            s_issued = first;
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int j = warp + kWarps * (r0 + r);
+            if (r0 + r < kT16XPerWarp && j < nb) {
+                const float2 sp = x_item_i8<Q8>(v[r][0], v[r][1], lane, xw + (r0 + r) * kI8Bytes);
+                if (lane == 0) s_sc[j] = sp;
+            }
+        }
+    }
+    __syncwarp();
+
+    const PairSel psel = pair_sel(t);
+    int consumed = 0;
+    for (int ti_idx = 0; ti_idx < my_tiles; ++ti_idx) {
+        const int tile = static_cast<int>(blockIdx.x) + ti_idx * static_cast<int>(gridDim.x);
+        const TileInfo ti = tile_info<kT16Rows>(args, tile);
+        float acc[1][2] = {{0.f, 0.f}};
+        for (int st = 0; st < spt; ++st) {
+            const int slot = consumed % kT16Stages;
+            const uint32_t phase = static_cast<uint32_t>((consumed / kT16Stages) & 1);
+            if (!*(volatile int *)&s_abort && !mbar_wait_bounded(smem_u32(&full[slot]), phase, args.wait_ns)) {
+                atomicOr(&g_device_error, 1u);
+                s_abort = 1;
+            }
+            auto release = [&]() {
+                // the last of the 8 warps to leave the slot refills it
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence_block();
+                    const int prev = atomicAdd(&s_slot_done[slot], 1);
+                    if (prev % kWarps == kWarps - 1) {
+                        const int next = consumed + kT16Stages;
+                        if (next < total && !*(volatile int *)&s_abort) {
+                            issue(next);
+                            atomicAdd(&s_issued, 1);
+                        }
+                    }
+                }
+                ++consumed;
+            };
+            // this warp's super-block of the stage: the first j >= j0 with j % 8 == warp
+            const int j0 = st * kT16Sb;
+            const int jw = j0 + ((warp - j0 % kWarps) + kWarps) % kWarps;
+            if (jw < min(j0 + kT16Sb, nb) && !*(volatile int *)&s_abort) {
+                const uint8_t *ra = ring + static_cast<size_t>(slot) * kT16StageBytes +
+                                    g * (kT16Sb * kBlockBytes) + (jw - j0) * kBlockBytes;
+                const uint8_t *rb = ra + 8 * (kT16Sb * kBlockBytes);
+                const float2 sp = s_sc[jw];
+                stage_compute_i8<Q8>(ra, rb, xw + (jw / kWarps) * kI8Bytes, t, psel, sp.x, sp.y, acc, release);
+            } else {
+                release();
+            }
+        }
+        // tile epilogue: the four pair lanes of each row, then the 8 warps in order
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            acc[0][h] += __shfl_xor_sync(0xffffffffu, acc[0][h], 1);
+            acc[0][h] += __shfl_xor_sync(0xffffffffu, acc[0][h], 2);
+        }
+        const int buf = ti_idx & 1;
+        if (t == 0) {
+            s_red[buf][warp][g] = acc[0][0];
+            s_red[buf][warp][g + 8] = acc[0][1];
+        }
+        named_bar_sync(1, kThreads);
+        if (tid < kT16Rows && !*(volatile int *)&s_abort) {
+            float sum = s_red[buf][0][tid];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) sum += s_red[buf][w][tid];
+            const int row = ti.row0 + tid;
+            if (row < ti.N && ti.y) ti.y[row] = sum;
+        }
+    }
+
+    // after a timed-out wait: wait (bounded) for the copies still in flight
+    __syncthreads();
+    if (*(volatile int *)&s_abort && tid == 0) {
+        for (int i = max(0, s_issued - kT16Stages); i < s_issued; ++i)
+            (void)mbar_wait_bounded(smem_u32(&full[i % kT16Stages]), static_cast<uint32_t>((i / kT16Stages) & 1),
+                                    args.wait_ns);
+    }
+}
+
 
 // ---------------------------------------------------------------------------
 // Host side
@@ -790,6 +989,79 @@ static cudaError_t launch_gemv(const GemvPlan &p, const void *const *Ws, int64_t
 }
 
 static int row_tiles(int64_t N) { return static_cast<int>((N + kRows - 1) / kRows); }
+static int row_tiles16(int64_t N) { return static_cast<int>((N + kT16Rows - 1) / kT16Rows); }
+
+// W as [N rows] x [K/256 * 18 words] with a box of kT16Sb super-blocks of 16
+// rows (columns past K and rows past N are zero-filled by the TMA unit).
+static bool encode_w_map16(CUtensorMap *map, const void *W, int64_t N, int64_t K)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int64_t nb = K / 256;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(nb * (kBlockBytes / 8)), static_cast<cuuint64_t>(N)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(nb * kBlockBytes)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kT16Sb * (kBlockBytes / 8)), static_cast<cuuint32_t>(kT16Rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void *>(W), gdim, gstride, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Batch 1 on the 16-row kernel: automatically when the 128-row plan would
+// split K over CTAs (too few row tiles) and x fits the per-warp area, or on
+// request (Q4K_FLAG_ROWS16).  A forced split keeps the 128-row kernel.
+static bool use_rows16(const GemvPlan &p, int batch, int64_t K, const q4k_launch_opts *opts)
+{
+    if (batch != 1 || p.xm == 0 || K / 256 > kT16MaxNb) return false;
+    if (opts && (opts->flags & Q4K_FLAG_ROWS16)) return true;
+    if (opts && opts->split_k > 0) return false;
+    return p.split > 1;
+}
+
+// a.tile_start and a.tiles in 16-row tiles.
+static cudaError_t launch_rows16(int xm, const void *const *Ws, int64_t K, const GemvArgs &a, int sms,
+                                 cudaStream_t stream, bool pdl)
+{
+    WMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    for (int g = 0; g < a.ngroups; ++g)
+        if (!encode_w_map16(&maps.m[g], Ws[g], a.N[g], K)) return cudaErrorInvalidValue;
+    void (*kern)(const WMaps, const GemvArgs) = (xm == 2) ? q4k_gemv_rows16_kernel<2> : q4k_gemv_rows16_kernel<1>;
+    static std::mutex mu;
+    static bool attr_set[64][2] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        bool &done = attr_set[dev & 63][xm == 2 ? 1 : 0];
+        if (!done) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(t16_smem_bytes()));
+            if (e != cudaSuccess) return e;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+            if (e != cudaSuccess) return e;
+            done = true;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(std::min(a.tiles, 2 * sms), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = t16_smem_bytes();
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelEx(&cfg, kern, maps, a);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return e;
+}
 
 // Wait bound and the test-only stall of the launch options.
 static void set_wait_opts(GemvArgs &a, const q4k_launch_opts *opts)
@@ -841,6 +1113,13 @@ q4k_status gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t
         if (batch != 1 || (opts->flags & Q4K_FLAG_TENSOR_CORE)) return Q4K_ERR_INVALID_ARG;
         p.xm = 2;
     }
+    if (opts && (opts->flags & Q4K_FLAG_ROWS16) && (batch != 1 || p.xm == 0 || K / 256 > kT16MaxNb))
+        return Q4K_ERR_INVALID_ARG;
+    if (use_rows16(p, batch, K, opts)) {
+        a.tile_start[1] = a.tiles = row_tiles16(N);
+        cudaError_t e = launch_rows16(p.xm, &W, K, a, sms, static_cast<cudaStream_t>(stream), pdl);
+        return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
+    }
     cudaError_t e = launch_gemv<false>(p, &W, K, a, static_cast<cudaStream_t>(stream), pdl);
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
 }
@@ -887,6 +1166,18 @@ q4k_status gemv_grouped_impl(const q4k_gemv_group *groups, int ngroups, const fl
     if (opts && (opts->flags & Q4K_FLAG_Q8K_X)) {
         if (batch != 1 || (opts->flags & Q4K_FLAG_TENSOR_CORE)) return Q4K_ERR_INVALID_ARG;
         p.xm = 2;
+    }
+    if (opts && (opts->flags & Q4K_FLAG_ROWS16) && (batch != 1 || p.xm == 0 || K / 256 > kT16MaxNb))
+        return Q4K_ERR_INVALID_ARG;
+    if (use_rows16(p, batch, K, opts)) {
+        int t16 = 0;
+        for (int g = 0; g < a.ngroups; ++g) {
+            a.tile_start[g] = t16;
+            t16 += row_tiles16(a.N[g]);
+        }
+        a.tile_start[a.ngroups] = a.tiles = t16;
+        cudaError_t e = launch_rows16(p.xm, Ws, K, a, sms, static_cast<cudaStream_t>(stream), pdl);
+        return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
     }
     cudaError_t e = launch_gemv<false>(p, Ws, K, a, static_cast<cudaStream_t>(stream), pdl);
     return e == cudaSuccess ? Q4K_OK : Q4K_ERR_CUDA;
@@ -1009,6 +1300,13 @@ q4k_status gemv_plan_impl(int64_t N, int64_t K, int batch, int out[4])
     q4k_status st = check_device(&sms);
     if (st != Q4K_OK) return st;
     GemvPlan p = make_plan(row_tiles(N), K, batch, sms, 0);
+    if (use_rows16(p, batch, K, nullptr)) {
+        out[0] = 1;
+        out[1] = std::min(row_tiles16(N), 2 * sms);
+        out[2] = kT16Rows;
+        out[3] = static_cast<int>(K / 256);
+        return Q4K_OK;
+    }
     out[0] = p.split;
     out[1] = p.grid_x * p.split;
     out[2] = kRows;

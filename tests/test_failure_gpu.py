@@ -25,7 +25,8 @@ def env():
     return q4k, oracle
 
 
-@pytest.mark.parametrize("N,K,B,split", [(700, 1024, 1, 0), (3584, 3584, 1, 0), (300, 2048, 5, 0), (150, 2304, 1, 3)])
+@pytest.mark.parametrize("N,K,B,split", [(700, 1024, 1, 0), (3584, 3584, 1, 0), (300, 2048, 5, 0), (150, 2304, 1, 3),
+                                         (3584, 18944, 1, 0)])
 def test_wait_runs_out_then_recovers(env, N, K, B, split):
     q4k, oracle = env
     torch.cuda.synchronize()

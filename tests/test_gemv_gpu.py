@@ -368,3 +368,86 @@ def test_q8k_grouped_and_guards(env):
         q4k.gemv(W, _dev(synth.normal_f32((2, K), 57)), q8k=True)          # batch 1 only
     with pytest.raises(q4k.Q4KError):
         q4k.gemv(W, _dev(x), q8k=True, tensor_core=True)                   # one inner product at a time
+
+
+# ---------------------------------------------------------------- 16-row tiles (batch 1)
+ROWS16 = [
+    (1, 256), (15, 512), (16, 1792), (17, 3584), (100, 1792), (333, 2048), (129, 8192), (4608, 3584),
+    (5000, 1536),
+]
+
+
+@pytest.mark.parametrize("N,K", ROWS16)
+def test_rows16_shapes(env, N, K):
+    """The 16-row-tile kernel (one CTA per 16 rows over the whole K, the K split
+    between its warps): ragged row counts, 1 to 32 super-blocks per row (a
+    stage holds 7: full, partial and single-super-block stages), more tiles
+    than resident CTAs (5000 rows: CTAs take two tiles), against the oracle;
+    deterministic run to run."""
+    q4k, oracle = env
+    W = synth.q4k_weights(N, K, (61, N, K))
+    x = synth.normal_f32((1, K), (62, N, K))
+    x[0, :256] *= np.float32(1e-3)          # super-blocks of very different size
+    y = _run(q4k, W, x, rows16=True)
+    assert_close(y, oracle.gemv(W, x, N, K), x, K, f"rows16 N={N} K={K}")
+    assert np.array_equal(y, _run(q4k, W, x, rows16=True))
+
+
+def test_rows16_is_the_automatic_choice(env):
+    """Batch 1 with too few 128-row tiles and K <= 8192 takes the 16-row kernel
+    (the plan reports 16-row tiles and no split); a long K or a larger batch
+    keeps the 128-row kernel; both agree within the tolerance."""
+    q4k, oracle = env
+    assert q4k.gemv_plan(4608, 3584, 1)["rows_per_tile"] == 16
+    assert q4k.gemv_plan(3584, 3584, 1)["split_k"] == 1
+    assert q4k.gemv_plan(3584, 18944, 1)["rows_per_tile"] == 128
+    assert q4k.gemv_plan(4608, 3584, 2)["rows_per_tile"] == 128
+    assert q4k.gemv_plan(37888, 3584, 1)["rows_per_tile"] == 128    # enough 128-row tiles
+    N, K = 640, 4096
+    W = synth.q4k_weights(N, K, 63)
+    x = synth.normal_f32((1, K), 64)
+    ref = oracle.gemv(W, x, N, K)
+    y16, y128 = _run(q4k, W, x), _run(q4k, W, x, split_k=5)
+    assert_close(y16, ref, x, K, "automatic (16-row)")
+    assert_close(y128, ref, x, K, "forced split (128-row)")
+    assert np.array_equal(y16, _run(q4k, W, x, rows16=True))
+
+
+def test_rows16_grouped_q8k_and_guards(env):
+    """Fused q/k/v-style launch with ragged and empty matrices on the 16-row
+    kernel (batch 1), its Q8_K mode against the oracle's Q8_K product, the
+    output guards, and the argument checks of the flag."""
+    q4k, oracle = env
+    K = 1024
+    shapes = [130, 0, 7, 300]
+    Wn = [synth.q4k_weights(N, K, (65, i)) for i, N in enumerate(shapes)]
+    x = synth.normal_f32((1, K), 66)
+    Wd = [_dev(W) if W.size else torch.empty((0, 576), dtype=torch.uint8, device="cuda") for W in Wn]
+    ys = q4k.gemv_grouped(Wd, _dev(x), rows16=True)
+    torch.cuda.synchronize()
+    for N, W, y in zip(shapes, Wn, ys):
+        if N:
+            assert_close(y.cpu().numpy(), oracle.gemv(W, x, N, K), x, K, f"rows16 grouped N={N}")
+    # Q8_K activations on the same kernel
+    xq = _q8k_input(K, 67)
+    q, d = oracle.q8k_quantize(xq[0], K)
+    yq = _run(q4k, Wn[3], xq, q8k=True, rows16=True)[0]
+    D = oracle.dequant_matrix(Wn[3], 300, K)
+    xt = np.repeat(d.astype(np.float64), 256) * q.astype(np.float64)
+    assert np.all(np.abs(yq - oracle.gemv_q8k(Wn[3], q, d, 300, K)) <= 1e-5 * (np.abs(D) @ np.abs(xt)) + 1e-30)
+    # writes stay inside y
+    N = 77
+    buf = torch.full((N + 2048,), 12345.0, dtype=torch.float32, device="cuda")
+    y = buf[1024:1024 + N].view(1, N)
+    q4k.gemv(_dev(Wn[3][:N]), _dev(x), y, rows16=True)
+    torch.cuda.synchronize()
+    assert torch.all(buf[:1024] == 12345.0) and torch.all(buf[1024 + N:] == 12345.0)
+    # the flag is batch 1, integer path, K <= 8192 only
+    W = _dev(Wn[0])
+    with pytest.raises(q4k.Q4KError):
+        q4k.gemv(W, _dev(synth.normal_f32((2, K), 68)), rows16=True)
+    with pytest.raises(q4k.Q4KError):
+        q4k.gemv(W, _dev(x), rows16=True, tensor_core=True)
+    Kl = 8448
+    with pytest.raises(q4k.Q4KError):
+        q4k.gemv(_dev(synth.q4k_weights(16, Kl, 69)), _dev(synth.normal_f32((1, Kl), 70)), rows16=True)
