@@ -516,10 +516,21 @@ def run_ours(args):
         y6 = torch.empty((1, N6), dtype=torch.float32, device=dev)
         g = capture(lambda: [q4k.q6k_gemv(Wq, x6, y6, stream=stream) for Wq in W6s])
         ms = time_graph(g, max(4, args.steps // (4 * nc6)), args.warmup) / nc6
-        del g, W6s, W6
+        del g
+        # the same matrix in planar form (repacked once, as at model load)
+        W6ps = [q4k.q6k_repack_planar(Wq, K6, stream=stream) for Wq in W6s]
+        stream.synchronize()
+        g = capture(lambda: [q4k.q6k_gemv_planar(Wp, x6, N6, y6, stream=stream) for Wp in W6ps])
+        msp = time_graph(g, max(4, args.steps // (4 * nc6)), args.warmup) / nc6
+        del g, W6s, W6, W6ps
         b6 = N6 * (K6 // 256) * 210 + 4 * K6 + 4 * N6
-        q6[f"{name6}_{N6}x{K6}"] = {"us": ms * 1e3, "gbs": b6 / (ms * 1e-3) / 1e9,
-                                   "frac_of_peak": b6 / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "weight_copies": nc6}
+        b6p = q4k.q6k_planar_bytes(N6, K6) + 4 * K6 + 4 * N6
+        q6[f"{name6}_{N6}x{K6}"] = {
+            "us": msp * 1e3, "gbs": b6p / (msp * 1e-3) / 1e9, "frac_of_peak": b6p / (msp * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "path": "q6k_gemv_planar (weights repacked once into 16-byte aligned planes)",
+            "gguf_form": {"us": ms * 1e3, "gbs": b6 / (ms * 1e-3) / 1e9,
+                          "frac_of_peak": b6 / (ms * 1e-3) / 1e9 / pk["hbm_gbs"], "path": "q6k_gemv"},
+            "weight_copies": nc6}
 
     # ---- one 4096 x 4096 GEMV at batch 1.  Its 9.5 MB of weights fit in L2,
     # so the timed launches cycle through byte copies of W totalling 4x the L2
@@ -686,7 +697,7 @@ def run_ours(args):
 
 def run_profile_case(spec: str, iters: int):
     """One op repeated `iters` times on seeded inputs, for ncu captures.
-    spec = gemv:N:K:B | argmax:N:K:B | prefill:N:K:T | q6k:N:K:B"""
+    spec = gemv:N:K:B | argmax:N:K:B | prefill:N:K:T | q6k:N:K:B | q6kp:N:K:B"""
     import numpy as np
     import torch
 
@@ -720,6 +731,18 @@ def run_profile_case(spec: str, iters: int):
         torch.cuda.synchronize()
         print(f"profile case {spec} x{iters} done")
         return
+    if kind == "q6kp":
+        # q6kp:N:K:B -- the Q6_K GEMV on the planar form
+        W6 = torch.from_numpy(synth.q6k_weights(N, K, (9, N, K))).cuda()
+        Wp = q4k.q6k_repack_planar(W6, K)
+        del W6
+        x = torch.from_numpy(synth.normal_f32((B, K), (9, B))).cuda()
+        y = torch.empty((B, N), dtype=torch.float32, device="cuda")
+        for _ in range(iters):
+            q4k.q6k_gemv_planar(Wp, x, N, y)
+        torch.cuda.synchronize()
+        print(f"profile case {spec} x{iters} done")
+        return
     W = torch.from_numpy(synth.q4k_weights(N, K, (9, N, K))).cuda()
     if kind == "prefill":
         X = torch.from_numpy(synth.normal_bf16_bits((B, K), (9, B)).view(np.int16)).cuda().view(torch.bfloat16)
@@ -748,7 +771,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--skip-cpu-configs", action="store_true", help="time the oracle on the headline sample only")
-    ap.add_argument("--profile-case", default=None, help="gemv:N:K:B | argmax:N:K:B | prefill:N:K:T | q6k:N:K:B | decode:L:B (ncu helper)")
+    ap.add_argument("--profile-case", default=None, help="gemv:N:K:B | argmax:N:K:B | prefill:N:K:T | q6k:N:K:B | q6kp:N:K:B | decode:L:B (ncu helper)")
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
     if args.profile_case:

@@ -21,7 +21,11 @@
  *                      weight tiles).
  *   - q6k_gemv         y = W x for a Q6_K matrix, the other block format of
  *                      Q4_K_M files ("custom quantized GEMV for decode (Q8_0,
- *                      Q4_K, Q6_K)", same page and item).
+ *                      Q4_K, Q6_K)", same page and item); q6k_repack_planar
+ *                      and q6k_gemv_planar: the same product on a copy of
+ *                      the matrix split into aligned planes once, at load
+ *                      time (the dotLLM README repacks its weights at model
+ *                      load time too: News 2026-03, the R4 row interleave).
  *
  * ---------------------------------------------------------------------------
  * Q4_K super-block (144 bytes, 256 weights, 4.5 bits per weight)
@@ -187,6 +191,44 @@ q4k_status q4k_gemv_argmax_noalloc(const void *W, const float *x, int32_t *idx, 
  * Errors: INVALID_ARG, MISALIGNED (W or x), UNSUPPORTED_DEVICE, CUDA.
  */
 q4k_status q6k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream);
+
+/*
+ * Planar Q6_K: the bytes of a Q6_K matrix regrouped so that every block's
+ * codes and scales start on a 16-byte boundary (GGUF blocks are only 2-byte
+ * aligned), for the GEMV below.  For N rows and nb = K/256 blocks per row,
+ * with DP = 2*nb rounded up to a multiple of 16, the planar buffer holds
+ *   QS  [N][nb][208]  bytes 0..207 of each block (ql, qh, sc), unchanged
+ *   D   [N][DP]       d of block j at bytes 2j, 2j+1 of the row; the rest 0
+ * QS at byte 0 and D at byte N*nb*208, q6k_planar_bytes(N, K) =
+ * N * (nb*208 + DP) bytes in all (2940 + 4 bytes per row for K = 3584).  The
+ * weights it encodes are exactly those of the GGUF matrix.  Returns -1 for
+ * N < 0 or K not a positive multiple of 256.
+ */
+int64_t q6k_planar_bytes(int64_t N, int64_t K);
+
+/*
+ * Wp = the planar form of the Q6_K matrix W (above).  W uint8 [N][K/256*210]
+ * (16-byte aligned); Wp device memory of q6k_planar_bytes(N, K) bytes
+ * (16-byte aligned), not overlapping W; asynchronous on stream.  N >= 0 (0:
+ * no-op), K a positive multiple of 256.  Errors: INVALID_ARG, MISALIGNED,
+ * UNSUPPORTED_DEVICE, CUDA.
+ */
+q4k_status q6k_repack_planar(const void *W, void *Wp, int64_t N, int64_t K, void *stream);
+
+/*
+ * y = W x as q6k_gemv computes it, from the planar form Wp of W: the same
+ * arguments, with Wp (q6k_planar_bytes(N, K) bytes, 16-byte aligned) in place
+ * of W.  Every block is read once for all batch rows.  The planes stream into
+ * shared memory as 2-D TMA boxes of 128 rows (one block per stage), so each
+ * thread reads its codes, scales and d with 16-byte loads; x enters per
+ * 256-block as the two int8 parts of q6k_gemv's integer path and the codes
+ * meet them in exact int32 dot products (batch rows 1..4 per launch; larger
+ * batches take one launch per four rows).  Deterministic; K splits over the
+ * CTAs of a cluster add their partial rows in rank order.
+ * Errors: INVALID_ARG, MISALIGNED (Wp or x), UNSUPPORTED_DEVICE, CUDA.
+ */
+q4k_status q6k_gemv_planar(const void *Wp, const float *x, float *y, int64_t N, int64_t K, int batch,
+                           void *stream);
 
 /*
  * Y[t][n] = sum_k w[n][k] * X[t][k]   for t < T, n < N (prefill).

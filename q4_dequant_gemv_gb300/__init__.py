@@ -47,7 +47,8 @@ class GemvGroup(ctypes.Structure):
 EXPORTS = ("q4k_status_string", "q4k_abi_version", "q4k_gemv", "q4k_gemv_argmax", "q4k_gemv_argmax_debug",
            "q4k_gemv_argmax_noalloc", "q4k_gemm_prefill", "q4k_gemm_prefill_exact", "q4k_gemv_ex",
            "q4k_gemv_grouped", "q4k_gemv_plan",
-           "q4k_device_error_flags", "q4k_device_error_clear", "q4k_stream_read", "q6k_gemv")
+           "q4k_device_error_flags", "q4k_device_error_clear", "q4k_stream_read", "q6k_gemv",
+           "q6k_planar_bytes", "q6k_repack_planar", "q6k_gemv_planar")
 
 
 def lib():
@@ -80,6 +81,12 @@ def lib():
         L.q4k_gemm_prefill_exact.restype = I
         L.q6k_gemv.argtypes = [P, P, P, I64, I64, I, P]
         L.q6k_gemv.restype = I
+        L.q6k_planar_bytes.argtypes = [I64, I64]
+        L.q6k_planar_bytes.restype = I64
+        L.q6k_repack_planar.argtypes = [P, P, I64, I64, P]
+        L.q6k_repack_planar.restype = I
+        L.q6k_gemv_planar.argtypes = [P, P, P, I64, I64, I, P]
+        L.q6k_gemv_planar.restype = I
         L.q4k_gemm_prefill.restype = I
         L.q4k_gemv_plan.argtypes = [I64, I64, I, ctypes.POINTER(ctypes.c_int * 4)]
         L.q4k_gemv_plan.restype = I
@@ -181,6 +188,51 @@ def q6k_gemv(W, x, y=None, *, stream=None):
         raise ValueError("y has the wrong size")
     st = lib().q6k_gemv(W.data_ptr(), x2.data_ptr(), y.data_ptr(), N, K, B, _stream_ptr(stream))
     _check("q6k_gemv", st)
+    return y.view(N) if squeeze and y.dim() == 2 else y
+
+
+def q6k_planar_bytes(N: int, K: int) -> int:
+    """Size in bytes of the planar form of an N x K Q6_K matrix."""
+    n = lib().q6k_planar_bytes(N, K)
+    if n < 0:
+        raise ValueError(f"bad Q6_K shape {N} x {K}")
+    return n
+
+
+def q6k_repack_planar(W, K: int, Wp=None, *, stream=None):
+    """The planar form (flat uint8 tensor) of the Q6_K matrix W [N, K/256*210]."""
+    import torch
+    _dev(W, "W", torch.uint8)
+    if K % 256 or W.dim() != 2 or W.shape[1] != (K // 256) * 210:
+        raise ValueError(f"W must be [N, {(K // 256) * 210}] uint8 for K={K}")
+    N = W.shape[0]
+    nbytes = q6k_planar_bytes(N, K)
+    if Wp is None:
+        Wp = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    _dev(Wp, "Wp", torch.uint8)
+    if Wp.numel() != nbytes:
+        raise ValueError(f"Wp must hold {nbytes} bytes")
+    _check("q6k_repack_planar", lib().q6k_repack_planar(W.data_ptr(), Wp.data_ptr(), N, K, _stream_ptr(stream)))
+    return Wp
+
+
+def q6k_gemv_planar(Wp, x, N: int, y=None, *, stream=None):
+    """y [B, N] (fp32) = W x from the planar form Wp of W; x [B, K] (fp32) or [K]."""
+    import torch
+    _dev(Wp, "Wp", torch.uint8)
+    _dev(x, "x", torch.float32)
+    squeeze = x.dim() == 1
+    x2 = x.view(1, -1) if squeeze else x
+    B, K = x2.shape
+    if Wp.numel() != q6k_planar_bytes(N, K):
+        raise ValueError("Wp does not hold a planar N x K matrix")
+    if y is None:
+        y = torch.empty((B, N), dtype=torch.float32, device=x.device)
+    _dev(y, "y", torch.float32)
+    if y.numel() != B * N:
+        raise ValueError("y has the wrong size")
+    _check("q6k_gemv_planar", lib().q6k_gemv_planar(Wp.data_ptr(), x2.data_ptr(), y.data_ptr(), N, K, B,
+                                                    _stream_ptr(stream)))
     return y.view(N) if squeeze and y.dim() == 2 else y
 
 

@@ -30,6 +30,18 @@ q4k_status q6k_gemv(const void *W, const float *x, float *y, int64_t N, int64_t 
     return q4k::q6k_gemv_impl(W, x, y, N, K, batch, stream);
 }
 
+int64_t q6k_planar_bytes(int64_t N, int64_t K) { return q4k::q6k_planar_bytes_impl(N, K); }
+
+q4k_status q6k_repack_planar(const void *W, void *Wp, int64_t N, int64_t K, void *stream)
+{
+    return q4k::q6k_repack_planar_impl(W, Wp, N, K, stream);
+}
+
+q4k_status q6k_gemv_planar(const void *Wp, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream)
+{
+    return q4k::q6k_gemv_planar_impl(Wp, x, y, N, K, batch, stream);
+}
+
 q4k_status q4k_gemv_ex(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream,
                        const q4k_launch_opts *opts)
 {
@@ -87,13 +99,14 @@ q4k_status q4k_gemv_plan(int64_t N, int64_t K, int batch, int out[4])
  * out and the kernel wound down early).  Synchronous; 0 means no error. */
 unsigned int q4k_device_error_flags(void)
 {
-    return q4k::read_device_error() | q4k::read_prefill_error() | q4k::read_q6k_error() | q4k::read_probe_error();
+    return q4k::read_device_error() | q4k::read_prefill_error() | q4k::read_q6k_error() | q4k::read_q6p_error() |
+           q4k::read_probe_error();
 }
 
 q4k_status q4k_device_error_clear(void)
 {
     const bool ok = q4k::clear_device_error() & q4k::clear_prefill_error() & q4k::clear_q6k_error() &
-                    q4k::clear_probe_error();
+                    q4k::clear_q6p_error() & q4k::clear_probe_error();
     return ok ? Q4K_OK : Q4K_ERR_CUDA;
 }
 

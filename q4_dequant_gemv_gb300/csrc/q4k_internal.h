@@ -22,17 +22,23 @@ q4k_status gemv_grouped_impl(const q4k_gemv_group *groups, int ngroups, const fl
 q4k_status gemv_argmax_noalloc_impl(const void *W, const float *x, int32_t *idx, int64_t N, int64_t K, int batch,
                                     void *stream);
 q4k_status q6k_gemv_impl(const void *W, const float *x, float *y, int64_t N, int64_t K, int batch, void *stream);
+int64_t q6k_planar_bytes_impl(int64_t N, int64_t K);
+q4k_status q6k_repack_planar_impl(const void *W, void *Wp, int64_t N, int64_t K, void *stream);
+q4k_status q6k_gemv_planar_impl(const void *Wp, const float *x, float *y, int64_t N, int64_t K, int batch,
+                                void *stream);
 q4k_status prefill_impl(const void *W, const void *X, float *Y, int64_t N, int64_t K, int64_t T, void *stream,
                         bool exact);
 unsigned int read_device_error();
 unsigned int read_prefill_error();
 unsigned int read_q6k_error();
+unsigned int read_q6p_error();
 unsigned int read_probe_error();
 q4k_status stream_read_impl(const void *buf, int64_t bytes, int64_t *bytes_read, void *stream);
 // Reset the sticky device-side error flag of each translation unit (false on a CUDA error).
 bool clear_device_error();
 bool clear_prefill_error();
 bool clear_q6k_error();
+bool clear_q6p_error();
 bool clear_probe_error();
 // cuTensorMapEncodeTiled from the CUDA driver API (null if unavailable).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();

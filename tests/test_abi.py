@@ -173,3 +173,12 @@ def test_binding_refuses_host_tensors(q4k):
                  lambda: q4k.gemm_prefill(W, torch.zeros((32, 256), dtype=torch.bfloat16))):
         with pytest.raises((ValueError, TypeError, RuntimeError)):
             call()
+
+
+def test_q6k_planar_bytes_host_only(q4k):
+    """The planar Q6_K size is a host computation: N * (nb*208 + 2*nb rounded up to 16)."""
+    L = q4k.lib()
+    assert L.q6k_planar_bytes(152064, 3584) == 152064 * (14 * 208 + 32)
+    assert L.q6k_planar_bytes(3, 18944) == 3 * (74 * 208 + 160)
+    assert L.q6k_planar_bytes(0, 256) == 0
+    assert L.q6k_planar_bytes(5, 100) == -1 and L.q6k_planar_bytes(-1, 256) == -1

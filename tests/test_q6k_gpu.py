@@ -79,3 +79,96 @@ def test_q6k_deterministic_and_guards(env):
         q4k.q6k_gemv(W, xm)                                          # x not 16-byte aligned
     empty = q4k.q6k_gemv(torch.zeros((0, (K // 256) * 210), dtype=torch.uint8, device="cuda"), x)
     assert empty.shape == (2, 0)
+
+
+# ---------------------------------------------------------------- planar form (q6k_repack_planar / q6k_gemv_planar)
+def _planar(q4k, W, K):
+    Wp = q4k.q6k_repack_planar(_dev(W), K)
+    torch.cuda.synchronize()
+    return Wp
+
+
+def test_q6k_planar_layout(env):
+    """The planar form holds each block's bytes 0..207 unchanged in the QS plane
+    and the d bytes of the row's blocks, zero-padded to 16 bytes, in the D plane."""
+    q4k, _ = env
+    for N, K in ((5, 256), (37, 3584), (130, 2048), (3, 18944)):
+        W = synth.q6k_weights(N, K, (81, N, K))
+        nb = K // 256
+        dp = -(-2 * nb // 16) * 16
+        Wp = _planar(q4k, W, K).cpu().numpy()
+        assert Wp.size == q4k.q6k_planar_bytes(N, K) == N * (nb * 208 + dp)
+        blocks = W.reshape(N, nb, 210)
+        assert np.array_equal(Wp[:N * nb * 208].reshape(N, nb, 208), blocks[:, :, :208])
+        D = Wp[N * nb * 208:].reshape(N, dp)
+        assert np.array_equal(D[:, :2 * nb].reshape(N, nb, 2), blocks[:, :, 208:210])
+        assert not D[:, 2 * nb:].any()
+
+
+# row tiles of 128 with a tail, one tile, K splits over clusters (few tiles), x in several chunks (long
+# K), batch 1..16 (launches of up to four batch rows)
+PLANAR = [(1, 256, 1), (7, 512, 1), (129, 3584, 1), (300, 4096, 3), (1000, 3584, 1), (24, 18944, 1),
+          (3584, 18944, 1), (1500, 2304, 4), (200, 1024, 5), (136, 4096, 16), (2000, 3584, 2), (640, 11008, 4)]
+
+
+@pytest.mark.parametrize("N,K,B", PLANAR)
+def test_q6k_planar_shapes(env, N, K, B):
+    q4k, oracle = env
+    W = synth.q6k_weights(N, K, (N, K, 82))
+    x = synth.normal_f32((B, K), (N, K, B, 83))
+    x[:, :256] *= np.float32(1e-3)      # blocks of x of very different size
+    Wp = _planar(q4k, W, K)
+    y = q4k.q6k_gemv_planar(Wp, _dev(x), N)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), oracle.q6k_gemv(W, x, N, K), x, K, f"q6k planar N={N} K={K} B={B}")
+    y2 = q4k.q6k_gemv_planar(Wp, _dev(x), N)
+    assert torch.equal(y, y2)
+
+
+def test_q6k_planar_lm_head_sampled(env):
+    """The 152064 x 3584 LM head on the planar form at batch 1: sampled rows
+    against the oracle, every row against the GGUF-form kernel."""
+    q4k, oracle = env
+    N, K = 152064, 3584
+    W = synth.q6k_weights(N, K, (84, 1))
+    x = synth.normal_f32((1, K), (85, 1))
+    Wp = _planar(q4k, W, K)
+    y = q4k.q6k_gemv_planar(Wp, _dev(x), N).cpu().numpy()
+    rows = np.unique(np.concatenate([np.random.default_rng(3).integers(0, N, 64), [0, 1, 127, 128, N - 1]]))
+    ref = oracle.q6k_gemv_rows(W, x, N, K, rows)
+    assert_close(y[:, rows], ref, x, K, "q6k planar lm head")
+    y_gguf = _run(q4k, W, x)
+    scale = np.abs(y_gguf).max()
+    assert np.abs(y - y_gguf).max() <= 2e-3 * scale
+
+
+def test_q6k_planar_extremes_and_guards(env):
+    q4k, oracle = env
+    N, K = 260, 1536
+    W = synth.q6k_weights(N, K, 86)
+    x = synth.normal_f32((1, K), 87)
+    x[0, 0:256] *= np.float32(1e-30)     # below 2^-64 relative scale
+    x[0, 256:512] = 0.0                   # an all-zero block
+    x[0, 700] = 3.0e4                     # one large entry
+    Wp = _planar(q4k, W, K)
+    y = q4k.q6k_gemv_planar(Wp, _dev(x), N)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), oracle.q6k_gemv(W, x, N, K), x, K, "q6k planar extremes")
+    assert np.all(q4k.q6k_gemv_planar(Wp, _dev(np.zeros((1, K), np.float32)), N).cpu().numpy() == 0.0)
+    # writes stay inside y
+    buf = torch.full((N + 2048,), 12345.0, dtype=torch.float32, device="cuda")
+    q4k.q6k_gemv_planar(Wp, _dev(x), N, buf[1024:1024 + N].view(1, N))
+    torch.cuda.synchronize()
+    assert torch.all(buf[:1024] == 12345.0) and torch.all(buf[1024 + N:] == 12345.0)
+    with pytest.raises(q4k.Q4KError):
+        q4k.q6k_gemv_planar(Wp, _dev(synth.normal_f32((17, K), 88)), N)      # batch above 16
+    xm = torch.zeros(K + 4, dtype=torch.float32, device="cuda")[1:K + 1].view(1, K)
+    with pytest.raises(q4k.Q4KError):
+        q4k.q6k_gemv_planar(Wp, xm, N)                                     # x not 16-byte aligned
+    nbytes = q4k.q6k_planar_bytes(N, K)
+    both = torch.zeros(W.size + nbytes + 16, dtype=torch.uint8, device="cuda")
+    both[:W.size] = _dev(W.reshape(-1))
+    with pytest.raises(q4k.Q4KError):                                      # W and Wp overlap
+        q4k.q6k_repack_planar(both[:W.size].view(N, -1), K, both[16:16 + nbytes])
+    empty = q4k.q6k_gemv_planar(torch.zeros(0, dtype=torch.uint8, device="cuda"), _dev(x), 0)
+    assert empty.shape == (1, 0)
