@@ -172,3 +172,29 @@ def test_q6k_planar_extremes_and_guards(env):
         q4k.q6k_repack_planar(both[:W.size].view(N, -1), K, both[16:16 + nbytes])
     empty = q4k.q6k_gemv_planar(torch.zeros(0, dtype=torch.uint8, device="cuda"), _dev(x), 0)
     assert empty.shape == (1, 0)
+
+
+def test_q6k_planar_graph_capture(env):
+    """Planar GEMVs captured in a CUDA graph on a side stream replay to the eager results."""
+    q4k, _ = env
+    mats = [(synth.q6k_weights(n, k, (89, i)), n, k) for i, (n, k) in enumerate([(640, 3584), (300, 18944)])]
+    Wps = [q4k.q6k_repack_planar(_dev(w), k) for w, _, k in mats]
+    xs = [_dev(synth.normal_f32((1, k), (90, i))) for i, (_, _, k) in enumerate(mats)]
+    ys = [torch.empty((1, n), device="cuda") for _, n, _ in mats]
+    for Wp, x, y, (_, n, _) in zip(Wps, xs, ys, mats):
+        q4k.q6k_gemv_planar(Wp, x, n, y)
+    torch.cuda.synchronize()
+    eager = [y.clone() for y in ys]
+    for y in ys:
+        y.zero_()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for Wp, x, y, (_, n, _) in zip(Wps, xs, ys, mats):
+                q4k.q6k_gemv_planar(Wp, x, n, y, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, ys):
+        assert torch.equal(a, b)
