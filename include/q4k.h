@@ -222,8 +222,8 @@ q4k_status q6k_repack_planar(const void *W, void *Wp, int64_t N, int64_t K, void
  * shared memory as 2-D TMA boxes of 128 rows (one block per stage), so each
  * thread reads its codes, scales and d with 16-byte loads; x enters per
  * 256-block as the two int8 parts of q6k_gemv's integer path and the codes
- * meet them in exact int32 dot products (batch rows 1..4 per launch; larger
- * batches take one launch per four rows).  Deterministic; K splits over the
+ * meet them in exact int32 dot products (batch rows 1..8 per launch; larger
+ * batches take one launch per eight rows).  Deterministic; K splits over the
  * CTAs of a cluster add their partial rows in rank order.
  * Errors: INVALID_ARG, MISALIGNED (Wp or x), UNSUPPORTED_DEVICE, CUDA.
  */

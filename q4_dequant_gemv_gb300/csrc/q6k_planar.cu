@@ -31,7 +31,7 @@
 //   * Few row tiles: the K range splits over the CTAs of a cluster (up to 8)
 //     and the partial rows are added in rank order through distributed shared
 //     memory (deterministic).  Otherwise CTAs loop over row tiles.
-//   * Batch rows 1..4 per launch (the dp4a work grows with each row).
+//   * Batch rows 1..8 per launch (the dp4a work grows with each row).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -61,8 +61,11 @@ constexpr int kXItem = 576;                   // x of one (batch row, block): xh
 constexpr int kMaxItems = 40;                 // x items held at once (per chunk); two CTAs per SM
 constexpr int kRedRows = kRows + 16;          // split-K receive rows (one slot per source rank)
 constexpr int kMaxSplit = 8;
+constexpr int kMaxB = 8;                      // batch rows per launch
 constexpr size_t kSmemBytes = static_cast<size_t>(kStages) * kStageBytes + static_cast<size_t>(kMaxItems) * kXItem +
-                              static_cast<size_t>(kRedRows) * 4 * 4;
+                              static_cast<size_t>(kRedRows) * kMaxB * 4;
+// two CTAs per SM: (dynamic + 1 KB static + 1 KB reserved) x 2 <= 228 KB
+static_assert(2 * (kSmemBytes + 2048) <= 228 * 1024, "two CTAs per SM");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
 __device__ unsigned int g_q6p_error = 0;   // bit 0: a bounded wait timed out
@@ -223,6 +226,7 @@ __device__ __forceinline__ int sbyte(uint32_t w)
 template <int BMAX>
 __global__ void __launch_bounds__(kThreads, 2) q6k_planar_kernel(const __grid_constant__ Maps maps, const Args args)
 {
+    static_assert(BMAX <= kMaxB, "the split-K receive buffer holds kMaxB batch rows");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *ring = smem_raw;
     uint8_t *xa = smem_raw + static_cast<size_t>(kStages) * kStageBytes;
@@ -281,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 2) q6k_planar_kernel(const __grid_co
     const int h = t >> 1, p = t & 1;
     const int offA = 64 * h + 16 * p, offB = offA + 32, offH = 128 + 32 * h + 16 * p, offS = 192 + 8 * h;
     // x chunk: items (batch row, block) of kc blocks of this CTA's K slice,
-    // item (bl, b) at (bl * BMAX + b) * kXItem
+    // item (bl, b) at (bl * B + b) * kXItem
     auto convert = [&](int kb0, int cn, bool first_chunk) {
         const int items = cn * B;
         float4 v[2][2];
@@ -308,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 2) q6k_planar_kernel(const __grid_co
                 const int it = it0 + r * kWarps;
                 if (it < items) {
                     const int bl = it / B, b = it - bl * B;
-                    const float2 up = x_item(v[r][0], v[r][1], lane, xa + static_cast<size_t>(bl * BMAX + b) * kXItem);
-                    if (lane == 0) s_up[bl * BMAX + b] = up;
+                    const float2 up = x_item(v[r][0], v[r][1], lane, xa + static_cast<size_t>(bl * B + b) * kXItem);
+                    if (lane == 0) s_up[bl * B + b] = up;
                 }
             }
         }
@@ -374,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 2) q6k_planar_kernel(const __grid_co
 #pragma unroll
             for (int b = 0; b < BMAX; ++b) {
                 if (b >= B) break;
-                const uint8_t *xi = xa + static_cast<size_t>(blk * BMAX + b) * kXItem;
+                const uint8_t *xi = xa + static_cast<size_t>(blk * B + b) * kXItem;
                 // x parts of the thread's weights: 16 bytes per c, xh then xl
                 uint4 xh[4], xl[4];
 #pragma unroll
@@ -383,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 2) q6k_planar_kernel(const __grid_co
                     xl[c] = *reinterpret_cast<const uint4 *>(xi + 256 + 128 * h + 32 * c + 16 * p);
                 }
                 const int4 sums = *reinterpret_cast<const int4 *>(xi + 512 + 16 * t);
-                const float2 up = s_up[blk * BMAX + b];
+                const float2 up = s_up[blk * B + b];
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const uint32_t A[4] = {qa[r].x, qa[r].y, qa[r].z, qa[r].w};
@@ -653,8 +657,8 @@ q4k_status q6k_gemv_planar_impl(const void *Wp, const float *x, float *y, int64_
     const int tiles = static_cast<int>((N + q6p::kRows - 1) / q6p::kRows);
     const int split = choose_split(tiles, static_cast<int>(nb), sms);
     const int grid_x = (split > 1) ? tiles : std::min(tiles, 2 * sms);
-    for (int b0 = 0; b0 < batch; b0 += 4) {
-        const int B = std::min(4, batch - b0);
+    for (int b0 = 0; b0 < batch; b0 += q6p::kMaxB) {
+        const int B = std::min(q6p::kMaxB, batch - b0);
         q6p::Args a{};
         a.x = x + static_cast<size_t>(b0) * K;
         a.y = y + static_cast<size_t>(b0) * N;
@@ -663,10 +667,12 @@ q4k_status q6k_gemv_planar_impl(const void *Wp, const float *x, float *y, int64_
         a.B = B;
         a.tiles = tiles;
         const int ks_max = static_cast<int>((nb + split - 1) / split);
-        a.kc = std::min(ks_max, q6p::kMaxItems / (B == 1 ? 1 : 4));
+        a.kc = std::min(ks_max, q6p::kMaxItems / B);
         a.wait_ns = q6p::kWaitLimitNs;
-        cudaError_t e = (B == 1) ? launch<1>(maps, a, split, grid_x, static_cast<cudaStream_t>(stream))
-                                 : launch<4>(maps, a, split, grid_x, static_cast<cudaStream_t>(stream));
+        const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+        cudaError_t e = (B == 1)   ? launch<1>(maps, a, split, grid_x, cs)
+                        : (B <= 4) ? launch<4>(maps, a, split, grid_x, cs)
+                                   : launch<8>(maps, a, split, grid_x, cs);
         if (e != cudaSuccess) return Q4K_ERR_CUDA;
     }
     return Q4K_OK;
