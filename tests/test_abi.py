@@ -162,6 +162,28 @@ def test_q6k_host_validation(q4k):
     assert q6(0, ok, 0, 0, 256, 1) in (0, 3, 4)      # N == 0: no weight or output pointer needed
 
 
+def test_q6k_planar_host_validation(q4k):
+    """q6k_repack_planar and q6k_gemv_planar argument errors come back before any
+    device call (1 = INVALID_ARG, 2 = MISALIGNED)."""
+    ok = 0x10000
+    rp = lambda W, Wp, N, K: q4k.raw_call("q6k_repack_planar", P(W), P(Wp), N, K, P(0))
+    gp = lambda Wp, x, y, N, K, B: q4k.raw_call("q6k_gemv_planar", P(Wp), P(x), P(y), N, K, B, P(0))
+    assert rp(0, ok, 64, 256) == 1
+    assert rp(ok, 0, 64, 256) == 1
+    assert rp(ok, 0x100000, 64, 300) == 1
+    assert rp(ok, 0x100000, -1, 256) == 1
+    assert rp(ok + 2, 0x100000, 64, 256) == 2
+    assert rp(ok, 0x100000 + 8, 64, 256) == 2
+    assert gp(0, ok, ok, 64, 256, 1) == 1
+    assert gp(ok, 0, ok, 64, 256, 1) == 1
+    assert gp(ok, ok, 0, 64, 256, 1) == 1
+    assert gp(ok, ok, ok, 64, 300, 1) == 1
+    assert gp(ok, ok, ok, 64, 256, 0) == 1
+    assert gp(ok, ok, ok, 64, 256, 17) == 1
+    assert gp(ok + 2, ok, ok, 64, 256, 1) == 2
+    assert gp(ok, ok + 4, ok, 64, 256, 1) == 2
+
+
 def test_binding_refuses_host_tensors(q4k):
     """The Python entry points take device tensors only: host tensors raise
     before anything is computed (there is no CPU path)."""
