@@ -285,9 +285,7 @@ q4k_status q4k_gemm_prefill_exact(const void *W, const void *X_bf16, float *Y, i
  *            kernel may start streaming W while the previous kernel on the
  *            stream is still running.  W must then not be written by that
  *            previous kernel (weights are constant during decode); x is still
- *            read only after the previous kernel has completed.  Batch-1
- *            launches whose K split exceeds 8 CTAs ignore it (their clusters,
- *            placed beside the previous kernel's CTAs, ran slower).
+ *            read only after the previous kernel has completed.
  *            Q4K_FLAG_TENSOR_CORE: batch 1 uses the tensor-core inner product
  *            of the larger batches instead of the integer one.
  *            Q4K_FLAG_Q8K_X: batch 1 with x quantized Q8_K style (dotLLM README,

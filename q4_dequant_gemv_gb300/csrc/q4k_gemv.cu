@@ -953,11 +953,7 @@ static cudaError_t launch_one(const GemvPlan &p, const WMaps &maps, const GemvAr
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
-    // Batch-1 launches with clusters above 8 CTAs go without PDL: placed early
-    // beside the previous kernel's CTAs, not all of their clusters found room
-    // at once (measured: the down projection after gate/up, 15.9 us with PDL,
-    // 13.8 us without; the tensor-core kernels gain from PDL there).
-    if (pdl && !(XM != 0 && p.split > 8)) {
+    if (pdl) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
