@@ -451,3 +451,41 @@ def test_rows16_grouped_q8k_and_guards(env):
     Kl = 8448
     with pytest.raises(q4k.Q4KError):
         q4k.gemv(_dev(synth.q4k_weights(16, Kl, 69)), _dev(synth.normal_f32((1, Kl), 70)), rows16=True)
+
+
+def test_pdl_ten_cta_clusters_bitwise_equal(env):
+    """The down-projection shape (K split over clusters of more than 8 CTAs)
+    launched with PDL, back to back on a side stream and captured in a graph,
+    gives bitwise the results of plain launches, and stays within the
+    tolerance of the oracle on sampled rows."""
+    q4k, oracle = env
+    N, K = 3584, 18944
+    assert q4k.gemv_plan(N, K, 1)["split_k"] > 8
+    W = synth.q4k_weights(N, K, (91, 1))
+    Wd = _dev(W)
+    xs = [_dev(synth.normal_f32((1, K), (92, i))) for i in range(3)]
+    ref = [q4k.gemv(Wd, x) for x in xs]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    ys = [torch.empty_like(r) for r in ref]
+    with torch.cuda.stream(s):
+        for x, y in zip(xs, ys):
+            q4k.gemv(Wd, x, y, pdl=True, stream=s)
+    s.synchronize()
+    for a, b in zip(ref, ys):
+        assert torch.equal(a, b)
+    for y in ys:
+        y.zero_()
+    g = torch.cuda.CUDAGraph()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for x, y in zip(xs, ys):
+                q4k.gemv(Wd, x, y, pdl=True, stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(ref, ys):
+        assert torch.equal(a, b)
+    rows = np.array([0, 1, 127, 128, 1000, N - 1])
+    x0 = xs[0].cpu().numpy()
+    assert_close(ref[0].cpu().numpy()[:, rows], oracle.gemv_rows(W, x0, N, K, rows), x0, K, "down shape, PDL")
