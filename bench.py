@@ -318,29 +318,32 @@ def run_ours(args):
         Ws.append([torch.from_numpy(W).to(dev) for _, _, _, W in lw])
     # Activations: q/k/v share one input, gate/up share one (as in a decoder
     # layer); o and down have their own.  All live in one flat buffer per batch
-    # size so that the end-to-end run moves them with a single copy each way.
+    # size, layer-major, so that the end-to-end run moves each layer's inputs
+    # and outputs as one contiguous range.
     kinds = (("attn", 3584, 50), ("o", 3584, 51), ("mlp", 3584, 52), ("down", 18944, 53))
-    x_elems_per_row = LAYERS * sum(K for _, K, _ in kinds)
-    y_elems_per_row = LAYERS * sum(N for _, N, _ in shapes)
+    x_per_layer = sum(K for _, K, _ in kinds)
+    y_per_layer = sum(N for _, N, _ in shapes)
+    x_elems_per_row = LAYERS * x_per_layer
+    y_elems_per_row = LAYERS * y_per_layer
     x_flat = torch.empty(16 * x_elems_per_row, dtype=torch.float32, device=dev)
     y_flat = torch.empty(16 * y_elems_per_row, dtype=torch.float32, device=dev)
 
-    kind_base = {}
+    kind_off = {}
     acc = 0
     for kname, K, _ in kinds:
-        kind_base[kname] = (acc, K)
-        acc += LAYERS * K
+        kind_off[kname] = (acc, K)
+        acc += K
 
     def x_view(B, layer, kind):
         """[B, K] activations of one (layer, consumer); contiguous, batch-major."""
-        base, K = kind_base[kind]
-        start = B * (base + layer * K)
+        off, K = kind_off[kind]
+        start = B * (layer * x_per_layer + off)
         return x_flat[start:start + B * K].view(B, K)
 
     def y_view(B, layer, mi):
-        base = LAYERS * sum(N for _, N, _ in shapes[:mi])
+        off = sum(N for _, N, _ in shapes[:mi])
         N = shapes[mi][1]
-        start = B * (base + layer * N)
+        start = B * (layer * y_per_layer + off)
         return y_flat[start:start + B * N].view(B, N)
 
     g_x = synth.rng(7, 7)
@@ -351,12 +354,16 @@ def run_ours(args):
     def step_bytes(B):
         return LAYERS * sum(N * (K // 256) * 144 + 4 * B * K + 4 * B * N for _, N, K in shapes)
 
-    def decode_step(B, pdl=True, fused=True, tc=False, q8=False):
+    def decode_step(B, pdl=True, fused=True, tc=False, q8=False, hook=None):
         """One decode step: 28 layers x 7 GEMVs.  fused: q/k/v share one launch
         and gate/up share one (4 launches per layer); otherwise 7 launches.
         tc: batch 1 on the tensor-core inner product instead of the integer one.
-        q8: batch 1 with x quantized Q8_K style (its own error bound)."""
+        q8: batch 1 with x quantized Q8_K style (its own error bound).
+        hook(layer, when) runs before ("pre") and after ("post") each layer's
+        launches (the end-to-end step issues its copies there)."""
         for layer in range(LAYERS):
+            if hook is not None:
+                hook(layer, "pre")
             W, y = Ws[layer], (lambda mi: y_view(B, layer, mi))
             if fused:
                 q4k.gemv_grouped(W[0:3], x_view(B, layer, "attn"), [y(0), y(1), y(2)], stream=stream, pdl=pdl,
@@ -368,6 +375,8 @@ def run_ours(args):
             else:
                 for mi, (name, N, K) in enumerate(shapes):
                     q4k.gemv(W[mi], x_view(B, layer, src[name]), y(mi), stream=stream, pdl=pdl, tensor_core=tc)
+            if hook is not None:
+                hook(layer, "post")
 
     def capture(fn):
         g = torch.cuda.CUDAGraph()
@@ -566,31 +575,71 @@ def run_ours(args):
               "weight_copies": ncopy, "launches_timed": len(per) * ncopy,
               "l2": f"{ncopy} distinct copies of W ({ncopy * N0 * (K0 // 256) * 144 / 1e6:.0f} MB) cycled, 4x L2"}
 
-    # ---- end to end through the public API with host buffers (batch 1):
-    # one H2D copy of every activation of the step, the graph of the step's
-    # launches, one D2H copy of every output.
+    # ---- end to end through the public API with host buffers (batch 1): every
+    # step copies all of its activations in from pinned host memory and all of
+    # its outputs back out.  The copies run on a second stream beside the
+    # launches: layer 0's inputs first, the other layers' inputs while layer 0
+    # runs, and each group of layers' outputs while later layers run; only the
+    # last group's outputs follow the last launch.  Copies and launches are
+    # one graph.
+    # The host buffers are page-locked with cudaHostRegister rather than taken
+    # from torch's pinned-memory cache, whose copy bookkeeping records events
+    # that a graph capture cannot hold.
     nx1, ny1 = x_elems_per_row, y_elems_per_row
-    h_x = torch.empty(nx1, dtype=torch.float32).pin_memory()
+    host_arrays = [np.empty(nx1, dtype=np.float32), np.empty(ny1, dtype=np.float32)]
+    h_x, h_y = (torch.from_numpy(a) for a in host_arrays)
+    for t in (h_x, h_y):
+        torch.cuda.check_error(torch.cuda.cudart().cudaHostRegister(t.data_ptr(), t.numel() * 4, 0))
     h_x.copy_(x_flat[:nx1].cpu())
-    h_y = torch.empty(ny1, dtype=torch.float32).pin_memory()
     h2d, d2h = nx1 * 4, ny1 * 4
+    copy_stream = torch.cuda.Stream(device=dev)
+    out_groups = [(0, 4), (4, 8), (8, 12), (12, 16), (16, 20), (20, 24), (24, 27), (27, LAYERS)]
+
+    def e2e_hook(layer, when):
+        if when == "pre" and layer == 1:
+            stream.wait_stream(copy_stream)          # inputs of layers 1.. are in
+        if when != "post":
+            return
+        for lo, hi in out_groups:
+            if layer + 1 != hi:
+                continue
+            a, b = lo * y_per_layer, hi * y_per_layer
+            if hi == LAYERS:                          # the last group: in order
+                h_y[a:b].copy_(y_flat[a:b], non_blocking=True)
+            else:
+                copy_stream.wait_stream(stream)
+                with torch.cuda.stream(copy_stream):
+                    h_y[a:b].copy_(y_flat[a:b], non_blocking=True)
 
     def e2e_step():
-        x_flat[:nx1].copy_(h_x, non_blocking=True)
-        g1.replay()
-        h_y.copy_(y_flat[:ny1], non_blocking=True)
+        copy_stream.wait_stream(stream)
+        x_flat[:x_per_layer].copy_(h_x[:x_per_layer], non_blocking=True)
+        with torch.cuda.stream(copy_stream):
+            x_flat[x_per_layer:nx1].copy_(h_x[x_per_layer:], non_blocking=True)
+        decode_step(1, hook=e2e_hook)
+        stream.wait_stream(copy_stream)
 
+    g_e2e = capture(e2e_step)
+    y_flat[:ny1].fill_(float("nan"))
+    h_y.fill_(float("nan"))
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            e2e_step()
+            g_e2e.replay()
         stream.synchronize()
+        e2e_copies_exact = bool(torch.equal(h_y, y_flat[:ny1].cpu()))
         barrier()
         t0 = time.perf_counter()
         e2e_steps = max(10, args.steps // 4)
         for _ in range(e2e_steps):
-            e2e_step()
+            g_e2e.replay()
         stream.synchronize()
         e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_steps, device=dev)
+    del g_e2e
+    stream.synchronize()
+    for t in (h_x, h_y):
+        torch.cuda.check_error(torch.cuda.cudart().cudaHostUnregister(t.data_ptr()))
+    if not e2e_copies_exact:
+        raise RuntimeError("end-to-end step: the outputs copied to the host differ from the device outputs")
     e2e_val = whole_job_rate(bytes1, world, e2e_ms * 1e-3) / 1e9
 
     # ---- roofline of the dominant kernel (the batch-1 GEMV; the step is only its launches)
@@ -669,7 +718,7 @@ def run_ours(args):
         "prefill": prefill,
         "roofline": roof,
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms, "path": "one pinned H2D of all step activations, graph of the 112 launches, one D2H of all outputs"},
+                "ms_per_step": e2e_ms, "path": "pinned H2D of all step activations and D2H of all outputs on a second stream overlapped with the 112 launches (layer 0 inputs first, outputs in 8 layer groups, the last one layer), one graph per step"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": ck,
         "peaks": pk,
